@@ -1,0 +1,62 @@
+"""Indexer scores and per-query top-K selection (CSA2 FULL / REINDEX / REUSE).
+
+Ref: "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression",
+picx.dev summary, Methodology / Architecture Components / 2. Compressed Sparse
+Attention 2: a FULL layer computes its own indexer K and top-K indices, a
+REINDEX layer computes fresh top-K indices, a REUSE layer takes the preceding
+layer's indices unchanged.
+
+Readings (the page names the indexer but prints no formula):
+  * score I[n] = sum_h w[h] * max(0, q[h] . z[n]) over H_I indexer heads, with
+    a per-query weight vector w (the multi-head ReLU scalar score);
+  * top-K keeps the K largest scores among the visible entries n < n_visible;
+    equal scores go to the lower index; the result is listed in ascending
+    index order and padded with -1 when fewer than K entries are visible.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def scores(q_idx: np.ndarray, w_idx: np.ndarray, z: np.ndarray) -> np.ndarray:
+    """I[t, n] for one sequence: q_idx [T, H_I, D_I], w_idx [T, H_I], z [N, D_I] -> [T, N] float64."""
+    q = np.asarray(q_idx, dtype=np.float64)
+    w = np.asarray(w_idx, dtype=np.float64)
+    zz = np.asarray(z, dtype=np.float64)
+    dots = np.einsum("thd,nd->thn", q, zz)             # per-head dot products
+    return np.einsum("th,thn->tn", w, np.maximum(dots, 0.0))
+
+
+def topk(score_row: np.ndarray, n_visible: int, K: int) -> np.ndarray:
+    """Indices of the K best visible entries, ascending, -1 padded (int32 [K])."""
+    n_visible = int(n_visible)
+    s = np.asarray(score_row[:n_visible], dtype=np.float64)
+    order = np.lexsort((np.arange(n_visible), -s))     # primary: score desc; secondary: index asc
+    take = np.sort(order[: min(K, n_visible)])
+    out = np.full(K, -1, dtype=np.int32)
+    out[: take.size] = take
+    return out
+
+
+def kth_score(score_row: np.ndarray, n_visible: int, K: int) -> float:
+    """Score of the K-th selected entry (the selection threshold), or -inf if all are taken."""
+    s = np.sort(np.asarray(score_row[: int(n_visible)], dtype=np.float64))[::-1]
+    if K >= s.size or s.size == 0:
+        return -np.inf
+    return float(s[K - 1])
+
+
+def index_topk(mode: int, q_idx, w_idx, z, n_visible, K: int, prev_idx=None):
+    """One sequence's indices for a layer of the given mode (0 FULL, 1 REINDEX, 2 REUSE).
+
+    FULL and REINDEX compute the same thing from their own query and keys (the
+    difference between them is which main KV the attention reads); REUSE
+    returns the preceding layer's indices.
+    """
+    if mode == 2:
+        if prev_idx is None:
+            raise ValueError("REUSE needs the preceding layer's indices")
+        return np.array(prev_idx, dtype=np.int32, copy=True)
+    I = scores(q_idx, w_idx, z)
+    T = I.shape[0]
+    return np.stack([topk(I[t], n_visible[t], K) for t in range(T)])
