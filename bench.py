@@ -1,0 +1,500 @@
+#!/usr/bin/env python
+"""Benchmark of the CSA2 FP4 sparse-decode hot path on B300.
+
+Workload (one "step"): a decode step of a three-layer CSA2 group FULL -> REINDEX ->
+REUSE for 32 sequences at 128K context (32768 compressed entries each), 64 query
+heads, latent 512 + rope 64 in FP4 (E2M1 + E4M3 per 16), indexer 8 x 64 in bf16,
+top-K 2048, sliding window 128. Per layer: csa2_index_topk -> csa2_sparse_decode ->
+csa2_swa_merge (REUSE skips the indexer). The KV caches and keys are resident in HBM
+(written before timing); each timed step re-reads them.
+
+Prints one JSON line (rank 0). --impl reference times the CPU oracle on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import csa2_inputs as ci  # noqa: E402
+
+METRIC = "CSA2 FP4 decode steps/s + HBM GB/s vs 8 TB/s; CED KV-proj TFLOP/s"
+CFG = ci.DECODE_128K
+ENTRY_BYTES = 288 + 36
+KEY_BYTES = 64 * 2
+SWA_ROW_BYTES = 576 * 2
+TARGET_HBM_GBS = 8000.0
+
+
+def algorithmic_bytes_per_step(cfg=CFG) -> int:
+    """Indexer keys (FULL, REINDEX) + K selected entries + SWA window, per sequence per layer."""
+    per_seq = 0
+    for m in cfg.modes:
+        if m != ci.REUSE:
+            per_seq += cfg.N * KEY_BYTES
+        per_seq += cfg.K * ENTRY_BYTES + cfg.W * SWA_ROW_BYTES
+    return per_seq * cfg.B
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """The CPU oracle on one sequence of the workload, one layer at a time.
+
+    Set-up (untimed) encodes the sequence's latent KV to FP4, as the cache exists
+    before a decode step; a timed layer runs the indexer and top-K (FULL,
+    REINDEX), dequantises the selected entries, and runs the sparse attention,
+    the SWA branch and the merge."""
+
+    def __init__(self, cfg, inp, b: int):
+        from oracle import fp4
+        self.cfg, self.inp, self.b = cfg, inp, b
+        X = ci.latent_rows(cfg, 0, b, np.arange(cfg.N))
+        self.codes, self.scales = fp4.encode(X)
+        self.prev = None
+
+    def layer_seconds(self, li: int) -> float:
+        from oracle import attention, fp4, indexer
+        cfg, b, L = self.cfg, self.b, self.inp.layers[li]
+        f64 = lambda a: ci.bf16_bits_to_f32(a).astype(np.float64)
+        t0 = time.perf_counter()
+        if L.mode != ci.REUSE:
+            I = indexer.scores(f64(L.q_idx[b]), L.w_idx[b], f64(L.z[b]))
+            idx = np.stack([indexer.topk(I[t], cfg.N, cfg.K) for t in range(cfg.T)])
+        else:
+            idx = self.prev
+        for t in range(cfg.T):
+            sel = idx[t][idx[t] >= 0]
+            rows = fp4.decode(self.codes[sel], self.scales[sel])
+            q = f64(L.q[b, t])
+            og, lg = attention.attend(q, rows, cfg.d_v, cfg.softmax_scale)
+            os_, ls = attention.swa_branch(q, f64(L.swa[b]), 0, cfg.W, cfg.d_v, cfg.softmax_scale)
+            attention.merge(og, lg, os_, ls)
+        self.prev = idx
+        return time.perf_counter() - t0
+
+
+def cpu_cores() -> int:
+    return len(os.sched_getaffinity(0))
+
+
+def oracle_step_seconds(cfg, inp, n_layer_samples: int, warmup: int = 0, seqs=(0, 1)):
+    """Mean oracle time per layer (by layer index) over rotating (sequence, layer) samples;
+    returns the extrapolated seconds of one full step (all layers, all sequences)."""
+    nl = len(cfg.modes)
+    samples = {i: [] for i in range(nl)}
+    k = 0
+    si = 0
+    while k < warmup + n_layer_samples:
+        smp = OracleSample(cfg, inp, seqs[si % len(seqs)])
+        si += 1
+        for li in range(nl):
+            t = smp.layer_seconds(li)
+            if k >= warmup:
+                samples[li].append(t)
+            k += 1
+            if k >= warmup + n_layer_samples and all(samples[j] for j in range(nl)):
+                break
+    per_layer = [statistics.mean(samples[li]) for li in range(nl)]
+    return sum(per_layer) * cfg.B, per_layer
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    inp = ci.make_decode_inputs(CFG, with_x=False)
+    nl = len(CFG.modes)
+    step_s, per_layer = oracle_step_seconds(CFG, inp, max(args.steps, nl), warmup=args.warmup,
+                                            seqs=tuple(range(min(CFG.B, 4))))
+    value = 1.0 / step_s
+    sample = (f"each step = one (sequence, layer) of the group, rotating over {nl} layers and 4 sequences; "
+              f"per-layer means {[round(x, 4) for x in per_layer]} s, summed and x{CFG.B} sequences")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(),
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block():
+    return {"workload": "csa2_decode_group_b32_ctx128k_full_reindex_reuse", "batch": CFG.B,
+            "entries": CFG.N, "context_tokens": CFG.ctx, "heads": CFG.H, "indexer_heads": CFG.H_I,
+            "top_k": CFG.K, "n_win": CFG.W, "layers": "FULL,REINDEX,REUSE",
+            "kv_format": "e2m1 + e4m3/16 (324 B/entry)", "l2": "flushed between timed steps (256 MiB write)"}
+
+
+# ---------------------------------------------------------------------------
+# Clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    from cuda.bindings import driver as cu
+
+    import sparse_attention_kv_decode_b300 as csa2
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    L = csa2.lib()
+    cfg = CFG
+    inp = ci.make_decode_inputs(cfg)
+    b16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    X = t32(inp.layers[0].X)
+    codes, scales = csa2.csa2_encode_kv(X)
+    del X
+    inp.layers[0].X = None
+    nvis, wst, wln = t32(inp.n_visible), t32(inp.win_start), t32(inp.win_len)
+    dl = []
+    for Lr in inp.layers:
+        d = dict(mode=Lr.mode, q=b16(Lr.q), swa=b16(Lr.swa))
+        if Lr.mode != ci.REUSE:
+            d.update(q_idx=b16(Lr.q_idx), w=t32(Lr.w_idx), z=b16(Lr.z))
+        d["o"] = torch.empty((cfg.B, cfg.T, cfg.H, cfg.d_v), dtype=torch.float32, device=dev)
+        d["lse"] = torch.empty((cfg.B, cfg.T, cfg.H), dtype=torch.float32, device=dev)
+        dl.append(d)
+    idx_bufs = [torch.empty((cfg.B, cfg.T, cfg.K), dtype=torch.int32, device=dev) for _ in range(2)]
+    ws = csa2.csa2_workspace(cfg.B, cfg.T, cfg.H, cfg.N, cfg.K, device=dev)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    scale = ctypes.c_float(cfg.softmax_scale)
+    P = lambda t: t.data_ptr()
+    wsp, wsn = P(ws), ws.numel()
+
+    # the step as a list of (name, kind, thunk) C-ABI calls on `stream`
+    calls = []
+    cur = None
+    for li, d in enumerate(dl):
+        mode = d["mode"]
+        if mode != ci.REUSE:
+            cur = idx_bufs[li % 2]
+            calls.append((f"index_topk[{ci.MODE_NAMES[mode]}]", "index",
+                          (lambda d=d, cur=cur, mode=mode: L.csa2_index_topk(
+                              mode, cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N, P(nvis),
+                              cfg.K, None, P(cur), None, wsp, wsn, sp))))
+        else:
+            calls.append(("index_topk[REUSE]", "reuse",
+                          (lambda cur=cur: L.csa2_index_topk(2, cfg.B, cfg.T, 0, None, None, None, 0, None,
+                                                             cfg.K, P(cur), P(cur), None, None, 0, sp))))
+        calls.append((f"sparse_decode[{ci.MODE_NAMES[mode]}]", "sparse",
+                      (lambda d=d, cur=cur: L.csa2_sparse_decode(
+                          cfg.B, cfg.T, cfg.H, P(d["q"]), P(codes), P(scales), cfg.N, P(cur), cfg.K, cfg.d_v,
+                          scale, P(d["o"]), P(d["lse"]), wsp, wsn, sp))))
+        calls.append((f"swa_merge[{ci.MODE_NAMES[mode]}]", "swa",
+                      (lambda d=d: L.csa2_swa_merge(
+                          cfg.B, cfg.T, cfg.H, P(d["q"]), P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v,
+                          scale, P(d["o"]), P(d["lse"]), P(d["o"]), P(d["lse"]), wsp, wsn, sp))))
+    launches_per_call = {"index": 2, "reuse": 0, "sparse": 2, "swa": 2}
+
+    def cuchk(r):
+        err = r[0] if isinstance(r, tuple) else r
+        if int(err) != 0:
+            raise RuntimeError(f"CUDA driver error {err}")
+        return r[1] if isinstance(r, tuple) and len(r) > 1 else None
+
+    events = [cuchk(cu.cuEventCreate(0)) for _ in range(len(calls) + 1)]
+
+    def enqueue_step(record=True):
+        for i, (name, _, fn) in enumerate(calls):
+            if record:
+                cuchk(cu.cuEventRecordWithFlags(events[i], sp, cu.CUevent_record_flags.CU_EVENT_RECORD_EXTERNAL))
+            st = fn()
+            if st != 0:
+                raise RuntimeError(f"{name} returned {st}")
+        if record:
+            cuchk(cu.cuEventRecordWithFlags(events[-1], sp, cu.CUevent_record_flags.CU_EVENT_RECORD_EXTERNAL))
+
+    # warm once eagerly (sets kernel attributes), then capture the step as a CUDA graph
+    with torch.cuda.stream(stream):
+        enqueue_step(record=False)
+    stream.synchronize()
+    st, flags = csa2.csa2_read_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        enqueue_step(record=True)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        graph.replay()
+    torch.cuda.synchronize()
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not gpu_uuid.startswith("GPU-"):
+            gpu_uuid = "GPU-" + gpu_uuid
+    except Exception:
+        gpu_uuid = None
+    clocks = ClockSampler(gpu_uuid)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    per_call = [[] for _ in calls]
+    step_ms = []
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+        graph.replay()
+        stream.synchronize()
+        for i in range(len(calls)):
+            per_call[i].append(cuchk(cu.cuEventElapsedTime(events[i], events[i + 1])))
+        step_ms.append(cuchk(cu.cuEventElapsedTime(events[0], events[-1])))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+
+    total_s = sum(step_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    ms_per_step = total_s * 1e3 / args.steps
+    value = world * args.steps / total_s
+    peaks = load_peaks()
+    bytes_step = algorithmic_bytes_per_step(cfg)
+
+    # per-call breakdown and roofline of the dominant call
+    kinds = {}
+    breakdown = []
+    for (name, kind, _), ts in zip(calls, per_call):
+        avg = statistics.mean(ts) * 1e-3
+        breakdown.append({"call": name, "us": round(avg * 1e6, 2)})
+        k = kinds.setdefault(kind, [0.0, 0])
+        k[0] += avg
+        k[1] += 1
+    Q = cfg.B * cfg.T
+    flops_sparse = 2.0 * Q * cfg.H * cfg.K * (576 + cfg.d_v)
+    flops_swa = 2.0 * Q * cfg.H * cfg.W * (576 + cfg.d_v)
+    models = {
+        "index": ("hbm", Q * cfg.N * KEY_BYTES, "GB/s", peaks["hbm"]),
+        "sparse": ("tensor", flops_sparse, "TFLOP/s", peaks["bf16"]),
+        "swa": ("tensor", flops_swa, "TFLOP/s", peaks["bf16"]),
+    }
+    dom = max((k for k in kinds if k in models), key=lambda k: kinds[k][0])
+    bound, work, unit, peak = models[dom]
+    t_launch = kinds[dom][0] / kinds[dom][1]
+    achieved = work / t_launch / (1e9 if unit == "GB/s" else 1e12)
+    rows = {}
+    for k, (b, w, u, pk) in models.items():
+        if k in kinds:
+            tl = kinds[k][0] / kinds[k][1]
+            a = w / tl / (1e9 if u == "GB/s" else 1e12)
+            rows[k] = {"bound": b, "achieved": round(a, 2), "peak": pk, "unit": u, "frac": round(a / pk, 4),
+                       "us_per_call": round(tl * 1e6, 2)}
+    roofline = {"kernel": {"index": "csa2_index_topk (indexer score + top-K select kernels)",
+                           "sparse": "csa2_sparse_decode (gather/dequant/MMA + combine kernels)",
+                           "swa": "csa2_swa_merge"}[dom],
+                "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "peak_source": peaks["src"], "traffic": None}
+
+    e2e = None if args.no_e2e else run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs,
+                                           ws, world, dev)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        step_s, per_layer = oracle_step_seconds(cfg, inp, 2 * len(cfg.modes), seqs=(0, 1))
+        cpu = {"value": 1.0 / step_s, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"2 of {cfg.B} sequences x {len(cfg.modes)} layers (indexer, top-K, dequant of the "
+                         f"selected entries, attention, SWA, merge), extrapolated x{cfg.B}; per-layer means "
+                         f"{[round(x, 4) for x in per_layer]} s"}
+
+    n_launch = sum(launches_per_call[k] for _, k, _ in calls) * args.steps
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16/fp16 mma, fp32 acc (fp4 e2m1+e4m3 cache)", "data": "synthetic",
+            "config": config_block(),
+            "hbm_gbs_step": round(bytes_step / (ms_per_step * 1e-3) / 1e9, 1),
+            "frac_of_8tbs": round(bytes_step / (ms_per_step * 1e-3) / 1e9 / TARGET_HBM_GBS, 4),
+            "bytes_per_step": bytes_step,
+            "roofline": roofline, "roofline_by_call": rows, "calls": breakdown,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": n_launch,
+            "wall_s_timed_loop": round(wall, 3),
+            "ced_projection": None,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs, ws, world, dev):
+    """Same step through the C ABI with host buffers: per step, H2D of the step's queries
+    (pinned) and D2H of every layer's output; no graph, one ctypes call per ABI call."""
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    scale = ctypes.c_float(cfg.softmax_scale)
+    P = lambda t: t.data_ptr()
+    host_in, host_out = [], []
+    h2d = d2h = 0
+    for d in dl:
+        for k in ("q", "q_idx", "w"):
+            if k in d:
+                h = torch.empty(d[k].shape, dtype=d[k].dtype, pin_memory=True)
+                h.copy_(d[k].cpu())
+                host_in.append((h, d[k]))
+                h2d += h.numel() * h.element_size()
+        for k in ("o", "lse"):
+            h = torch.empty(d[k].shape, dtype=d[k].dtype, pin_memory=True)
+            host_out.append((h, d[k]))
+            d2h += h.numel() * h.element_size()
+    wsp, wsn = P(ws), ws.numel()
+
+    def step():
+        with torch.cuda.stream(stream):
+            for h, dd in host_in:
+                dd.copy_(h, non_blocking=True)
+        cur = None
+        for li, d in enumerate(dl):
+            if d["mode"] != ci.REUSE:
+                cur = idx_bufs[li % 2]
+                r = L.csa2_index_topk(d["mode"], cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N,
+                                      P(nvis), cfg.K, None, P(cur), None, wsp, wsn, sp)
+                assert r == 0
+            r = L.csa2_sparse_decode(cfg.B, cfg.T, cfg.H, P(d["q"]), P(codes), P(scales), cfg.N, P(cur), cfg.K,
+                                     cfg.d_v, scale, P(d["o"]), P(d["lse"]), wsp, wsn, sp)
+            assert r == 0
+            r = L.csa2_swa_merge(cfg.B, cfg.T, cfg.H, P(d["q"]), P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W,
+                                 cfg.d_v, scale, P(d["o"]), P(d["lse"]), P(d["o"]), P(d["lse"]), wsp, wsn, sp)
+            assert r == 0
+        with torch.cuda.stream(stream):
+            for h, dd in host_out:
+                h.copy_(dd, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 4)):
+        step()
+    stream.synchronize()
+    n = max(10, args.steps // 10)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    stream.synchronize()
+    total = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total = float(t.item())
+    return {"value": world * n / total, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "note": "C-ABI calls without a graph; pinned host inputs/outputs copied every step"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

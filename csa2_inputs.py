@@ -32,11 +32,19 @@ COMPRESS = 4  # raw tokens per compressed entry
 # bf16 storage helpers (input preparation only)
 # ----------------------------------------------------------------------------
 def bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round fp32 values to bf16 (nearest, ties to even); return the uint16 bit patterns."""
+    """Round finite fp32 values to bf16 (nearest, ties to even); return the uint16 bit patterns.
+
+    For finite inputs u + 0x7FFF + lsb stays below 2^32, so uint32 arithmetic is exact."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return rounded.astype(np.uint16)
+    u = x.reshape(-1).view(np.uint32)
+    out = np.empty(u.shape, dtype=np.uint16)
+    step = 1 << 22
+    for i in range(0, u.size, step):
+        c = u[i:i + step]
+        r = c + np.uint32(0x7FFF)
+        r += (c >> np.uint32(16)) & np.uint32(1)
+        out[i:i + step] = r >> np.uint32(16)
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -166,40 +174,78 @@ def visibility(cfg: DecodeConfig) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
     return rep(nvis), rep(wstart), rep(wlen)
 
 
-def make_decode_inputs(cfg: DecodeConfig) -> DecodeInputs:
-    """Draw every input of a decode group from PCG64(seed), in a fixed order.
+def _stream(seed: int, *key: int) -> np.random.Generator:
+    """Independent PCG64 stream for one tensor, keyed by (seed, layer, tensor tag)."""
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, *key])))
 
-    Per layer: X (FULL only), z (FULL, REINDEX), q_idx, w_idx (FULL, REINDEX), q, swa.
-    All draws are standard normal in fp32; w_idx takes absolute values; every
+
+_TAG = {"u": 0, "X": 1, "z": 2, "q_idx": 3, "w_idx": 4, "q": 5, "swa": 6}
+
+
+def _per_sequence_normal(seed: int, layer: int, tag: int, B: int, shape) -> np.ndarray:
+    """fp32 N(0,1) array [B, *shape]; sequence b drawn from stream (seed, layer, tag, b).
+
+    Sequences are drawn on a thread pool (NumPy releases the GIL while filling)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    out = np.empty((B,) + tuple(shape), dtype=np.float32)
+
+    def fill(b):
+        _stream(seed, layer, tag, b).standard_normal(tuple(shape), dtype=np.float32, out=out[b])
+
+    n = min(B, max(1, len(os.sched_getaffinity(0))))
+    if n == 1:
+        for b in range(B):
+            fill(b)
+    else:
+        with ThreadPoolExecutor(n) as ex:
+            list(ex.map(fill, range(B)))
+    return out
+
+
+def make_decode_inputs(cfg: DecodeConfig, with_x: bool = True) -> DecodeInputs:
+    """Draw every input of a decode group; each tensor has its own PCG64 stream.
+
+    Per layer: X (FULL only), z (FULL, REINDEX), q_idx, w_idx (FULL, REINDEX), q, swa;
+    X and z have one stream per sequence.
+    Every draw is standard normal in fp32; w_idx takes absolute values; every
     bf16 tensor is rounded to nearest-even. With planted_bias > 0 a unit vector
-    u is drawn first and keys get z[b, n] += bias * n/(N-1) * u, which makes
-    the indexer prefer recent entries for heads aligned with u.
+    u is drawn and keys get z[b, n] += bias * n/(N-1) * u, which makes the
+    indexer prefer recent entries for heads aligned with u. with_x=False skips
+    the fp32 latent KV (the other tensors are unchanged, their streams being
+    independent).
     """
-    rng = np.random.Generator(np.random.PCG64(cfg.seed))
     B, T, N, H, H_I = cfg.B, cfg.T, cfg.N, cfg.H, cfg.H_I
     u = None
     if cfg.planted_bias:
-        u = rng.standard_normal(D_IDX, dtype=np.float32)
+        u = _stream(cfg.seed, 0, _TAG["u"]).standard_normal(D_IDX, dtype=np.float32)
         u = (u / np.linalg.norm(u)).astype(np.float32)
     layers: List[LayerInputs] = []
-    for mode in cfg.modes:
+    for li, mode in enumerate(cfg.modes):
         X = z = q_idx = w_idx = None
-        if mode == FULL:
-            X = rng.standard_normal((B, N, D_KV), dtype=np.float32)
+        if mode == FULL and with_x:
+            X = _per_sequence_normal(cfg.seed, li, _TAG["X"], B, (N, D_KV))
         if mode in (FULL, REINDEX):
-            zf = rng.standard_normal((B, N, D_IDX), dtype=np.float32)
+            zf = _per_sequence_normal(cfg.seed, li, _TAG["z"], B, (N, D_IDX))
             if u is not None:
                 ramp = (np.arange(N, dtype=np.float32) / np.float32(max(N - 1, 1)))
                 zf += (np.float32(cfg.planted_bias) * ramp)[None, :, None] * u[None, None, :]
             z = bf16_bits(zf)
             del zf
-            q_idx = bf16_bits(rng.standard_normal((B, T, H_I, D_IDX), dtype=np.float32))
-            w_idx = np.abs(rng.standard_normal((B, T, H_I), dtype=np.float32))
-        q = bf16_bits(rng.standard_normal((B, T, H, D_KV), dtype=np.float32))
-        swa = bf16_bits(rng.standard_normal((B, cfg.S, D_KV), dtype=np.float32))
+            q_idx = bf16_bits(_stream(cfg.seed, li, _TAG["q_idx"]).standard_normal((B, T, H_I, D_IDX),
+                                                                                    dtype=np.float32))
+            w_idx = np.abs(_stream(cfg.seed, li, _TAG["w_idx"]).standard_normal((B, T, H_I), dtype=np.float32))
+        q = bf16_bits(_stream(cfg.seed, li, _TAG["q"]).standard_normal((B, T, H, D_KV), dtype=np.float32))
+        swa = bf16_bits(_stream(cfg.seed, li, _TAG["swa"]).standard_normal((B, cfg.S, D_KV), dtype=np.float32))
         layers.append(LayerInputs(mode, X, z, q_idx, w_idx, q, swa))
     nvis, wstart, wlen = visibility(cfg)
     return DecodeInputs(cfg, layers, nvis, wstart, wlen)
+
+
+def latent_rows(cfg: DecodeConfig, layer: int, b: int, rows: np.ndarray) -> np.ndarray:
+    """Rows of the FULL layer's fp32 latent KV for one sequence (regenerated from its stream)."""
+    X = _stream(cfg.seed, layer, _TAG["X"], b).standard_normal((cfg.N, D_KV), dtype=np.float32)
+    return X[rows]
 
 
 @dataclass
@@ -211,16 +257,17 @@ class CedInputs:
 
 
 def make_ced_inputs(cfg: CedConfig) -> CedInputs:
-    """H ~ N(0,1)/64 and W ~ N(0, 1/d_model), all rounded to bf16, drawn H, W_kv, W_z."""
-    rng = np.random.Generator(np.random.PCG64(cfg.seed))
-    Hm = bf16_bits(rng.standard_normal((cfg.rows, cfg.d_model), dtype=np.float32) / np.float32(64))
+    """H ~ N(0,1)/64 and W ~ N(0, 1/d_model), all rounded to bf16 (one stream per tensor)."""
+    Hm = bf16_bits(_stream(cfg.seed, 0, 0).standard_normal((cfg.rows, cfg.d_model), dtype=np.float32)
+                   / np.float32(64))
     ws = np.float32(1.0 / np.sqrt(cfg.d_model))
-    Wkv = bf16_bits(rng.standard_normal((cfg.n_layers, D_KV, cfg.d_model), dtype=np.float32) * ws)
-    Wz = bf16_bits(rng.standard_normal((cfg.n_layers, D_IDX, cfg.d_model), dtype=np.float32) * ws)
+    Wkv = bf16_bits(_stream(cfg.seed, 0, 1).standard_normal((cfg.n_layers, D_KV, cfg.d_model),
+                                                            dtype=np.float32) * ws)
+    Wz = bf16_bits(_stream(cfg.seed, 0, 2).standard_normal((cfg.n_layers, D_IDX, cfg.d_model),
+                                                           dtype=np.float32) * ws)
     return CedInputs(cfg, Hm, Wkv, Wz)
 
 
 def encode_rows_input(rows: int, seed: int, scale: float = 1.0) -> np.ndarray:
     """fp32 [rows, 576] N(0, scale^2) rows for quantise-only encode tests."""
-    rng = np.random.Generator(np.random.PCG64(seed))
-    return rng.standard_normal((rows, D_KV), dtype=np.float32) * np.float32(scale)
+    return _stream(seed, 0, 0).standard_normal((rows, D_KV), dtype=np.float32) * np.float32(scale)

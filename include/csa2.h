@@ -1,0 +1,185 @@
+/*
+ * csa2.h - C ABI of the CSA2 FP4 sparse-decode library (libcsa2.so, sm_103a).
+ *
+ * Decode-time global attention of Compressed Sparse Attention 2 over an FP4
+ * compressed KV cache, and the CED projection that fills that cache, as
+ * described in "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache
+ * Compression" (picx.dev summary, Methodology / Architecture Components:
+ * 1. CED, Eq. (1); 2. CSA2 layer modes; 5. FP4 Main KV Cache; and the blog
+ * repost's description of sparse attention combined with a sliding window).
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise. The
+ *    caller owns all buffers; the library never allocates or frees memory and
+ *    keeps no state beyond per-device kernel attributes set on first use.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Calls only enqueue work: they are asynchronous and stream-ordered.
+ *    Calls are thread-safe.
+ *  - Arguments are validated on the host before anything is launched; a failed
+ *    check returns a non-zero csa2_status and launches nothing. A launch error
+ *    returns CSA2_ERR_CUDA.
+ *  - Problems only the device can see (an index outside the cache, a window
+ *    outside the store) never trap: the offending element is skipped and a bit
+ *    is set in the status word at the start of the workspace; read it with
+ *    csa2_read_device_status.
+ *  - bf16 tensors are IEEE bfloat16 bit patterns (uint16). Shapes are given
+ *    row-major, innermost last.
+ *  - FP4 main-KV layout: an entry of 576 channels (512 latent + 64 rope) is
+ *    288 bytes of E2M1 codes (channel 2i in the low nibble of byte i, 2i+1 in
+ *    the high nibble; sign in bit 3 of the nibble) and 36 bytes of E4M3 scales
+ *    (scale j covers channels 16j..16j+15). dequant = e2m1(code) * e4m3(scale).
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CSA2_API __attribute__((visibility("default")))
+#else
+#define CSA2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or mode   */
+  CSA2_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels cover */
+  CSA2_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required   */
+  CSA2_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed         */
+  CSA2_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up            */
+  CSA2_ERR_DEVICE_CHECK = 6   /* a device-side bounds check fired              */
+} csa2_status;
+
+typedef enum { CSA2_MODE_FULL = 0, CSA2_MODE_REINDEX = 1, CSA2_MODE_REUSE = 2 } csa2_mode;
+typedef enum { CSA2_F32 = 0, CSA2_BF16 = 1 } csa2_dtype;
+
+/* Fixed dimensions of the format. */
+#define CSA2_D_KV 576        /* latent 512 + rope 64 channels per entry      */
+#define CSA2_D_LATENT 512
+#define CSA2_D_IDX 64        /* indexer key / query width                    */
+#define CSA2_CODE_BYTES 288  /* E2M1 bytes per entry                         */
+#define CSA2_SCALE_BYTES 36  /* E4M3 scale bytes per entry                   */
+
+/* Device status bits (csa2_read_device_status). */
+#define CSA2_DEV_BAD_INDEX 0x1u   /* sparse_decode saw idx >= n_stride or < -1 */
+#define CSA2_DEV_BAD_WINDOW 0x2u  /* swa_merge window outside [0, s_stride)    */
+#define CSA2_DEV_TOPK_LEVELS 0x4u /* top-K refinement did not settle           */
+
+/*
+ * csa2_encode_kv - write the FP4 main KV cache.
+ *
+ * (a) Quantise-only (w_kv == NULL and w_z == NULL): h is [rows][576] in
+ *     h_dtype (fp32 or bf16), d_model must be 576, n_layers must be 1 and
+ *     z_out must be NULL. Writes kv_codes [rows][288] and kv_scales [rows][36].
+ *     Per 16-channel block: s = E4M3_RNE_satfinite(fl32(amax / 6)); each code
+ *     = E2M1_RNE_satfinite(fl32(x / s)); a zero scale stores zero codes and a
+ *     value rounding to zero stores +0. (FP4 Main KV Cache, picx.dev summary.)
+ * (b) CED projection, Eq. (1): C_l = H W_l^KV and Z_l = H W_l^Z for
+ *     l = 0..n_layers-1. h is bf16 [rows][d_model]; w_kv is bf16
+ *     [n_layers][576][d_model] and w_z bf16 [n_layers][64][d_model] (row c
+ *     holds the weights of output channel c, i.e. W^T). Writes kv_codes
+ *     [n_layers][rows][288] and kv_scales [n_layers][rows][36] (C_l quantised
+ *     as in (a) from its fp32 value) and z_out bf16 [n_layers][rows][64]
+ *     (round to nearest even). Requires h_dtype == CSA2_BF16,
+ *     d_model % 64 == 0, 16-byte aligned h/w_kv/w_z/kv_codes/z_out.
+ * ws/ws_bytes are unused (pass NULL, 0).
+ */
+CSA2_API int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_model,
+                   const void* w_kv, const void* w_z, int n_layers,
+                   uint8_t* kv_codes, uint8_t* kv_scales, void* z_out,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * csa2_index_topk - per-query top-K entry selection of a CSA2 layer.
+ *
+ * FULL / REINDEX: scores every visible entry n < n_visible[b*T+t] with
+ *   I[n] = sum_h w_idx[h] * max(0, q_idx[h] . z[n])   (h < H_I)
+ * and writes the K best to out_idx [B][T][K] int32, ascending by index, with
+ * equal scores going to the lower index and -1 padding when fewer than K are
+ * visible; out_scores [B][T][K] (nullable) receives their fp32 scores (NaN at
+ * padding). The two modes compute the same selection from the layer's own
+ * indexer query and keys; they differ in which main KV the caller attends
+ * over (CSA2 layer modes, picx.dev summary). The score formula is this
+ * library's reading: the pages name the indexer but print no formula.
+ * q_idx: bf16 [B][T][H_I][64]; w_idx: fp32 [B][T][H_I]; z: bf16
+ * [B][n_stride][64]; n_visible: int32 [B*T], each in [0, n_stride].
+ * Limits: 1 <= H_I <= 16, 1 <= K <= 4096, n_stride <= 524288.
+ * REUSE: copies prev_idx [B][T][K] to out_idx (nothing to do when they are
+ *   the same pointer); q_idx, w_idx, z, n_visible and out_scores are ignored.
+ * ws: at least csa2_workspace_bytes(B, T, *, n_stride, K) bytes, prepared
+ * once by csa2_workspace_init.
+ */
+CSA2_API int csa2_index_topk(int mode, int B, int T, int H_I,
+                    const void* q_idx, const float* w_idx,
+                    const void* z, int64_t n_stride, const int32_t* n_visible,
+                    int K, const int32_t* prev_idx, int32_t* out_idx, float* out_scores,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * csa2_sparse_decode - global branch: sparse MQA over the selected FP4 entries.
+ *
+ * For each query (b, t) and head h < H:
+ *   s_j = softmax_scale * q[b,t,h,:] . C[b, idx[b,t,j], :]   (576 channels)
+ *   O_g[b,t,h,:] = sum_j softmax(s)_j * C[b, idx_j, 0:d_v],
+ *   LSE_g[b,t,h] = log sum_j exp(s_j)  (natural log),
+ * over the j with idx >= 0; C is dequantised in registers from kv_codes
+ * [B][n_stride][288] / kv_scales [B][n_stride][36]. One KV entry is shared by
+ * all heads (MQA). An empty selection gives O_g = 0 and LSE_g = -inf.
+ * q: bf16 [B][T][H][576]; idx: int32 [B][T][K]; o_g: fp32 [B][T][H][d_v];
+ * lse_g: fp32 [B][T][H]. Limits: H % 16 == 0, H <= 64, d_v == 512, K <= 4096.
+ * Indices outside [-1, n_stride) are skipped and set CSA2_DEV_BAD_INDEX.
+ */
+CSA2_API int csa2_sparse_decode(int B, int T, int H, const void* q,
+                       const uint8_t* kv_codes, const uint8_t* kv_scales, int64_t n_stride,
+                       const int32_t* idx, int K, int d_v, float softmax_scale,
+                       float* o_g, float* lse_g, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * csa2_swa_merge - sliding-window branch and its log-sum-exp merge.
+ *
+ * For each query, attends (same head/score convention as sparse_decode) over
+ * the raw bf16 rows swa_kv[b, win_start[b*T+t] + r, :] for r < win_len[b*T+t]
+ * (keys: 576 channels, values: first d_v), then combines with the global
+ * branch as one softmax over the union of both key sets:
+ *   LSE = logaddexp(LSE_g, LSE_s),  O = e^(LSE_g-LSE) O_g + e^(LSE_s-LSE) O_s.
+ * swa_kv: bf16 [B][s_stride][576]; win_start, win_len: int32 [B*T] with
+ * 0 <= win_len <= n_win <= 256; o_g, lse_g: the global branch (may be the
+ * outputs of csa2_sparse_decode); o_out: fp32 [B][T][H][d_v] (may alias
+ * o_g); lse_out: fp32 [B][T][H] (nullable, may alias lse_g).
+ * A window outside [0, s_stride) is clipped and sets CSA2_DEV_BAD_WINDOW.
+ */
+CSA2_API int csa2_swa_merge(int B, int T, int H, const void* q,
+                   const void* swa_kv, int64_t s_stride,
+                   const int32_t* win_start, const int32_t* win_len, int n_win,
+                   int d_v, float softmax_scale, const float* o_g, const float* lse_g,
+                   float* o_out, float* lse_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes that cover every call above with these or smaller sizes. */
+CSA2_API size_t csa2_workspace_bytes(int B, int T, int H, int64_t n_max, int K);
+
+/* Zero the workspace's status word and counters (once after allocation). */
+CSA2_API int csa2_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, copy the device status word to *flags (host pointer,
+ * nullable) and clear it. Returns CSA2_OK when no bit was set,
+ * CSA2_ERR_TIMEOUT when only CSA2_DEV_TOPK_LEVELS is set, and
+ * CSA2_ERR_DEVICE_CHECK otherwise.
+ */
+CSA2_API int csa2_read_device_status(void* ws, void* stream, uint32_t* flags);
+
+/* Static text for a csa2_status value. */
+CSA2_API const char* csa2_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+CSA2_API int csa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H_ */

@@ -1,0 +1,221 @@
+// C ABI of libcsa2: host-side validation, workspace checks and dispatch.
+// Every entry point validates on the host and launches nothing on a failed
+// check; kernels are enqueued on the caller's stream and nothing is allocated.
+#include <mutex>
+
+#include "csa2_internal.cuh"
+
+namespace csa2 {
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+cudaError_t set_attr_once(int slot, const void* fn, cudaFuncAttribute attr, int value) {
+  static std::mutex mu;
+  static bool done[64][16] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || slot < 0 || slot >= 16) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev][slot]) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, attr, value);
+  if (e == cudaSuccess) done[dev][slot] = true;
+  return e;
+}
+
+int attn_splits(int64_t Q, int K, int n_sm) {
+  if (Q <= 0) return 1;
+  int64_t s = (n_sm + Q - 1) / Q;        // about one wave of CTAs
+  int64_t max_by_k = (K + 127) / 128;    // at least two 64-key tiles per split
+  if (s > max_by_k) s = max_by_k;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s < 1) s = 1;
+  return (int)s;
+}
+
+}  // namespace csa2
+
+using namespace csa2;
+
+static inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+#define CHECK_ARG(cond)                       \
+  do {                                        \
+    if (!(cond)) return CSA2_ERR_INVALID_ARG; \
+  } while (0)
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+extern "C" {
+
+int csa2_version(void) { return 100; }
+
+const char* csa2_status_string(int s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_INVALID_ARG: return "invalid argument";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CSA2_ERR_WORKSPACE: return "workspace missing or too small";
+    case CSA2_ERR_CUDA: return "CUDA error";
+    case CSA2_ERR_TIMEOUT: return "device-side wait or refinement limit reached";
+    case CSA2_ERR_DEVICE_CHECK: return "device-side bounds check fired";
+    default: return "unknown status";
+  }
+}
+
+size_t csa2_workspace_bytes(int B, int T, int H, int64_t n_max, int K) {
+  if (B < 0 || T < 0 || H < 0 || n_max < 0 || K < 0) return 0;
+  const int64_t Q = (int64_t)B * T;
+  int ns = attn_splits(Q, K, device_sm_count());
+  if (ns < swa_splits(kMaxWin)) ns = swa_splits(kMaxWin);
+  size_t a = scores_bytes(Q, n_max), b = partials_bytes(Q, ns, H);
+  return kWsHeader + (a > b ? a : b);
+}
+
+int csa2_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  CHECK_ARG(ws != nullptr && ws_bytes >= kWsHeader && aligned(ws, 256));
+  return cuda_status(cudaMemsetAsync(ws, 0, kWsHeader, (cudaStream_t)stream));
+}
+
+int csa2_read_device_status(void* ws, void* stream, uint32_t* flags) {
+  CHECK_ARG(ws != nullptr);
+  uint32_t v = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, 4, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  if (flags) *flags = v;
+  if (v == 0) return CSA2_OK;
+  if (v == CSA2_DEV_TOPK_LEVELS) return CSA2_ERR_TIMEOUT;
+  return CSA2_ERR_DEVICE_CHECK;
+}
+
+int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_model, const void* w_kv,
+                   const void* w_z, int n_layers, uint8_t* kv_codes, uint8_t* kv_scales,
+                   void* z_out, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  CHECK_ARG(rows >= 0 && n_layers >= 1);
+  CHECK_ARG(h_dtype == CSA2_F32 || h_dtype == CSA2_BF16);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (w_kv == nullptr && w_z == nullptr) {
+    CHECK_ARG(d_model == CSA2_D_KV && n_layers == 1 && z_out == nullptr);
+    if (rows == 0) return CSA2_OK;
+    CHECK_ARG(h && kv_codes && kv_scales);
+    CHECK_ARG(aligned(h, 16) && aligned(kv_codes, 8));
+    return cuda_status(launch_encode_quant(h, h_dtype, rows, kv_codes, kv_scales, st));
+  }
+  CHECK_ARG(w_kv && w_z && z_out);
+  CHECK_ARG(h_dtype == CSA2_BF16);
+  CHECK_ARG(d_model >= 64 && d_model % 64 == 0);
+  if (rows == 0) return CSA2_OK;
+  CHECK_ARG(h && kv_codes && kv_scales);
+  CHECK_ARG(aligned(h, 16) && aligned(w_kv, 16) && aligned(w_z, 16) && aligned(kv_codes, 16) &&
+            aligned(z_out, 16));
+  return cuda_status(
+      launch_ced_project(h, rows, d_model, w_kv, w_z, n_layers, kv_codes, kv_scales, z_out, st));
+}
+
+int csa2_index_topk(int mode, int B, int T, int H_I, const void* q_idx, const float* w_idx,
+                    const void* z, int64_t n_stride, const int32_t* n_visible, int K,
+                    const int32_t* prev_idx, int32_t* out_idx, float* out_scores, void* ws,
+                    size_t ws_bytes, void* stream) {
+  CHECK_ARG(mode == CSA2_MODE_FULL || mode == CSA2_MODE_REINDEX || mode == CSA2_MODE_REUSE);
+  CHECK_ARG(B >= 0 && T >= 0 && K >= 1);
+  if (K > kMaxK) return CSA2_ERR_UNSUPPORTED;
+  const int64_t Q = (int64_t)B * T;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (mode == CSA2_MODE_REUSE) {
+    CHECK_ARG(prev_idx != nullptr);
+    if (Q == 0) return CSA2_OK;
+    CHECK_ARG(out_idx != nullptr);
+    return cuda_status(launch_copy_idx(prev_idx, out_idx, Q * K, st));
+  }
+  CHECK_ARG(H_I >= 1 && n_stride >= 0);
+  if (H_I > 16 || n_stride > kMaxNStride) return CSA2_ERR_UNSUPPORTED;
+  if (Q == 0) return CSA2_OK;
+  CHECK_ARG(q_idx && w_idx && n_visible && out_idx);
+  CHECK_ARG(n_stride == 0 || z != nullptr);
+  CHECK_ARG(aligned(q_idx, 16) && aligned(z, 16) && aligned(w_idx, 4) && aligned(out_idx, 4) &&
+            aligned(n_visible, 4) && aligned(out_scores, 4));
+  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
+  CHECK_ARG(aligned(ws, 256));
+  if (ws_bytes < kWsHeader + scores_bytes(Q, n_stride)) return CSA2_ERR_WORKSPACE;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* scores = reinterpret_cast<float*>(wsb + kWsHeader);
+  uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
+  const int64_t stride = score_pad(n_stride);
+  cudaError_t e = launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores,
+                                     stride, st);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  return cuda_status(launch_topk_select(scores, stride, n_visible, (int)Q, n_stride, K, out_idx,
+                                        out_scores, status, st));
+}
+
+int csa2_sparse_decode(int B, int T, int H, const void* q, const uint8_t* kv_codes,
+                       const uint8_t* kv_scales, int64_t n_stride, const int32_t* idx, int K,
+                       int d_v, float softmax_scale, float* o_g, float* lse_g, void* ws,
+                       size_t ws_bytes, void* stream) {
+  CHECK_ARG(B >= 0 && T >= 0 && H >= 1 && K >= 1 && n_stride >= 0);
+  CHECK_ARG(softmax_scale == softmax_scale);  // not NaN
+  if (H % 16 != 0 || H > 64 || d_v != CSA2_D_LATENT || K > kMaxK) return CSA2_ERR_UNSUPPORTED;
+  const int64_t Q = (int64_t)B * T;
+  if (Q == 0) return CSA2_OK;
+  CHECK_ARG(q && idx && o_g && lse_g);
+  CHECK_ARG(n_stride == 0 || (kv_codes && kv_scales));
+  CHECK_ARG(aligned(q, 16) && aligned(kv_codes, 16) && aligned(kv_scales, 4) &&
+            aligned(o_g, 16) && aligned(lse_g, 4) && aligned(idx, 4));
+  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
+  CHECK_ARG(aligned(ws, 256));
+  const int nsplit = attn_splits(Q, K, device_sm_count());
+  if (ws_bytes < kWsHeader + partials_bytes(Q, nsplit, H)) return CSA2_ERR_WORKSPACE;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* partials = reinterpret_cast<float*>(wsb + kWsHeader);
+  uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
+  const float scale_log2 = softmax_scale * 1.4426950408889634074f;
+  return cuda_status(launch_sparse_attn(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K,
+                                        scale_log2, o_g, lse_g, partials, nsplit, status,
+                                        (cudaStream_t)stream));
+}
+
+int csa2_swa_merge(int B, int T, int H, const void* q, const void* swa_kv, int64_t s_stride,
+                   const int32_t* win_start, const int32_t* win_len, int n_win, int d_v,
+                   float softmax_scale, const float* o_g, const float* lse_g, float* o_out,
+                   float* lse_out, void* ws, size_t ws_bytes, void* stream) {
+  CHECK_ARG(B >= 0 && T >= 0 && H >= 1 && s_stride >= 0 && n_win >= 0);
+  CHECK_ARG(softmax_scale == softmax_scale);
+  if (H % 16 != 0 || H > 64 || d_v != CSA2_D_LATENT || n_win > kMaxWin) return CSA2_ERR_UNSUPPORTED;
+  const int64_t Q = (int64_t)B * T;
+  if (Q == 0) return CSA2_OK;
+  CHECK_ARG(q && win_start && win_len && o_g && lse_g && o_out);
+  CHECK_ARG(s_stride == 0 || swa_kv != nullptr);
+  CHECK_ARG(aligned(q, 16) && aligned(swa_kv, 16) && aligned(o_g, 16) && aligned(lse_g, 4) &&
+            aligned(o_out, 16) && aligned(lse_out, 4) && aligned(win_start, 4) &&
+            aligned(win_len, 4));
+  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
+  CHECK_ARG(aligned(ws, 256));
+  if (ws_bytes < kWsHeader + partials_bytes(Q, swa_splits(n_win), H)) return CSA2_ERR_WORKSPACE;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* partials = reinterpret_cast<float*>(wsb + kWsHeader);
+  uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
+  const float scale_log2 = softmax_scale * 1.4426950408889634074f;
+  return cuda_status(launch_swa_merge(B, T, H, q, swa_kv, s_stride, win_start, win_len, n_win,
+                                      scale_log2, o_g, lse_g, o_out, lse_out, partials, status,
+                                      (cudaStream_t)stream));
+}
+
+}  // extern "C"

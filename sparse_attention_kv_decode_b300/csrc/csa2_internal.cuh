@@ -1,0 +1,205 @@
+// Internal declarations and device helpers of libcsa2 (sm_103a only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+
+namespace csa2 {
+
+// ---------------------------------------------------------------------------
+// Workspace layout (byte offsets from the caller's workspace pointer)
+//   [0, 256)   header: device status word (u32) at offset 0
+//   [256, ..)  scratch, used by one call at a time (calls on one workspace are
+//              stream-ordered): fp32 indexer scores [Q][n_pad] for
+//              csa2_index_topk, or fp32 attention partials [Q][nsplit][H][514]
+//              for csa2_sparse_decode / csa2_swa_merge.
+// ---------------------------------------------------------------------------
+constexpr size_t kWsHeader = 256;
+constexpr int kMaxSplits = 16;
+constexpr int kScoreTile = 1024;  // keys per indexer CTA
+constexpr int kMaxK = 4096;
+constexpr int64_t kMaxNStride = 524288;
+constexpr int kMaxWin = 256;
+constexpr int kPartStride = 514;  // floats per (query, split, head) partial: O[512], m, l
+
+inline int64_t score_pad(int64_t n) { return (n + kScoreTile - 1) / kScoreTile * kScoreTile; }
+
+// Number of key splits per query for the sparse attention (about one wave of
+// CTAs when the batch is small; one split per query when there are many).
+int attn_splits(int64_t Q, int K, int n_sm);
+inline int swa_splits(int n_win) { return n_win > 0 ? (n_win + 63) / 64 : 1; }
+
+inline size_t scores_bytes(int64_t Q, int64_t n_stride) {
+  return (size_t)Q * (size_t)score_pad(n_stride) * 4;
+}
+inline size_t partials_bytes(int64_t Q, int nsplit, int H) {
+  return (size_t)Q * (size_t)nsplit * (size_t)H * kPartStride * 4;
+}
+
+int device_sm_count();
+
+// Sets a kernel attribute once per (device, slot): launchers call this instead of
+// cudaFuncSetAttribute so that no attribute call happens while a stream is
+// being captured into a CUDA graph (after the first, eager, call on a device).
+cudaError_t set_attr_once(int slot, const void* fn, cudaFuncAttribute attr, int value);
+
+// Kernel launchers (return cudaError_t of the launch).
+cudaError_t launch_encode_quant(const void* h, int h_dtype, int64_t rows, uint8_t* codes,
+                                uint8_t* scales, cudaStream_t st);
+cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void* z,
+                               int64_t n_stride, const int32_t* n_visible, int B, int T,
+                               int H_I, float* scores, int64_t score_stride, cudaStream_t st);
+cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
+                               int Q, int64_t n_stride, int K, int32_t* out_idx, float* out_scores,
+                               uint32_t* status, cudaStream_t st);
+cudaError_t launch_copy_idx(const int32_t* src, int32_t* dst, int64_t n, cudaStream_t st);
+cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t* codes,
+                               const uint8_t* scales, int64_t n_stride, const int32_t* idx,
+                               int K, float scale_log2, float* o_g, float* lse_g,
+                               float* partials, int nsplit, uint32_t* status, cudaStream_t st);
+cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa,
+                             int64_t s_stride, const int32_t* win_start, const int32_t* win_len,
+                             int n_win, float scale_log2, const float* o_g, const float* lse_g,
+                             float* o_out, float* lse_out, float* partials, uint32_t* status,
+                             cudaStream_t st);
+cudaError_t launch_ced_project(const void* h, int64_t rows, int d_model, const void* w_kv,
+                               const void* w_z, int n_layers, uint8_t* codes, uint8_t* scales,
+                               void* z_out, cudaStream_t st);
+cudaError_t launch_memset_u32(uint32_t* p, size_t n, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// E4M3 code of a non-negative fp32 value, round to nearest even, saturating.
+__device__ __forceinline__ uint32_t e4m3_rn_sat(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return r & 0xFFu;
+}
+
+// fp32 value of an E4M3 code (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  uint32_t h2;
+  uint16_t c = (uint16_t)(code & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+// fp16x2 pair of an E4M3 code placed in both halves (exact).
+__device__ __forceinline__ uint32_t e4m3_to_h2(uint32_t code) {
+  uint32_t h2;
+  uint16_t c = (uint16_t)((code & 0xFFu) * 0x0101u);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+  return h2;
+}
+
+// Eight E2M1 codes (one per nibble, element 0 in the low nibble) from 8 fp32
+// values, round to nearest even, saturating at +-6, with -0 stored as +0.
+__device__ __forceinline__ uint32_t e2m1x8(const float* v) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  uint32_t mag = out & 0x77777777u;
+  uint32_t nz = (mag + 0x77777777u) & 0x88888888u;  // bit 3 set where magnitude != 0
+  return mag | (out & nz);
+}
+
+// Four E2M1 codes (low 16 bits, element 0 lowest nibble) -> four fp16 values (2 regs).
+__device__ __forceinline__ void e2m1x4_to_h2x2(uint32_t codes16, uint32_t& lo, uint32_t& hi) {
+  uint16_t c = (uint16_t)codes16;
+  asm("{\n\t.reg .b8 t0, t1;\n\tmov.b16 {t0, t1}, %2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, t1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "h"(c));
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n));
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  int n = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N)); }
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D += A * B, m16n8k16, fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Convert two bf16 (packed) to fp16x2 (exact for |x| in fp16 normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t v) {
+  return pack_h2(bf16_lo(v), bf16_hi(v));
+}
+
+#endif  // __CUDACC__
+
+}  // namespace csa2

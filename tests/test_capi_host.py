@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "csa2.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from sparse_attention_kv_decode_b300 import _build
+    _build.build()
+    import sparse_attention_kv_decode_b300 as csa2
+    return csa2.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CSA2_API\s+[\w\s\*]*?\b(csa2_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_four_path_calls():
+    names = declared_symbols()
+    for n in ("csa2_encode_kv", "csa2_index_topk", "csa2_sparse_decode", "csa2_swa_merge"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    assert L.csa2_version() == 100
+    for s in range(7):
+        assert L.csa2_status_string(s)
+    assert L.csa2_status_string(99) == b"unknown status"
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
+
+
+def test_index_topk_validation(L):
+    r = L.csa2_index_topk
+    assert r(7, 1, 1, 4, FAKE, FAKE, FAKE, 1024, FAKE, 128, None, FAKE, None, FAKE, 1 << 30, None) == 1
+    assert r(0, 1, 1, 4, FAKE, FAKE, FAKE, 1024, FAKE, 5000, None, FAKE, None, FAKE, 1 << 30, None) == 2
+    assert r(0, 1, 1, 17, FAKE, FAKE, FAKE, 1024, FAKE, 128, None, FAKE, None, FAKE, 1 << 30, None) == 2
+    assert r(0, 1, 1, 4, FAKE, FAKE, FAKE, 1 << 21, FAKE, 128, None, FAKE, None, FAKE, 1 << 30, None) == 2
+    assert r(0, 1, 1, 4, None, FAKE, FAKE, 1024, FAKE, 128, None, FAKE, None, FAKE, 1 << 30, None) == 1
+    assert r(0, 1, 1, 4, FAKE + 2, FAKE, FAKE, 1024, FAKE, 128, None, FAKE, None, FAKE, 1 << 30, None) == 1
+    assert r(0, 1, 1, 4, FAKE, FAKE, FAKE, 1024, FAKE, 128, None, FAKE, None, None, 0, None) == 3
+    assert r(0, 1, 1, 4, FAKE, FAKE, FAKE, 1024, FAKE, 128, None, FAKE, None, FAKE, 1024, None) == 3
+    assert r(0, 1, 1, 4, FAKE, FAKE, FAKE, 1024, FAKE, 128, None, FAKE, None, FAKE + 16, 1 << 30, None) == 1
+    # REUSE needs the preceding layer's indices
+    assert r(2, 1, 1, 0, None, None, None, 0, None, 128, None, FAKE, None, None, 0, None) == 1
+    # REUSE with out == prev is a no-op that launches nothing
+    assert r(2, 1, 1, 0, None, None, None, 0, None, 128, FAKE, FAKE, None, None, 0, None) == 0
+
+
+def test_sparse_decode_validation(L):
+    r = L.csa2_sparse_decode
+    ok = dict()
+    assert r(1, 1, 20, FAKE, FAKE, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(0.04), FAKE, FAKE, FAKE, 1 << 30, None) == 2
+    assert r(1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 128, 576, ctypes.c_float(0.04), FAKE, FAKE, FAKE, 1 << 30, None) == 2
+    assert r(1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 8192, 512, ctypes.c_float(0.04), FAKE, FAKE, FAKE, 1 << 30, None) == 2
+    assert r(1, 1, 64, None, FAKE, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(0.04), FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert r(1, 1, 64, FAKE, FAKE + 8, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(0.04), FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert r(1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(float("nan")), FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert r(1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(0.04), FAKE, FAKE, None, 0, None) == 3
+    assert r(1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(0.04), FAKE, FAKE, FAKE, 4096, None) == 3
+    # empty batch: nothing to do
+    assert r(0, 1, 64, None, None, None, 0, None, 128, 512, ctypes.c_float(0.04), None, None, None, 0, None) == 0
+
+
+def test_swa_merge_validation(L):
+    r = L.csa2_swa_merge
+    f = ctypes.c_float(0.04)
+    assert r(1, 1, 64, FAKE, FAKE, 128, FAKE, FAKE, 300, 512, f, FAKE, FAKE, FAKE, None, FAKE, 1 << 30, None) == 2
+    assert r(1, 1, 64, FAKE, FAKE, 128, FAKE, FAKE, 128, 512, f, None, FAKE, FAKE, None, FAKE, 1 << 30, None) == 1
+    assert r(1, 1, 64, FAKE, FAKE, 128, FAKE, FAKE, 128, 512, f, FAKE, FAKE, FAKE, None, None, 0, None) == 3
+    assert r(1, 1, 64, FAKE, FAKE, -1, FAKE, FAKE, 128, 512, f, FAKE, FAKE, FAKE, None, FAKE, 1 << 30, None) == 1
+
+
+def test_encode_validation(L):
+    r = L.csa2_encode_kv
+    # quantise-only needs d_model == 576 and n_layers == 1
+    assert r(FAKE, 0, 16, 512, None, None, 1, FAKE, FAKE, None, None, 0, None) == 1
+    assert r(FAKE, 0, 16, 576, None, None, 2, FAKE, FAKE, None, None, 0, None) == 1
+    assert r(FAKE, 5, 16, 576, None, None, 1, FAKE, FAKE, None, None, 0, None) == 1
+    assert r(FAKE + 4, 0, 16, 576, None, None, 1, FAKE, FAKE, None, None, 0, None) == 1
+    # projection: bf16 only, d_model multiple of 64, all outputs present
+    assert r(FAKE, 0, 16, 4096, FAKE, FAKE, 20, FAKE, FAKE, FAKE, None, 0, None) == 1
+    assert r(FAKE, 1, 16, 4000, FAKE, FAKE, 20, FAKE, FAKE, FAKE, None, 0, None) == 1
+    assert r(FAKE, 1, 16, 4096, FAKE, FAKE, 20, FAKE, FAKE, None, None, 0, None) == 1
+    assert r(FAKE, 1, 0, 4096, FAKE, FAKE, 20, FAKE, FAKE, FAKE, None, 0, None) == 0
+
+
+def test_workspace_size_monotone(L):
+    a = L.csa2_workspace_bytes(32, 1, 64, 32768, 2048)
+    b = L.csa2_workspace_bytes(32, 1, 64, 65536, 2048)
+    c = L.csa2_workspace_bytes(64, 1, 64, 65536, 2048)
+    assert 256 < a <= b <= c
+    assert L.csa2_workspace_bytes(-1, 1, 64, 10, 10) == 0

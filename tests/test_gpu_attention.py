@@ -1,0 +1,199 @@
+"""Sparse decode + SWA merge parity against the FP64 oracle (max-abs 2e-3, rel-L2 1e-3).
+
+Ref: "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression": sparse attention
+over the whole context combined with a sliding-window branch (blog repost), the CSA2
+layer modes and the FP4 main KV (picx.dev summary, Methodology / 2 and / 5).
+The oracle attends over the GPU's own index set (which may differ from the oracle's only
+inside the top-K tie band, checked separately).
+"""
+import numpy as np
+import pytest
+import torch
+
+import csa2_inputs as ci
+import sparse_attention_kv_decode_b300 as csa2
+from oracle import attention, fp4, indexer
+from tests._util import check_attention, check_index_set, check_lse, f64, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _cache(X):
+    codes, scales = csa2.csa2_encode_kv(to_dev(X, DEV))
+    return codes, scales
+
+
+def _oracle_query(q_bits_bt, rows_of, idx, swa_bits_b, ws, wl, cfg):
+    """Oracle global branch over idx, SWA branch, merge. rows_of(idx array) -> dequantised rows."""
+    q = f64(q_bits_bt)
+    sel = idx[idx >= 0]
+    og, lg = attention.attend(q, rows_of(sel), cfg.d_v, cfg.softmax_scale)
+    os_, ls = attention.swa_branch(q, f64(swa_bits_b), int(ws), int(wl), cfg.d_v, cfg.softmax_scale)
+    O, L = attention.merge(og, lg, os_, ls)
+    return og, lg, O, L
+
+
+def _run_group(cfg, inp, sample=None):
+    """Run every layer of the group on the GPU; compare (sampled) queries with the oracle."""
+    B, T = cfg.B, cfg.T
+    ws = csa2.csa2_workspace(B, T, cfg.H, cfg.N, cfg.K, device=DEV)
+    nvis = to_dev(inp.n_visible, DEV)
+    wst, wln = to_dev(inp.win_start, DEV), to_dev(inp.win_len, DEV)
+    codes = scales = None
+    prev = None
+    kv_host = {}
+    results = []
+    for li, L in enumerate(inp.layers):
+        if L.mode == ci.FULL:
+            codes, scales = _cache(L.X)
+            kv_host = dict(X=L.X)
+        before = (codes.clone(), scales.clone()) if L.mode != ci.FULL else None
+        qd = to_dev_bf16(L.q, DEV)
+        kw = {}
+        if L.mode != ci.REUSE:
+            kw = dict(q_idx=to_dev_bf16(L.q_idx, DEV), w_idx=to_dev(L.w_idx, DEV), z=to_dev_bf16(L.z, DEV),
+                      n_visible=nvis)
+        o, lse, idx = csa2.decode_layer(L.mode, qd, codes, scales, to_dev_bf16(L.swa, DEV), wst, wln, cfg.W,
+                                        cfg.K, prev_idx=prev, ws=ws, **kw)
+        torch.cuda.synchronize()
+        st, flags = csa2.csa2_read_device_status(ws)
+        assert st == 0, (st, flags)
+        if before is not None:   # REINDEX / REUSE leave the main KV untouched
+            assert torch.equal(before[0], codes) and torch.equal(before[1], scales)
+        idx_h = idx.cpu().numpy()
+        if L.mode == ci.REUSE:
+            assert np.array_equal(idx_h, prev.cpu().numpy())
+        results.append((L, o.cpu().numpy(), lse.cpu().numpy(), idx_h))
+        prev = idx
+
+    bs = range(B) if sample is None else sample
+    X = kv_host["X"]
+    for b in bs:
+        cache_rows = {}
+
+        def rows_of(sel, b=b):
+            out = np.empty((sel.size, 576))
+            miss = [i for i in sel.tolist() if i not in cache_rows]
+            if miss:
+                miss = np.array(sorted(set(miss)))
+                dq = fp4.decode(*fp4.encode(X[b, miss]))
+                for i, r in zip(miss.tolist(), dq):
+                    cache_rows[i] = r
+            for k, i in enumerate(sel.tolist()):
+                out[k] = cache_rows[i]
+            return out
+
+        for (L, o, lse, idx_h) in results:
+            if L.mode != ci.REUSE:
+                I = indexer.scores(f64(L.q_idx[b]), L.w_idx[b], f64(L.z[b]))
+            for t in range(T):
+                qi = b * T + t
+                if L.mode != ci.REUSE:
+                    want = indexer.topk(I[t], inp.n_visible[qi], cfg.K)
+                    check_index_set(idx_h[b, t], want, I[t], inp.n_visible[qi], cfg.K)
+                _, _, O, LSE = _oracle_query(L.q[b, t], rows_of, idx_h[b, t], L.swa[b], inp.win_start[qi],
+                                             inp.win_len[qi], cfg)
+                check_attention(o[b, t], O, f"layer {ci.MODE_NAMES[L.mode]} b={b} t={t}")
+                check_lse(lse[b, t], LSE, f"layer {ci.MODE_NAMES[L.mode]} b={b} t={t}")
+    return results
+
+
+def test_tiny_config_layer():
+    _run_group(ci.TINY, ci.make_decode_inputs(ci.TINY))
+
+
+def test_scaled_group_full_reindex_reuse():
+    cfg = ci.scaled(ci.DECODE_128K, B=3, N=4096, K=512)
+    _run_group(cfg, ci.make_decode_inputs(cfg))
+
+
+@pytest.mark.parametrize("H,K,W", [(16, 200, 100), (32, 1000, 1), (48, 64, 256), (64, 130, 0)])
+def test_ragged_shapes(H, K, W):
+    cfg = ci.scaled(ci.DECODE_128K, B=2, N=1500, H=H, K=K, W=max(W, 1), modes=(ci.FULL, ci.REUSE))
+    inp = ci.make_decode_inputs(cfg)
+    if W == 0:
+        inp.win_len[:] = 0
+    _run_group(cfg, inp)
+
+
+def test_prefill_like_many_queries_causal():
+    cfg = ci.scaled(ci.PREFILL_CHUNK, T=37, N=1200, K=256, W=16)
+    _run_group(cfg, ci.make_decode_inputs(cfg))
+
+
+def test_global_equals_dense_when_k_covers_all():
+    cfg = ci.scaled(ci.TINY, N=300, K=512, H=32, W=8)
+    inp = ci.make_decode_inputs(cfg)
+    L = inp.layers[0]
+    codes, scales = _cache(L.X)
+    idx = torch.from_numpy(np.tile(np.concatenate([np.arange(300), -np.ones(212)]).astype(np.int32),
+                                   (1, 1, 1))).to(DEV)
+    o, lse = csa2.csa2_sparse_decode(to_dev_bf16(L.q, DEV), codes, scales, idx, cfg.softmax_scale)
+    torch.cuda.synchronize()
+    rows = fp4.decode(*fp4.encode(L.X[0]))
+    O, LSE = attention.attend(f64(L.q[0, 0]), rows, 512, cfg.softmax_scale)
+    check_attention(o[0, 0].cpu().numpy(), O, "dense")
+    check_lse(lse[0, 0].cpu().numpy(), LSE, "dense")
+
+
+def test_empty_selection_and_pure_swa():
+    cfg = ci.scaled(ci.TINY, N=64, K=64, H=16, W=32)
+    inp = ci.make_decode_inputs(cfg)
+    L = inp.layers[0]
+    codes, scales = _cache(L.X)
+    idx = torch.full((1, 1, 64), -1, dtype=torch.int32, device=DEV)
+    q = to_dev_bf16(L.q, DEV)
+    o_g, lse_g = csa2.csa2_sparse_decode(q, codes, scales, idx, cfg.softmax_scale)
+    o, lse = csa2.csa2_swa_merge(q, to_dev_bf16(L.swa, DEV), to_dev(inp.win_start, DEV), to_dev(inp.win_len, DEV),
+                                 cfg.W, o_g, lse_g, cfg.softmax_scale)
+    torch.cuda.synchronize()
+    assert torch.all(o_g == 0) and torch.all(torch.isneginf(lse_g))
+    O, LSE = attention.swa_branch(f64(L.q[0, 0]), f64(L.swa[0]), 0, cfg.W, 512, cfg.softmax_scale)
+    check_attention(o[0, 0].cpu().numpy(), O, "swa only")
+    # both branches empty
+    o2, lse2 = csa2.csa2_swa_merge(q, to_dev_bf16(L.swa, DEV), to_dev(inp.win_start, DEV),
+                                   torch.zeros(1, dtype=torch.int32, device=DEV), cfg.W, o_g, lse_g)
+    torch.cuda.synchronize()
+    assert torch.all(o2 == 0) and torch.all(torch.isneginf(lse2))
+
+
+def test_device_checks_flag_bad_index_and_window():
+    cfg = ci.scaled(ci.TINY, N=64, K=64, H=16, W=32)
+    inp = ci.make_decode_inputs(cfg)
+    L = inp.layers[0]
+    codes, scales = _cache(L.X)
+    ws = csa2.csa2_workspace(1, 1, 16, 64, 64, device=DEV)
+    idx = torch.arange(64, dtype=torch.int32, device=DEV).reshape(1, 1, 64).clone()
+    idx[0, 0, 5] = 64          # outside the cache: skipped and flagged
+    idx[0, 0, 6] = -9
+    q = to_dev_bf16(L.q, DEV)
+    o_g, lse_g = csa2.csa2_sparse_decode(q, codes, scales, idx, cfg.softmax_scale, ws=ws)
+    st, flags = csa2.csa2_read_device_status(ws)
+    assert st == 6 and flags & csa2.DEV_BAD_INDEX
+    keep = np.array([i for i in range(64) if i not in (5, 6)])
+    rows = fp4.decode(*fp4.encode(L.X[0]))
+    O, _ = attention.attend(f64(L.q[0, 0]), rows[keep], 512, cfg.softmax_scale)
+    check_attention(o_g[0, 0].cpu().numpy(), O, "bad index skipped")
+    st, flags = csa2.csa2_read_device_status(ws)
+    assert st == 0 and flags == 0
+    csa2.csa2_swa_merge(q, to_dev_bf16(L.swa, DEV), torch.tensor([20], dtype=torch.int32, device=DEV),
+                        torch.tensor([32], dtype=torch.int32, device=DEV), cfg.W, o_g, lse_g, ws=ws)
+    st, flags = csa2.csa2_read_device_status(ws)
+    assert st == 6 and flags & csa2.DEV_BAD_WINDOW
+
+
+def test_full_size_decode_128k_group_sampled():
+    """The bench workload: 32 x 32768 entries, 64 heads, K = 2048, FULL -> REINDEX -> REUSE,
+    in the bench's launch configuration; 3 sequences checked against the oracle."""
+    cfg = ci.DECODE_128K
+    _run_group(cfg, ci.make_decode_inputs(cfg), sample=[0, 17, 31])
+
+
+def test_deterministic_outputs():
+    cfg = ci.scaled(ci.DECODE_128K, B=2, N=2048, K=256, modes=(ci.FULL,))
+    inp = ci.make_decode_inputs(cfg)
+    a = _run_group(cfg, inp)
+    b = _run_group(cfg, inp)
+    for (_, oa, la, ia), (_, ob, lb, ib) in zip(a, b):
+        assert np.array_equal(oa, ob) and np.array_equal(la, lb) and np.array_equal(ia, ib)

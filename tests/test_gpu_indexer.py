@@ -1,0 +1,138 @@
+"""Indexer + top-K parity: CUDA index sets equal the oracle's up to ties within 1e-6
+relative of the K-th score; exact when the arithmetic is exact (integer data).
+
+Ref: "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression", picx.dev summary,
+Methodology / 2. CSA2 (FULL / REINDEX compute fresh top-K, REUSE repeats them).
+"""
+import numpy as np
+import pytest
+import torch
+
+import csa2_inputs as ci
+import sparse_attention_kv_decode_b300 as csa2
+from oracle import indexer
+from tests._util import check_index_set, f64, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q_bits, w, z_bits, nvis, K, mode=csa2.FULL, with_scores=True):
+    B, T, H_I, _ = q_bits.shape
+    dev = "cuda"
+    out_s = torch.empty((B, T, K), dtype=torch.float32, device=dev) if with_scores else None
+    idx = csa2.csa2_index_topk(mode, to_dev_bf16(q_bits, dev), to_dev(w, dev), to_dev_bf16(z_bits, dev),
+                               to_dev(nvis.astype(np.int32), dev), K, out_scores=out_s)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), (out_s.cpu().numpy() if with_scores else None)
+
+
+def _check_all(q_bits, w, z_bits, nvis, K):
+    B, T = q_bits.shape[:2]
+    got, gs = _run(q_bits, w, z_bits, nvis, K)
+    ndiff = 0
+    for b in range(B):
+        I = indexer.scores(f64(q_bits[b]), w[b], f64(z_bits[b]))
+        for t in range(T):
+            nv = int(nvis[b * T + t])
+            want = indexer.topk(I[t], nv, K)
+            ndiff += check_index_set(got[b, t], want, I[t], nv, K)
+            sel = got[b, t][got[b, t] >= 0]
+            # returned scores are the fp32 scores of the returned indices
+            np.testing.assert_allclose(gs[b, t, :sel.size], I[t][sel], rtol=2e-5, atol=2e-5)
+            assert np.all(np.isnan(gs[b, t, sel.size:]))
+    return got, ndiff
+
+
+def test_tiny_config():
+    cfg = ci.TINY
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    L = inp.layers[0]
+    _check_all(L.q_idx, L.w_idx, L.z, inp.n_visible, cfg.K)
+
+
+@pytest.mark.parametrize("N,K,H_I", [(4096, 512, 8), (3000, 256, 4), (5000, 2048, 16), (1, 4, 3), (700, 700, 8)])
+def test_scaled_decode_shapes(N, K, H_I):
+    cfg = ci.scaled(ci.DECODE_128K, B=3, N=N, H=16, H_I=H_I, K=K, W=8, modes=(ci.FULL,))
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    L = inp.layers[0]
+    _check_all(L.q_idx, L.w_idx, L.z, inp.n_visible, K)
+
+
+def test_causal_visibility_and_padding():
+    rng = np.random.default_rng(21)
+    B, T, N, H_I, K = 2, 5, 2000, 8, 300
+    q = ci.bf16_bits(rng.standard_normal((B, T, H_I, 64), dtype=np.float32))
+    w = np.abs(rng.standard_normal((B, T, H_I), dtype=np.float32))
+    z = ci.bf16_bits(rng.standard_normal((B, N, 64), dtype=np.float32))
+    nvis = np.array([0, 1, 299, 300, 301, 2000, 1999, 5, 1024, 1500], dtype=np.int32)
+    _check_all(q, w, z, nvis, K)
+
+
+def test_exact_ties_resolved_to_lower_index():
+    """Small integers make every dot product exact in fp32 and fp64, so scores tie
+    exactly and the selection must equal the oracle's with no tolerance."""
+    rng = np.random.default_rng(22)
+    B, T, N, H_I, K = 2, 2, 9000, 8, 1000
+    q = ci.bf16_bits(rng.integers(-2, 3, (B, T, H_I, 64)).astype(np.float32))
+    w = rng.integers(0, 3, (B, T, H_I)).astype(np.float32)
+    z = ci.bf16_bits(rng.integers(-1, 2, (B, N, 64)).astype(np.float32))
+    nvis = np.array([N, 7000, N, 4321], dtype=np.int32)
+    got, _ = _run(q, w, z, nvis, K)
+    for b in range(B):
+        I = indexer.scores(f64(q[b]), w[b], f64(z[b]))
+        for t in range(T):
+            assert np.array_equal(got[b, t], indexer.topk(I[t], nvis[b * T + t], K))
+
+
+def test_all_scores_equal():
+    B, T, N, H_I, K = 1, 1, 5000, 8, 777
+    q = np.zeros((B, T, H_I, 64), np.uint16)
+    w = np.ones((B, T, H_I), np.float32)
+    z = ci.bf16_bits(np.random.default_rng(23).standard_normal((B, N, 64), dtype=np.float32))
+    got, _ = _run(q, w, z, np.array([N], np.int32), K)
+    assert np.array_equal(got[0, 0], np.arange(K))
+
+
+def test_k_at_least_visible_selects_all():
+    rng = np.random.default_rng(24)
+    q = ci.bf16_bits(rng.standard_normal((1, 1, 8, 64), dtype=np.float32))
+    w = np.abs(rng.standard_normal((1, 1, 8), dtype=np.float32))
+    z = ci.bf16_bits(rng.standard_normal((1, 600, 64), dtype=np.float32))
+    got, _ = _run(q, w, z, np.array([600], np.int32), 1024)
+    assert np.array_equal(got[0, 0, :600], np.arange(600)) and np.all(got[0, 0, 600:] == -1)
+
+
+def test_full_size_decode_128k_layer():
+    """32 sequences x 32768 entries, K = 2048, the planted recency bias: all 32 queries."""
+    cfg = ci.scaled(ci.DECODE_128K, modes=(ci.FULL,))
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    L = inp.layers[0]
+    _, ndiff = _check_all(L.q_idx, L.w_idx, L.z, inp.n_visible, cfg.K)
+    print("tie-band differences:", ndiff)
+
+
+def test_full_size_decode_1m():
+    """4 sequences x 262144 entries (16-CTA clusters), K = 2048."""
+    cfg = ci.DECODE_1M
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    L = inp.layers[0]
+    _check_all(L.q_idx, L.w_idx, L.z, inp.n_visible, cfg.K)
+
+
+def test_reuse_copies_and_aliases():
+    prev = torch.arange(3 * 2 * 16, dtype=torch.int32, device="cuda").reshape(3, 2, 16)
+    out = torch.full_like(prev, -7)
+    r = csa2.csa2_index_topk(csa2.REUSE, None, None, None, None, 16, prev_idx=prev, out_idx=out)
+    torch.cuda.synchronize()
+    assert torch.equal(r, prev) and torch.equal(out, prev)
+    same = csa2.csa2_index_topk(csa2.REUSE, None, None, None, None, 16, prev_idx=prev, out_idx=prev)
+    assert torch.equal(same, prev)
+
+
+def test_deterministic_repeat():
+    cfg = ci.scaled(ci.DECODE_128K, B=4, N=8192, K=1024, modes=(ci.FULL,))
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    L = inp.layers[0]
+    a, _ = _run(L.q_idx, L.w_idx, L.z, inp.n_visible, cfg.K)
+    b, _ = _run(L.q_idx, L.w_idx, L.z, inp.n_visible, cfg.K)
+    assert np.array_equal(a, b)
