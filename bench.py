@@ -306,8 +306,9 @@ def run_ours(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
-        graph.replay()
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            graph.replay()
     torch.cuda.synchronize()
 
     gpu_uuid = None
@@ -329,7 +330,7 @@ def run_ours(args):
     for _ in range(args.steps):
         with torch.cuda.stream(stream):
             flush.fill_(1)
-        graph.replay()
+            graph.replay()
         stream.synchronize()
         for i in range(len(calls)):
             per_call[i].append(cuchk(cu.cuEventElapsedTime(events[i], events[i + 1])))

@@ -69,6 +69,7 @@ typedef enum { CSA2_F32 = 0, CSA2_BF16 = 1 } csa2_dtype;
 #define CSA2_DEV_BAD_INDEX 0x1u   /* sparse_decode saw idx >= n_stride or < -1 */
 #define CSA2_DEV_BAD_WINDOW 0x2u  /* swa_merge window outside [0, s_stride)    */
 #define CSA2_DEV_TOPK_LEVELS 0x4u /* top-K refinement did not settle           */
+#define CSA2_DEV_PIPELINE_TIMEOUT 0x8u /* a bounded mbarrier wait gave up       */
 
 /*
  * csa2_encode_kv - write the FP4 main KV cache.
@@ -86,8 +87,13 @@ typedef enum { CSA2_F32 = 0, CSA2_BF16 = 1 } csa2_dtype;
  *     [n_layers][rows][288] and kv_scales [n_layers][rows][36] (C_l quantised
  *     as in (a) from its fp32 value) and z_out bf16 [n_layers][rows][64]
  *     (round to nearest even). Requires h_dtype == CSA2_BF16,
- *     d_model % 64 == 0, 16-byte aligned h/w_kv/w_z/kv_codes/z_out.
- * ws/ws_bytes are unused (pass NULL, 0).
+ *     d_model % 64 == 0, rows <= 2^30, 16-byte aligned h/w_kv/w_z/kv_codes/
+ *     z_out. The fp32 product is accumulated by the tensor cores, so a block
+ *     whose exact product sits within the accumulation error of a rounding
+ *     boundary may round either way. ws must hold at least 256 bytes (the
+ *     status word); a bounded device wait that gives up sets
+ *     CSA2_DEV_PIPELINE_TIMEOUT there.
+ * (a) ignores ws (pass NULL, 0).
  */
 CSA2_API int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_model,
                    const void* w_kv, const void* w_z, int n_layers,
@@ -168,8 +174,8 @@ CSA2_API int csa2_workspace_init(void* ws, size_t ws_bytes, void* stream);
 /*
  * Synchronise `stream`, copy the device status word to *flags (host pointer,
  * nullable) and clear it. Returns CSA2_OK when no bit was set,
- * CSA2_ERR_TIMEOUT when only CSA2_DEV_TOPK_LEVELS is set, and
- * CSA2_ERR_DEVICE_CHECK otherwise.
+ * CSA2_ERR_TIMEOUT when only CSA2_DEV_TOPK_LEVELS and/or
+ * CSA2_DEV_PIPELINE_TIMEOUT are set, and CSA2_ERR_DEVICE_CHECK otherwise.
  */
 CSA2_API int csa2_read_device_status(void* ws, void* stream, uint32_t* flags);
 

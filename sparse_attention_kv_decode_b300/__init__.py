@@ -34,7 +34,7 @@ CODE_BYTES, SCALE_BYTES = 288, 36
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3: "CSA2_ERR_WORKSPACE",
           4: "CSA2_ERR_CUDA", 5: "CSA2_ERR_TIMEOUT", 6: "CSA2_ERR_DEVICE_CHECK"}
-DEV_BAD_INDEX, DEV_BAD_WINDOW, DEV_TOPK_LEVELS = 0x1, 0x2, 0x4
+DEV_BAD_INDEX, DEV_BAD_WINDOW, DEV_TOPK_LEVELS, DEV_PIPELINE_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 _LIB = None
 
@@ -135,7 +135,7 @@ def csa2_read_device_status(ws: torch.Tensor, stream=None) -> Tuple[int, int]:
 # ---------------------------------------------------------------------------
 def csa2_encode_kv(h: torch.Tensor, w_kv: Optional[torch.Tensor] = None, w_z: Optional[torch.Tensor] = None,
                    kv_codes: Optional[torch.Tensor] = None, kv_scales: Optional[torch.Tensor] = None,
-                   z_out: Optional[torch.Tensor] = None, stream=None):
+                   z_out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None):
     """Quantise rows h [..., 576] (fp32/bf16) to FP4, or run the CED projection.
 
     Quantise-only returns (codes [..., 288] u8, scales [..., 36] u8).
@@ -173,8 +173,10 @@ def csa2_encode_kv(h: torch.Tensor, w_kv: Optional[torch.Tensor] = None, w_z: Op
     _dev(kv_codes, "kv_codes", (torch.uint8,), (n_layers, rows, CODE_BYTES))
     _dev(kv_scales, "kv_scales", (torch.uint8,), (n_layers, rows, SCALE_BYTES))
     _dev(z_out, "z_out", _B16, (n_layers, rows, D_IDX))
+    if ws is None:
+        ws = csa2_workspace(0, 0, 0, 0, 0, device=h.device, stream=stream)
     _check(L.csa2_encode_kv(_ptr(h), BF16, rows, d_model, _ptr(w_kv), _ptr(w_z), n_layers, _ptr(kv_codes),
-                            _ptr(kv_scales), _ptr(z_out), None, 0, _stream(stream)), "csa2_encode_kv")
+                            _ptr(kv_scales), _ptr(z_out), _ptr(ws), ws.numel(), _stream(stream)), "csa2_encode_kv")
     return kv_codes, kv_scales, z_out
 
 

@@ -101,14 +101,13 @@ int csa2_read_device_status(void* ws, void* stream, uint32_t* flags) {
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
   if (flags) *flags = v;
   if (v == 0) return CSA2_OK;
-  if (v == CSA2_DEV_TOPK_LEVELS) return CSA2_ERR_TIMEOUT;
+  if ((v & ~(CSA2_DEV_TOPK_LEVELS | CSA2_DEV_PIPELINE_TIMEOUT)) == 0) return CSA2_ERR_TIMEOUT;
   return CSA2_ERR_DEVICE_CHECK;
 }
 
 int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_model, const void* w_kv,
                    const void* w_z, int n_layers, uint8_t* kv_codes, uint8_t* kv_scales,
                    void* z_out, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
   CHECK_ARG(rows >= 0 && n_layers >= 1);
   CHECK_ARG(h_dtype == CSA2_F32 || h_dtype == CSA2_BF16);
   cudaStream_t st = (cudaStream_t)stream;
@@ -125,9 +124,13 @@ int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_model, const 
   if (rows == 0) return CSA2_OK;
   CHECK_ARG(h && kv_codes && kv_scales);
   CHECK_ARG(aligned(h, 16) && aligned(w_kv, 16) && aligned(w_z, 16) && aligned(kv_codes, 16) &&
-            aligned(z_out, 16));
-  return cuda_status(
-      launch_ced_project(h, rows, d_model, w_kv, w_z, n_layers, kv_codes, kv_scales, z_out, st));
+            aligned(kv_scales, 4) && aligned(z_out, 16));
+  if (rows > ((int64_t)1 << 30)) return CSA2_ERR_UNSUPPORTED;
+  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
+  CHECK_ARG(aligned(ws, 256));
+  if (ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
+  return cuda_status(launch_ced_project(h, rows, d_model, w_kv, w_z, n_layers, kv_codes, kv_scales,
+                                        z_out, static_cast<uint32_t*>(ws), st));
 }
 
 int csa2_index_topk(int mode, int B, int T, int H_I, const void* q_idx, const float* w_idx,

@@ -68,7 +68,7 @@ cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa
                              cudaStream_t st);
 cudaError_t launch_ced_project(const void* h, int64_t rows, int d_model, const void* w_kv,
                                const void* w_z, int n_layers, uint8_t* codes, uint8_t* scales,
-                               void* z_out, cudaStream_t st);
+                               void* z_out, uint32_t* status, cudaStream_t st);
 cudaError_t launch_memset_u32(uint32_t* p, size_t n, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
@@ -198,6 +198,26 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 // Convert two bf16 (packed) to fp16x2 (exact for |x| in fp16 normal range).
 __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t v) {
   return pack_h2(bf16_lo(v), bf16_hi(v));
+}
+
+// Quantise one 16-value block. Returns the 8 code bytes (as two u32) and the
+// E4M3 scale code.
+__device__ __forceinline__ void quant_block16(const float* v, uint32_t& lo, uint32_t& hi,
+                                              uint32_t& scode) {
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  scode = e4m3_rn_sat(__fdiv_rn(amax, 6.0f));
+  float s = e4m3_to_f32(scode);
+  if (s == 0.f) {
+    lo = hi = 0u;
+    return;
+  }
+  float r[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) r[k] = __fdiv_rn(v[k], s);
+  lo = e2m1x8(r);
+  hi = e2m1x8(r + 8);
 }
 
 #endif  // __CUDACC__

@@ -10,26 +10,6 @@
 
 namespace csa2 {
 
-// Quantise one 16-value block. Returns the 8 code bytes (as two u32) and the
-// E4M3 scale code.
-__device__ __forceinline__ void quant_block16(const float* v, uint32_t& lo, uint32_t& hi,
-                                              uint32_t& scode) {
-  float amax = 0.f;
-#pragma unroll
-  for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
-  scode = e4m3_rn_sat(__fdiv_rn(amax, 6.0f));
-  float s = e4m3_to_f32(scode);
-  if (s == 0.f) {
-    lo = hi = 0u;
-    return;
-  }
-  float r[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) r[k] = __fdiv_rn(v[k], s);
-  lo = e2m1x8(r);
-  hi = e2m1x8(r + 8);
-}
-
 template <bool kBf16>
 __global__ void __launch_bounds__(256) encode_quant_kernel(const void* __restrict__ h,
                                                            int64_t nblk,

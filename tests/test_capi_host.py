@@ -97,6 +97,9 @@ def test_encode_validation(L):
     assert r(FAKE, 1, 16, 4000, FAKE, FAKE, 20, FAKE, FAKE, FAKE, None, 0, None) == 1
     assert r(FAKE, 1, 16, 4096, FAKE, FAKE, 20, FAKE, FAKE, None, None, 0, None) == 1
     assert r(FAKE, 1, 0, 4096, FAKE, FAKE, 20, FAKE, FAKE, FAKE, None, 0, None) == 0
+    # projection needs the workspace status word
+    assert r(FAKE, 1, 16, 4096, FAKE, FAKE, 20, FAKE, FAKE, FAKE, None, 0, None) == 3
+    assert r(FAKE, 1, 16, 4096, FAKE, FAKE, 20, FAKE, FAKE, FAKE, FAKE, 128, None) == 3
 
 
 def test_workspace_size_monotone(L):
