@@ -385,6 +385,12 @@ def run_ours(args):
                 "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "peak_source": peaks["src"], "traffic": None}
 
+    ced = None
+    if not args.no_ced:
+        try:
+            ced = run_ced(args, torch, csa2, dev, peaks)
+        except Exception as ex:  # reported, not hidden
+            ced = {"error": repr(ex)}
     e2e = None if args.no_e2e else run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs,
                                            ws, world, dev)
     cpu = None
@@ -408,12 +414,54 @@ def run_ours(args):
             "roofline": roofline, "roofline_by_call": rows, "calls": breakdown,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": n_launch,
             "wall_s_timed_loop": round(wall, 3),
-            "ced_projection": None,
+            "ced_projection": ced,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def run_ced(args, torch, csa2, dev, peaks):
+    """CED projection, Eq. (1), with the fused FP4 cache write: 32768 x 4096 against
+    20 layers x (576 + 64) columns. Timed alone with CUDA events (inputs > L2)."""
+    cfg = ci.CED_PROJ
+    inp = ci.make_ced_inputs(cfg)
+    b16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    h, wkv, wz = b16(inp.H), b16(inp.W_kv), b16(inp.W_z)
+    del inp
+    codes = torch.empty((cfg.n_layers, cfg.rows, 288), dtype=torch.uint8, device=dev)
+    scales = torch.empty((cfg.n_layers, cfg.rows, 36), dtype=torch.uint8, device=dev)
+    z = torch.empty((cfg.n_layers, cfg.rows, 64), dtype=torch.bfloat16, device=dev)
+    ws = csa2.csa2_workspace(0, 0, 0, 0, 0, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    L = csa2.lib()
+    args_c = (h.data_ptr(), csa2.BF16, cfg.rows, cfg.d_model, wkv.data_ptr(), wz.data_ptr(), cfg.n_layers,
+              codes.data_ptr(), scales.data_ptr(), z.data_ptr(), ws.data_ptr(), ws.numel(), stream.cuda_stream)
+    for _ in range(3):
+        r = L.csa2_encode_kv(*args_c)
+        if r != 0:
+            return {"error": f"csa2_encode_kv returned {r}"}
+    st, flags = csa2.csa2_read_device_status(ws, stream)
+    if st != 0:
+        return {"error": f"device status {st} flags {flags}"}
+    n = 20
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    times = []
+    for i in range(n):
+        ev[i].record(stream)
+        L.csa2_encode_kv(*args_c)
+        ev[i + 1].record(stream)
+    stream.synchronize()
+    times = [ev[i].elapsed_time(ev[i + 1]) * 1e-3 for i in range(n)]
+    t = statistics.mean(times)
+    flops = 2.0 * cfg.rows * cfg.d_model * cfg.n_layers * (576 + 64)
+    tf = flops / t / 1e12
+    return {"config": {"workload": cfg.name, "rows": cfg.rows, "d_model": cfg.d_model, "n_layers": cfg.n_layers},
+            "value": round(tf, 1), "unit": "TFLOP/s", "ms_per_launch": round(t * 1e3, 4), "launches": n,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": round(tf / peaks["bf16"], 4), "peak_source": peaks["src"] + " bf16 burst",
+                         "frac_of_sustained": round(tf / peaks["bf16_sus"], 4), "traffic": None}}
 
 
 def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs, ws, world, dev):
@@ -489,6 +537,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ced", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

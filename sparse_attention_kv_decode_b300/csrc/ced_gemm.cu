@@ -20,6 +20,9 @@
 // Every mbarrier wait is bounded; a wait that gives up sets a status bit, the
 // CTA stops issuing work, drains what it started and frees its TMEM.
 #include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "csa2_internal.cuh"
 
@@ -353,12 +356,30 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
   }
 }
 
+// cuTensorMapEncodeTiled is reached through the runtime's driver entry point,
+// so the library does not link against the driver library.
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
 bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  auto encode = encode_tiled_fn();
+  if (encode == nullptr) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {(cuuint32_t)kBK, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = cuTensorMapEncodeTiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
                                       dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
