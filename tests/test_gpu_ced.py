@@ -60,10 +60,17 @@ def _check_layer(Hrows, Wkv_l, Wz_l, gc, gs, gz):
         sv = fp4.e4m3_value(gs)[:, :, None]
         bound = sv + np.maximum(0, amax[:, :, None] - 6 * sv) + Eb
         assert np.all(np.abs(d - Cb)[amb] <= bound[amb] + 1e-12)
-    # Z: within one bf16 ulp of the exact value rounded to bf16
+    # Z: the device rounds its fp32 product (within Ez of the exact Z) to bf16, so it is
+    # within Ez + one bf16 ulp of |Z| + Ez of the exact value; away from cancellation this
+    # is within 1 ulp of the correctly rounded bf16 value.
     zg = f64(gz)
-    ulp = np.ldexp(1.0, np.frexp(np.abs(oz))[1] - 8)
-    assert np.all(np.abs(zg - oz) <= ulp), "Z off by more than 1 bf16 ulp"
+    Ez = ced.ambiguity_bound(Hrows, Wz_l)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(Z) + Ez)[1] - 8)
+    viol = np.abs(zg - Z) - (Ez + ulp)
+    assert np.all(viol <= 0), f"Z: worst excess {viol.max():.3e} at |Z|={np.abs(Z).flat[viol.argmax()]:.3e}"
+    far = Ez < ulp / 4
+    ulp_r = np.ldexp(1.0, np.frexp(np.abs(oz))[1] - 8)
+    assert np.all((np.abs(zg - oz) <= ulp_r)[far]), "Z off by more than 1 bf16 ulp away from cancellation"
     return int(amb.sum())
 
 
