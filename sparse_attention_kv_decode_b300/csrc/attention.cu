@@ -62,16 +62,30 @@ struct SwaSource {
 };
 
 // Stage Q (bf16 [H][576]) into fp16 rows of the swizzled Q buffer; rows >= H are zero.
+// Loads are issued in batches of 6 per thread before any conversion, so their
+// latencies overlap instead of forming a chain.
 __device__ __forceinline__ void stage_q(uint8_t* smem, const uint16_t* q, int H) {
-  for (int i = threadIdx.x; i < 64 * kChunks; i += kAttnThreads) {
-    const int row = i / kChunks, ch = i % kChunks;
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (row < H) {
-      uint4 v = *reinterpret_cast<const uint4*>(q + (int64_t)row * CSA2_D_KV + ch * 8);
-      o.x = bf16x2_to_h2(v.x); o.y = bf16x2_to_h2(v.y);
-      o.z = bf16x2_to_h2(v.z); o.w = bf16x2_to_h2(v.w);
+  constexpr int kPer = 64 * kChunks / kAttnThreads;  // 18
+  constexpr int kBatch = 6;
+#pragma unroll
+  for (int b0 = 0; b0 < kPer; b0 += kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = threadIdx.x + (b0 + k) * kAttnThreads;
+      const int row = i / kChunks, ch = i % kChunks;
+      v[k] = row < H ? *reinterpret_cast<const uint4*>(q + (int64_t)row * CSA2_D_KV + ch * 8)
+                     : make_uint4(0, 0, 0, 0);
     }
-    *reinterpret_cast<uint4*>(smem + AttnSmem::kQ + swz(row, ch)) = o;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = threadIdx.x + (b0 + k) * kAttnThreads;
+      const int row = i / kChunks, ch = i % kChunks;
+      uint4 o;
+      o.x = bf16x2_to_h2(v[k].x); o.y = bf16x2_to_h2(v[k].y);
+      o.z = bf16x2_to_h2(v[k].z); o.w = bf16x2_to_h2(v[k].w);
+      *reinterpret_cast<uint4*>(smem + AttnSmem::kQ + swz(row, ch)) = o;
+    }
   }
 }
 
@@ -126,19 +140,31 @@ __device__ __forceinline__ void fp4_dequant(uint8_t* smem, int buf) {
   }
 }
 
-// Raw bf16 window rows [r0, r0+64) (clipped to r_end) -> fp16 C tile.
+// Raw bf16 window rows [r0, r0+64) (clipped to r_end) -> fp16 C tile (batched loads).
 __device__ __forceinline__ void swa_load(uint8_t* smem, const uint16_t* rows, int r0, int r_end) {
   int* valid = reinterpret_cast<int*>(smem + AttnSmem::kValidSwa);
   if (threadIdx.x < kTE) valid[threadIdx.x] = (r0 + (int)threadIdx.x < r_end) ? 1 : -1;
-  for (int i = threadIdx.x; i < kTE * kChunks; i += kAttnThreads) {
-    const int e = i / kChunks, ch = i % kChunks;
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (r0 + e < r_end) {
-      uint4 v = *reinterpret_cast<const uint4*>(rows + (int64_t)(r0 + e) * CSA2_D_KV + ch * 8);
-      o.x = bf16x2_to_h2(v.x); o.y = bf16x2_to_h2(v.y);
-      o.z = bf16x2_to_h2(v.z); o.w = bf16x2_to_h2(v.w);
+  constexpr int kPer = kTE * kChunks / kAttnThreads;  // 18
+  constexpr int kBatch = 6;
+#pragma unroll
+  for (int b0 = 0; b0 < kPer; b0 += kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = threadIdx.x + (b0 + k) * kAttnThreads;
+      const int e = i / kChunks, ch = i % kChunks;
+      v[k] = (r0 + e < r_end) ? *reinterpret_cast<const uint4*>(rows + (int64_t)(r0 + e) * CSA2_D_KV + ch * 8)
+                              : make_uint4(0, 0, 0, 0);
     }
-    *reinterpret_cast<uint4*>(smem + AttnSmem::kC + swz(e, ch)) = o;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int i = threadIdx.x + (b0 + k) * kAttnThreads;
+      const int e = i / kChunks, ch = i % kChunks;
+      uint4 o;
+      o.x = bf16x2_to_h2(v[k].x); o.y = bf16x2_to_h2(v[k].y);
+      o.z = bf16x2_to_h2(v[k].z); o.w = bf16x2_to_h2(v[k].w);
+      *reinterpret_cast<uint4*>(smem + AttnSmem::kC + swz(e, ch)) = o;
+    }
   }
 }
 
@@ -346,7 +372,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) swa_attn_partial_kernel(
 }
 
 // Merge nsplit partials (and optionally an external normalised branch with
-// natural-log LSE) into normalised O and natural-log LSE. grid: (H/16, Q), 256 threads.
+// natural-log LSE) into normalised O and natural-log LSE. One warp per (query,
+// head): the split maxima and sums are loaded in parallel by the lanes, then
+// every lane combines 16 value dims. grid: (ceil(H/8), Q), 256 threads.
 __global__ void __launch_bounds__(256) attn_combine_kernel(
     const float* __restrict__ partials, int nsplit, int H, const float* __restrict__ o_ext,
     const float* __restrict__ lse_ext, float* __restrict__ o_out, float* __restrict__ lse_out) {
@@ -354,48 +382,67 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
   constexpr int kPS = kDV + 2;
   const int qi = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // 8 warps x 2 heads each = 16 heads per CTA
-  for (int hh = 0; hh < 2; ++hh) {
-    const int h = blockIdx.x * 16 + warp * 2 + hh;
-    if (h >= H) continue;
-    float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s)
-      M = fmaxf(M, partials[((int64_t)(qi * nsplit + s) * H + h) * kPS + kDV]);
-    float ext_m = -INFINITY;
-    if (o_ext) {
-      const float le = lse_ext[(int64_t)qi * H + h];
-      ext_m = le * kLog2e;  // log2-domain log-sum-exp of the external branch
-      M = fmaxf(M, ext_m);
-    }
-    const float Mu = M == -INFINITY ? 0.f : M;
-    float L = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float* p = partials + ((int64_t)(qi * nsplit + s) * H + h) * kPS;
-      L += p[kDV + 1] * exp2f(p[kDV] - Mu);
-    }
-    const float we = o_ext ? exp2f(ext_m - Mu) : 0.f;  // external branch is normalised: weight 2^(lse2-M)
-    L += we;
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int d = lane * 4; d < kDV; d += 128) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s = 0; s < nsplit; ++s) {
-        const float* p = partials + ((int64_t)(qi * nsplit + s) * H + h) * kPS;
-        const float w = exp2f(p[kDV] - Mu);
-        const float2 x0 = *reinterpret_cast<const float2*>(p + d);
-        const float2 x1 = *reinterpret_cast<const float2*>(p + d + 2);
-        acc.x += w * x0.x; acc.y += w * x0.y; acc.z += w * x1.x; acc.w += w * x1.y;
-      }
-      if (o_ext && we > 0.f) {
-        const float4 e = *reinterpret_cast<const float4*>(o_ext + ((int64_t)qi * H + h) * kDV + d);
-        acc.x += we * e.x; acc.y += we * e.y; acc.z += we * e.z; acc.w += we * e.w;
-      }
-      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-      *reinterpret_cast<float4*>(o_out + ((int64_t)qi * H + h) * kDV + d) = acc;
-    }
-    __syncwarp();
-    if (lane == 0 && lse_out)
-      lse_out[(int64_t)qi * H + h] = L > 0.f ? (Mu + log2f(L)) * kLn2 : -INFINITY;
+  const int h = blockIdx.x * 8 + warp;
+  if (h >= H) return;
+  // lane s < nsplit holds split s; lane 31 holds the external branch
+  float m = -INFINITY, l = 0.f;
+  if (lane < nsplit) {
+    const float* p = partials + ((int64_t)(qi * nsplit + lane) * H + h) * kPS;
+    m = p[kDV];
+    l = p[kDV + 1];
+  } else if (lane == 31 && o_ext) {
+    m = lse_ext[(int64_t)qi * H + h] * kLog2e;  // a normalised branch: sum 1 at max lse
+    l = m == -INFINITY ? 0.f : 1.f;
   }
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float Mu = M == -INFINITY ? 0.f : M;
+  const float w = l > 0.f ? exp2f(m - Mu) : 0.f;   // weight of this lane's branch
+  float L = l * w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < nsplit; ++s) {
+    const float ws = __shfl_sync(0xffffffffu, w, s);
+    if (ws == 0.f) continue;
+    const float* p = partials + ((int64_t)(qi * nsplit + s) * H + h) * kPS;
+    float2 x[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[2 * j] = *reinterpret_cast<const float2*>(p + j * 128 + lane * 4);
+      x[2 * j + 1] = *reinterpret_cast<const float2*>(p + j * 128 + lane * 4 + 2);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j].x += ws * x[2 * j].x; acc[j].y += ws * x[2 * j].y;
+      acc[j].z += ws * x[2 * j + 1].x; acc[j].w += ws * x[2 * j + 1].y;
+    }
+  }
+  const float we = __shfl_sync(0xffffffffu, w, 31);
+  if (o_ext && we > 0.f) {
+    const float* e = o_ext + ((int64_t)qi * H + h) * kDV;
+    float4 x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = *reinterpret_cast<const float4*>(e + j * 128 + lane * 4);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j].x += we * x[j].x; acc[j].y += we * x[j].y;
+      acc[j].z += we * x[j].z; acc[j].w += we * x[j].w;
+    }
+  }
+  __syncwarp();
+  float* out = o_out + ((int64_t)qi * H + h) * kDV;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float4 r = acc[j];
+    r.x *= inv; r.y *= inv; r.z *= inv; r.w *= inv;
+    *reinterpret_cast<float4*>(out + j * 128 + lane * 4) = r;
+  }
+  if (lane == 0 && lse_out) lse_out[(int64_t)qi * H + h] = L > 0.f ? (Mu + log2f(L)) * kLn2 : -INFINITY;
 }
 
 static cudaError_t set_smem(int slot, const void* fn, int bytes) {
@@ -417,7 +464,7 @@ cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t
       static_cast<const uint16_t*>(q), src, T, H, scale_log2, nsplit, split_len, partials, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3((H + 15) / 16, Q), 256, 0, st>>>(partials, nsplit, H, nullptr,
+  attn_combine_kernel<<<dim3((H + 7) / 8, Q), 256, 0, st>>>(partials, nsplit, H, nullptr,
                                                               nullptr, o_g, lse_g);
   return cudaGetLastError();
 }
@@ -437,7 +484,7 @@ cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa
       static_cast<const uint16_t*>(q), src, T, H, scale_log2, nsplit, partials, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3((H + 15) / 16, Q), 256, 0, st>>>(partials, nsplit, H, o_g, lse_g,
+  attn_combine_kernel<<<dim3((H + 7) / 8, Q), 256, 0, st>>>(partials, nsplit, H, o_g, lse_g,
                                                               o_out, lse_out);
   return cudaGetLastError();
 }

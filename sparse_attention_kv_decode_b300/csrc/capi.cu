@@ -38,7 +38,7 @@ cudaError_t set_attr_once(int slot, const void* fn, cudaFuncAttribute attr, int 
 
 int attn_splits(int64_t Q, int K, int n_sm) {
   if (Q <= 0) return 1;
-  int64_t s = (n_sm + Q - 1) / Q;        // about one wave of CTAs
+  int64_t s = n_sm / Q;                  // at most one wave of one-CTA-per-SM blocks
   int64_t max_by_k = (K + 127) / 128;    // at least two 64-key tiles per split
   if (s > max_by_k) s = max_by_k;
   if (s > kMaxSplits) s = kMaxSplits;
@@ -163,7 +163,7 @@ int csa2_index_topk(int mode, int B, int T, int H_I, const void* q_idx, const fl
   uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
   const int64_t stride = score_pad(n_stride);
   cudaError_t e = launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores,
-                                     stride, st);
+                                     stride, status, st);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
   return cuda_status(launch_topk_select(scores, stride, n_visible, (int)Q, n_stride, K, out_idx,
                                         out_scores, status, st));

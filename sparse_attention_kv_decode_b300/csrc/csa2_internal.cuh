@@ -1,6 +1,7 @@
 // Internal declarations and device helpers of libcsa2 (sm_103a only).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,7 +53,8 @@ cudaError_t launch_encode_quant(const void* h, int h_dtype, int64_t rows, uint8_
                                 uint8_t* scales, cudaStream_t st);
 cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void* z,
                                int64_t n_stride, const int32_t* n_visible, int B, int T,
-                               int H_I, float* scores, int64_t score_stride, cudaStream_t st);
+                               int H_I, float* scores, int64_t score_stride, uint32_t* status,
+                               cudaStream_t st);
 cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
                                int Q, int64_t n_stride, int K, int32_t* out_idx, float* out_scores,
                                uint32_t* status, cudaStream_t st);
@@ -218,6 +220,57 @@ __device__ __forceinline__ void quant_block16(const float* v, uint32_t& lo, uint
   for (int k = 0; k < 16; ++k) r[k] = __fdiv_rn(v[k], s);
   lo = e2m1x8(r);
   hi = e2m1x8(r + 8);
+}
+
+// ---- mbarrier and bulk-copy helpers (shared by the TMA-fed kernels)
+// Bound on the polls of one mbarrier wait (with back-off, a few seconds).
+constexpr uint32_t kMbarWaitLimit = 1u << 25;
+
+__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t a, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the completion of the phase with the given parity.
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
+  for (uint32_t i = 0; i < kMbarWaitLimit; ++i) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (i > 256) __nanosleep(64);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(mbar)
+      : "memory");
 }
 
 #endif  // __CUDACC__

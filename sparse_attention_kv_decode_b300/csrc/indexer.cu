@@ -13,39 +13,35 @@
 // per query: every CTA keeps its slice of scores in shared memory and the
 // cluster agrees on the K-th score through a few histogram rounds exchanged
 // over distributed shared memory (no global atomics, no spin waits).
-#include <cooperative_groups.h>
-
 #include "csa2_internal.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace csa2 {
 
 // ---------------------------------------------------------------------------
 // Scoring
 // ---------------------------------------------------------------------------
-// Each thread (g = lane/4, tig = lane%4) loads, for key rows g and g+8 of a
-// 16-key tile, the 16-byte pieces at byte offsets 16*tig and 64+16*tig. The
-// MMA's k-slots are assigned to channels so that the A fragment registers are
-// exactly those loaded words, and the B fragment (indexer query of head g) is
-// read from the same offsets: the contraction order is a permutation of the
-// 64 channels, which leaves the dot products unchanged.
-template <int NT>
-__global__ void __launch_bounds__(256) index_score_kernel(
-    const uint16_t* __restrict__ q_idx, const float* __restrict__ w_idx,
-    const uint16_t* __restrict__ z, int64_t n_stride, const int32_t* __restrict__ n_visible, int T,
-    int H_I, float* __restrict__ scores, int64_t score_stride) {
-  const int qi = blockIdx.y;
-  const int b = qi / T;
-  int nvis = n_visible[qi];
-  nvis = nvis < 0 ? 0 : (nvis > n_stride ? (int)n_stride : nvis);
-  const int64_t base = (int64_t)blockIdx.x * kScoreTile;
-  if (base >= nvis) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tig = lane & 3;
+// A persistent kernel streams the keys through a ring of shared-memory stages
+// filled by bulk copies (one 16 KB stage = 128 keys of one query), so each SM
+// keeps ~200 KB of key reads in flight with a single issuing thread. The stages
+// of all queries form one list that CTAs walk with a grid stride.
+//
+// Each consumer warp scores 16 keys of a stage with four m16n8k16 bf16 MMAs per
+// group of 8 indexer heads. Thread (g = lane/4, tig = lane%4) takes, for key
+// rows g and g+8, the 16-byte pieces at byte offsets 16*tig and 64+16*tig; the
+// MMA's k-slots are assigned to channels so that these words are exactly the
+// A fragment, and the B fragment (indexer query of head g) is read from the
+// same offsets: the contraction order is a permutation of the 64 channels,
+// which leaves each dot product unchanged.
+constexpr int kStageKeys = 128;
+constexpr int kStageBytes = kStageKeys * CSA2_D_IDX * 2;  // 16 KB
+constexpr int kScoreStages = 4;
+constexpr int kScoreThreads = 256;
+constexpr int kScoreSmem = kScoreStages * kStageBytes + 2 * kScoreStages * 8;
 
-  uint32_t qa[NT][8];
-  float wv[NT][2];
+template <int NT>
+__device__ __forceinline__ void load_q_frag(const uint16_t* q_idx, const float* w_idx, int qi,
+                                            int H_I, int g, int tig, uint32_t (&qa)[NT][8],
+                                            float (&wv)[NT][2]) {
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int head = nt * 8 + g;
@@ -63,46 +59,114 @@ __global__ void __launch_bounds__(256) index_score_kernel(
     wv[nt][0] = h0 < H_I ? w_idx[(int64_t)qi * H_I + h0] : 0.f;
     wv[nt][1] = h0 + 1 < H_I ? w_idx[(int64_t)qi * H_I + h0 + 1] : 0.f;
   }
+}
 
-  const uint16_t* zb = z + (int64_t)b * n_stride * CSA2_D_IDX;
-  float* srow = scores + (int64_t)qi * score_stride;
-  constexpr int kTilesPerWarp = kScoreTile / 16 / 8;  // 8
-  constexpr int kU = 4;
-#pragma unroll 1
-  for (int t0 = 0; t0 < kTilesPerWarp; t0 += kU) {
-    uint32_t ra[kU][16];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int64_t kg = base + (int64_t)(warp * kTilesPerWarp + t0 + u) * 16 + g;
-      const int64_t kg8 = kg + 8;
-      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0, v2 = v0, v3 = v0;
-      if (kg < nvis) {
-        const uint16_t* p = zb + kg * CSA2_D_IDX;
-        v0 = ldg_stream(p + 8 * tig);
-        v1 = ldg_stream(p + 32 + 8 * tig);
-      }
-      if (kg8 < nvis) {
-        const uint16_t* p = zb + kg8 * CSA2_D_IDX;
-        v2 = ldg_stream(p + 8 * tig);
-        v3 = ldg_stream(p + 32 + 8 * tig);
-      }
-      ra[u][0] = v0.x; ra[u][1] = v0.y; ra[u][2] = v0.z; ra[u][3] = v0.w;
-      ra[u][4] = v1.x; ra[u][5] = v1.y; ra[u][6] = v1.z; ra[u][7] = v1.w;
-      ra[u][8] = v2.x; ra[u][9] = v2.y; ra[u][10] = v2.z; ra[u][11] = v2.w;
-      ra[u][12] = v3.x; ra[u][13] = v3.y; ra[u][14] = v3.z; ra[u][15] = v3.w;
+__device__ __forceinline__ int clamp_nvis(const int32_t* n_visible, int qi, int64_t n_stride) {
+  int v = n_visible[qi];
+  return v < 0 ? 0 : (v > n_stride ? (int)n_stride : v);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
+    const uint16_t* __restrict__ q_idx, const float* __restrict__ w_idx,
+    const uint16_t* __restrict__ z, int64_t n_stride, const int32_t* __restrict__ n_visible, int T,
+    int H_I, int Q, float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ status) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + kScoreStages * kStageBytes;
+  const uint32_t bar_empty = bar_full + kScoreStages * 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  const int stages_per_q = (int)((n_stride + kStageKeys - 1) / kStageKeys);
+  const int total = Q * stages_per_q;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScoreStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kScoreThreads / 32);
     }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // the CTA's work list: global stage ids blockIdx.x, +gridDim.x, ... that hold visible keys
+  auto stage_keys = [&](int gs, int& qi, int64_t& key0) -> int {
+    qi = gs / stages_per_q;
+    key0 = (int64_t)(gs - qi * stages_per_q) * kStageKeys;
+    const int nv = clamp_nvis(n_visible, qi, n_stride);
+    const int64_t k = nv - key0;
+    return k <= 0 ? 0 : (k > kStageKeys ? kStageKeys : (int)k);
+  };
+
+  bool ok = true;
+  int prod_gs = blockIdx.x;   // next stage id the producer will consider
+  int prod_n = 0;             // stages produced so far (ring position)
+  auto produce_next = [&]() {
+    while (prod_gs < total) {
+      int qi;
+      int64_t key0;
+      const int keys = stage_keys(prod_gs, qi, key0);
+      const int gs = prod_gs;
+      prod_gs += gridDim.x;
+      if (keys == 0) continue;
+      const int slot = prod_n % kScoreStages;
+      if (prod_n >= kScoreStages) {
+        if (!mbar_wait(bar_empty + 8 * slot, ((prod_n / kScoreStages) - 1) & 1)) {
+          atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+          ok = false;
+          prod_gs = total;
+          return;
+        }
+      }
+      const int b = qi / T;
+      const uint16_t* src = z + ((int64_t)b * n_stride + key0) * CSA2_D_IDX;
+      const uint32_t bytes = (uint32_t)keys * CSA2_D_IDX * 2;
+      mbar_arrive_expect_tx(bar_full + 8 * slot, bytes);
+      bulk_g2s(sbase + slot * kStageBytes, src, bytes, bar_full + 8 * slot);
+      ++prod_n;
+      (void)gs;
+      return;
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kScoreStages; ++i) produce_next();
+
+  uint32_t qa[NT][8];
+  float wv[NT][2];
+  int cur_q = -1;
+  int cons_n = 0;
+  for (int gs = blockIdx.x; gs < total; gs += gridDim.x) {
+    int qi;
+    int64_t key0;
+    const int keys = stage_keys(gs, qi, key0);
+    if (keys == 0) continue;
+    const int slot = cons_n % kScoreStages;
+    const bool ready = mbar_wait(bar_full + 8 * slot, (cons_n / kScoreStages) & 1);
+    if (!__all_sync(0xffffffffu, ready)) {
+      if (lane == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+      break;
+    }
+    if (qi != cur_q) {
+      load_q_frag<NT>(q_idx, w_idx, qi, H_I, g, tig, qa, wv);
+      cur_q = qi;
+    }
+    const int r0 = warp * 16;
+    if (r0 < keys) {
+      const uint8_t* st = smem + slot * kStageBytes;
+      const uint4 v0 = *reinterpret_cast<const uint4*>(st + (r0 + g) * 128 + 16 * tig);
+      const uint4 v1 = *reinterpret_cast<const uint4*>(st + (r0 + g) * 128 + 64 + 16 * tig);
+      const uint4 v2 = *reinterpret_cast<const uint4*>(st + (r0 + g + 8) * 128 + 16 * tig);
+      const uint4 v3 = *reinterpret_cast<const uint4*>(st + (r0 + g + 8) * 128 + 64 + 16 * tig);
+      const uint32_t ra[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
+                               v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
       float pg = 0.f, pg8 = 0.f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          // k-step j uses words 2j, 2j+1 of the row-g / row-g+8 register sets
-          mma_bf16(acc, ra[u][2 * j], ra[u][8 + 2 * j], ra[u][2 * j + 1], ra[u][8 + 2 * j + 1],
-                   qa[nt][2 * j], qa[nt][2 * j + 1]);
-        }
+        for (int j = 0; j < 4; ++j)
+          mma_bf16(acc, ra[2 * j], ra[8 + 2 * j], ra[2 * j + 1], ra[8 + 2 * j + 1], qa[nt][2 * j],
+                   qa[nt][2 * j + 1]);
         pg += wv[nt][0] * fmaxf(acc[0], 0.f) + wv[nt][1] * fmaxf(acc[1], 0.f);
         pg8 += wv[nt][0] * fmaxf(acc[2], 0.f) + wv[nt][1] * fmaxf(acc[3], 0.f);
       }
@@ -110,38 +174,80 @@ __global__ void __launch_bounds__(256) index_score_kernel(
       pg += __shfl_xor_sync(0xffffffffu, pg, 2);
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 1);
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 2);
-      const int64_t kg = base + (int64_t)(warp * kTilesPerWarp + t0 + u) * 16 + g;
-      if (tig == 0 && kg < nvis) srow[kg] = pg;
-      if (tig == 1 && kg + 8 < nvis) srow[kg + 8] = pg8;
+      float* srow = scores + (int64_t)qi * score_stride + key0;
+      if (tig == 0 && r0 + g < keys) srow[r0 + g] = pg;
+      if (tig == 1 && r0 + g + 8 < keys) srow[r0 + g + 8] = pg8;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
+    ++cons_n;
+    if (threadIdx.x == 0 && ok) produce_next();
+  }
+  // drain: copies in flight must land before the CTA exits
+  if (threadIdx.x == 0) {
+    const int first = prod_n > kScoreStages ? prod_n - kScoreStages : 0;
+    for (int n = first; n < prod_n; ++n)
+      mbar_wait(bar_full + 8 * (n % kScoreStages), (n / kScoreStages) & 1);
   }
 }
 
 cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void* z,
                                int64_t n_stride, const int32_t* n_visible, int B, int T, int H_I,
-                               float* scores, int64_t score_stride, cudaStream_t st) {
+                               float* scores, int64_t score_stride, uint32_t* status,
+                               cudaStream_t st) {
   const int Q = B * T;
-  dim3 grid((unsigned)((n_stride + kScoreTile - 1) / kScoreTile), (unsigned)Q);
-  if (grid.x == 0 || Q == 0) return cudaSuccess;
+  if (n_stride == 0 || Q == 0) return cudaSuccess;
+  const int64_t total = (int64_t)Q * ((n_stride + kStageKeys - 1) / kStageKeys);
+  if (total > INT32_MAX / 2) return cudaErrorInvalidValue;
+  const int n_sm = device_sm_count();
+  int64_t grid = (int64_t)n_sm * 3;
+  if (grid > total) grid = total;
   auto qp = static_cast<const uint16_t*>(q_idx);
   auto zp = static_cast<const uint16_t*>(z);
-  if (H_I <= 8)
-    index_score_kernel<1><<<grid, 256, 0, st>>>(qp, w_idx, zp, n_stride, n_visible, T, H_I, scores,
-                                                score_stride);
-  else
-    index_score_kernel<2><<<grid, 256, 0, st>>>(qp, w_idx, zp, n_stride, n_visible, T, H_I, scores,
-                                                score_stride);
+  cudaError_t e;
+  if (H_I <= 8) {
+    e = set_attr_once(5, (const void*)index_score_kernel<1>,
+                      cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
+    if (e != cudaSuccess) return e;
+    index_score_kernel<1><<<(unsigned)grid, kScoreThreads, kScoreSmem, st>>>(
+        qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores, score_stride, status);
+  } else {
+    e = set_attr_once(6, (const void*)index_score_kernel<2>,
+                      cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
+    if (e != cudaSuccess) return e;
+    index_score_kernel<2><<<(unsigned)grid, kScoreThreads, kScoreSmem, st>>>(
+        qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores, score_stride, status);
+  }
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
 // Top-K selection: one cluster of C CTAs per query
 // ---------------------------------------------------------------------------
+// CTA r of the cluster owns the visible entries [r*slice, (r+1)*slice) and keeps
+// their scores in shared memory. Every exchange is a push: before a cluster
+// barrier each CTA writes its record into slot r of every peer's receive
+// buffer (distributed shared memory stores, no remote loads), so after the
+// barrier all reads are local and no CTA touches a peer once it has passed
+// the last barrier.
+//   round 0  min / max / count of the surviving candidates (+ the candidate
+//            list itself when small enough) -> every CTA knows the range
+//   round 1  histogram of the candidates over kNB monotone bins of that range
+//            -> the bin b* holding the K-th score: higher bins are selected,
+//            lower ones dropped; repeat from round 0 on the bin-b* survivors
+//   exact    when at most kCandCap candidates survive, each CTA ranks its own
+//            candidates against all of them by (score desc, index asc);
+//            when they all tie, the lowest indices win
+//   output   selected counts are pushed, each CTA writes its selected indices
+//            at its prefix offset (ascending by construction).
+// The bin map floor((s - lo) * kNB / (hi - lo)) is monotone in s, so bins
+// never reorder scores; equal scores always share a bin.
 constexpr int kSelThreads = 512;
-constexpr int kNB = 1024;          // histogram bins per refinement round
-constexpr int kCandCap = 1024;     // candidates resolved exactly by ranking
+constexpr int kNB = 512;            // histogram bins per refinement round
+constexpr int kCandCap = 512;       // candidates resolved exactly by ranking
 constexpr int kMaxLevels = 12;
-constexpr size_t kSelSmemMax = 220 * 1024;
+constexpr int kMaxCluster = 16;
+constexpr size_t kSelSmemMax = 200 * 1024;
 
 struct SelRec {
   float lo, hi;
@@ -149,20 +255,19 @@ struct SelRec {
 };
 
 struct SelShared {
-  uint32_t hist[kNB];
-  uint32_t ghist[kNB];
-  SelRec rec[kMaxLevels + 1];
-  int sel_cnt;
-  int bstar;
+  uint32_t hist_in[kMaxCluster][kNB];   // pushed histograms
+  SelRec rec_in[kMaxCluster];           // pushed candidate statistics
+  int sel_in[kMaxCluster];              // pushed selected counts
+  uint32_t hist_local[kNB];
   int scan[kSelThreads / 32];
   float red_f[2][kSelThreads / 32];
   int red_i[kSelThreads / 32];
-  int cand_n;
-  float cand_s[kCandCap];
+  int bstar, above, cand_n;
+  float cand_s[kCandCap];               // own candidates (compacted)
   int cand_i[kCandCap];
-  float all_s[kCandCap];
-  int all_i[kCandCap];
 };
+// followed in dynamic shared memory by: float cand_in_s[C][kCandCap], int cand_in_i[C][kCandCap],
+// float sc[slice_cap], uint8_t state[slice_cap]
 
 __device__ __forceinline__ int bin_of(float s, float lo, float scl) {
   float t = (s - lo) * scl;
@@ -197,24 +302,43 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scan, int& total) {
   return pre;
 }
 
+__device__ __forceinline__ void st_remote_u32(uint32_t* local_addr, int rank, uint32_t v) {
+  uint32_t la = smem_u32(local_addr), ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ra), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_remote_v4(void* local_addr, int rank, uint4 v) {
+  uint32_t la = smem_u32(local_addr), ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ n_visible,
     int64_t n_stride, int K, int slice_cap, int32_t* __restrict__ out_idx,
     float* __restrict__ out_scores, uint32_t* __restrict__ status) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
-  float* sc = reinterpret_cast<float*>(smem_raw + sizeof(SelShared));
+  uint32_t C, r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  float* cand_in_s = reinterpret_cast<float*>(smem_raw + sizeof(SelShared));
+  int* cand_in_i = reinterpret_cast<int*>(cand_in_s + C * kCandCap);
+  float* sc = reinterpret_cast<float*>(cand_in_i + C * kCandCap);
   uint8_t* state = reinterpret_cast<uint8_t*>(sc + slice_cap);
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int C = (int)cluster.num_blocks();
-  const int r = (int)cluster.block_rank();
   const int tid = threadIdx.x;
   const int qi = blockIdx.y;
   int nvis = n_visible[qi];
   nvis = nvis < 0 ? 0 : (nvis > n_stride ? (int)n_stride : nvis);
-  const int slice = (nvis + C - 1) / C;
-  const int my0 = r * slice;
+  const int slice = (nvis + (int)C - 1) / (int)C;
+  const int my0 = (int)r * slice;
   int my_len = nvis - my0;
   my_len = my_len < 0 ? 0 : (my_len > slice ? slice : my_len);
   const int need = nvis < K ? nvis : K;
@@ -230,16 +354,15 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
 
   if (nvis > K) {
     int remaining = need;
-    int level = 0;
-    for (;; ++level) {
-      // ---- local statistics of the surviving candidates
+    for (int level = 0;; ++level) {
+      // ---- round 0: statistics (and small lists) of the surviving candidates
       float lo = INFINITY, hi = -INFINITY;
       int cnt = 0;
       for (int e = tid; e < my_len; e += kSelThreads)
         if (state[e] == 0) {
-          float s = sc[e];
-          lo = fminf(lo, s);
-          hi = fmaxf(hi, s);
+          const float v = sc[e];
+          lo = fminf(lo, v);
+          hi = fmaxf(hi, v);
           ++cnt;
         }
 #pragma unroll
@@ -255,72 +378,66 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
       }
       if (tid == 0) sh.cand_n = 0;
       __syncthreads();
-      if (tid == 0) {
-        float l = INFINITY, h = -INFINITY;
-        int c = 0;
-        for (int w = 0; w < kSelThreads / 32; ++w) {
-          l = fminf(l, sh.red_f[0][w]);
-          h = fmaxf(h, sh.red_f[1][w]);
-          c += sh.red_i[w];
-        }
-        sh.rec[level].lo = l;
-        sh.rec[level].hi = h;
-        sh.rec[level].cnt = c;
+      SelRec mine;
+      mine.lo = INFINITY; mine.hi = -INFINITY; mine.cnt = 0; mine.pad = 0;
+      for (int w = 0; w < kSelThreads / 32; ++w) {
+        mine.lo = fminf(mine.lo, sh.red_f[0][w]);
+        mine.hi = fmaxf(mine.hi, sh.red_f[1][w]);
+        mine.cnt += sh.red_i[w];
       }
-      __syncthreads();
-      const int my_cnt = sh.rec[level].cnt;
-      if (my_cnt <= kCandCap) {
+      if (mine.cnt <= kCandCap) {
         for (int e = tid; e < my_len; e += kSelThreads)
           if (state[e] == 0) {
-            int p = atomicAdd(&sh.cand_n, 1);
+            const int p = atomicAdd(&sh.cand_n, 1);
             sh.cand_s[p] = sc[e];
             sh.cand_i[p] = my0 + e;
           }
       }
-      cluster.sync();  // publish rec[level] and the candidate list
-
+      __syncthreads();
+      if (tid < (int)C)
+        st_remote_v4(&sh.rec_in[r], tid,
+                     make_uint4(__float_as_uint(mine.lo), __float_as_uint(mine.hi), (uint32_t)mine.cnt, 0u));
+      if (mine.cnt <= kCandCap) {
+        for (int j = tid; j < (int)C * mine.cnt; j += kSelThreads) {
+          const int peer = j / mine.cnt, k = j % mine.cnt;
+          st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_s[r * kCandCap + k]), peer,
+                        __float_as_uint(sh.cand_s[k]));
+          st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_i[r * kCandCap + k]), peer,
+                        (uint32_t)sh.cand_i[k]);
+        }
+      }
+      cluster_barrier();
       float glo = INFINITY, ghi = -INFINITY;
       int gcnt = 0, pre_cnt = 0;
-      for (int rr = 0; rr < C; ++rr) {
-        const SelRec* rec = cluster.map_shared_rank(&sh.rec[level], rr);
-        SelRec v = *rec;
+      for (int rr = 0; rr < (int)C; ++rr) {
+        const SelRec v = sh.rec_in[rr];
         if (v.cnt > 0) {
           glo = fminf(glo, v.lo);
           ghi = fmaxf(ghi, v.hi);
         }
-        if (rr < r) pre_cnt += v.cnt;
+        if (rr < (int)r) pre_cnt += v.cnt;
         gcnt += v.cnt;
       }
-
       if (remaining >= gcnt) {
-        // every surviving candidate is needed
         for (int e = tid; e < my_len; e += kSelThreads)
           if (state[e] == 0) state[e] = 1;
         __syncthreads();
         break;
       }
       if (gcnt <= kCandCap) {
-        // exact resolution: rank own candidates among all, by (score desc, index asc)
-        int off = 0;
-        for (int rr = 0; rr < C; ++rr) {
-          const SelRec* rec = cluster.map_shared_rank(&sh.rec[level], rr);
-          const int n = rec->cnt;
-          const float* rs = cluster.map_shared_rank(sh.cand_s, rr);
-          const int* ri = cluster.map_shared_rank(sh.cand_i, rr);
-          for (int j = tid; j < n; j += kSelThreads) {
-            sh.all_s[off + j] = rs[j];
-            sh.all_i[off + j] = ri[j];
-          }
-          off += n;
-        }
-        __syncthreads();
-        for (int j = tid; j < my_cnt; j += kSelThreads) {
+        // exact: rank own candidates among all, by (score desc, index asc)
+        for (int j = tid; j < mine.cnt; j += kSelThreads) {
           const float s = sh.cand_s[j];
           const int i = sh.cand_i[j];
           int rank = 0;
-          for (int c = 0; c < gcnt; ++c) {
-            const float t = sh.all_s[c];
-            rank += (t > s) || (t == s && sh.all_i[c] < i);
+          for (int rr = 0; rr < (int)C; ++rr) {
+            const int n = sh.rec_in[rr].cnt;
+            const float* cs = cand_in_s + rr * kCandCap;
+            const int* ci = cand_in_i + rr * kCandCap;
+            for (int c = 0; c < n; ++c) {
+              const float t = cs[c];
+              rank += (t > s) || (t == s && ci[c] < i);
+            }
           }
           state[i - my0] = rank < remaining ? 1 : 2;
         }
@@ -344,42 +461,33 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
         __syncthreads();
         break;
       }
-      // ---- histogram refinement round
+      // ---- round 1: histogram refinement over [glo, ghi]
       const float scl = (float)kNB / (ghi - glo);
-      for (int i = tid; i < kNB; i += kSelThreads) sh.hist[i] = 0u;
+      for (int i = tid; i < kNB; i += kSelThreads) sh.hist_local[i] = 0u;
       __syncthreads();
       for (int e = tid; e < my_len; e += kSelThreads)
-        if (state[e] == 0) atomicAdd(&sh.hist[bin_of(sc[e], glo, scl)], 1u);
-      cluster.sync();  // publish hist
-      for (int i = tid; i < kNB; i += kSelThreads) {
-        uint32_t s = 0;
-        for (int rr = 0; rr < C; ++rr) s += *cluster.map_shared_rank(&sh.hist[i], rr);
-        sh.ghist[i] = s;
-      }
+        if (state[e] == 0) atomicAdd(&sh.hist_local[bin_of(sc[e], glo, scl)], 1u);
       __syncthreads();
-      // suffix sums from the top bin: find b* with above(b*) < remaining <= above(b*) + h(b*)
+      for (int j = tid; j < (int)C * (kNB / 4); j += kSelThreads) {
+        const int peer = j / (kNB / 4), q4 = j % (kNB / 4);
+        st_remote_v4(&sh.hist_in[r][4 * q4], peer, *reinterpret_cast<const uint4*>(&sh.hist_local[4 * q4]));
+      }
+      cluster_barrier();
       {
-        constexpr int kPer = kNB / kSelThreads;  // 2 bins per thread, thread 0 owns the top
-        const int bhi = kNB - 1 - tid * kPer;
-        int mine = 0;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) mine += (int)sh.ghist[bhi - k];
+        // thread t owns bin kNB-1-t (kNB == kSelThreads): suffix counts from the top bin
+        const int bb = kNB - 1 - tid;
+        uint32_t h = 0;
+        for (int rr = 0; rr < (int)C; ++rr) h += sh.hist_in[rr][bb];
         int total;
-        int above = block_excl_scan(mine, sh.scan, total);
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-          const int bb = bhi - k;
-          const int h = (int)sh.ghist[bb];
-          if (above < remaining && remaining <= above + h) {
-            sh.bstar = bb;
-            sh.red_i[0] = above;
-          }
-          above += h;
+        const int above = block_excl_scan((int)h, sh.scan, total);
+        if (above < remaining && remaining <= above + (int)h) {
+          sh.bstar = bb;
+          sh.above = above;
         }
       }
       __syncthreads();
       const int bstar = sh.bstar;
-      remaining -= sh.red_i[0];
+      remaining -= sh.above;
       for (int e = tid; e < my_len; e += kSelThreads)
         if (state[e] == 0) {
           const int bi = bin_of(sc[e], glo, scl);
@@ -396,12 +504,12 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   for (int e = e0; e < e1; ++e) c += state[e] == 1;
   int my_sel;
   int pos = block_excl_scan(c, sh.scan, my_sel);
-  if (tid == 0) sh.sel_cnt = my_sel;
-  cluster.sync();  // publish sel_cnt
+  if (tid < (int)C) st_remote_u32(reinterpret_cast<uint32_t*>(&sh.sel_in[r]), tid, (uint32_t)my_sel);
+  cluster_barrier();
   int offset = 0, total_sel = 0;
-  for (int rr = 0; rr < C; ++rr) {
-    const int v = *cluster.map_shared_rank(&sh.sel_cnt, rr);
-    if (rr < r) offset += v;
+  for (int rr = 0; rr < (int)C; ++rr) {
+    const int v = sh.sel_in[rr];
+    if (rr < (int)r) offset += v;
     total_sel += v;
   }
   pos += offset;
@@ -418,24 +526,24 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
       out[p] = -1;
       if (outs) outs[p] = __int_as_float(0x7fc00000);
     }
-  cluster.sync();  // keep shared memory alive until every remote read is done
 }
 
 static int select_cluster_size(int64_t n_stride) {
   int64_t per = (n_stride + 4095) / 4096;
   int c = 1;
-  while (c < per && c < 16) c <<= 1;
+  while (c < per && c < kMaxCluster) c <<= 1;
   return c;
 }
 
 cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
                                int Q, int64_t n_stride, int K, int32_t* out_idx, float* out_scores,
                                uint32_t* status, cudaStream_t st) {
+  static_assert(kNB == kSelThreads, "one histogram bin per thread");
   if (Q == 0) return cudaSuccess;
   const int C = select_cluster_size(n_stride);
   int slice_cap = (int)((n_stride + C - 1) / C);
   slice_cap = (slice_cap + 15) & ~15;
-  const size_t smem = sizeof(SelShared) + (size_t)slice_cap * 5;
+  const size_t smem = sizeof(SelShared) + (size_t)C * kCandCap * 8 + (size_t)slice_cap * 5;
   if (smem > kSelSmemMax) return cudaErrorInvalidValue;
   cudaError_t e = set_attr_once(0, (const void*)topk_select_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemMax);
