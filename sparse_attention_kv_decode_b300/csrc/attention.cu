@@ -7,369 +7,530 @@
 // global KV and its top-K indices; 5. FP4 Main KV Cache), and the wesearch.press
 // card (head-count reduction: one latent KV shared by every query head).
 //
-// One CTA handles one query token and a split of its key set: a tile of 64
-// keys is staged (cp.async gather of FP4 codes + scales, or bf16 window rows),
-// converted to fp16 in shared memory (FP4 -> fp16 is exact), and attended by 8
-// warps with m16n8k16 fp16 MMAs and an online softmax in the exp2 domain.
-// Partials (unnormalised O, running max, running sum) of every split are then
-// merged by a combine kernel, which also folds in an external branch for the
-// SWA merge.
+// One CTA attends one query token over a split of its keys, 128 keys per tile,
+// on the 5th-generation tensor cores with the scores transposed so that the
+// 128 keys fill the MMA's M dimension (64 heads are N):
+//   S^T[key, head]  = C[key, 0:576] . Q[head, 0:576]^T     (K-major A and B)
+//   O^T[dim, head] += V^T[dim, key] . P^T[key, head]        (MN-major A and B)
+// C is the tile's key rows in fp16 (FP4 entries dequantise exactly to fp16;
+// bf16 window rows are converted), V = C[:, 0:512], and both products read the
+// same 128-byte-swizzled shared-memory tile. S^T (two buffers) and the four
+// 128x64 O^T accumulators live in TMEM.
+// Warp roles (288 threads):
+//   warps 0-3  loaders: stage Q; per tile, gather + dequantise one key row per
+//              thread (FP4) or convert TMA-loaded window rows (bf16)
+//   warps 4-7  softmax: one key row (TMEM lane) per thread; running max per head
+//              kept lazily (rescale only when a score exceeds it by 2^8), P^T
+//              written over the rope chunk of C once the S^T product has read it
+//   warp 8     TMEM allocation and the single-thread MMA issuer
+// Partials (unnormalised O, max, sum per head) of every split are merged by the
+// combine kernel, which also folds in the global branch for the SWA merge.
 #include "csa2_internal.cuh"
 
 namespace csa2 {
 
-constexpr int kTE = 64;            // keys per tile
-constexpr int kRowBytes = 1152;    // 576 fp16
-constexpr int kChunks = 72;        // 16-byte chunks per row
 constexpr int kDV = 512;
 static_assert(kPartStride == kDV + 2, "partial layout");
-constexpr int kSxStride = 68;      // floats per S-exchange row (64 + pad)
-constexpr int kAttnThreads = 256;
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return (uint32_t)(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
-}
+namespace {
 
-struct AttnSmem {
-  static constexpr int kQ = 0;
-  static constexpr int kC = kQ + 64 * kRowBytes;
-  static constexpr int kS = kC + kTE * kRowBytes;
-  static constexpr int kStage = kS + 64 * kSxStride * 4;
-  static constexpr int kStageCodes = kTE * CSA2_CODE_BYTES;    // 18432
-  static constexpr int kStageScales = kTE * CSA2_SCALE_BYTES;  // 2304
-  static constexpr int kStageBytes = kStageCodes + kStageScales;
-  static constexpr int kValid = kStage + 2 * kStageBytes;
-  static constexpr int kTotalFp4 = kValid + 2 * kTE * 4;
-  static constexpr int kValidSwa = kStage;
-  static constexpr int kTotalSwa = kValidSwa + kTE * 4;
+constexpr int kTK = 128;                 // keys per tile
+constexpr int kQChunk = 64 * 128;        // 64 heads x 64 dims fp16
+constexpr int kCChunk = kTK * 128;       // 128 keys x 64 dims fp16
+constexpr int kQBytes = 9 * kQChunk;
+constexpr int kCBytes = 9 * kCChunk;
+constexpr int kThreadsTC = 288;
+constexpr int kTmemCols = 512;
+constexpr int kColS = 0;                 // S^T buffers at columns [0, 64) and [64, 128)
+constexpr int kColO = 128;               // O^T M-tile i at columns [128 + 64 i, +64)
+constexpr float kRescale = 8.0f;         // lazy-max slack, log2 units (factor 256)
+constexpr int kMiscBytes = 4096;
+constexpr int kSmemTC = 1024 + kQBytes + kCBytes + kMiscBytes;
+
+// mbarrier slots (8 bytes each) in the misc area
+enum Bar { kQReady = 0, kChunkFull = 1, kGroupFree = 6, kSFull = 11, kPFull = 13, kTmaFull = 14,
+           kDrain = 15, kNumBars = 16 };
+
+struct Misc {
+  uint64_t bars[kNumBars];
+  uint32_t tmem_base;
+  int abort_flag;
+  int vote[2];
+  int valid[2][kTK];
+  float mrun[64];
+  float mnew[64];
+  float alpha[64];
+  float red[4][64];
 };
+static_assert(sizeof(Misc) <= kMiscBytes, "misc area");
 
-// Source of keys for one query: FP4 entries named by an index list, or a
-// contiguous window of raw bf16 rows.
-struct Fp4Source {
+struct Fp4Src {
   const uint8_t* codes;   // [B][n_stride][288]
   const uint8_t* scales;  // [B][n_stride][36]
   int64_t n_stride;
   const int32_t* idx;     // [Q][K]
   int K;
 };
-struct SwaSource {
-  const uint16_t* rows;   // [B][s_stride][576]
+struct RowSrc {
   int64_t s_stride;
   const int32_t* win_start;
   const int32_t* win_len;
   int n_win;
 };
 
-// Stage Q (bf16 [H][576]) into fp16 rows of the swizzled Q buffer; rows >= H are zero.
-// Loads are issued in batches of 6 per thread before any conversion, so their
-// latencies overlap instead of forming a chain.
-__device__ __forceinline__ void stage_q(uint8_t* smem, const uint16_t* q, int H) {
-  constexpr int kPer = 64 * kChunks / kAttnThreads;  // 18
-  constexpr int kBatch = 6;
-#pragma unroll
-  for (int b0 = 0; b0 < kPer; b0 += kBatch) {
-    uint4 v[kBatch];
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int i = threadIdx.x + (b0 + k) * kAttnThreads;
-      const int row = i / kChunks, ch = i % kChunks;
-      v[k] = row < H ? *reinterpret_cast<const uint4*>(q + (int64_t)row * CSA2_D_KV + ch * 8)
-                     : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int i = threadIdx.x + (b0 + k) * kAttnThreads;
-      const int row = i / kChunks, ch = i % kChunks;
-      uint4 o;
-      o.x = bf16x2_to_h2(v[k].x); o.y = bf16x2_to_h2(v[k].y);
-      o.z = bf16x2_to_h2(v[k].z); o.w = bf16x2_to_h2(v[k].w);
-      *reinterpret_cast<uint4*>(smem + AttnSmem::kQ + swz(row, ch)) = o;
-    }
-  }
+// AND of a predicate over the `n` threads of named barrier `id` (all get the result).
+__device__ __forceinline__ bool named_and(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 
-// Issue the cp.async gather of one FP4 tile (entries [p0, p0+64) of the index list).
-__device__ __forceinline__ void fp4_prefetch(uint8_t* smem, int buf, const Fp4Source& src, int b,
-                                             const int32_t* idx_row, int p0, int p_end,
-                                             uint32_t* status) {
-  uint8_t* stage = smem + AttnSmem::kStage + buf * AttnSmem::kStageBytes;
-  int* valid = reinterpret_cast<int*>(smem + AttnSmem::kValid) + buf * kTE;
-  const uint8_t* cbase = src.codes + (int64_t)b * src.n_stride * CSA2_CODE_BYTES;
-  const uint8_t* sbase = src.scales + (int64_t)b * src.n_stride * CSA2_SCALE_BYTES;
-  if (threadIdx.x < kTE) {
-    const int p = p0 + threadIdx.x;
-    int e = p < p_end ? idx_row[p] : -1;
-    if (e < -1 || e >= src.n_stride) {
-      atomicOr(status, CSA2_DEV_BAD_INDEX);
-      e = -1;
-    }
-    valid[threadIdx.x] = e;
+__device__ __forceinline__ uint32_t cswz(int c, int row, int j) {
+  // byte offset of 16-byte piece j of row `row` in 128-byte-swizzled chunk c
+  return (uint32_t)(c * kCChunk + row * 128 + ((j ^ (row & 7)) << 4));
+}
+
+// Reduce 64 per-thread values over the 128 softmax threads (4 warps): max or sum.
+// Reduce-scatter inside each warp (62 shuffles), then across warps in shared memory.
+template <bool kMax>
+__device__ __forceinline__ void reduce64(const float (&v)[64], Misc& ms, float* out, int lane, int w) {
+  float a[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const bool hi = lane & 16;
+    const float mine = hi ? v[32 + i] : v[i];
+    const float send = hi ? v[i] : v[32 + i];
+    const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+    a[i] = kMax ? fmaxf(mine, got) : mine + got;
   }
+  float b[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const bool hi = lane & 8;
+    const float mine = hi ? a[16 + i] : a[i];
+    const float send = hi ? a[i] : a[16 + i];
+    const float got = __shfl_xor_sync(0xffffffffu, send, 8);
+    b[i] = kMax ? fmaxf(mine, got) : mine + got;
+  }
+  float c[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool hi = lane & 4;
+    const float mine = hi ? b[8 + i] : b[i];
+    const float send = hi ? b[i] : b[8 + i];
+    const float got = __shfl_xor_sync(0xffffffffu, send, 4);
+    c[i] = kMax ? fmaxf(mine, got) : mine + got;
+  }
+  float d[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 2;
+    const float mine = hi ? c[4 + i] : c[i];
+    const float send = hi ? c[i] : c[4 + i];
+    const float got = __shfl_xor_sync(0xffffffffu, send, 2);
+    d[i] = kMax ? fmaxf(mine, got) : mine + got;
+  }
+  float e[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 1;
+    const float mine = hi ? d[2 + i] : d[i];
+    const float send = hi ? d[i] : d[2 + i];
+    const float got = __shfl_xor_sync(0xffffffffu, send, 1);
+    e[i] = kMax ? fmaxf(mine, got) : mine + got;
+  }
+  // lane holds heads base, base+1 with base = 32*b4 + 16*b3 + 8*b2 + 4*b1 + 2*b0
+  const int base = ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 +
+                   ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
+  ms.red[w][base] = e[0];
+  ms.red[w][base + 1] = e[1];
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+  const int t = w * 32 + lane;
+  if (t < 64) {
+    float r = ms.red[0][t];
+#pragma unroll
+    for (int k = 1; k < 4; ++k) r = kMax ? fmaxf(r, ms.red[k][t]) : r + ms.red[k][t];
+    out[t] = r;
+  }
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+template <bool kFp4>
+__global__ void __maxnreg__(224) attn_tc_kernel(
+    const uint16_t* __restrict__ q, Fp4Src fsrc, RowSrc rsrc, const __grid_constant__ CUtensorMap tm_rows,
+    int T, int H, float scale_log2, int nsplit, int split_len, float* __restrict__ partials,
+    uint32_t* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sC = smem + kQBytes;
+  Misc& ms = *reinterpret_cast<Misc*>(smem + kQBytes + kCBytes);
+  const uint32_t uQ = smem_u32(sQ), uC = smem_u32(sC);
+  const uint32_t uP = uC + 8 * kCChunk;
+  auto bar = [&](int i) { return smem_u32(&ms.bars[i]); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sp = blockIdx.x, qi = blockIdx.y, b = qi / T;
+
+  // key range of this CTA
+  int p_begin, p_end;
+  int row_base = 0;  // window rows: first store row of this split (SWA)
+  if (kFp4) {
+    p_begin = sp * split_len;
+    p_end = min(p_begin + split_len, fsrc.K);
+  } else {
+    int ws = rsrc.win_start[qi], wl = rsrc.win_len[qi];
+    if (wl > rsrc.n_win) wl = rsrc.n_win;
+    if (ws < 0 || wl < 0 || (int64_t)ws + wl > rsrc.s_stride) {
+      if (sp == 0 && threadIdx.x == 0) atomicOr(status, CSA2_DEV_BAD_WINDOW);
+      if (wl < 0) wl = 0;
+      if (ws < 0) { wl += ws; ws = 0; if (wl < 0) wl = 0; }
+      if ((int64_t)ws + wl > rsrc.s_stride) wl = (int)(rsrc.s_stride > ws ? rsrc.s_stride - ws : 0);
+    }
+    p_begin = sp * split_len;
+    p_end = min(p_begin + split_len, wl);
+    row_base = (int)((int64_t)b * rsrc.s_stride + ws);
+  }
+  const int ntiles = p_end > p_begin ? (p_end - p_begin + kTK - 1) / kTK : 0;
+  float* part = partials + ((int64_t)qi * nsplit + sp) * H * kPartStride;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kQReady), 128);
+    for (int g = 0; g < 5; ++g) {
+      mbar_init(bar(kChunkFull + g), 128);
+      mbar_init(bar(kGroupFree + g), 1);
+    }
+    mbar_init(bar(kSFull), 1);
+    mbar_init(bar(kSFull + 1), 1);
+    mbar_init(bar(kPFull), 128);
+    mbar_init(bar(kTmaFull), 1);
+    mbar_init(bar(kDrain), 1);
+    ms.abort_flag = 0;
+    ms.vote[0] = ms.vote[1] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 8) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ms.tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
   __syncthreads();
-  for (int i = threadIdx.x; i < kTE * 18; i += kAttnThreads) {
-    const int e = i / 18, c = i % 18;
-    const int ent = valid[e];
-    const uint8_t* g = cbase + (int64_t)(ent < 0 ? 0 : ent) * CSA2_CODE_BYTES + c * 16;
-    cp_async16(smem_u32(stage + e * CSA2_CODE_BYTES + c * 16), g, ent >= 0);
-  }
-  for (int i = threadIdx.x; i < kTE * 9; i += kAttnThreads) {
-    const int e = i / 9, w = i % 9;
-    const int ent = valid[e];
-    const uint8_t* g = sbase + (int64_t)(ent < 0 ? 0 : ent) * CSA2_SCALE_BYTES + w * 4;
-    cp_async4(smem_u32(stage + AttnSmem::kStageCodes + e * CSA2_SCALE_BYTES + w * 4), g, ent >= 0);
-  }
-}
+  tc_fence_after();
+  const uint32_t tmem = ms.tmem_base;
+  volatile int* abort_flag = &ms.abort_flag;
+  auto fail = [&]() {
+    atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+    *abort_flag = 1;
+  };
 
-// FP4 stage -> fp16 C tile (exact: e2m1 * e4m3 fits fp16).
-__device__ __forceinline__ void fp4_dequant(uint8_t* smem, int buf) {
-  const uint8_t* stage = smem + AttnSmem::kStage + buf * AttnSmem::kStageBytes;
-  for (int i = threadIdx.x; i < kTE * 36; i += kAttnThreads) {
-    const int e = i / 36, bk = i % 36;
-    const uint2 cw = *reinterpret_cast<const uint2*>(stage + e * CSA2_CODE_BYTES + bk * 8);
-    const uint32_t s2 = e4m3_to_h2(stage[AttnSmem::kStageCodes + e * CSA2_SCALE_BYTES + bk]);
-    uint32_t h[8];
-    e2m1x4_to_h2x2(cw.x & 0xFFFFu, h[0], h[1]);
-    e2m1x4_to_h2x2(cw.x >> 16, h[2], h[3]);
-    e2m1x4_to_h2x2(cw.y & 0xFFFFu, h[4], h[5]);
-    e2m1x4_to_h2x2(cw.y >> 16, h[6], h[7]);
+  if (warp < 4) {
+    // ======================= loaders =======================
+    const int e = threadIdx.x;  // key row within a tile / staging thread
+    // stage Q: bf16 [H][576] -> fp16, K-major swizzled chunks of 64 dims
+    {
+      const uint16_t* qrow = q + (int64_t)qi * H * CSA2_D_KV;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) h[k] = hmul2_u32(h[k], s2);
-    *reinterpret_cast<uint4*>(smem + AttnSmem::kC + swz(e, 2 * bk)) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(smem + AttnSmem::kC + swz(e, 2 * bk + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-  }
-}
-
-// Raw bf16 window rows [r0, r0+64) (clipped to r_end) -> fp16 C tile (batched loads).
-__device__ __forceinline__ void swa_load(uint8_t* smem, const uint16_t* rows, int r0, int r_end) {
-  int* valid = reinterpret_cast<int*>(smem + AttnSmem::kValidSwa);
-  if (threadIdx.x < kTE) valid[threadIdx.x] = (r0 + (int)threadIdx.x < r_end) ? 1 : -1;
-  constexpr int kPer = kTE * kChunks / kAttnThreads;  // 18
-  constexpr int kBatch = 6;
+      for (int b0 = 0; b0 < 36; b0 += 6) {
+        uint4 v[6];
 #pragma unroll
-  for (int b0 = 0; b0 < kPer; b0 += kBatch) {
-    uint4 v[kBatch];
+        for (int k = 0; k < 6; ++k) {
+          const int i = e + (b0 + k) * 128;
+          const int h = i / 72, pc = i % 72;
+          v[k] = h < H ? *reinterpret_cast<const uint4*>(qrow + (int64_t)h * CSA2_D_KV + pc * 8)
+                       : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int i = threadIdx.x + (b0 + k) * kAttnThreads;
-      const int e = i / kChunks, ch = i % kChunks;
-      v[k] = (r0 + e < r_end) ? *reinterpret_cast<const uint4*>(rows + (int64_t)(r0 + e) * CSA2_D_KV + ch * 8)
-                              : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < 6; ++k) {
+          const int i = e + (b0 + k) * 128;
+          const int h = i / 72, pc = i % 72;
+          uint4 o;
+          o.x = bf16x2_to_h2(v[k].x); o.y = bf16x2_to_h2(v[k].y);
+          o.z = bf16x2_to_h2(v[k].z); o.w = bf16x2_to_h2(v[k].w);
+          *reinterpret_cast<uint4*>(sQ + (pc >> 3) * kQChunk + h * 128 + (((pc & 7) ^ (h & 7)) << 4)) = o;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kQReady));
     }
+    if (kFp4) {
+      const uint8_t* cbase = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
+      const uint8_t* sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
+      const int32_t* idx_row = fsrc.idx + (int64_t)qi * fsrc.K;
+      uint4 cw[18];
+      uint32_t sw[9];
+      int ent = -1;
+      auto load_tile = [&](int t) {
+        const int p = p_begin + t * kTK + e;
+        ent = p < p_end ? idx_row[p] : -1;
+        if (ent < -1 || ent >= fsrc.n_stride) {
+          atomicOr(status, CSA2_DEV_BAD_INDEX);
+          ent = -1;
+        }
+        if (ent >= 0) {
+          const uint4* cp = reinterpret_cast<const uint4*>(cbase + (int64_t)ent * CSA2_CODE_BYTES);
+          const uint32_t* spt = reinterpret_cast<const uint32_t*>(sbase + (int64_t)ent * CSA2_SCALE_BYTES);
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int i = threadIdx.x + (b0 + k) * kAttnThreads;
-      const int e = i / kChunks, ch = i % kChunks;
-      uint4 o;
-      o.x = bf16x2_to_h2(v[k].x); o.y = bf16x2_to_h2(v[k].y);
-      o.z = bf16x2_to_h2(v[k].z); o.w = bf16x2_to_h2(v[k].w);
-      *reinterpret_cast<uint4*>(smem + AttnSmem::kC + swz(e, ch)) = o;
-    }
-  }
-}
-
-// Per-warp running state of the online softmax for 16 heads x 256 value dims.
-struct WarpAcc {
-  float o[32][4];
-  float m0, m1;   // running max (log2 domain) of rows g, g+8
-  float l0, l1;   // running (thread-partial) sums
-};
-
-// Phase A: S = (Q . C^T) * scale_log2 for heads 16hg.. and keys 32eh.. -> S exchange.
-__device__ __forceinline__ void phase_qk(uint8_t* smem, const int* valid, float scale_log2) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hg = warp & 3, eh = warp >> 2;
-  const int g = lane >> 2, tig = lane & 3;
-  const uint32_t qb = smem_u32(smem + AttnSmem::kQ);
-  const uint32_t cb = smem_u32(smem + AttnSmem::kC);
-  float acc[4][4];
+          for (int k = 0; k < 18; ++k) cw[k] = __ldg(cp + k);
 #pragma unroll
-  for (int n = 0; n < 4; ++n)
+          for (int k = 0; k < 9; ++k) sw[k] = __ldg(spt + k);
+        } else {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[n][k] = 0.f;
-  const int arow = hg * 16 + (lane & 15);
-  const int brow0 = eh * 32 + (lane & 7) + ((lane >> 4) << 3);
-#pragma unroll 4
-  for (int j = 0; j < 36; ++j) {
-    uint32_t a0, a1, a2, a3;
-    ldsm_x4(qb + swz(arow, 2 * j + (lane >> 4)), a0, a1, a2, a3);
+          for (int k = 0; k < 18; ++k) cw[k] = make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int np = 0; np < 2; ++np) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(cb + swz(brow0 + np * 16, 2 * j + ((lane >> 3) & 1)), b0, b1, b2, b3);
-      mma_f16(acc[2 * np], a0, a1, a2, a3, b0, b1);
-      mma_f16(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-    }
-  }
-  float* Sx = reinterpret_cast<float*>(smem + AttnSmem::kS);
+          for (int k = 0; k < 9; ++k) sw[k] = 0u;
+        }
+      };
+      if (ntiles > 0) load_tile(0);
+      bool lok = true;
+      for (int t = 0; t < ntiles && lok; ++t) {
+        if (*abort_flag) break;
 #pragma unroll
-  for (int n = 0; n < 4; ++n) {
-    const int e = eh * 32 + n * 8 + 2 * tig;
-    const bool v0 = valid[e] >= 0, v1 = valid[e + 1] >= 0;
-    float2 r0 = make_float2(v0 ? acc[n][0] * scale_log2 : -INFINITY, v1 ? acc[n][1] * scale_log2 : -INFINITY);
-    float2 r1 = make_float2(v0 ? acc[n][2] * scale_log2 : -INFINITY, v1 ? acc[n][3] * scale_log2 : -INFINITY);
-    *reinterpret_cast<float2*>(Sx + (hg * 16 + g) * kSxStride + e) = r0;
-    *reinterpret_cast<float2*>(Sx + (hg * 16 + g + 8) * kSxStride + e) = r1;
-  }
-}
-
-// Phases B and C: online softmax of the tile's scores and O += P . V.
-__device__ __forceinline__ void phase_softmax_pv(uint8_t* smem, WarpAcc& A) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hg = warp & 3, dh = warp >> 2;
-  const int g = lane >> 2, tig = lane & 3;
-  const float* Sx = reinterpret_cast<const float*>(smem + AttnSmem::kS);
-  float s[8][4];
+        for (int g = 0; g < 5; ++g) {
+          if (lok && t > 0 && !mbar_wait(bar(kGroupFree + g), (t - 1) & 1)) { fail(); lok = false; }
+          if (lok) {
+            if (g == 0) ms.valid[t & 1][e] = ent;
+            const int blk0 = g < 4 ? 8 * g : 32, nblk = g < 4 ? 8 : 4;
 #pragma unroll
-  for (int n = 0; n < 8; ++n) {
-    float2 r0 = *reinterpret_cast<const float2*>(Sx + (hg * 16 + g) * kSxStride + n * 8 + 2 * tig);
-    float2 r1 = *reinterpret_cast<const float2*>(Sx + (hg * 16 + g + 8) * kSxStride + n * 8 + 2 * tig);
-    s[n][0] = r0.x; s[n][1] = r0.y; s[n][2] = r1.x; s[n][3] = r1.y;
-  }
-  float mx0 = -INFINITY, mx1 = -INFINITY;
+            for (int kb = 0; kb < nblk; ++kb) {
+              const int blk = blk0 + kb;
+              // 16 codes of block blk: bytes [8 blk, 8 blk + 8) of the row
+              const uint4 w4 = cw[blk >> 1];
+              const uint32_t lo = (blk & 1) ? w4.z : w4.x, hi = (blk & 1) ? w4.w : w4.y;
+              const uint32_t s2 = e4m3_to_h2((sw[blk >> 2] >> (8 * (blk & 3))) & 0xFFu);
+              uint32_t hv[8];
+              e2m1x4_to_h2x2(lo & 0xFFFFu, hv[0], hv[1]);
+              e2m1x4_to_h2x2(lo >> 16, hv[2], hv[3]);
+              e2m1x4_to_h2x2(hi & 0xFFFFu, hv[4], hv[5]);
+              e2m1x4_to_h2x2(hi >> 16, hv[6], hv[7]);
 #pragma unroll
-  for (int n = 0; n < 8; ++n) {
-    mx0 = fmaxf(mx0, fmaxf(s[n][0], s[n][1]));
-    mx1 = fmaxf(mx1, fmaxf(s[n][2], s[n][3]));
-  }
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-  const float mn0 = fmaxf(A.m0, mx0), mn1 = fmaxf(A.m1, mx1);
-  const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-  const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-  const float al0 = exp2f(A.m0 - mu0), al1 = exp2f(A.m1 - mu1);
-  A.m0 = mn0;
-  A.m1 = mn1;
-  float ps0 = 0.f, ps1 = 0.f;
-  uint32_t pa[4][4];
-#pragma unroll
-  for (int n = 0; n < 8; ++n) {
-    const float p0 = exp2f(s[n][0] - mu0), p1 = exp2f(s[n][1] - mu0);
-    const float p2 = exp2f(s[n][2] - mu1), p3 = exp2f(s[n][3] - mu1);
-    ps0 += p0 + p1;
-    ps1 += p2 + p3;
-    pa[n >> 1][(n & 1) * 2 + 0] = pack_h2(p0, p1);
-    pa[n >> 1][(n & 1) * 2 + 1] = pack_h2(p2, p3);
-  }
-  A.l0 = A.l0 * al0 + ps0;
-  A.l1 = A.l1 * al1 + ps1;
-#pragma unroll
-  for (int n = 0; n < 32; ++n) {
-    A.o[n][0] *= al0; A.o[n][1] *= al0;
-    A.o[n][2] *= al1; A.o[n][3] *= al1;
-  }
-  const uint32_t cb = smem_u32(smem + AttnSmem::kC);
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    const int erow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-    for (int cc = 0; cc < 16; ++cc) {
-      const int ch = dh * 32 + 2 * cc + (lane >> 4);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(cb + swz(erow, ch), b0, b1, b2, b3);
-      // pa[kk] = {rows g k0-7 (n=2kk), rows g+8 k0-7, rows g k8-15 (n=2kk+1), rows g+8 k8-15}
-      mma_f16(A.o[2 * cc], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b0, b1);
-      mma_f16(A.o[2 * cc + 1], pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], b2, b3);
-    }
-  }
-}
-
-// Write this CTA's partial (unnormalised O, max, sum) for its 16 heads x 256 dims.
-__device__ __forceinline__ void write_partial(float* part, int H, WarpAcc& A) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hg = warp & 3, dh = warp >> 2;
-  const int g = lane >> 2, tig = lane & 3;
-  float l0 = A.l0, l1 = A.l1;
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const int h0 = hg * 16 + g, h1 = h0 + 8;
-  constexpr int kPS = kDV + 2;
-#pragma unroll
-  for (int n = 0; n < 32; ++n) {
-    const int d = dh * 256 + n * 8 + 2 * tig;
-    if (h0 < H) *reinterpret_cast<float2*>(part + h0 * kPS + d) = make_float2(A.o[n][0], A.o[n][1]);
-    if (h1 < H) *reinterpret_cast<float2*>(part + h1 * kPS + d) = make_float2(A.o[n][2], A.o[n][3]);
-  }
-  if (dh == 0 && tig == 0) {
-    if (h0 < H) { part[h0 * kPS + kDV] = A.m0; part[h0 * kPS + kDV + 1] = l0; }
-    if (h1 < H) { part[h1 * kPS + kDV] = A.m1; part[h1 * kPS + kDV + 1] = l1; }
-  }
-}
-
-__device__ __forceinline__ void init_acc(WarpAcc& A) {
-#pragma unroll
-  for (int n = 0; n < 32; ++n) A.o[n][0] = A.o[n][1] = A.o[n][2] = A.o[n][3] = 0.f;
-  A.m0 = A.m1 = -INFINITY;
-  A.l0 = A.l1 = 0.f;
-}
-
-// grid: (nsplit, Q). Partials: [Q][nsplit][H][514].
-__global__ void __launch_bounds__(kAttnThreads, 1) sparse_attn_partial_kernel(
-    const uint16_t* __restrict__ q, Fp4Source src, int T, int H, float scale_log2, int nsplit,
-    int split_len, float* __restrict__ partials, uint32_t* __restrict__ status) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int sp = blockIdx.x, qi = blockIdx.y, b = qi / T;
-  stage_q(smem, q + (int64_t)qi * H * CSA2_D_KV, H);
-  const int p_begin = sp * split_len;
-  const int p_end = min(p_begin + split_len, src.K);
-  const int ntiles = p_end > p_begin ? (p_end - p_begin + kTE - 1) / kTE : 0;
-  const int32_t* idx_row = src.idx + (int64_t)qi * src.K;
-  WarpAcc A;
-  init_acc(A);
-  if (ntiles > 0) {
-    fp4_prefetch(smem, 0, src, b, idx_row, p_begin, p_end, status);
-    cp_async_commit();
-  }
-  for (int it = 0; it < ntiles; ++it) {
-    const int buf = it & 1;
-    if (it + 1 < ntiles) {
-      fp4_prefetch(smem, buf ^ 1, src, b, idx_row, p_begin + (it + 1) * kTE, p_end, status);
-      cp_async_commit();
-      cp_async_wait<1>();
+              for (int k = 0; k < 8; ++k) hv[k] = hmul2_u32(hv[k], s2);
+              const int c = blk >> 2, j = (blk & 3) * 2;
+              *reinterpret_cast<uint4*>(sC + cswz(c, e, j)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+              *reinterpret_cast<uint4*>(sC + cswz(c, e, j + 1)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kChunkFull + g));
+          }
+        }
+        if (lok && t + 1 < ntiles) load_tile(t + 1);
+      }
     } else {
-      cp_async_wait<0>();
+      int issued_t = -1, waited_t = -1;
+      for (int t = 0; t < ntiles; ++t) {
+        if (*abort_flag) break;
+        if (t > 0 && !mbar_wait(bar(kGroupFree + 4), (t - 1) & 1)) { fail(); break; }
+        if (e == 0) {
+          mbar_arrive_expect_tx(bar(kTmaFull), 9 * kCChunk);
+          for (int c = 0; c < 9; ++c)
+            tma_load_2d(uC + c * kCChunk, &tm_rows, 64 * c, row_base + p_begin + t * kTK, bar(kTmaFull));
+          issued_t = t;
+        }
+        const int key = p_begin + t * kTK + e;
+        ms.valid[t & 1][e] = key < p_end ? 1 : -1;
+        if (!mbar_wait(bar(kTmaFull), t & 1)) { fail(); break; }
+        waited_t = t;
+        // bf16 -> fp16 in place, one row per thread
+        for (int g = 0; g < 5; ++g) {
+          const int c0 = g < 4 ? 2 * g : 8, nc = g < 4 ? 2 : 1;
+          for (int cc = 0; cc < nc; ++cc) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint4* pp = reinterpret_cast<uint4*>(sC + cswz(c0 + cc, e, j));
+              uint4 v = *pp;
+              v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
+              v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
+              *pp = v;
+            }
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(kChunkFull + g));
+        }
+      }
+      // copies in flight must land before the CTA exits
+      if (e == 0 && issued_t > waited_t) mbar_wait(bar(kTmaFull), issued_t & 1);
     }
-    __syncthreads();
-    fp4_dequant(smem, buf);
-    __syncthreads();
-    phase_qk(smem, reinterpret_cast<const int*>(smem + AttnSmem::kValid) + buf * kTE, scale_log2);
-    __syncthreads();
-    phase_softmax_pv(smem, A);
+  } else if (warp < 8) {
+    // ======================= softmax =======================
+    const int w = warp - 4;          // TMEM lane quarter
+    const int ts = w * 32 + lane;    // key row (S^T lane) / value dim row (O^T lane)
+    const uint32_t lane_off = (uint32_t)(w * 32) << 16;
+    float l[64];
+#pragma unroll
+    for (int h = 0; h < 64; ++h) l[h] = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int sb = t & 1;
+      bool got = !*abort_flag && mbar_wait(bar(kSFull + sb), (t >> 1) & 1) &&
+                 mbar_wait(bar(kChunkFull + 4), t & 1);
+      if (!named_and(1, 128, got)) { if (ts == 0) fail(); ok = false; break; }
+      tc_fence_after();
+      float s[64];
+      {
+        uint32_t r[64];
+        tmem_ld32(tmem + lane_off + kColS + 64 * sb, r);
+        tmem_ld32(tmem + lane_off + kColS + 64 * sb + 32, r + 32);
+        tmem_wait_ld();
+        const bool vld = ms.valid[sb][ts] >= 0;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) s[h] = vld ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
+      }
+      if (t == 0) {
+        reduce64<true>(s, ms, ms.mrun, lane, w);
+      } else {
+        bool need = false;
+#pragma unroll
+        for (int h = 0; h < 64; ++h) need |= s[h] > ms.mrun[h] + kRescale;
+        if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&ms.vote[sb], 1);
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        const bool rescale = ms.vote[sb] != 0;
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (ts == 0) ms.vote[sb] = 0;
+        if (rescale) {
+          reduce64<true>(s, ms, ms.mnew, lane, w);
+          // O^T must be final for tile t-1 before it is rescaled
+          if (!named_and(1, 128, mbar_wait(bar(kGroupFree + 4), (t - 1) & 1))) {
+            if (ts == 0) fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (ts < 64) {
+            const float mo = ms.mrun[ts], mn = fmaxf(mo, ms.mnew[ts]);
+            ms.alpha[ts] = mo == mn ? 1.f : exp2f(mo - mn);
+          }
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+          for (int h = 0; h < 64; ++h) l[h] *= ms.alpha[h];
+          for (int i = 0; i < 8; ++i) {
+            uint32_t r[32];
+            const uint32_t ta = tmem + lane_off + kColO + 32 * i;
+            tmem_ld32(ta, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              r[k] = __float_as_uint(__uint_as_float(r[k]) * ms.alpha[(32 * i + k) & 63]);
+            tmem_st32(ta, r);
+          }
+          tmem_wait_st();
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+          if (ts < 64) ms.mrun[ts] = fmaxf(ms.mrun[ts], ms.mnew[ts]);
+          asm volatile("bar.sync 1, 128;" ::: "memory");
+        }
+      }
+      // P^T row of this key: exp2(s - m), fp16, over the rope chunk (QK of this tile is done)
+      uint32_t pk[32];
+#pragma unroll
+      for (int h = 0; h < 64; h += 2) {
+        const float m0 = ms.mrun[h], m1 = ms.mrun[h + 1];
+        const float p0 = exp2f(s[h] - (m0 == -INFINITY ? 0.f : m0));
+        const float p1 = exp2f(s[h + 1] - (m1 == -INFINITY ? 0.f : m1));
+        l[h] += p0;
+        l[h + 1] += p1;
+        pk[h >> 1] = pack_h2(p0, p1);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(sC + cswz(8, ts, j)) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(kPFull));
+    }
+    // ---- epilogue: partial O (unnormalised), max and sum per head
+    if (ok && ntiles > 0) {
+      ok = named_and(1, 128, mbar_wait(bar(kGroupFree + 4), (ntiles - 1) & 1));
+      if (!ok && ts == 0) fail();
+    }
+    reduce64<false>(l, ms, ms.mnew, lane, w);
+    if (ok && ntiles > 0) {
+      tc_fence_after();
+      for (int i = 0; i < 8; ++i) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + kColO + 32 * i, r);
+        tmem_wait_ld();
+        const int d = 128 * (i >> 1) + ts, h0 = 32 * (i & 1);
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (h0 + k < H) part[(h0 + k) * kPartStride + d] = __uint_as_float(r[k]);
+      }
+    } else {
+      for (int i = 0; i < 4; ++i)
+        for (int h = 0; h < H; ++h) part[h * kPartStride + 128 * i + ts] = 0.f;
+    }
+    if (ts < H) {
+      const bool has = ok && ntiles > 0;
+      part[ts * kPartStride + kDV] = has ? ms.mrun[ts] : -INFINITY;
+      part[ts * kPartStride + kDV + 1] = has ? ms.mnew[ts] : 0.f;
+    }
+  } else {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(kTK, 64, 0, 0, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_f16(kTK, 64, 0, 0, 1, 1);
+      bool issued = false;
+      bool ok = mbar_wait(bar(kQReady), 0);
+      if (!ok) fail();
+      for (int t = 0; t < ntiles && ok; ++t) {
+        if (*abort_flag) break;
+        const int sb = t & 1;
+        const uint32_t d_s = tmem + kColS + 64 * sb;
+        for (int g = 0; g < 5 && ok; ++g) {
+          if (!mbar_wait(bar(kChunkFull + g), t & 1)) { fail(); ok = false; break; }
+          tc_fence_after();
+          const int c0 = g < 4 ? 2 * g : 8, nc = g < 4 ? 2 : 1;
+          for (int cc = 0; cc < nc; ++cc) {
+            const int c = c0 + cc;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t a = umma_desc_sw128(uC + c * kCChunk + 32 * k);
+              const uint64_t bq = umma_desc_sw128(uQ + c * kQChunk + 32 * k);
+              umma_f16(d_s, a, bq, idesc_qk, (c | k) != 0);
+              issued = true;
+            }
+          }
+        }
+        if (!ok) break;
+        umma_commit(bar(kSFull + sb));
+        if (!mbar_wait(bar(kPFull), t & 1)) { fail(); ok = false; break; }
+        tc_fence_after();
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int kk = 0; kk < kTK / 16; ++kk) {
+            const uint64_t a = umma_desc_sw128_mn(uC + 2 * i * kCChunk + kk * 2048, kCChunk, 1024);
+            const uint64_t bp = umma_desc_sw128_mn(uP + kk * 2048, kCChunk, 1024);
+            umma_f16(tmem + kColO + 64 * i, a, bp, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(bar(kGroupFree + i));
+        }
+        umma_commit(bar(kGroupFree + 4));
+      }
+      if (issued) {
+        umma_commit(bar(kDrain));
+        mbar_wait(bar(kDrain), 0);
+      }
+    }
   }
-  write_partial(partials + ((int64_t)qi * nsplit + sp) * H * (kDV + 2), H, A);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  }
 }
 
-// grid: (nsplit, Q); split sp covers window rows [sp*64, sp*64+64).
-__global__ void __launch_bounds__(kAttnThreads, 1) swa_attn_partial_kernel(
-    const uint16_t* __restrict__ q, SwaSource src, int T, int H, float scale_log2, int nsplit,
-    float* __restrict__ partials, uint32_t* __restrict__ status) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int sp = blockIdx.x, qi = blockIdx.y, b = qi / T;
-  int ws = src.win_start[qi], wl = src.win_len[qi];
-  if (wl > src.n_win) wl = src.n_win;
-  if (ws < 0 || wl < 0 || (int64_t)ws + wl > src.s_stride) {
-    if (sp == 0 && threadIdx.x == 0) atomicOr(status, CSA2_DEV_BAD_WINDOW);
-    if (wl < 0) wl = 0;
-    if (ws < 0) { wl += ws; ws = 0; if (wl < 0) wl = 0; }
-    if ((int64_t)ws + wl > src.s_stride) wl = (int)(src.s_stride > ws ? src.s_stride - ws : 0);
-  }
-  WarpAcc A;
-  init_acc(A);
-  const int r0 = sp * kTE;
-  if (r0 < wl) {
-    stage_q(smem, q + (int64_t)qi * H * CSA2_D_KV, H);
-    swa_load(smem, src.rows + ((int64_t)b * src.s_stride + ws) * CSA2_D_KV, r0, wl);
-    __syncthreads();
-    phase_qk(smem, reinterpret_cast<const int*>(smem + AttnSmem::kValidSwa), scale_log2);
-    __syncthreads();
-    phase_softmax_pv(smem, A);
-  }
-  write_partial(partials + ((int64_t)qi * nsplit + sp) * H * (kDV + 2), H, A);
-}
+}  // namespace
 
 // Merge nsplit partials (and optionally an external normalised branch with
 // natural-log LSE) into normalised O and natural-log LSE. One warp per (query,
@@ -406,21 +567,30 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
   float4 acc[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < nsplit; ++s) {
-    const float ws = __shfl_sync(0xffffffffu, w, s);
-    if (ws == 0.f) continue;
-    const float* p = partials + ((int64_t)(qi * nsplit + s) * H + h) * kPS;
-    float2 x[8];
+  // splits in groups of 4 with all loads of a group issued before the FMAs
+  for (int s0 = 0; s0 < nsplit; s0 += 4) {
+    float4 x[4][4];
+    float ws[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[2 * j] = *reinterpret_cast<const float2*>(p + j * 128 + lane * 4);
-      x[2 * j + 1] = *reinterpret_cast<const float2*>(p + j * 128 + lane * 4 + 2);
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u;
+      ws[u] = __shfl_sync(0xffffffffu, w, s < nsplit ? s : 0);
+      if (s >= nsplit) ws[u] = 0.f;
+      const float* p = partials + ((int64_t)(qi * nsplit + (s < nsplit ? s : 0)) * H + h) * kPS;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 a = *reinterpret_cast<const float2*>(p + j * 128 + lane * 4);
+        const float2 b = *reinterpret_cast<const float2*>(p + j * 128 + lane * 4 + 2);
+        x[u][j] = make_float4(a.x, a.y, b.x, b.y);
+      }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[j].x += ws * x[2 * j].x; acc[j].y += ws * x[2 * j].y;
-      acc[j].z += ws * x[2 * j + 1].x; acc[j].w += ws * x[2 * j + 1].y;
-    }
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        acc[j].x += ws[u] * x[u][j].x; acc[j].y += ws[u] * x[u][j].y;
+        acc[j].z += ws[u] * x[u][j].z; acc[j].w += ws[u] * x[u][j].w;
+      }
   }
   const float we = __shfl_sync(0xffffffffu, w, 31);
   if (o_ext && we > 0.f) {
@@ -445,8 +615,12 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(
   if (lane == 0 && lse_out) lse_out[(int64_t)qi * H + h] = L > 0.f ? (Mu + log2f(L)) * kLn2 : -INFINITY;
 }
 
-static cudaError_t set_smem(int slot, const void* fn, int bytes) {
-  return set_attr_once(slot, fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+
+static cudaError_t launch_combine(const float* partials, int nsplit, int Q, int H, const float* o_ext,
+                                  const float* lse_ext, float* o_out, float* lse_out, cudaStream_t st) {
+  attn_combine_kernel<<<dim3((H + 7) / 8, Q), 256, 0, st>>>(partials, nsplit, H, o_ext, lse_ext, o_out,
+                                                            lse_out);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t* codes,
@@ -455,18 +629,20 @@ cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t
                                int nsplit, uint32_t* status, cudaStream_t st) {
   const int Q = B * T;
   if (Q == 0) return cudaSuccess;
-  cudaError_t e = set_smem(2, (const void*)sparse_attn_partial_kernel, AttnSmem::kTotalFp4);
+  cudaError_t e = set_attr_once(2, (const void*)attn_tc_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTC);
   if (e != cudaSuccess) return e;
   int split_len = (K + nsplit - 1) / nsplit;
-  split_len = (split_len + kTE - 1) / kTE * kTE;
-  Fp4Source src{codes, scales, n_stride, idx, K};
-  sparse_attn_partial_kernel<<<dim3(nsplit, Q), kAttnThreads, AttnSmem::kTotalFp4, st>>>(
-      static_cast<const uint16_t*>(q), src, T, H, scale_log2, nsplit, split_len, partials, status);
+  split_len = (split_len + kTK - 1) / kTK * kTK;
+  Fp4Src f{codes, scales, n_stride, idx, K};
+  RowSrc r{0, nullptr, nullptr, 0};
+  CUtensorMap dummy;
+  memset(&dummy, 0, sizeof(dummy));
+  attn_tc_kernel<true><<<dim3(nsplit, Q), kThreadsTC, kSmemTC, st>>>(
+      static_cast<const uint16_t*>(q), f, r, dummy, T, H, scale_log2, nsplit, split_len, partials, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3((H + 7) / 8, Q), 256, 0, st>>>(partials, nsplit, H, nullptr,
-                                                              nullptr, o_g, lse_g);
-  return cudaGetLastError();
+  return launch_combine(partials, nsplit, Q, H, nullptr, nullptr, o_g, lse_g, st);
 }
 
 cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa,
@@ -476,17 +652,24 @@ cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa
                              cudaStream_t st) {
   const int Q = B * T;
   if (Q == 0) return cudaSuccess;
-  cudaError_t e = set_smem(3, (const void*)swa_attn_partial_kernel, AttnSmem::kTotalSwa);
-  if (e != cudaSuccess) return e;
   const int nsplit = swa_splits(n_win);
-  SwaSource src{static_cast<const uint16_t*>(swa), s_stride, win_start, win_len, n_win};
-  swa_attn_partial_kernel<<<dim3(nsplit, Q), kAttnThreads, AttnSmem::kTotalSwa, st>>>(
-      static_cast<const uint16_t*>(q), src, T, H, scale_log2, nsplit, partials, status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_combine_kernel<<<dim3((H + 7) / 8, Q), 256, 0, st>>>(partials, nsplit, H, o_g, lse_g,
-                                                              o_out, lse_out);
-  return cudaGetLastError();
+  if (n_win > 0 && s_stride > 0) {
+    cudaError_t e = set_attr_once(3, (const void*)attn_tc_kernel<false>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTC);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tm;
+    if (!encode_tensor_map_2d_bf16(&tm, swa, CSA2_D_KV, (uint64_t)B * s_stride, 64, kTK))
+      return cudaErrorInvalidValue;
+    Fp4Src f{nullptr, nullptr, 0, nullptr, 0};
+    RowSrc r{s_stride, win_start, win_len, n_win};
+    attn_tc_kernel<false><<<dim3(nsplit, Q), kThreadsTC, kSmemTC, st>>>(
+        static_cast<const uint16_t*>(q), f, r, tm, T, H, scale_log2, nsplit, kTK, partials, status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_combine(partials, nsplit, Q, H, o_g, lse_g, o_out, lse_out, st);
+  }
+  // empty window: the merge is the global branch itself
+  return launch_combine(partials, 0, Q, H, o_g, lse_g, o_out, lse_out, st);
 }
 
 }  // namespace csa2

@@ -1,6 +1,8 @@
 // C ABI of libcsa2: host-side validation, workspace checks and dispatch.
 // Every entry point validates on the host and launches nothing on a failed
 // check; kernels are enqueued on the caller's stream and nothing is allocated.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "csa2_internal.cuh"
@@ -36,10 +38,41 @@ cudaError_t set_attr_once(int slot, const void* fn, cudaFuncAttribute attr, int 
   return e;
 }
 
+// cuTensorMapEncodeTiled is reached through the runtime's driver entry point,
+// so the library does not link against the driver library.
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                               uint32_t box_inner, uint32_t box_outer) {
+  auto encode = encode_tiled_fn();
+  if (encode == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int attn_splits(int64_t Q, int K, int n_sm) {
   if (Q <= 0) return 1;
   int64_t s = n_sm / Q;                  // at most one wave of one-CTA-per-SM blocks
-  int64_t max_by_k = (K + 127) / 128;    // at least two 64-key tiles per split
+  int64_t max_by_k = (K + 127) / 128;    // at least one 128-key tile per split
   if (s > max_by_k) s = max_by_k;
   if (s > kMaxSplits) s = kMaxSplits;
   if (s < 1) s = 1;

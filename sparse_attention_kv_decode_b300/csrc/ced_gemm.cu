@@ -20,10 +20,6 @@
 // Every mbarrier wait is bounded; a wait that gives up sets a status bit, the
 // CTA stops issuing work, drains what it started and frees its TMEM.
 #include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "csa2_internal.cuh"
 
 namespace csa2 {
@@ -40,59 +36,6 @@ constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kGroupM = 16;                     // m-tiles per raster group
 constexpr size_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
-
-// Shared-memory matrix descriptor: K-major operand written by TMA with the
-// 128-byte swizzle, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)1u << 16;              // leading byte offset (unused with 128B swizzle, K-major)
-  d |= (uint64_t)(1024u >> 4) << 32;    // stride byte offset: next 8-row group
-  d |= (uint64_t)1u << 46;              // descriptor version
-  d |= (uint64_t)2u << 61;              // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   mbar)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 
 struct TileMap {
   int m_tiles, n_tiles, total;
@@ -317,36 +260,6 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
   }
 }
 
-// cuTensorMapEncodeTiled is reached through the runtime's driver entry point,
-// so the library does not link against the driver library.
-PFN_cuTensorMapEncodeTiled_v12000 encode_tiled_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-  auto encode = encode_tiled_fn();
-  if (encode == nullptr) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-                                      dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_ced_project(const void* h, int64_t rows, int d_model, const void* w_kv,
@@ -355,9 +268,9 @@ cudaError_t launch_ced_project(const void* h, int64_t rows, int d_model, const v
   if (rows <= 0 || n_layers <= 0) return cudaSuccess;
   if (rows > (int64_t)1 << 30) return cudaErrorInvalidValue;
   CUtensorMap ta, tkv, tz;
-  if (!make_map(&ta, h, (uint64_t)d_model, (uint64_t)rows, kBM) ||
-      !make_map(&tkv, w_kv, (uint64_t)d_model, (uint64_t)n_layers * CSA2_D_KV, 64) ||
-      !make_map(&tz, w_z, (uint64_t)d_model, (uint64_t)n_layers * CSA2_D_IDX, 64))
+  if (!encode_tensor_map_2d_bf16(&ta, h, (uint64_t)d_model, (uint64_t)rows, kBK, kBM) ||
+      !encode_tensor_map_2d_bf16(&tkv, w_kv, (uint64_t)d_model, (uint64_t)n_layers * CSA2_D_KV, kBK, 64) ||
+      !encode_tensor_map_2d_bf16(&tz, w_z, (uint64_t)d_model, (uint64_t)n_layers * CSA2_D_IDX, kBK, 64))
     return cudaErrorInvalidValue;
   cudaError_t e = set_attr_once(4, (const void*)ced_proj_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);

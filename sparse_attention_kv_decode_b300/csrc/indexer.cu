@@ -23,7 +23,8 @@ namespace csa2 {
 // A persistent kernel streams the keys through a ring of shared-memory stages
 // filled by bulk copies (one 16 KB stage = 128 keys of one query), so each SM
 // keeps ~200 KB of key reads in flight with a single issuing thread. The stages
-// of all queries form one list that CTAs walk with a grid stride.
+// of all queries form one list; each CTA takes a contiguous, balanced range of
+// it, so it stays on one query (and one stretch of keys) for many stages.
 //
 // Each consumer warp scores 16 keys of a stage with four m16n8k16 bf16 MMAs per
 // group of 8 indexer heads. Thread (g = lane/4, tig = lane%4) takes, for key
@@ -98,23 +99,25 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
     return k <= 0 ? 0 : (k > kStageKeys ? kStageKeys : (int)k);
   };
 
+  const int gs_begin = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
+  const int gs_end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
   bool ok = true;
-  int prod_gs = blockIdx.x;   // next stage id the producer will consider
+  int prod_gs = gs_begin;     // next stage id the producer will consider
   int prod_n = 0;             // stages produced so far (ring position)
   auto produce_next = [&]() {
-    while (prod_gs < total) {
+    while (prod_gs < gs_end) {
       int qi;
       int64_t key0;
       const int keys = stage_keys(prod_gs, qi, key0);
       const int gs = prod_gs;
-      prod_gs += gridDim.x;
+      prod_gs += 1;
       if (keys == 0) continue;
       const int slot = prod_n % kScoreStages;
       if (prod_n >= kScoreStages) {
         if (!mbar_wait(bar_empty + 8 * slot, ((prod_n / kScoreStages) - 1) & 1)) {
           atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
           ok = false;
-          prod_gs = total;
+          prod_gs = gs_end;
           return;
         }
       }
@@ -135,7 +138,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
   float wv[NT][2];
   int cur_q = -1;
   int cons_n = 0;
-  for (int gs = blockIdx.x; gs < total; gs += gridDim.x) {
+  for (int gs = gs_begin; gs < gs_end; ++gs) {
     int qi;
     int64_t key0;
     const int keys = stage_keys(gs, qi, key0);
@@ -346,9 +349,22 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   float* outs = out_scores ? out_scores + (int64_t)qi * K : nullptr;
   const float* srow = scores + (int64_t)qi * score_stride + my0;
 
-  for (int e = tid; e < my_len; e += kSelThreads) {
-    sc[e] = srow[e];
-    state[e] = (nvis <= K) ? 1 : 0;
+  // batched loads (8 in flight per thread) so their latencies overlap
+  for (int e0 = 0; e0 < my_len; e0 += 8 * kSelThreads) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = e0 + k * kSelThreads + tid;
+      v[k] = e < my_len ? srow[e] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = e0 + k * kSelThreads + tid;
+      if (e < my_len) {
+        sc[e] = v[k];
+        state[e] = (nvis <= K) ? 1 : 0;
+      }
+    }
   }
   __syncthreads();
 
