@@ -182,6 +182,10 @@ CSA2_API int csa2_read_device_status(void* ws, void* stream, uint32_t* flags);
 /* Static text for a csa2_status value. */
 CSA2_API const char* csa2_status_string(int status);
 
+/* Text of the last CUDA error a call on this thread turned into CSA2_ERR_CUDA
+ * (static storage; "no error" before the first one). */
+CSA2_API const char* csa2_last_cuda_error(void);
+
 /* Library ABI version (major * 100 + minor). */
 CSA2_API int csa2_version(void);
 

@@ -42,7 +42,10 @@ _LIB = None
 class Csa2Error(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {STATUS.get(status, status)} ({_lib().csa2_status_string(status).decode()})")
+        msg = f"{what}: {STATUS.get(status, status)} ({_lib().csa2_status_string(status).decode()})"
+        if status == 4:
+            msg += f": {_lib().csa2_last_cuda_error().decode()}"
+        super().__init__(msg)
 
 
 def _lib():
@@ -64,6 +67,8 @@ def _lib():
     L.csa2_status_string.argtypes = [i32]
     L.csa2_status_string.restype = ctypes.c_char_p
     L.csa2_version.argtypes = []
+    L.csa2_last_cuda_error.argtypes = []
+    L.csa2_last_cuda_error.restype = ctypes.c_char_p
     for fn in ("csa2_encode_kv", "csa2_index_topk", "csa2_sparse_decode", "csa2_swa_merge",
                "csa2_workspace_init", "csa2_read_device_status", "csa2_version"):
         getattr(L, fn).restype = ctypes.c_int

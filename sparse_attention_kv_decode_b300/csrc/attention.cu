@@ -95,73 +95,73 @@ __device__ __forceinline__ uint32_t cswz(int c, int row, int j) {
   return (uint32_t)(c * kCChunk + row * 128 + ((j ^ (row & 7)) << 4));
 }
 
-// Reduce 64 per-thread values over the 128 softmax threads (4 warps): max or sum.
-// Reduce-scatter inside each warp (62 shuffles), then across warps in shared memory.
+// Reduce 32 per-thread values (heads h0..h0+31) over the 128 softmax threads
+// (4 warps), max or sum, into out[h0 .. h0+31]. Reduce-scatter inside each warp
+// (31 shuffles: lane ends with one head), then across the warps in shared
+// memory. All 128 threads must call it (named barrier 1).
 template <bool kMax>
-__device__ __forceinline__ void reduce64(const float (&v)[64], Misc& ms, float* out, int lane, int w) {
-  float a[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const bool hi = lane & 16;
-    const float mine = hi ? v[32 + i] : v[i];
-    const float send = hi ? v[i] : v[32 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 16);
-    a[i] = kMax ? fmaxf(mine, got) : mine + got;
-  }
-  float b[16];
+__device__ __forceinline__ float red_op(float a, float b) { return kMax ? fmaxf(a, b) : a + b; }
+
+template <bool kMax>
+__device__ __forceinline__ void reduce32(const float (&v)[32], Misc& ms, float* out, int h0, int lane,
+                                         int w) {
+  float a[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const bool hi = lane & 8;
-    const float mine = hi ? a[16 + i] : a[i];
-    const float send = hi ? a[i] : a[16 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 8);
-    b[i] = kMax ? fmaxf(mine, got) : mine + got;
+    const bool hi = lane & 16;
+    const float got = __shfl_xor_sync(0xffffffffu, hi ? v[i] : v[16 + i], 16);
+    a[i] = red_op<kMax>(hi ? v[16 + i] : v[i], got);
   }
-  float c[8];
+  float b[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const bool hi = lane & 4;
-    const float mine = hi ? b[8 + i] : b[i];
-    const float send = hi ? b[i] : b[8 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 4);
-    c[i] = kMax ? fmaxf(mine, got) : mine + got;
+    const bool hi = lane & 8;
+    const float got = __shfl_xor_sync(0xffffffffu, hi ? a[i] : a[8 + i], 8);
+    b[i] = red_op<kMax>(hi ? a[8 + i] : a[i], got);
   }
-  float d[4];
+  float c[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const bool hi = lane & 2;
-    const float mine = hi ? c[4 + i] : c[i];
-    const float send = hi ? c[i] : c[4 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 2);
-    d[i] = kMax ? fmaxf(mine, got) : mine + got;
+    const bool hi = lane & 4;
+    const float got = __shfl_xor_sync(0xffffffffu, hi ? b[i] : b[4 + i], 4);
+    c[i] = red_op<kMax>(hi ? b[4 + i] : b[i], got);
   }
-  float e[2];
+  float d[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const bool hi = lane & 1;
-    const float mine = hi ? d[2 + i] : d[i];
-    const float send = hi ? d[i] : d[2 + i];
-    const float got = __shfl_xor_sync(0xffffffffu, send, 1);
-    e[i] = kMax ? fmaxf(mine, got) : mine + got;
+    const bool hi = lane & 2;
+    const float got = __shfl_xor_sync(0xffffffffu, hi ? c[i] : c[2 + i], 2);
+    d[i] = red_op<kMax>(hi ? c[2 + i] : c[i], got);
   }
-  // lane holds heads base, base+1 with base = 32*b4 + 16*b3 + 8*b2 + 4*b1 + 2*b0
-  const int base = ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 +
-                   ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
-  ms.red[w][base] = e[0];
-  ms.red[w][base + 1] = e[1];
+  const bool hi = lane & 1;
+  const float got = __shfl_xor_sync(0xffffffffu, hi ? d[0] : d[1], 1);
+  const float e = red_op<kMax>(hi ? d[1] : d[0], got);
+  // lane holds head index 16*b4 + 8*b3 + 4*b2 + 2*b1 + b0 of the 32
+  const int idx = ((lane >> 4) & 1) * 16 + ((lane >> 3) & 1) * 8 + ((lane >> 2) & 1) * 4 +
+                  ((lane >> 1) & 1) * 2 + (lane & 1);
+  ms.red[w][h0 + idx] = e;
   asm volatile("bar.sync 1, 128;" ::: "memory");
   const int t = w * 32 + lane;
-  if (t < 64) {
-    float r = ms.red[0][t];
+  if (t < 32) {
+    float r = ms.red[0][h0 + t];
 #pragma unroll
-    for (int k = 1; k < 4; ++k) r = kMax ? fmaxf(r, ms.red[k][t]) : r + ms.red[k][t];
-    out[t] = r;
+    for (int k = 1; k < 4; ++k) r = red_op<kMax>(r, ms.red[k][h0 + t]);
+    out[h0 + t] = r;
   }
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// Scaled, masked scores of this thread's key row for heads h0..h0+31 (from S^T in TMEM).
+__device__ __forceinline__ void load_scores32(uint32_t taddr, bool valid, float scale_log2, float (&s)[32]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_wait_ld();
+#pragma unroll
+  for (int h = 0; h < 32; ++h) s[h] = valid ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
+}
+
 template <bool kFp4>
-__global__ void __maxnreg__(224) attn_tc_kernel(
+__global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     const uint16_t* __restrict__ q, Fp4Src fsrc, RowSrc rsrc, const __grid_constant__ CUtensorMap tm_rows,
     int T, int H, float scale_log2, int nsplit, int split_len, float* __restrict__ partials,
     uint32_t* __restrict__ status) {
@@ -363,7 +363,7 @@ __global__ void __maxnreg__(224) attn_tc_kernel(
     const int w = warp - 4;          // TMEM lane quarter
     const int ts = w * 32 + lane;    // key row (S^T lane) / value dim row (O^T lane)
     const uint32_t lane_off = (uint32_t)(w * 32) << 16;
-    float l[64];
+    float l[64];                     // running sums of this key row's p, per head
 #pragma unroll
     for (int h = 0; h < 64; ++h) l[h] = 0.f;
     bool ok = true;
@@ -373,29 +373,36 @@ __global__ void __maxnreg__(224) attn_tc_kernel(
                  mbar_wait(bar(kChunkFull + 4), t & 1);
       if (!named_and(1, 128, got)) { if (ts == 0) fail(); ok = false; break; }
       tc_fence_after();
-      float s[64];
-      {
-        uint32_t r[64];
-        tmem_ld32(tmem + lane_off + kColS + 64 * sb, r);
-        tmem_ld32(tmem + lane_off + kColS + 64 * sb + 32, r + 32);
-        tmem_wait_ld();
-        const bool vld = ms.valid[sb][ts] >= 0;
-#pragma unroll
-        for (int h = 0; h < 64; ++h) s[h] = vld ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
-      }
+      const bool vld = ms.valid[sb][ts] >= 0;
+      const uint32_t ts_addr = tmem + lane_off + kColS + 64 * sb;
       if (t == 0) {
-        reduce64<true>(s, ms, ms.mrun, lane, w);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float s[32];
+          load_scores32(ts_addr + 32 * hh, vld, scale_log2, s);
+          reduce32<true>(s, ms, ms.mrun, 32 * hh, lane, w);
+        }
       } else {
         bool need = false;
 #pragma unroll
-        for (int h = 0; h < 64; ++h) need |= s[h] > ms.mrun[h] + kRescale;
+        for (int hh = 0; hh < 2; ++hh) {
+          float s[32];
+          load_scores32(ts_addr + 32 * hh, vld, scale_log2, s);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) need |= s[h] > ms.mrun[32 * hh + h] + kRescale;
+        }
         if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&ms.vote[sb], 1);
         asm volatile("bar.sync 1, 128;" ::: "memory");
         const bool rescale = ms.vote[sb] != 0;
         asm volatile("bar.sync 1, 128;" ::: "memory");
         if (ts == 0) ms.vote[sb] = 0;
         if (rescale) {
-          reduce64<true>(s, ms, ms.mnew, lane, w);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            float s[32];
+            load_scores32(ts_addr + 32 * hh, vld, scale_log2, s);
+            reduce32<true>(s, ms, ms.mnew, 32 * hh, lane, w);
+          }
           // O^T must be final for tile t-1 before it is rescaled
           if (!named_and(1, 128, mbar_wait(bar(kGroupFree + 4), (t - 1) & 1))) {
             if (ts == 0) fail();
@@ -426,21 +433,27 @@ __global__ void __maxnreg__(224) attn_tc_kernel(
           asm volatile("bar.sync 1, 128;" ::: "memory");
         }
       }
-      // P^T row of this key: exp2(s - m), fp16, over the rope chunk (QK of this tile is done)
-      uint32_t pk[32];
+      // P^T row of this key: exp2(s - m) in fp16, written over the rope chunk (the S^T
+      // product of this tile has consumed it)
 #pragma unroll
-      for (int h = 0; h < 64; h += 2) {
-        const float m0 = ms.mrun[h], m1 = ms.mrun[h + 1];
-        const float p0 = exp2f(s[h] - (m0 == -INFINITY ? 0.f : m0));
-        const float p1 = exp2f(s[h + 1] - (m1 == -INFINITY ? 0.f : m1));
-        l[h] += p0;
-        l[h + 1] += p1;
-        pk[h >> 1] = pack_h2(p0, p1);
+      for (int hh = 0; hh < 2; ++hh) {
+        float s[32];
+        load_scores32(ts_addr + 32 * hh, vld, scale_log2, s);
+        uint32_t pk[16];
+#pragma unroll
+        for (int h = 0; h < 32; h += 2) {
+          const float m0 = ms.mrun[32 * hh + h], m1 = ms.mrun[32 * hh + h + 1];
+          const float p0 = exp2f(s[h] - (m0 == -INFINITY ? 0.f : m0));
+          const float p1 = exp2f(s[h + 1] - (m1 == -INFINITY ? 0.f : m1));
+          l[32 * hh + h] += p0;
+          l[32 * hh + h + 1] += p1;
+          pk[h >> 1] = pack_h2(p0, p1);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(sC + cswz(8, ts, 4 * hh + j)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<uint4*>(sC + cswz(8, ts, j)) =
-            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kPFull));
@@ -450,7 +463,13 @@ __global__ void __maxnreg__(224) attn_tc_kernel(
       ok = named_and(1, 128, mbar_wait(bar(kGroupFree + 4), (ntiles - 1) & 1));
       if (!ok && ts == 0) fail();
     }
-    reduce64<false>(l, ms, ms.mnew, lane, w);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float v[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) v[h] = l[32 * hh + h];
+      reduce32<false>(v, ms, ms.mnew, 32 * hh, lane, w);
+    }
     if (ok && ntiles > 0) {
       tc_fence_after();
       for (int i = 0; i < 8; ++i) {

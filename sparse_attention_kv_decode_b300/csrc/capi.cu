@@ -90,11 +90,19 @@ static inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) 
     if (!(cond)) return CSA2_ERR_INVALID_ARG; \
   } while (0)
 
-static int cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+static thread_local const char* g_last_cuda_error = "no error";
+
+static int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return CSA2_OK;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return CSA2_ERR_CUDA;
+}
 
 extern "C" {
 
 int csa2_version(void) { return 100; }
+
+const char* csa2_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char* csa2_status_string(int s) {
   switch (s) {
@@ -131,7 +139,7 @@ int csa2_read_device_status(void* ws, void* stream, uint32_t* flags) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, 4, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   if (flags) *flags = v;
   if (v == 0) return CSA2_OK;
   if ((v & ~(CSA2_DEV_TOPK_LEVELS | CSA2_DEV_PIPELINE_TIMEOUT)) == 0) return CSA2_ERR_TIMEOUT;
@@ -197,7 +205,7 @@ int csa2_index_topk(int mode, int B, int T, int H_I, const void* q_idx, const fl
   const int64_t stride = score_pad(n_stride);
   cudaError_t e = launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores,
                                      stride, status, st);
-  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_topk_select(scores, stride, n_visible, (int)Q, n_stride, K, out_idx,
                                         out_scores, status, st));
 }
