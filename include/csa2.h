@@ -114,7 +114,7 @@ CSA2_API int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_mode
  * library's reading: the pages name the indexer but print no formula.
  * q_idx: bf16 [B][T][H_I][64]; w_idx: fp32 [B][T][H_I]; z: bf16
  * [B][n_stride][64]; n_visible: int32 [B*T], each in [0, n_stride].
- * Limits: 1 <= H_I <= 16, 1 <= K <= 4096, n_stride <= 524288.
+ * Limits: 1 <= H_I <= 16, 1 <= K <= 4096, n_stride <= 262144 (1M tokens at 4:1).
  * REUSE: copies prev_idx [B][T][K] to out_idx (nothing to do when they are
  *   the same pointer); q_idx, w_idx, z, n_visible and out_scores are ignored.
  * ws: at least csa2_workspace_bytes(B, T, *, n_stride, K) bytes, prepared

@@ -49,7 +49,7 @@ constexpr int kSmemTC = 1024 + kQBytes + kCBytes + kMiscBytes;
 
 // mbarrier slots (8 bytes each) in the misc area
 enum Bar { kQReady = 0, kChunkFull = 1, kGroupFree = 6, kSFull = 11, kPFull = 13, kTmaFull = 14,
-           kDrain = 15, kNumBars = 16 };
+           kDrain = 15, kQTma = 16, kNumBars = 17 };
 
 struct Misc {
   uint64_t bars[kNumBars];
@@ -162,9 +162,9 @@ __device__ __forceinline__ void load_scores32(uint32_t taddr, bool valid, float 
 
 template <bool kFp4>
 __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
-    const uint16_t* __restrict__ q, Fp4Src fsrc, RowSrc rsrc, const __grid_constant__ CUtensorMap tm_rows,
-    int T, int H, float scale_log2, int nsplit, int split_len, float* __restrict__ partials,
-    uint32_t* __restrict__ status) {
+    const __grid_constant__ CUtensorMap tm_q, Fp4Src fsrc, RowSrc rsrc,
+    const __grid_constant__ CUtensorMap tm_rows, int T, int H, float scale_log2, int nsplit,
+    int split_len, float* __restrict__ partials, uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     mbar_init(bar(kPFull), 128);
     mbar_init(bar(kTmaFull), 1);
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kQTma), 1);
     ms.abort_flag = 0;
     ms.vote[0] = ms.vote[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -235,32 +236,31 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
   if (warp < 4) {
     // ======================= loaders =======================
     const int e = threadIdx.x;  // key row within a tile / staging thread
-    // stage Q: bf16 [H][576] -> fp16, K-major swizzled chunks of 64 dims
-    {
-      const uint16_t* qrow = q + (int64_t)qi * H * CSA2_D_KV;
-#pragma unroll
-      for (int b0 = 0; b0 < 36; b0 += 6) {
-        uint4 v[6];
-#pragma unroll
-        for (int k = 0; k < 6; ++k) {
-          const int i = e + (b0 + k) * 128;
-          const int h = i / 72, pc = i % 72;
-          v[k] = h < H ? *reinterpret_cast<const uint4*>(qrow + (int64_t)h * CSA2_D_KV + pc * 8)
-                       : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < 6; ++k) {
-          const int i = e + (b0 + k) * 128;
-          const int h = i / 72, pc = i % 72;
-          uint4 o;
-          o.x = bf16x2_to_h2(v[k].x); o.y = bf16x2_to_h2(v[k].y);
-          o.z = bf16x2_to_h2(v[k].z); o.w = bf16x2_to_h2(v[k].w);
-          *reinterpret_cast<uint4*>(sQ + (pc >> 3) * kQChunk + h * 128 + (((pc & 7) ^ (h & 7)) << 4)) = o;
-        }
+    // Q (bf16 rows qi*H .. qi*H+63) arrives by TMA in nine 64x64 swizzled boxes and is
+    // converted to fp16 in place; rows past H belong to other queries (or are zero) and
+    // only feed heads that are never written out.
+    if (e == 0) {
+      mbar_arrive_expect_tx(bar(kQTma), 9 * kQChunk);
+      for (int c = 0; c < 9; ++c) tma_load_2d(uQ + c * kQChunk, &tm_q, 64 * c, qi * H, bar(kQTma));
+    }
+    bool q_ok = true;
+    auto convert_q = [&]() {
+      q_ok = mbar_wait(bar(kQTma), 0);
+      if (!q_ok) { fail(); return; }
+      // 64 rows x 72 pieces: thread e converts rows e/2 (half e&1 of the pieces)
+      const int h = e >> 1;
+#pragma unroll 4
+      for (int k = 0; k < 36; ++k) {
+        const int pc = (e & 1) * 36 + k;
+        uint4* pp = reinterpret_cast<uint4*>(sQ + (pc >> 3) * kQChunk + h * 128 + (((pc & 7) ^ (h & 7)) << 4));
+        uint4 v = *pp;
+        v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
+        v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
+        *pp = v;
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(kQReady));
-    }
+    };
     if (kFp4) {
       const uint8_t* cbase = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
       const uint8_t* sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         }
       };
       if (ntiles > 0) load_tile(0);
-      bool lok = true;
+      convert_q();
+      bool lok = q_ok;
       for (int t = 0; t < ntiles && lok; ++t) {
         if (*abort_flag) break;
 #pragma unroll
@@ -325,7 +326,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       }
     } else {
       int issued_t = -1, waited_t = -1;
-      for (int t = 0; t < ntiles; ++t) {
+      convert_q();
+      for (int t = 0; t < ntiles && q_ok; ++t) {
         if (*abort_flag) break;
         if (t > 0 && !mbar_wait(bar(kGroupFree + 4), (t - 1) & 1)) { fail(); break; }
         if (e == 0) {
@@ -358,6 +360,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       // copies in flight must land before the CTA exits
       if (e == 0 && issued_t > waited_t) mbar_wait(bar(kTmaFull), issued_t & 1);
     }
+    if (e == 0 && !q_ok) mbar_wait(bar(kQTma), 0);
   } else if (warp < 8) {
     // ======================= softmax =======================
     const int w = warp - 4;          // TMEM lane quarter
@@ -655,10 +658,11 @@ cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t
   split_len = (split_len + kTK - 1) / kTK * kTK;
   Fp4Src f{codes, scales, n_stride, idx, K};
   RowSrc r{0, nullptr, nullptr, 0};
-  CUtensorMap dummy;
+  CUtensorMap tq, dummy;
   memset(&dummy, 0, sizeof(dummy));
+  if (!encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64)) return cudaErrorInvalidValue;
   attn_tc_kernel<true><<<dim3(nsplit, Q), kThreadsTC, kSmemTC, st>>>(
-      static_cast<const uint16_t*>(q), f, r, dummy, T, H, scale_log2, nsplit, split_len, partials, status);
+      tq, f, r, dummy, T, H, scale_log2, nsplit, split_len, partials, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_combine(partials, nsplit, Q, H, nullptr, nullptr, o_g, lse_g, st);
@@ -676,13 +680,14 @@ cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa
     cudaError_t e = set_attr_once(3, (const void*)attn_tc_kernel<false>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTC);
     if (e != cudaSuccess) return e;
-    CUtensorMap tm;
-    if (!encode_tensor_map_2d_bf16(&tm, swa, CSA2_D_KV, (uint64_t)B * s_stride, 64, kTK))
+    CUtensorMap tm, tq;
+    if (!encode_tensor_map_2d_bf16(&tm, swa, CSA2_D_KV, (uint64_t)B * s_stride, 64, kTK) ||
+        !encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64))
       return cudaErrorInvalidValue;
     Fp4Src f{nullptr, nullptr, 0, nullptr, 0};
     RowSrc r{s_stride, win_start, win_len, n_win};
     attn_tc_kernel<false><<<dim3(nsplit, Q), kThreadsTC, kSmemTC, st>>>(
-        static_cast<const uint16_t*>(q), f, r, tm, T, H, scale_log2, nsplit, kTK, partials, status);
+        tq, f, r, tm, T, H, scale_log2, nsplit, kTK, partials, status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_combine(partials, nsplit, Q, H, o_g, lse_g, o_out, lse_out, st);

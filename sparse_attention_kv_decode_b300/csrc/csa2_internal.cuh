@@ -23,7 +23,7 @@ constexpr size_t kWsHeader = 256;
 constexpr int kMaxSplits = 16;
 constexpr int kScoreTile = 1024;  // keys per indexer CTA
 constexpr int kMaxK = 4096;
-constexpr int64_t kMaxNStride = 524288;
+constexpr int64_t kMaxNStride = 262144;  // 1M tokens at 4:1
 constexpr int kMaxWin = 256;
 constexpr int kPartStride = 514;  // floats per (query, split, head) partial: O[512], m, l
 

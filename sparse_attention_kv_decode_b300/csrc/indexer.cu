@@ -246,7 +246,8 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
 // The bin map floor((s - lo) * kNB / (hi - lo)) is monotone in s, so bins
 // never reorder scores; equal scores always share a bin.
 constexpr int kSelThreads = 512;
-constexpr int kNB = 512;            // histogram bins per refinement round
+constexpr int kNBMax = 2048;        // histogram bins per refinement round (small clusters)
+constexpr int kNBMin = 512;         // (clusters of more than 4 CTAs)
 constexpr int kCandCap = 512;       // candidates resolved exactly by ranking
 constexpr int kMaxLevels = 12;
 constexpr int kMaxCluster = 16;
@@ -258,10 +259,9 @@ struct SelRec {
 };
 
 struct SelShared {
-  uint32_t hist_in[kMaxCluster][kNB];   // pushed histograms
   SelRec rec_in[kMaxCluster];           // pushed candidate statistics
   int sel_in[kMaxCluster];              // pushed selected counts
-  uint32_t hist_local[kNB];
+  uint32_t hist_local[kNBMax];
   int scan[kSelThreads / 32];
   float red_f[2][kSelThreads / 32];
   int red_i[kSelThreads / 32];
@@ -269,13 +269,14 @@ struct SelShared {
   float cand_s[kCandCap];               // own candidates (compacted)
   int cand_i[kCandCap];
 };
-// followed in dynamic shared memory by: float cand_in_s[C][kCandCap], int cand_in_i[C][kCandCap],
-// float sc[slice_cap], uint8_t state[slice_cap]
+// followed in dynamic shared memory by: uint32_t hist_in[C][NB] (pushed histograms),
+// float cand_in_s[C][kCandCap], int cand_in_i[C][kCandCap], float sc[slice_cap],
+// uint8_t state[slice_cap]
 
-__device__ __forceinline__ int bin_of(float s, float lo, float scl) {
+__device__ __forceinline__ int bin_of(float s, float lo, float scl, int nb) {
   float t = (s - lo) * scl;
   int bi = (int)t;
-  return bi < 0 ? 0 : (bi > kNB - 1 ? kNB - 1 : bi);
+  return bi < 0 ? 0 : (bi > nb - 1 ? nb - 1 : bi);
 }
 
 // Block-wide exclusive scan of one int per thread; returns the prefix, writes the total.
@@ -331,7 +332,9 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   uint32_t C, r;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  float* cand_in_s = reinterpret_cast<float*>(smem_raw + sizeof(SelShared));
+  const int NB = C <= 4 ? kNBMax : kNBMin;
+  uint32_t* hist_in = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SelShared));
+  float* cand_in_s = reinterpret_cast<float*>(hist_in + C * NB);
   int* cand_in_i = reinterpret_cast<int*>(cand_in_s + C * kCandCap);
   float* sc = reinterpret_cast<float*>(cand_in_i + C * kCandCap);
   uint8_t* state = reinterpret_cast<uint8_t*>(sc + slice_cap);
@@ -478,27 +481,43 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
         break;
       }
       // ---- round 1: histogram refinement over [glo, ghi]
-      const float scl = (float)kNB / (ghi - glo);
-      for (int i = tid; i < kNB; i += kSelThreads) sh.hist_local[i] = 0u;
+      const float scl = (float)NB / (ghi - glo);
+      for (int i = tid; i < NB; i += kSelThreads) sh.hist_local[i] = 0u;
       __syncthreads();
       for (int e = tid; e < my_len; e += kSelThreads)
-        if (state[e] == 0) atomicAdd(&sh.hist_local[bin_of(sc[e], glo, scl)], 1u);
+        if (state[e] == 0) atomicAdd(&sh.hist_local[bin_of(sc[e], glo, scl, NB)], 1u);
       __syncthreads();
-      for (int j = tid; j < (int)C * (kNB / 4); j += kSelThreads) {
-        const int peer = j / (kNB / 4), q4 = j % (kNB / 4);
-        st_remote_v4(&sh.hist_in[r][4 * q4], peer, *reinterpret_cast<const uint4*>(&sh.hist_local[4 * q4]));
+      for (int j = tid; j < (int)C * (NB / 4); j += kSelThreads) {
+        const int peer = j / (NB / 4), q4 = j % (NB / 4);
+        st_remote_v4(&hist_in[r * NB + 4 * q4], peer, *reinterpret_cast<const uint4*>(&sh.hist_local[4 * q4]));
       }
       cluster_barrier();
       {
-        // thread t owns bin kNB-1-t (kNB == kSelThreads): suffix counts from the top bin
-        const int bb = kNB - 1 - tid;
-        uint32_t h = 0;
-        for (int rr = 0; rr < (int)C; ++rr) h += sh.hist_in[rr][bb];
+        // thread t owns bins NB-1-per*t .. NB-per*(t+1) (per = NB/kSelThreads): suffix counts from the top
+        const int per = NB / kSelThreads;
+        const int btop = NB - 1 - per * tid;
+        uint32_t hs[kNBMax / kSelThreads];
+        int mine = 0;
+#pragma unroll
+        for (int k = 0; k < kNBMax / kSelThreads; ++k) {
+          uint32_t h = 0;
+          if (k < per)
+            for (int rr = 0; rr < (int)C; ++rr) h += hist_in[rr * NB + btop - k];
+          hs[k] = h;
+          mine += (int)h;
+        }
         int total;
-        const int above = block_excl_scan((int)h, sh.scan, total);
-        if (above < remaining && remaining <= above + (int)h) {
-          sh.bstar = bb;
-          sh.above = above;
+        int above = block_excl_scan(mine, sh.scan, total);
+#pragma unroll
+        for (int k = 0; k < kNBMax / kSelThreads; ++k) {
+          if (k < per) {
+            const int h = (int)hs[k];
+            if (above < remaining && remaining <= above + h) {
+              sh.bstar = btop - k;
+              sh.above = above;
+            }
+            above += h;
+          }
         }
       }
       __syncthreads();
@@ -506,7 +525,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
       remaining -= sh.above;
       for (int e = tid; e < my_len; e += kSelThreads)
         if (state[e] == 0) {
-          const int bi = bin_of(sc[e], glo, scl);
+          const int bi = bin_of(sc[e], glo, scl, NB);
           state[e] = bi > bstar ? 1 : (bi < bstar ? 2 : 0);
         }
       __syncthreads();
@@ -545,7 +564,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
 }
 
 static int select_cluster_size(int64_t n_stride) {
-  int64_t per = (n_stride + 4095) / 4096;
+  int64_t per = (n_stride + 8191) / 8192;
   int c = 1;
   while (c < per && c < kMaxCluster) c <<= 1;
   return c;
@@ -554,12 +573,14 @@ static int select_cluster_size(int64_t n_stride) {
 cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
                                int Q, int64_t n_stride, int K, int32_t* out_idx, float* out_scores,
                                uint32_t* status, cudaStream_t st) {
-  static_assert(kNB == kSelThreads, "one histogram bin per thread");
+  static_assert(kNBMax % kSelThreads == 0 && kNBMin % kSelThreads == 0, "bins per thread");
   if (Q == 0) return cudaSuccess;
   const int C = select_cluster_size(n_stride);
+  const int NB = C <= 4 ? kNBMax : kNBMin;
   int slice_cap = (int)((n_stride + C - 1) / C);
   slice_cap = (slice_cap + 15) & ~15;
-  const size_t smem = sizeof(SelShared) + (size_t)C * kCandCap * 8 + (size_t)slice_cap * 5;
+  const size_t smem = sizeof(SelShared) + (size_t)C * NB * 4 + (size_t)C * kCandCap * 8 +
+                      (size_t)slice_cap * 5;
   if (smem > kSelSmemMax) return cudaErrorInvalidValue;
   cudaError_t e = set_attr_once(0, (const void*)topk_select_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemMax);
