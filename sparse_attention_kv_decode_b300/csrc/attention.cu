@@ -25,6 +25,8 @@
 //   warp 8     TMEM allocation and the single-thread MMA issuer
 // Partials (unnormalised O, max, sum per head) of every split are merged by the
 // combine kernel, which also folds in the global branch for the SWA merge.
+#include <cstddef>
+
 #include "csa2_internal.cuh"
 
 namespace csa2 {
@@ -53,7 +55,7 @@ enum Bar { kQReady = 0, kChunkFull = 1, kGroupFree = 6, kSFull = 11, kPFull = 13
 
 struct Misc {
   uint64_t bars[kNumBars];
-  uint32_t tmem_base;
+  alignas(16) uint32_t tmem_base;
   int abort_flag;
   int vote[2];
   int valid[2][kTK];
@@ -63,6 +65,7 @@ struct Misc {
   float red[4][64];
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc area");
+static_assert(offsetof(Misc, tmem_base) % 16 == 0, "TMEM address slot alignment");
 
 struct Fp4Src {
   const uint8_t* codes;   // [B][n_stride][288]

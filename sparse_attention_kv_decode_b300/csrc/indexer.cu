@@ -269,6 +269,9 @@ struct SelShared {
   float cand_s[kCandCap];               // own candidates (compacted)
   int cand_i[kCandCap];
 };
+// Regions after the header start at a 128-byte boundary (the histogram pushes
+// are 16-byte vector stores).
+constexpr size_t kSelHdr = (sizeof(SelShared) + 127) & ~size_t(127);
 // followed in dynamic shared memory by: uint32_t hist_in[C][NB] (pushed histograms),
 // float cand_in_s[C][kCandCap], int cand_in_i[C][kCandCap], float sc[slice_cap],
 // uint8_t state[slice_cap]
@@ -327,13 +330,13 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ n_visible,
     int64_t n_stride, int K, int slice_cap, int32_t* __restrict__ out_idx,
     float* __restrict__ out_scores, uint32_t* __restrict__ status) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
   uint32_t C, r;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   const int NB = C <= 4 ? kNBMax : kNBMin;
-  uint32_t* hist_in = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SelShared));
+  uint32_t* hist_in = reinterpret_cast<uint32_t*>(smem_raw + kSelHdr);
   float* cand_in_s = reinterpret_cast<float*>(hist_in + C * NB);
   int* cand_in_i = reinterpret_cast<int*>(cand_in_s + C * kCandCap);
   float* sc = reinterpret_cast<float*>(cand_in_i + C * kCandCap);
@@ -579,7 +582,7 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
   const int NB = C <= 4 ? kNBMax : kNBMin;
   int slice_cap = (int)((n_stride + C - 1) / C);
   slice_cap = (slice_cap + 15) & ~15;
-  const size_t smem = sizeof(SelShared) + (size_t)C * NB * 4 + (size_t)C * kCandCap * 8 +
+  const size_t smem = kSelHdr + (size_t)C * NB * 4 + (size_t)C * kCandCap * 8 +
                       (size_t)slice_cap * 5;
   if (smem > kSelSmemMax) return cudaErrorInvalidValue;
   cudaError_t e = set_attr_once(0, (const void*)topk_select_kernel,
