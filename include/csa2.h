@@ -165,7 +165,10 @@ CSA2_API int csa2_swa_merge(int B, int T, int H, const void* q,
                    int d_v, float softmax_scale, const float* o_g, const float* lse_g,
                    float* o_out, float* lse_out, void* ws, size_t ws_bytes, void* stream);
 
-/* Workspace bytes that cover every call above with these or smaller sizes. */
+/* Workspace bytes that cover every call above with these or smaller sizes: a
+ * 256-byte header (the device status word) plus the fp32 indexer scores of
+ * csa2_index_topk ([B*T][n_max rounded up to 1024]). The attention calls need
+ * only the header. One workspace serves one stream at a time. */
 CSA2_API size_t csa2_workspace_bytes(int B, int T, int H, int64_t n_max, int K);
 
 /* Zero the workspace's status word and counters (once after allocation). */

@@ -16,15 +16,21 @@
 // bf16 window rows are converted), V = C[:, 0:512], and both products read the
 // same 128-byte-swizzled shared-memory tile. S^T (two buffers) and the four
 // 128x64 O^T accumulators live in TMEM.
+//
 // Warp roles (288 threads):
-//   warps 0-3  loaders: stage Q; per tile, gather + dequantise one key row per
-//              thread (FP4) or convert TMA-loaded window rows (bf16)
-//   warps 4-7  softmax: one key row (TMEM lane) per thread; running max per head
-//              kept lazily (rescale only when a score exceeds it by 2^8), P^T
-//              written over the rope chunk of C once the S^T product has read it
-//   warp 8     TMEM allocation and the single-thread MMA issuer
-// Partials (unnormalised O, max, sum per head) of every split are merged by the
-// combine kernel, which also folds in the global branch for the SWA merge.
+//   warps 0-7  workers. Thread (warp w, lane) owns key row / TMEM lane
+//              32*(w%4)+lane and head half w/4: it dequantises half of its key
+//              row (FP4 gather prefetched one tile ahead in registers, or bf16
+//              rows landed by TMA), and runs the softmax for 32 heads of it:
+//              a lazy running max per head (rescale only when a score exceeds
+//              it by 2^8), p written as fp16 P^T over the rope chunk of C once
+//              the S^T product has read it.
+//   warp 8     TMEM allocation and the single-thread MMA issuer.
+// The splits of one query form a thread-block cluster. After the last P.V each
+// CTA pushes its (max, sum) per head and its unnormalised O^T rows to the CTA
+// that owns those value dims (distributed shared memory stores into the freed
+// tile buffer); each CTA then merges every split's contribution for its dims
+// (and, for the SWA merge, the global branch) and writes normalised O and LSE.
 #include <cstddef>
 
 #include "csa2_internal.cuh"
@@ -32,7 +38,6 @@
 namespace csa2 {
 
 constexpr int kDV = 512;
-static_assert(kPartStride == kDV + 2, "partial layout");
 
 namespace {
 
@@ -41,15 +46,22 @@ constexpr int kQChunk = 64 * 128;        // 64 heads x 64 dims fp16
 constexpr int kCChunk = kTK * 128;       // 128 keys x 64 dims fp16
 constexpr int kQBytes = 9 * kQChunk;
 constexpr int kCBytes = 9 * kCChunk;
-constexpr int kThreadsTC = 288;
+constexpr int kWorkers = 256;
+constexpr int kThreadsTC = kWorkers + 32;
 constexpr int kTmemCols = 512;
 constexpr int kColS = 0;                 // S^T buffers at columns [0, 64) and [64, 128)
 constexpr int kColO = 128;               // O^T M-tile i at columns [128 + 64 i, +64)
 constexpr float kRescale = 8.0f;         // lazy-max slack, log2 units (factor 256)
 constexpr int kMiscBytes = 4096;
 constexpr int kSmemTC = 1024 + kQBytes + kCBytes + kMiscBytes;
+constexpr int kMaxSplitsTC = 16;
+// merge buffers inside the (finished) tile buffer
+constexpr int kRecvStride = 68;          // floats per received O^T row (64 heads + pad)
+constexpr int kRecvBytes = kDV * kRecvStride * 4;                    // 139,264
+constexpr int kMlOffset = kRecvBytes;                                // [split][2][64] floats
+static_assert(kRecvBytes + kMaxSplitsTC * 2 * 64 * 4 <= kCBytes, "merge buffers fit the tile");
 
-// mbarrier slots (8 bytes each) in the misc area
+// mbarrier slots (8 bytes each)
 enum Bar { kQReady = 0, kChunkFull = 1, kGroupFree = 6, kSFull = 11, kPFull = 13, kTmaFull = 14,
            kDrain = 15, kQTma = 16, kNumBars = 17 };
 
@@ -57,11 +69,12 @@ struct Misc {
   uint64_t bars[kNumBars];
   alignas(16) uint32_t tmem_base;
   int abort_flag;
-  int vote[2];
-  int valid[2][kTK];
-  float mrun[64];
+  int vote[2][2];          // [head half][tile parity]
+  int valid[2][kTK];       // key validity of the tile, by tile parity
+  float mrun[64];          // running max per head (log2 domain)
   float mnew[64];
   float alpha[64];
+  float lsum[64];
   float red[4][64];
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc area");
@@ -80,6 +93,12 @@ struct RowSrc {
   const int32_t* win_len;
   int n_win;
 };
+struct OutArgs {
+  float* o;               // [Q][H][512]
+  float* lse;             // [Q][H] (nullable)
+  const float* o_ext;     // external normalised branch (SWA merge), nullable
+  const float* lse_ext;
+};
 
 // AND of a predicate over the `n` threads of named barrier `id` (all get the result).
 __device__ __forceinline__ bool named_and(int id, int n, bool v) {
@@ -92,22 +111,42 @@ __device__ __forceinline__ bool named_and(int id, int n, bool v) {
       : "memory");
   return r != 0;
 }
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ uint32_t map_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float a) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(a) : "memory");
+}
 
 __device__ __forceinline__ uint32_t cswz(int c, int row, int j) {
   // byte offset of 16-byte piece j of row `row` in 128-byte-swizzled chunk c
   return (uint32_t)(c * kCChunk + row * 128 + ((j ^ (row & 7)) << 4));
 }
 
-// Reduce 32 per-thread values (heads h0..h0+31) over the 128 softmax threads
-// (4 warps), max or sum, into out[h0 .. h0+31]. Reduce-scatter inside each warp
-// (31 shuffles: lane ends with one head), then across the warps in shared
-// memory. All 128 threads must call it (named barrier 1).
 template <bool kMax>
 __device__ __forceinline__ float red_op(float a, float b) { return kMax ? fmaxf(a, b) : a + b; }
 
+// Reduce 32 per-thread values (heads h0..h0+31) over the 128 threads of one head
+// half (4 warps, lane quarters 0..3), max or sum, into out[h0 .. h0+31].
+// Reduce-scatter inside each warp (31 shuffles), then across the 4 warps in
+// shared memory under named barrier `bid`.
 template <bool kMax>
 __device__ __forceinline__ void reduce32(const float (&v)[32], Misc& ms, float* out, int h0, int lane,
-                                         int w) {
+                                         int quarter, int bid) {
   float a[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -142,19 +181,18 @@ __device__ __forceinline__ void reduce32(const float (&v)[32], Misc& ms, float* 
   // lane holds head index 16*b4 + 8*b3 + 4*b2 + 2*b1 + b0 of the 32
   const int idx = ((lane >> 4) & 1) * 16 + ((lane >> 3) & 1) * 8 + ((lane >> 2) & 1) * 4 +
                   ((lane >> 1) & 1) * 2 + (lane & 1);
-  ms.red[w][h0 + idx] = e;
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-  const int t = w * 32 + lane;
-  if (t < 32) {
-    float r = ms.red[0][h0 + t];
+  ms.red[quarter][h0 + idx] = e;
+  named_sync(bid, 128);
+  if (quarter == 0) {
+    float r = ms.red[0][h0 + lane];
 #pragma unroll
-    for (int k = 1; k < 4; ++k) r = red_op<kMax>(r, ms.red[k][h0 + t]);
-    out[h0 + t] = r;
+    for (int k = 1; k < 4; ++k) r = red_op<kMax>(r, ms.red[k][h0 + lane]);
+    out[h0 + lane] = r;
   }
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  named_sync(bid, 128);
 }
 
-// Scaled, masked scores of this thread's key row for heads h0..h0+31 (from S^T in TMEM).
+// Scaled, masked scores of one key row for 32 heads (from S^T in TMEM).
 __device__ __forceinline__ void load_scores32(uint32_t taddr, bool valid, float scale_log2, float (&s)[32]) {
   uint32_t r[32];
   tmem_ld32(taddr, r);
@@ -162,12 +200,74 @@ __device__ __forceinline__ void load_scores32(uint32_t taddr, bool valid, float 
 #pragma unroll
   for (int h = 0; h < 32; ++h) s[h] = valid ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
 }
+// Same for 16 heads.
+__device__ __forceinline__ void load_scores16(uint32_t taddr, bool valid, float scale_log2, float (&s)[16]) {
+  uint32_t r[16];
+  tmem_ld16(taddr, r);
+  tmem_wait_ld();
+#pragma unroll
+  for (int h = 0; h < 16; ++h) s[h] = valid ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
+}
+
+// Dequantise FP4 blocks [18*HALF, 18*HALF+18) of key row e that fall in chunk
+// group G into C. cw/sw hold the row's code bytes [144*HALF, +144) and the scale
+// bytes from 16*HALF (5 words).
+template <int HALF, int G>
+__device__ __forceinline__ void dequant_group(uint8_t* sC, int e, const uint4 (&cw)[9], const uint32_t (&sw)[5]) {
+  constexpr int g_lo = G < 4 ? 8 * G : 32, g_hi = G < 4 ? 8 * G + 8 : 36;
+  constexpr int h_lo = 18 * HALF, h_hi = 18 * HALF + 18;
+  constexpr int lo = g_lo > h_lo ? g_lo : h_lo, hi_ = g_hi < h_hi ? g_hi : h_hi;
+#pragma unroll
+  for (int blk = lo; blk < hi_; ++blk) {
+    const int rb = blk - h_lo;                       // block within the half row
+    const uint4 w4 = cw[rb >> 1];
+    const uint32_t clo = (rb & 1) ? w4.z : w4.x, chi = (rb & 1) ? w4.w : w4.y;
+    const int sbyte = blk - 16 * HALF;               // byte within the 5 scale words
+    const uint32_t s2 = e4m3_to_h2((sw[sbyte >> 2] >> (8 * (sbyte & 3))) & 0xFFu);
+    uint32_t hv[8];
+    e2m1x4_to_h2x2(clo & 0xFFFFu, hv[0], hv[1]);
+    e2m1x4_to_h2x2(clo >> 16, hv[2], hv[3]);
+    e2m1x4_to_h2x2(chi & 0xFFFFu, hv[4], hv[5]);
+    e2m1x4_to_h2x2(chi >> 16, hv[6], hv[7]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) hv[k] = hmul2_u32(hv[k], s2);
+    const int c = blk >> 2, j = (blk & 3) * 2;
+    *reinterpret_cast<uint4*>(sC + cswz(c, e, j)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    *reinterpret_cast<uint4*>(sC + cswz(c, e, j + 1)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+  }
+}
+
+template <int HALF>
+__device__ __forceinline__ void load_half_row(const uint8_t* cbase, const uint8_t* sbase, int ent,
+                                              uint4 (&cw)[9], uint32_t (&sw)[5]) {
+  if (ent >= 0) {
+    const uint4* cp = reinterpret_cast<const uint4*>(cbase + (int64_t)ent * CSA2_CODE_BYTES) + 9 * HALF;
+    const uint32_t* spt =
+        reinterpret_cast<const uint32_t*>(sbase + (int64_t)ent * CSA2_SCALE_BYTES) + 4 * HALF;
+#pragma unroll
+    for (int k = 0; k < 9; ++k) cw[k] = __ldg(cp + k);
+#pragma unroll
+    for (int k = 0; k < 5; ++k) sw[k] = __ldg(spt + k);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 9; ++k) cw[k] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 5; ++k) sw[k] = 0u;
+  }
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 template <bool kFp4>
 __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, Fp4Src fsrc, RowSrc rsrc,
-    const __grid_constant__ CUtensorMap tm_rows, int T, int H, float scale_log2, int nsplit,
-    int split_len, float* __restrict__ partials, uint32_t* __restrict__ status) {
+    const __grid_constant__ CUtensorMap tm_rows, int T, int H, float scale_log2, int split_len,
+    OutArgs out, uint32_t* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -180,43 +280,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sp = blockIdx.x, qi = blockIdx.y, b = qi / T;
-
-  // key range of this CTA
-  int p_begin, p_end;
-  int row_base = 0;  // window rows: first store row of this split (SWA)
-  if (kFp4) {
-    p_begin = sp * split_len;
-    p_end = min(p_begin + split_len, fsrc.K);
-  } else {
-    int ws = rsrc.win_start[qi], wl = rsrc.win_len[qi];
-    if (wl > rsrc.n_win) wl = rsrc.n_win;
-    if (ws < 0 || wl < 0 || (int64_t)ws + wl > rsrc.s_stride) {
-      if (sp == 0 && threadIdx.x == 0) atomicOr(status, CSA2_DEV_BAD_WINDOW);
-      if (wl < 0) wl = 0;
-      if (ws < 0) { wl += ws; ws = 0; if (wl < 0) wl = 0; }
-      if ((int64_t)ws + wl > rsrc.s_stride) wl = (int)(rsrc.s_stride > ws ? rsrc.s_stride - ws : 0);
-    }
-    p_begin = sp * split_len;
-    p_end = min(p_begin + split_len, wl);
-    row_base = (int)((int64_t)b * rsrc.s_stride + ws);
-  }
-  const int ntiles = p_end > p_begin ? (p_end - p_begin + kTK - 1) / kTK : 0;
-  float* part = partials + ((int64_t)qi * nsplit + sp) * H * kPartStride;
+  uint32_t nsplit;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(nsplit));
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kQReady), 128);
+    mbar_init(bar(kQReady), kWorkers);
     for (int g = 0; g < 5; ++g) {
-      mbar_init(bar(kChunkFull + g), 128);
+      mbar_init(bar(kChunkFull + g), kWorkers);
       mbar_init(bar(kGroupFree + g), 1);
     }
     mbar_init(bar(kSFull), 1);
     mbar_init(bar(kSFull + 1), 1);
-    mbar_init(bar(kPFull), 128);
+    mbar_init(bar(kPFull), kWorkers);
     mbar_init(bar(kTmaFull), 1);
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kQTma), 1);
     ms.abort_flag = 0;
-    ms.vote[0] = ms.vote[1] = 0;
+    ms.vote[0][0] = ms.vote[0][1] = ms.vote[1][0] = ms.vote[1][1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 8) {
@@ -235,26 +315,74 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
     *abort_flag = 1;
   };
+  // Inputs may be written by the preceding kernel in the stream: nothing below
+  // reads global memory before it has completed.
+  grid_dependency_wait();
 
-  if (warp < 4) {
-    // ======================= loaders =======================
-    const int e = threadIdx.x;  // key row within a tile / staging thread
-    // Q (bf16 rows qi*H .. qi*H+63) arrives by TMA in nine 64x64 swizzled boxes and is
-    // converted to fp16 in place; rows past H belong to other queries (or are zero) and
-    // only feed heads that are never written out.
-    if (e == 0) {
+  // key range of this CTA
+  int p_begin, p_end, row_base = 0;
+  if (kFp4) {
+    p_begin = sp * split_len;
+    p_end = min(p_begin + split_len, fsrc.K);
+  } else {
+    int ws = rsrc.win_start[qi], wl = rsrc.win_len[qi];
+    if (wl > rsrc.n_win) wl = rsrc.n_win;
+    if (ws < 0 || wl < 0 || (int64_t)ws + wl > rsrc.s_stride) {
+      if (sp == 0 && threadIdx.x == 0) atomicOr(status, CSA2_DEV_BAD_WINDOW);
+      if (wl < 0) wl = 0;
+      if (ws < 0) { wl += ws; ws = 0; if (wl < 0) wl = 0; }
+      if ((int64_t)ws + wl > rsrc.s_stride) wl = (int)(rsrc.s_stride > ws ? rsrc.s_stride - ws : 0);
+    }
+    p_begin = sp * split_len;
+    p_end = min(p_begin + split_len, wl);
+    row_base = (int)((int64_t)b * rsrc.s_stride + ws);
+  }
+  const int ntiles = p_end > p_begin ? (p_end - p_begin + kTK - 1) / kTK : 0;
+
+  if (warp < 8) {
+    // ======================= workers: loads / dequant + softmax =======================
+    const int quarter = warp & 3, half = warp >> 2;
+    const int e = quarter * 32 + lane;        // key row of a tile; TMEM lane
+    const int wt = threadIdx.x;               // 0..255
+    const int bid = 1 + half;                 // named barrier of this head half
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    bool wok = true;                          // pipeline state (uniform within a head half)
+    // Q: nine 64x64 swizzled TMA boxes (rows qi*H ..), converted to fp16 in place;
+    // rows past H belong to other queries (or are zero) and feed unused heads.
+    if (wt == 0) {
       mbar_arrive_expect_tx(bar(kQTma), 9 * kQChunk);
       for (int c = 0; c < 9; ++c) tma_load_2d(uQ + c * kQChunk, &tm_q, 64 * c, qi * H, bar(kQTma));
     }
-    bool q_ok = true;
-    auto convert_q = [&]() {
-      q_ok = mbar_wait(bar(kQTma), 0);
-      if (!q_ok) { fail(); return; }
-      // 64 rows x 72 pieces: thread e converts rows e/2 (half e&1 of the pieces)
-      const int h = e >> 1;
-#pragma unroll 4
-      for (int k = 0; k < 36; ++k) {
-        const int pc = (e & 1) * 36 + k;
+    // the FP4 gather of tile 0 is issued before the Q conversion so the two overlap
+    const uint8_t* cbase = nullptr;
+    const uint8_t* sbase = nullptr;
+    const int32_t* idx_row = nullptr;
+    uint4 cw[9];
+    uint32_t sw[5];
+    int ent = -1;
+    auto fetch = [&](int t) {
+      const int p = p_begin + t * kTK + e;
+      ent = p < p_end ? idx_row[p] : -1;
+      if (ent < -1 || ent >= fsrc.n_stride) {
+        atomicOr(status, CSA2_DEV_BAD_INDEX);
+        ent = -1;
+      }
+      if (half == 0) load_half_row<0>(cbase, sbase, ent, cw, sw);
+      else load_half_row<1>(cbase, sbase, ent, cw, sw);
+    };
+    if (kFp4) {
+      cbase = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
+      sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
+      idx_row = fsrc.idx + (int64_t)qi * fsrc.K;
+      if (ntiles > 0) fetch(0);
+    }
+    wok = mbar_wait(bar(kQTma), 0);
+    if (!wok) fail();
+    else {
+      const int h = wt >> 2;  // 64 rows x 72 pieces: 4 threads per row, 18 pieces each
+#pragma unroll 6
+      for (int k = 0; k < 18; ++k) {
+        const int pc = (wt & 3) * 18 + k;
         uint4* pp = reinterpret_cast<uint4*>(sQ + (pc >> 3) * kQChunk + h * 128 + (((pc & 7) ^ (h & 7)) << 4));
         uint4 v = *pp;
         v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
@@ -262,240 +390,168 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         *pp = v;
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar(kQReady));
-    };
-    if (kFp4) {
-      const uint8_t* cbase = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
-      const uint8_t* sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
-      const int32_t* idx_row = fsrc.idx + (int64_t)qi * fsrc.K;
-      uint4 cw[18];
-      uint32_t sw[9];
-      int ent = -1;
-      auto load_tile = [&](int t) {
-        const int p = p_begin + t * kTK + e;
-        ent = p < p_end ? idx_row[p] : -1;
-        if (ent < -1 || ent >= fsrc.n_stride) {
-          atomicOr(status, CSA2_DEV_BAD_INDEX);
-          ent = -1;
-        }
-        if (ent >= 0) {
-          const uint4* cp = reinterpret_cast<const uint4*>(cbase + (int64_t)ent * CSA2_CODE_BYTES);
-          const uint32_t* spt = reinterpret_cast<const uint32_t*>(sbase + (int64_t)ent * CSA2_SCALE_BYTES);
+    }
+    mbar_arrive(bar(kQReady));
+
+    float l[32];  // running sums of this key row's p, for the 32 heads of this half
 #pragma unroll
-          for (int k = 0; k < 18; ++k) cw[k] = __ldg(cp + k);
-#pragma unroll
-          for (int k = 0; k < 9; ++k) sw[k] = __ldg(spt + k);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 18; ++k) cw[k] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-          for (int k = 0; k < 9; ++k) sw[k] = 0u;
-        }
-      };
-      if (ntiles > 0) load_tile(0);
-      convert_q();
-      bool lok = q_ok;
-      for (int t = 0; t < ntiles && lok; ++t) {
-        if (*abort_flag) break;
+    for (int h = 0; h < 32; ++h) l[h] = 0.f;
+    int issued_t = -1, waited_t = -1;  // TMA window loads (wt == 0)
+
+    for (int t = 0; t < ntiles; ++t) {
+      const int sb = t & 1;
+      // ---- stage the tile into C (group by group, as P.V of tile t-1 releases it)
+      if (kFp4) {
+        bool ok = wok && !*abort_flag;
 #pragma unroll
         for (int g = 0; g < 5; ++g) {
-          if (lok && t > 0 && !mbar_wait(bar(kGroupFree + g), (t - 1) & 1)) { fail(); lok = false; }
-          if (lok) {
-            if (g == 0) ms.valid[t & 1][e] = ent;
-            const int blk0 = g < 4 ? 8 * g : 32, nblk = g < 4 ? 8 : 4;
-#pragma unroll
-            for (int kb = 0; kb < nblk; ++kb) {
-              const int blk = blk0 + kb;
-              // 16 codes of block blk: bytes [8 blk, 8 blk + 8) of the row
-              const uint4 w4 = cw[blk >> 1];
-              const uint32_t lo = (blk & 1) ? w4.z : w4.x, hi = (blk & 1) ? w4.w : w4.y;
-              const uint32_t s2 = e4m3_to_h2((sw[blk >> 2] >> (8 * (blk & 3))) & 0xFFu);
-              uint32_t hv[8];
-              e2m1x4_to_h2x2(lo & 0xFFFFu, hv[0], hv[1]);
-              e2m1x4_to_h2x2(lo >> 16, hv[2], hv[3]);
-              e2m1x4_to_h2x2(hi & 0xFFFFu, hv[4], hv[5]);
-              e2m1x4_to_h2x2(hi >> 16, hv[6], hv[7]);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) hv[k] = hmul2_u32(hv[k], s2);
-              const int c = blk >> 2, j = (blk & 3) * 2;
-              *reinterpret_cast<uint4*>(sC + cswz(c, e, j)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-              *reinterpret_cast<uint4*>(sC + cswz(c, e, j + 1)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+          if (ok && t > 0 && !mbar_wait(bar(kGroupFree + g), (t - 1) & 1)) { fail(); ok = false; }
+          if (ok) {
+            if (g == 0 && half == 0) ms.valid[sb][e] = ent;
+            if (half == 0) {
+              if (g == 0) dequant_group<0, 0>(sC, e, cw, sw);
+              if (g == 1) dequant_group<0, 1>(sC, e, cw, sw);
+              if (g == 2) dequant_group<0, 2>(sC, e, cw, sw);
+            } else {
+              if (g == 2) dequant_group<1, 2>(sC, e, cw, sw);
+              if (g == 3) dequant_group<1, 3>(sC, e, cw, sw);
+              if (g == 4) dequant_group<1, 4>(sC, e, cw, sw);
             }
             fence_proxy_async_smem();
             mbar_arrive(bar(kChunkFull + g));
           }
         }
-        if (lok && t + 1 < ntiles) load_tile(t + 1);
-      }
-    } else {
-      int issued_t = -1, waited_t = -1;
-      convert_q();
-      for (int t = 0; t < ntiles && q_ok; ++t) {
-        if (*abort_flag) break;
-        if (t > 0 && !mbar_wait(bar(kGroupFree + 4), (t - 1) & 1)) { fail(); break; }
-        if (e == 0) {
+        wok = ok;
+        if (wok && t + 1 < ntiles) fetch(t + 1);
+      } else {
+        bool ok = wok && !*abort_flag;
+        if (ok && t > 0 && !mbar_wait(bar(kGroupFree + 4), (t - 1) & 1)) { fail(); ok = false; }
+        if (ok && wt == 0) {
           mbar_arrive_expect_tx(bar(kTmaFull), 9 * kCChunk);
           for (int c = 0; c < 9; ++c)
             tma_load_2d(uC + c * kCChunk, &tm_rows, 64 * c, row_base + p_begin + t * kTK, bar(kTmaFull));
           issued_t = t;
         }
-        const int key = p_begin + t * kTK + e;
-        ms.valid[t & 1][e] = key < p_end ? 1 : -1;
-        if (!mbar_wait(bar(kTmaFull), t & 1)) { fail(); break; }
-        waited_t = t;
-        // bf16 -> fp16 in place, one row per thread
-        for (int g = 0; g < 5; ++g) {
-          const int c0 = g < 4 ? 2 * g : 8, nc = g < 4 ? 2 : 1;
-          for (int cc = 0; cc < nc; ++cc) {
+        if (ok && half == 0) ms.valid[sb][e] = (p_begin + t * kTK + e < p_end) ? 1 : -1;
+        if (ok && !mbar_wait(bar(kTmaFull), t & 1)) { fail(); ok = false; }
+        if (ok && wt == 0) waited_t = t;
+        if (ok) {
+          // bf16 -> fp16 in place; half 0 converts the first 36 pieces of row e, half 1 the rest
+          for (int g = 0; g < 5; ++g) {
+            const int c0 = g < 4 ? 2 * g : 8, nc = g < 4 ? 2 : 1;
+            for (int cc = 0; cc < nc; ++cc) {
+              const int c = c0 + cc;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              uint4* pp = reinterpret_cast<uint4*>(sC + cswz(c0 + cc, e, j));
-              uint4 v = *pp;
-              v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
-              v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
-              *pp = v;
+              for (int j = 0; j < 8; ++j) {
+                if ((c * 8 + j < 36) != (half == 0)) continue;
+                uint4* pp = reinterpret_cast<uint4*>(sC + cswz(c, e, j));
+                uint4 v = *pp;
+                v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
+                v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
+                *pp = v;
+              }
             }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kChunkFull + g));
           }
-          fence_proxy_async_smem();
-          mbar_arrive(bar(kChunkFull + g));
         }
+        wok = ok;
       }
-      // copies in flight must land before the CTA exits
-      if (e == 0 && issued_t > waited_t) mbar_wait(bar(kTmaFull), issued_t & 1);
-    }
-    if (e == 0 && !q_ok) mbar_wait(bar(kQTma), 0);
-  } else if (warp < 8) {
-    // ======================= softmax =======================
-    const int w = warp - 4;          // TMEM lane quarter
-    const int ts = w * 32 + lane;    // key row (S^T lane) / value dim row (O^T lane)
-    const uint32_t lane_off = (uint32_t)(w * 32) << 16;
-    float l[64];                     // running sums of this key row's p, per head
-#pragma unroll
-    for (int h = 0; h < 64; ++h) l[h] = 0.f;
-    bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      const int sb = t & 1;
-      bool got = !*abort_flag && mbar_wait(bar(kSFull + sb), (t >> 1) & 1) &&
+
+      // ---- softmax of this tile for heads [32*half, 32*half+32)
+      bool got = wok && !*abort_flag && mbar_wait(bar(kSFull + sb), (t >> 1) & 1) &&
                  mbar_wait(bar(kChunkFull + 4), t & 1);
-      if (!named_and(1, 128, got)) { if (ts == 0) fail(); ok = false; break; }
+      if (!named_and(bid, 128, got)) { if (e == 0) fail(); wok = false; break; }
       tc_fence_after();
-      const bool vld = ms.valid[sb][ts] >= 0;
-      const uint32_t ts_addr = tmem + lane_off + kColS + 64 * sb;
+      const bool vld = ms.valid[sb][e] >= 0;
+      const uint32_t s_addr = tmem + lane_off + kColS + 64 * sb + 32 * half;
+      const int h0 = 32 * half;
       if (t == 0) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float s[32];
-          load_scores32(ts_addr + 32 * hh, vld, scale_log2, s);
-          reduce32<true>(s, ms, ms.mrun, 32 * hh, lane, w);
-        }
+        float s[32];
+        load_scores32(s_addr, vld, scale_log2, s);
+        reduce32<true>(s, ms, ms.mrun, h0, lane, quarter, bid);
       } else {
         bool need = false;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float s[32];
-          load_scores32(ts_addr + 32 * hh, vld, scale_log2, s);
+        for (int q16 = 0; q16 < 2; ++q16) {
+          float s[16];
+          load_scores16(s_addr + 16 * q16, vld, scale_log2, s);
 #pragma unroll
-          for (int h = 0; h < 32; ++h) need |= s[h] > ms.mrun[32 * hh + h] + kRescale;
+          for (int h = 0; h < 16; ++h) need |= s[h] > ms.mrun[h0 + 16 * q16 + h] + kRescale;
         }
-        if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&ms.vote[sb], 1);
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        const bool rescale = ms.vote[sb] != 0;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (ts == 0) ms.vote[sb] = 0;
+        if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&ms.vote[half][sb], 1);
+        named_sync(bid, 128);
+        const bool rescale = ms.vote[half][sb] != 0;
+        named_sync(bid, 128);
+        if (e == 0) ms.vote[half][sb] = 0;
         if (rescale) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
+          {
             float s[32];
-            load_scores32(ts_addr + 32 * hh, vld, scale_log2, s);
-            reduce32<true>(s, ms, ms.mnew, 32 * hh, lane, w);
+            load_scores32(s_addr, vld, scale_log2, s);
+            reduce32<true>(s, ms, ms.mnew, h0, lane, quarter, bid);
           }
           // O^T must be final for tile t-1 before it is rescaled
-          if (!named_and(1, 128, mbar_wait(bar(kGroupFree + 4), (t - 1) & 1))) {
-            if (ts == 0) fail();
-            ok = false;
+          if (!named_and(bid, 128, mbar_wait(bar(kGroupFree + 4), (t - 1) & 1))) {
+            if (e == 0) fail();
+            wok = false;
             break;
           }
           tc_fence_after();
-          if (ts < 64) {
-            const float mo = ms.mrun[ts], mn = fmaxf(mo, ms.mnew[ts]);
-            ms.alpha[ts] = mo == mn ? 1.f : exp2f(mo - mn);
+          if (quarter == 0) {
+            const float mo = ms.mrun[h0 + lane], mn = fmaxf(mo, ms.mnew[h0 + lane]);
+            ms.alpha[h0 + lane] = mo == mn ? 1.f : exp2f(mo - mn);
           }
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          named_sync(bid, 128);
 #pragma unroll
-          for (int h = 0; h < 64; ++h) l[h] *= ms.alpha[h];
-          for (int i = 0; i < 8; ++i) {
+          for (int h = 0; h < 32; ++h) l[h] *= ms.alpha[h0 + h];
+          for (int i = 0; i < 4; ++i) {
             uint32_t r[32];
-            const uint32_t ta = tmem + lane_off + kColO + 32 * i;
+            const uint32_t ta = tmem + lane_off + kColO + 64 * i + 32 * half;
             tmem_ld32(ta, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-              r[k] = __float_as_uint(__uint_as_float(r[k]) * ms.alpha[(32 * i + k) & 63]);
+            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * ms.alpha[h0 + k]);
             tmem_st32(ta, r);
           }
           tmem_wait_st();
-          asm volatile("bar.sync 1, 128;" ::: "memory");
-          if (ts < 64) ms.mrun[ts] = fmaxf(ms.mrun[ts], ms.mnew[ts]);
-          asm volatile("bar.sync 1, 128;" ::: "memory");
+          named_sync(bid, 128);
+          if (quarter == 0) ms.mrun[h0 + lane] = fmaxf(ms.mrun[h0 + lane], ms.mnew[h0 + lane]);
+          named_sync(bid, 128);
         }
       }
-      // P^T row of this key: exp2(s - m) in fp16, written over the rope chunk (the S^T
-      // product of this tile has consumed it)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float s[32];
-        load_scores32(ts_addr + 32 * hh, vld, scale_log2, s);
-        uint32_t pk[16];
+      for (int q16 = 0; q16 < 2; ++q16) {
+        // P^T row of this key, 16 heads: exp2(s - m) in fp16 over the rope chunk
+        float s[16];
+        load_scores16(s_addr + 16 * q16, vld, scale_log2, s);
+        uint32_t pk[8];
 #pragma unroll
-        for (int h = 0; h < 32; h += 2) {
-          const float m0 = ms.mrun[32 * hh + h], m1 = ms.mrun[32 * hh + h + 1];
+        for (int h = 0; h < 16; h += 2) {
+          const int hh = h0 + 16 * q16 + h;
+          const float m0 = ms.mrun[hh], m1 = ms.mrun[hh + 1];
           const float p0 = exp2f(s[h] - (m0 == -INFINITY ? 0.f : m0));
           const float p1 = exp2f(s[h + 1] - (m1 == -INFINITY ? 0.f : m1));
-          l[32 * hh + h] += p0;
-          l[32 * hh + h + 1] += p1;
+          l[16 * q16 + h] += p0;
+          l[16 * q16 + h + 1] += p1;
           pk[h >> 1] = pack_h2(p0, p1);
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(sC + cswz(8, ts, 4 * hh + j)) =
+        for (int j = 0; j < 2; ++j)
+          *reinterpret_cast<uint4*>(sC + cswz(8, e, 4 * half + 2 * q16 + j)) =
               make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kPFull));
     }
-    // ---- epilogue: partial O (unnormalised), max and sum per head
-    if (ok && ntiles > 0) {
-      ok = named_and(1, 128, mbar_wait(bar(kGroupFree + 4), (ntiles - 1) & 1));
-      if (!ok && ts == 0) fail();
+    if (!kFp4 && wt == 0 && issued_t > waited_t) mbar_wait(bar(kTmaFull), issued_t & 1);
+
+    // ---- wait for the last P.V, then the sums per head
+    if (wok && ntiles > 0) {
+      wok = named_and(bid, 128, mbar_wait(bar(kGroupFree + 4), (ntiles - 1) & 1));
+      if (!wok && e == 0) fail();
     }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      float v[32];
-#pragma unroll
-      for (int h = 0; h < 32; ++h) v[h] = l[32 * hh + h];
-      reduce32<false>(v, ms, ms.mnew, 32 * hh, lane, w);
-    }
-    if (ok && ntiles > 0) {
-      tc_fence_after();
-      for (int i = 0; i < 8; ++i) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kColO + 32 * i, r);
-        tmem_wait_ld();
-        const int d = 128 * (i >> 1) + ts, h0 = 32 * (i & 1);
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (h0 + k < H) part[(h0 + k) * kPartStride + d] = __uint_as_float(r[k]);
-      }
-    } else {
-      for (int i = 0; i < 4; ++i)
-        for (int h = 0; h < H; ++h) part[h * kPartStride + 128 * i + ts] = 0.f;
-    }
-    if (ts < H) {
-      const bool has = ok && ntiles > 0;
-      part[ts * kPartStride + kDV] = has ? ms.mrun[ts] : -INFINITY;
-      part[ts * kPartStride + kDV + 1] = has ? ms.mnew[ts] : 0.f;
-    }
+    reduce32<false>(l, ms, ms.lsum, 32 * half, lane, quarter, bid);
   } else {
     // ======================= MMA issuer =======================
     if (lane == 0) {
@@ -543,6 +599,112 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         mbar_wait(bar(kDrain), 0);
       }
     }
+    __syncwarp();
+  }
+
+  // ======================= merge the splits of this query =======================
+  allow_dependents();
+  __syncthreads();
+  const bool has = ntiles > 0 && !*abort_flag;
+  const int Dn = kDV / (int)nsplit;  // value dims owned by each CTA
+  float* recv = reinterpret_cast<float*>(sC);                     // [src][dl][kRecvStride]
+  float* ml = reinterpret_cast<float*>(sC + kMlOffset);           // [src][2][64]
+  // every CTA of the cluster is past its last P.V: tile buffers may be overwritten
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp < 8) {
+    const int quarter = warp & 3, half = warp >> 2;
+    const int e = quarter * 32 + lane;
+    const int wt = threadIdx.x;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // (max, sum) per head of this split -> ml[sp] of every CTA
+    if (wt < 64) {
+      const float m = has ? ms.mrun[wt] : -INFINITY;
+      const float s = has ? ms.lsum[wt] : 0.f;
+      for (uint32_t p = 0; p < nsplit; ++p) {
+        st_cluster_f32(map_rank(smem_u32(&ml[(sp * 2 + 0) * 64 + wt]), p), m);
+        st_cluster_f32(map_rank(smem_u32(&ml[(sp * 2 + 1) * 64 + wt]), p), s);
+      }
+    }
+    // unnormalised O^T rows (value dim 128 i + e, heads of this half) -> owner of the dim
+    for (int i = 0; i < 4; ++i) {
+      const int d = 128 * i + e;
+      const uint32_t owner = (uint32_t)(d / Dn);
+      const int dl = d - (int)owner * Dn;
+      uint32_t r[32];
+      if (has) {
+        tmem_ld32(tmem + lane_off + kColO + 64 * i + 32 * half, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) r[k] = 0u;
+      }
+      const uint32_t dst =
+          map_rank(smem_u32(&recv[((size_t)sp * Dn + dl) * kRecvStride + 32 * half]), owner);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        st_cluster_v4(dst + 16 * k, __uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                      __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  // weights per (split, head), the external branch, and normalised O for the owned dims
+  if (warp < 8) {
+    const int wt = threadIdx.x;
+    constexpr float kLn2 = 0.69314718055994530942f, kLog2e = 1.4426950408889634074f;
+    if (wt < 64) {
+      float M = -INFINITY;
+      for (uint32_t s = 0; s < nsplit; ++s) M = fmaxf(M, ml[(s * 2 + 0) * 64 + wt]);
+      float mext = -INFINITY;
+      if (out.o_ext) {
+        mext = out.lse_ext[(int64_t)qi * H + (wt < H ? wt : 0)] * kLog2e;
+        M = fmaxf(M, mext);
+      }
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float L = 0.f;
+      for (uint32_t s = 0; s < nsplit; ++s) {
+        const float ls = ml[(s * 2 + 1) * 64 + wt];
+        L += ls > 0.f ? ls * exp2f(ml[(s * 2 + 0) * 64 + wt] - Mu) : 0.f;
+      }
+      const float wext = (out.o_ext && mext != -INFINITY) ? exp2f(mext - Mu) : 0.f;
+      L += wext;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      // overwrite the pushed maxima with the per-split weights
+      for (uint32_t s = 0; s < nsplit; ++s) {
+        const float ls = ml[(s * 2 + 1) * 64 + wt];
+        ml[(s * 2 + 0) * 64 + wt] = ls > 0.f ? exp2f(ml[(s * 2 + 0) * 64 + wt] - Mu) * inv : 0.f;
+      }
+      ms.alpha[wt] = wext * inv;
+      if (sp == 0 && out.lse && wt < H)
+        out.lse[(int64_t)qi * H + wt] = L > 0.f ? (Mu + log2f(L)) * kLn2 : -INFINITY;
+    }
+    named_sync(1, kWorkers);
+    float* o = out.o + (int64_t)qi * H * kDV;
+    const float* oe = out.o_ext ? out.o_ext + (int64_t)qi * H * kDV : nullptr;
+    const int base = sp * Dn;
+    for (int j = wt; j < Dn * 16; j += kWorkers) {
+      const int dl = j % Dn, hq = j / Dn;   // value dim, head quad
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (uint32_t s = 0; s < nsplit; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(&recv[((size_t)s * Dn + dl) * kRecvStride + 4 * hq]);
+        const float4 w = *reinterpret_cast<const float4*>(&ml[(s * 2 + 0) * 64 + 4 * hq]);
+        acc.x += w.x * v.x; acc.y += w.y * v.y; acc.z += w.z * v.z; acc.w += w.w * v.w;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int h = 4 * hq + k;
+        if (h < H) {
+          float val = k == 0 ? acc.x : (k == 1 ? acc.y : (k == 2 ? acc.z : acc.w));
+          if (oe) {
+            const float we = ms.alpha[h];
+            if (we > 0.f) val += we * oe[(int64_t)h * kDV + base + dl];
+          }
+          o[(int64_t)h * kDV + base + dl] = val;
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -557,106 +719,44 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
 
 }  // namespace
 
-// Merge nsplit partials (and optionally an external normalised branch with
-// natural-log LSE) into normalised O and natural-log LSE. One warp per (query,
-// head): the split maxima and sums are loaded in parallel by the lanes, then
-// every lane combines 16 value dims. grid: (ceil(H/8), Q), 256 threads.
-__global__ void __launch_bounds__(256) attn_combine_kernel(
-    const float* __restrict__ partials, int nsplit, int H, const float* __restrict__ o_ext,
-    const float* __restrict__ lse_ext, float* __restrict__ o_out, float* __restrict__ lse_out) {
-  constexpr float kLn2 = 0.69314718055994530942f, kLog2e = 1.4426950408889634074f;
-  constexpr int kPS = kDV + 2;
-  const int qi = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x * 8 + warp;
-  if (h >= H) return;
-  // lane s < nsplit holds split s; lane 31 holds the external branch
-  float m = -INFINITY, l = 0.f;
-  if (lane < nsplit) {
-    const float* p = partials + ((int64_t)(qi * nsplit + lane) * H + h) * kPS;
-    m = p[kDV];
-    l = p[kDV + 1];
-  } else if (lane == 31 && o_ext) {
-    m = lse_ext[(int64_t)qi * H + h] * kLog2e;  // a normalised branch: sum 1 at max lse
-    l = m == -INFINITY ? 0.f : 1.f;
-  }
-  float M = m;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float Mu = M == -INFINITY ? 0.f : M;
-  const float w = l > 0.f ? exp2f(m - Mu) : 0.f;   // weight of this lane's branch
-  float L = l * w;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  float4 acc[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-  // splits in groups of 4 with all loads of a group issued before the FMAs
-  for (int s0 = 0; s0 < nsplit; s0 += 4) {
-    float4 x[4][4];
-    float ws[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int s = s0 + u;
-      ws[u] = __shfl_sync(0xffffffffu, w, s < nsplit ? s : 0);
-      if (s >= nsplit) ws[u] = 0.f;
-      const float* p = partials + ((int64_t)(qi * nsplit + (s < nsplit ? s : 0)) * H + h) * kPS;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 a = *reinterpret_cast<const float2*>(p + j * 128 + lane * 4);
-        const float2 b = *reinterpret_cast<const float2*>(p + j * 128 + lane * 4 + 2);
-        x[u][j] = make_float4(a.x, a.y, b.x, b.y);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        acc[j].x += ws[u] * x[u][j].x; acc[j].y += ws[u] * x[u][j].y;
-        acc[j].z += ws[u] * x[u][j].z; acc[j].w += ws[u] * x[u][j].w;
-      }
-  }
-  const float we = __shfl_sync(0xffffffffu, w, 31);
-  if (o_ext && we > 0.f) {
-    const float* e = o_ext + ((int64_t)qi * H + h) * kDV;
-    float4 x[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] = *reinterpret_cast<const float4*>(e + j * 128 + lane * 4);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      acc[j].x += we * x[j].x; acc[j].y += we * x[j].y;
-      acc[j].z += we * x[j].z; acc[j].w += we * x[j].w;
-    }
-  }
-  __syncwarp();
-  float* out = o_out + ((int64_t)qi * H + h) * kDV;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float4 r = acc[j];
-    r.x *= inv; r.y *= inv; r.z *= inv; r.w *= inv;
-    *reinterpret_cast<float4*>(out + j * 128 + lane * 4) = r;
-  }
-  if (lane == 0 && lse_out) lse_out[(int64_t)qi * H + h] = L > 0.f ? (Mu + log2f(L)) * kLn2 : -INFINITY;
-}
-
-
-static cudaError_t launch_combine(const float* partials, int nsplit, int Q, int H, const float* o_ext,
-                                  const float* lse_ext, float* o_out, float* lse_out, cudaStream_t st) {
-  attn_combine_kernel<<<dim3((H + 7) / 8, Q), 256, 0, st>>>(partials, nsplit, H, o_ext, lse_ext, o_out,
-                                                            lse_out);
-  return cudaGetLastError();
+// Launch the (split, query) grid as clusters of nsplit CTAs (a power of two <= 16),
+// allowing programmatic dependent launch after the preceding kernel.
+template <bool kFp4>
+static cudaError_t launch_tc(const CUtensorMap& tq, const Fp4Src& f, const RowSrc& r,
+                             const CUtensorMap& trows, int Q, int T, int H, float scale_log2,
+                             int nsplit, int split_len, const OutArgs& out, uint32_t* status,
+                             cudaStream_t st) {
+  cudaError_t e = set_attr_once(kFp4 ? 2 : 3, (const void*)attn_tc_kernel<kFp4>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTC);
+  if (e != cudaSuccess) return e;
+  e = set_attr_once(kFp4 ? 7 : 8, (const void*)attn_tc_kernel<kFp4>,
+                    cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nsplit, (unsigned)Q);
+  cfg.blockDim = dim3(kThreadsTC);
+  cfg.dynamicSmemBytes = kSmemTC;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kFp4>, tq, f, r, trows, T, H, scale_log2, split_len,
+                            out, status);
 }
 
 cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t* codes,
                                const uint8_t* scales, int64_t n_stride, const int32_t* idx, int K,
-                               float scale_log2, float* o_g, float* lse_g, float* partials,
-                               int nsplit, uint32_t* status, cudaStream_t st) {
+                               float scale_log2, float* o_g, float* lse_g, int nsplit,
+                               uint32_t* status, cudaStream_t st) {
   const int Q = B * T;
   if (Q == 0) return cudaSuccess;
-  cudaError_t e = set_attr_once(2, (const void*)attn_tc_kernel<true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTC);
-  if (e != cudaSuccess) return e;
+  if (nsplit < 1 || nsplit > kMaxSplitsTC || (nsplit & (nsplit - 1))) return cudaErrorInvalidValue;
   int split_len = (K + nsplit - 1) / nsplit;
   split_len = (split_len + kTK - 1) / kTK * kTK;
   Fp4Src f{codes, scales, n_stride, idx, K};
@@ -664,39 +764,28 @@ cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t
   CUtensorMap tq, dummy;
   memset(&dummy, 0, sizeof(dummy));
   if (!encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64)) return cudaErrorInvalidValue;
-  attn_tc_kernel<true><<<dim3(nsplit, Q), kThreadsTC, kSmemTC, st>>>(
-      tq, f, r, dummy, T, H, scale_log2, nsplit, split_len, partials, status);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_combine(partials, nsplit, Q, H, nullptr, nullptr, o_g, lse_g, st);
+  OutArgs out{o_g, lse_g, nullptr, nullptr};
+  return launch_tc<true>(tq, f, r, dummy, Q, T, H, scale_log2, nsplit, split_len, out, status, st);
 }
 
 cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa,
                              int64_t s_stride, const int32_t* win_start, const int32_t* win_len,
                              int n_win, float scale_log2, const float* o_g, const float* lse_g,
-                             float* o_out, float* lse_out, float* partials, uint32_t* status,
-                             cudaStream_t st) {
+                             float* o_out, float* lse_out, uint32_t* status, cudaStream_t st) {
   const int Q = B * T;
   if (Q == 0) return cudaSuccess;
-  const int nsplit = swa_splits(n_win);
-  if (n_win > 0 && s_stride > 0) {
-    cudaError_t e = set_attr_once(3, (const void*)attn_tc_kernel<false>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTC);
-    if (e != cudaSuccess) return e;
-    CUtensorMap tm, tq;
-    if (!encode_tensor_map_2d_bf16(&tm, swa, CSA2_D_KV, (uint64_t)B * s_stride, 64, kTK) ||
-        !encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64))
-      return cudaErrorInvalidValue;
-    Fp4Src f{nullptr, nullptr, 0, nullptr, 0};
-    RowSrc r{s_stride, win_start, win_len, n_win};
-    attn_tc_kernel<false><<<dim3(nsplit, Q), kThreadsTC, kSmemTC, st>>>(
-        tq, f, r, tm, T, H, scale_log2, nsplit, kTK, partials, status);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_combine(partials, nsplit, Q, H, o_g, lse_g, o_out, lse_out, st);
-  }
-  // empty window: the merge is the global branch itself
-  return launch_combine(partials, 0, Q, H, o_g, lse_g, o_out, lse_out, st);
+  int nsplit = 1;
+  while (nsplit * kTK < n_win) nsplit <<= 1;   // power of two covering the window
+  if (nsplit > kMaxSplitsTC) return cudaErrorInvalidValue;
+  CUtensorMap tm, tq;
+  memset(&tm, 0, sizeof(tm));
+  if (!encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64)) return cudaErrorInvalidValue;
+  if (s_stride > 0 && !encode_tensor_map_2d_bf16(&tm, swa, CSA2_D_KV, (uint64_t)B * s_stride, 64, kTK))
+    return cudaErrorInvalidValue;
+  Fp4Src f{nullptr, nullptr, 0, nullptr, 0};
+  RowSrc r{s_stride, win_start, win_len, n_win};
+  OutArgs out{o_out, lse_out, o_g, lse_g};
+  return launch_tc<false>(tq, f, r, tm, Q, T, H, scale_log2, nsplit, kTK, out, status, st);
 }
 
 }  // namespace csa2

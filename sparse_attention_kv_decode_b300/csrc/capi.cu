@@ -75,8 +75,9 @@ int attn_splits(int64_t Q, int K, int n_sm) {
   int64_t max_by_k = (K + 127) / 128;    // at least one 128-key tile per split
   if (s > max_by_k) s = max_by_k;
   if (s > kMaxSplits) s = kMaxSplits;
-  if (s < 1) s = 1;
-  return (int)s;
+  int p = 1;                             // splits form one cluster: a power of two
+  while (2 * p <= s) p *= 2;
+  return p;
 }
 
 }  // namespace csa2
@@ -119,11 +120,9 @@ const char* csa2_status_string(int s) {
 
 size_t csa2_workspace_bytes(int B, int T, int H, int64_t n_max, int K) {
   if (B < 0 || T < 0 || H < 0 || n_max < 0 || K < 0) return 0;
+  (void)H; (void)K;
   const int64_t Q = (int64_t)B * T;
-  int ns = attn_splits(Q, K, device_sm_count());
-  if (ns < swa_splits(kMaxWin)) ns = swa_splits(kMaxWin);
-  size_t a = scores_bytes(Q, n_max), b = partials_bytes(Q, ns, H);
-  return kWsHeader + (a > b ? a : b);
+  return kWsHeader + scores_bytes(Q, n_max);
 }
 
 int csa2_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -226,13 +225,11 @@ int csa2_sparse_decode(int B, int T, int H, const void* q, const uint8_t* kv_cod
   if (ws == nullptr) return CSA2_ERR_WORKSPACE;
   CHECK_ARG(aligned(ws, 256));
   const int nsplit = attn_splits(Q, K, device_sm_count());
-  if (ws_bytes < kWsHeader + partials_bytes(Q, nsplit, H)) return CSA2_ERR_WORKSPACE;
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  float* partials = reinterpret_cast<float*>(wsb + kWsHeader);
-  uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
+  if (ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
+  uint32_t* status = static_cast<uint32_t*>(ws);
   const float scale_log2 = softmax_scale * 1.4426950408889634074f;
   return cuda_status(launch_sparse_attn(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K,
-                                        scale_log2, o_g, lse_g, partials, nsplit, status,
+                                        scale_log2, o_g, lse_g, nsplit, status,
                                         (cudaStream_t)stream));
 }
 
@@ -252,13 +249,11 @@ int csa2_swa_merge(int B, int T, int H, const void* q, const void* swa_kv, int64
             aligned(win_len, 4));
   if (ws == nullptr) return CSA2_ERR_WORKSPACE;
   CHECK_ARG(aligned(ws, 256));
-  if (ws_bytes < kWsHeader + partials_bytes(Q, swa_splits(n_win), H)) return CSA2_ERR_WORKSPACE;
-  uint8_t* wsb = static_cast<uint8_t*>(ws);
-  float* partials = reinterpret_cast<float*>(wsb + kWsHeader);
-  uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
+  if (ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
+  uint32_t* status = static_cast<uint32_t*>(ws);
   const float scale_log2 = softmax_scale * 1.4426950408889634074f;
   return cuda_status(launch_swa_merge(B, T, H, q, swa_kv, s_stride, win_start, win_len, n_win,
-                                      scale_log2, o_g, lse_g, o_out, lse_out, partials, status,
+                                      scale_log2, o_g, lse_g, o_out, lse_out, status,
                                       (cudaStream_t)stream));
 }
 

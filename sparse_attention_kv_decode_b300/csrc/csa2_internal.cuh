@@ -14,31 +14,26 @@ namespace csa2 {
 // ---------------------------------------------------------------------------
 // Workspace layout (byte offsets from the caller's workspace pointer)
 //   [0, 256)   header: device status word (u32) at offset 0
-//   [256, ..)  scratch, used by one call at a time (calls on one workspace are
-//              stream-ordered): fp32 indexer scores [Q][n_pad] for
-//              csa2_index_topk, or fp32 attention partials [Q][nsplit][H][514]
-//              for csa2_sparse_decode / csa2_swa_merge.
+//   [256, ..)  scratch of csa2_index_topk: fp32 indexer scores [Q][n_pad]
+//              (calls on one workspace are stream-ordered). The attention calls
+//              use only the status word: their splits merge on chip.
 // ---------------------------------------------------------------------------
 constexpr size_t kWsHeader = 256;
-constexpr int kMaxSplits = 16;
+constexpr int kMaxSplits = 16;  // power-of-two key splits per query (one cluster)
 constexpr int kScoreTile = 1024;  // keys per indexer CTA
 constexpr int kMaxK = 4096;
 constexpr int64_t kMaxNStride = 262144;  // 1M tokens at 4:1
 constexpr int kMaxWin = 256;
-constexpr int kPartStride = 514;  // floats per (query, split, head) partial: O[512], m, l
 
 inline int64_t score_pad(int64_t n) { return (n + kScoreTile - 1) / kScoreTile * kScoreTile; }
 
 // Number of key splits per query for the sparse attention (about one wave of
 // CTAs when the batch is small; one split per query when there are many).
 int attn_splits(int64_t Q, int K, int n_sm);
-inline int swa_splits(int n_win) { return n_win > 0 ? (n_win + 127) / 128 : 1; }
+
 
 inline size_t scores_bytes(int64_t Q, int64_t n_stride) {
   return (size_t)Q * (size_t)score_pad(n_stride) * 4;
-}
-inline size_t partials_bytes(int64_t Q, int nsplit, int H) {
-  return (size_t)Q * (size_t)nsplit * (size_t)H * kPartStride * 4;
 }
 
 int device_sm_count();
@@ -66,13 +61,12 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
 cudaError_t launch_copy_idx(const int32_t* src, int32_t* dst, int64_t n, cudaStream_t st);
 cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t* codes,
                                const uint8_t* scales, int64_t n_stride, const int32_t* idx,
-                               int K, float scale_log2, float* o_g, float* lse_g,
-                               float* partials, int nsplit, uint32_t* status, cudaStream_t st);
+                               int K, float scale_log2, float* o_g, float* lse_g, int nsplit,
+                               uint32_t* status, cudaStream_t st);
 cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa,
                              int64_t s_stride, const int32_t* win_start, const int32_t* win_len,
                              int n_win, float scale_log2, const float* o_g, const float* lse_g,
-                             float* o_out, float* lse_out, float* partials, uint32_t* status,
-                             cudaStream_t st);
+                             float* o_out, float* lse_out, uint32_t* status, cudaStream_t st);
 cudaError_t launch_ced_project(const void* h, int64_t rows, int d_model, const void* w_kv,
                                const void* w_z, int n_layers, uint8_t* codes, uint8_t* scales,
                                void* z_out, uint32_t* status, cudaStream_t st);
@@ -328,6 +322,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() {

@@ -71,7 +71,7 @@ def test_sparse_decode_validation(L):
     assert r(1, 1, 64, FAKE, FAKE + 8, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(0.04), FAKE, FAKE, FAKE, 1 << 30, None) == 1
     assert r(1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(float("nan")), FAKE, FAKE, FAKE, 1 << 30, None) == 1
     assert r(1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(0.04), FAKE, FAKE, None, 0, None) == 3
-    assert r(1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(0.04), FAKE, FAKE, FAKE, 4096, None) == 3
+    assert r(1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 128, 512, ctypes.c_float(0.04), FAKE, FAKE, FAKE, 128, None) == 3
     # empty batch: nothing to do
     assert r(0, 1, 64, None, None, None, 0, None, 128, 512, ctypes.c_float(0.04), None, None, None, 0, None) == 0
 
@@ -107,4 +107,6 @@ def test_workspace_size_monotone(L):
     b = L.csa2_workspace_bytes(32, 1, 64, 65536, 2048)
     c = L.csa2_workspace_bytes(64, 1, 64, 65536, 2048)
     assert 256 < a <= b <= c
+    assert a == 256 + 32 * 32768 * 4                    # header + fp32 scores
+    assert L.csa2_workspace_bytes(1, 1, 64, 0, 2048) == 256
     assert L.csa2_workspace_bytes(-1, 1, 64, 10, 10) == 0
