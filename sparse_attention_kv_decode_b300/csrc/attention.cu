@@ -359,14 +359,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     const int32_t* idx_row = nullptr;
     uint4 cw[9];
     uint32_t sw[5];
-    int ent = -1;
-    auto fetch = [&](int t) {
+    int ent = -1, ent_next = -1;
+    // entry index of this thread's key row in tile t (read one tile ahead of its use)
+    auto read_idx = [&](int t) -> int {
       const int p = p_begin + t * kTK + e;
-      ent = p < p_end ? idx_row[p] : -1;
-      if (ent < -1 || ent >= fsrc.n_stride) {
+      int v = (t < ntiles && p < p_end) ? idx_row[p] : -1;
+      if (v < -1 || v >= fsrc.n_stride) {
         atomicOr(status, CSA2_DEV_BAD_INDEX);
-        ent = -1;
+        v = -1;
       }
+      return v;
+    };
+    auto fetch = [&](int which) {
+      ent = which;
       if (half == 0) load_half_row<0>(cbase, sbase, ent, cw, sw);
       else load_half_row<1>(cbase, sbase, ent, cw, sw);
     };
@@ -374,7 +379,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       cbase = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
       sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
       idx_row = fsrc.idx + (int64_t)qi * fsrc.K;
-      if (ntiles > 0) fetch(0);
+      if (ntiles > 0) fetch(read_idx(0));
+      ent_next = read_idx(1);
     }
     wok = mbar_wait(bar(kQTma), 0);
     if (!wok) fail();
@@ -422,7 +428,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
           }
         }
         wok = ok;
-        if (wok && t + 1 < ntiles) fetch(t + 1);
+        if (wok && t + 1 < ntiles) {
+          fetch(ent_next);
+          ent_next = read_idx(t + 2);
+        }
       } else {
         bool ok = wok && !*abort_flag;
         if (ok && t > 0 && !mbar_wait(bar(kGroupFree + 4), (t - 1) & 1)) { fail(); ok = false; }
@@ -466,30 +475,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       const bool vld = ms.valid[sb][e] >= 0;
       const uint32_t s_addr = tmem + lane_off + kColS + 64 * sb + 32 * half;
       const int h0 = 32 * half;
-      if (t == 0) {
-        float s[32];
-        load_scores32(s_addr, vld, scale_log2, s);
-        reduce32<true>(s, ms, ms.mrun, h0, lane, quarter, bid);
-      } else {
-        bool need = false;
+      float s[32];
+      load_scores32(s_addr, vld, scale_log2, s);
+      if (t == 0) reduce32<true>(s, ms, ms.mrun, h0, lane, quarter, bid);
+      // P^T row of this key for the 32 heads: exp2(s - m) in fp16, over the rope chunk
+      uint32_t pk[16];
+      bool need = false;
 #pragma unroll
-        for (int q16 = 0; q16 < 2; ++q16) {
-          float s[16];
-          load_scores16(s_addr + 16 * q16, vld, scale_log2, s);
-#pragma unroll
-          for (int h = 0; h < 16; ++h) need |= s[h] > ms.mrun[h0 + 16 * q16 + h] + kRescale;
-        }
+      for (int h = 0; h < 32; h += 2) {
+        const float m0 = ms.mrun[h0 + h], m1 = ms.mrun[h0 + h + 1];
+        need |= (s[h] > m0 + kRescale) | (s[h + 1] > m1 + kRescale);
+        pk[h >> 1] = pack_h2(exp2f(s[h] - (m0 == -INFINITY ? 0.f : m0)),
+                             exp2f(s[h + 1] - (m1 == -INFINITY ? 0.f : m1)));
+      }
+      if (t > 0) {
         if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&ms.vote[half][sb], 1);
         named_sync(bid, 128);
         const bool rescale = ms.vote[half][sb] != 0;
         named_sync(bid, 128);
         if (e == 0) ms.vote[half][sb] = 0;
         if (rescale) {
-          {
-            float s[32];
-            load_scores32(s_addr, vld, scale_log2, s);
-            reduce32<true>(s, ms, ms.mnew, h0, lane, quarter, bid);
-          }
+          reduce32<true>(s, ms, ms.mnew, h0, lane, quarter, bid);
           // O^T must be final for tile t-1 before it is rescaled
           if (!named_and(bid, 128, mbar_wait(bar(kGroupFree + 4), (t - 1) & 1))) {
             if (e == 0) fail();
@@ -517,29 +523,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
           named_sync(bid, 128);
           if (quarter == 0) ms.mrun[h0 + lane] = fmaxf(ms.mrun[h0 + lane], ms.mnew[h0 + lane]);
           named_sync(bid, 128);
+#pragma unroll
+          for (int h = 0; h < 32; h += 2) {
+            const float m0 = ms.mrun[h0 + h], m1 = ms.mrun[h0 + h + 1];
+            pk[h >> 1] = pack_h2(exp2f(s[h] - (m0 == -INFINITY ? 0.f : m0)),
+                                 exp2f(s[h + 1] - (m1 == -INFINITY ? 0.f : m1)));
+          }
         }
       }
+      // the sums use the fp16 p that P.V consumes
 #pragma unroll
-      for (int q16 = 0; q16 < 2; ++q16) {
-        // P^T row of this key, 16 heads: exp2(s - m) in fp16 over the rope chunk
-        float s[16];
-        load_scores16(s_addr + 16 * q16, vld, scale_log2, s);
-        uint32_t pk[8];
-#pragma unroll
-        for (int h = 0; h < 16; h += 2) {
-          const int hh = h0 + 16 * q16 + h;
-          const float m0 = ms.mrun[hh], m1 = ms.mrun[hh + 1];
-          const float p0 = exp2f(s[h] - (m0 == -INFINITY ? 0.f : m0));
-          const float p1 = exp2f(s[h + 1] - (m1 == -INFINITY ? 0.f : m1));
-          l[16 * q16 + h] += p0;
-          l[16 * q16 + h + 1] += p1;
-          pk[h >> 1] = pack_h2(p0, p1);
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-          *reinterpret_cast<uint4*>(sC + cswz(8, e, 4 * half + 2 * q16 + j)) =
-              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      for (int h = 0; h < 32; h += 2) {
+        const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pk[h >> 1]));
+        l[h] += pf.x;
+        l[h + 1] += pf.y;
       }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(sC + cswz(8, e, 4 * half + j)) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kPFull));
@@ -627,8 +629,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         st_cluster_f32(map_rank(smem_u32(&ml[(sp * 2 + 1) * 64 + wt]), p), s);
       }
     }
-    // unnormalised O^T rows (value dim 128 i + e, heads of this half) -> owner of the dim
-    for (int i = 0; i < 4; ++i) {
+    // unnormalised O^T rows (value dim 128 i + e, heads of this half) -> owner of the dim;
+    // the M-tile order is rotated by split rank so the CTAs of a cluster push to
+    // different owners at each step
+    for (int ii = 0; ii < 4; ++ii) {
+      const int i = (ii + sp) & 3;
       const int d = 128 * i + e;
       const uint32_t owner = (uint32_t)(d / Dn);
       const int dl = d - (int)owner * Dn;
@@ -684,24 +689,39 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     float* o = out.o + (int64_t)qi * H * kDV;
     const float* oe = out.o_ext ? out.o_ext + (int64_t)qi * H * kDV : nullptr;
     const int base = sp * Dn;
-    for (int j = wt; j < Dn * 16; j += kWorkers) {
-      const int dl = j % Dn, hq = j / Dn;   // value dim, head quad
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (uint32_t s = 0; s < nsplit; ++s) {
-        const float4 v = *reinterpret_cast<const float4*>(&recv[((size_t)s * Dn + dl) * kRecvStride + 4 * hq]);
-        const float4 w = *reinterpret_cast<const float4*>(&ml[(s * 2 + 0) * 64 + 4 * hq]);
-        acc.x += w.x * v.x; acc.y += w.y * v.y; acc.z += w.z * v.z; acc.w += w.w * v.w;
+    // item = (value dim dl, head quad hq) with dl fastest: the received rows are read
+    // as conflict-free 16-byte vectors, and each head's output row is written by
+    // consecutive threads (coalesced)
+    const int items = Dn * 16;
+    constexpr int kBatch = 4;
+    for (int j0 = 0; j0 < items; j0 += kWorkers * kBatch) {
+      float ext[kBatch][4];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * kWorkers + wt;
+        const int dl = j % Dn, hq = j / Dn;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int h = 4 * hq + k;
+          ext[u][k] = (oe && j < items && h < H && ms.alpha[h] > 0.f) ? oe[(int64_t)h * kDV + base + dl] : 0.f;
+        }
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int h = 4 * hq + k;
-        if (h < H) {
-          float val = k == 0 ? acc.x : (k == 1 ? acc.y : (k == 2 ? acc.z : acc.w));
-          if (oe) {
-            const float we = ms.alpha[h];
-            if (we > 0.f) val += we * oe[(int64_t)h * kDV + base + dl];
-          }
-          o[(int64_t)h * kDV + base + dl] = val;
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * kWorkers + wt;
+        if (j >= items) continue;
+        const int dl = j % Dn, hq = j / Dn;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (uint32_t s = 0; s < nsplit; ++s) {
+          const float4 v = *reinterpret_cast<const float4*>(&recv[((size_t)s * Dn + dl) * kRecvStride + 4 * hq]);
+          const float4 w = *reinterpret_cast<const float4*>(&ml[(s * 2 + 0) * 64 + 4 * hq]);
+          acc.x += w.x * v.x; acc.y += w.y * v.y; acc.z += w.z * v.z; acc.w += w.w * v.w;
+        }
+        const float r4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int h = 4 * hq + k;
+          if (h < H) o[(int64_t)h * kDV + base + dl] = r4[k] + ms.alpha[h] * ext[u][k];
         }
       }
     }
