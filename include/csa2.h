@@ -127,6 +127,31 @@ CSA2_API int csa2_index_topk(int mode, int B, int T, int H_I,
                     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * csa2_index_topk_noalloc - csa2_index_topk without a caller workspace.
+ *
+ * Not part of the method (the pages describe no such call): the same selection
+ * as csa2_index_topk (same arguments, kernels and results), with its scratch in
+ * a fixed 8 MiB + 256 B device array inside this library, so the call allocates
+ * nothing and needs no workspace.
+ * Limit: B * T * (n_stride rounded up to 1024) <= 2^21 scores (e.g. 32 queries
+ *   over 65,536 entries); larger calls return CSA2_ERR_WORKSPACE and launch
+ *   nothing. REUSE has no limit (it uses no scratch).
+ * Set-up: the first FULL/REINDEX call on each device looks up the array's
+ *   address (cudaGetSymbolAddress, which may load the module); make that first
+ *   call before any stream capture. A failed lookup returns CSA2_ERR_CUDA.
+ * Nothing has to start at zero: the scores are written before they are read.
+ *   Device-check bits (CSA2_DEV_*) are recorded in the array's status word and
+ *   are not reported; use csa2_index_topk with a workspace to read them.
+ * One scratch per device: calls that may overlap on a device (two streams, two
+ *   threads) race on it and must be serialised by the caller.
+ */
+CSA2_API int csa2_index_topk_noalloc(int mode, int B, int T, int H_I,
+                    const void* q_idx, const float* w_idx,
+                    const void* z, int64_t n_stride, const int32_t* n_visible,
+                    int K, const int32_t* prev_idx, int32_t* out_idx, float* out_scores,
+                    void* stream);
+
+/*
  * csa2_sparse_decode - global branch: sparse MQA over the selected FP4 entries.
  *
  * For each query (b, t) and head h < H:

@@ -58,6 +58,7 @@ def _lib():
     vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
     L.csa2_encode_kv.argtypes = [vp, i32, i64, i32, vp, vp, i32, vp, vp, vp, vp, sz, vp]
     L.csa2_index_topk.argtypes = [i32, i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, vp, vp, vp, sz, vp]
+    L.csa2_index_topk_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, vp, vp, vp]
     L.csa2_sparse_decode.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, vp, vp, vp, sz, vp]
     L.csa2_swa_merge.argtypes = [i32, i32, i32, vp, vp, i64, vp, vp, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp]
     L.csa2_workspace_bytes.argtypes = [i32, i32, i32, i64, i32]
@@ -225,6 +226,42 @@ def csa2_index_topk(mode: int, q_idx: Optional[torch.Tensor], w_idx: Optional[to
     _check(L.csa2_index_topk(mode, B_, T_, H_I, _ptr(q_idx), _ptr(w_idx), _ptr(z), N, _ptr(n_visible), K,
                              _ptr(prev_idx), _ptr(out_idx), _ptr(out_scores), _ptr(ws), ws.numel(),
                              _stream(stream)), "csa2_index_topk")
+    return out_idx
+
+
+def csa2_index_topk_noalloc(mode: int, q_idx: Optional[torch.Tensor], w_idx: Optional[torch.Tensor],
+                            z: Optional[torch.Tensor], n_visible: Optional[torch.Tensor], K: int,
+                            out_idx: torch.Tensor, prev_idx: Optional[torch.Tensor] = None,
+                            out_scores: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """csa2_index_topk on the library's fixed device scratch: no workspace, and
+    nothing is allocated (out_idx [B, T, K] int32 is the caller's)."""
+    L = _lib()
+    _dev(out_idx, "out_idx", (torch.int32,))
+    B_, T_, K_ = out_idx.shape
+    if K_ != K:
+        raise ValueError("out_idx must be [B, T, K]")
+    if mode == REUSE:
+        if prev_idx is None:
+            raise ValueError("REUSE needs prev_idx")
+        _dev(prev_idx, "prev_idx", (torch.int32,), out_idx.shape)
+        _check(L.csa2_index_topk_noalloc(REUSE, B_, T_, 0, None, None, None, 0, None, K, _ptr(prev_idx),
+                                         _ptr(out_idx), None, _stream(stream)), "csa2_index_topk_noalloc(REUSE)")
+        return out_idx
+    _dev(q_idx, "q_idx", _B16)
+    H_I = q_idx.shape[2]
+    if q_idx.shape != (B_, T_, H_I, D_IDX):
+        raise ValueError("q_idx must be [B, T, H_I, 64]")
+    _dev(w_idx, "w_idx", (torch.float32,), (B_, T_, H_I))
+    _dev(z, "z", _B16)
+    N = z.shape[1]
+    if z.shape != (B_, N, D_IDX):
+        raise ValueError("z must be [B, N, 64]")
+    _dev(n_visible, "n_visible", (torch.int32,), (B_ * T_,))
+    if out_scores is not None:
+        _dev(out_scores, "out_scores", (torch.float32,), (B_, T_, K))
+    _check(L.csa2_index_topk_noalloc(mode, B_, T_, H_I, _ptr(q_idx), _ptr(w_idx), _ptr(z), N, _ptr(n_visible), K,
+                                     None, _ptr(out_idx), _ptr(out_scores), _stream(stream)),
+           "csa2_index_topk_noalloc")
     return out_idx
 
 

@@ -99,6 +99,34 @@ static int cuda_status(cudaError_t e) {
   return CSA2_ERR_CUDA;
 }
 
+// Scratch of csa2_index_topk_noalloc: the 256-byte status header, then room for
+// 2^21 fp32 indexer scores (8 MiB), e.g. 32 queries over 65,536 entries or
+// 4 queries over 262,144. It is part of the module image (zero at load).
+constexpr size_t kStaticScratchBytes = kWsHeader + (size_t(1) << 23);
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch for the current device, looked up once per
+// device (the lookup may load this module, so it must not run inside a stream
+// capture for the first time).
+static int static_scratch(void** out) {
+  static std::mutex mu;
+  static void* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= 64) return CSA2_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (p == nullptr) return CSA2_ERR_CUDA;
+    cache[dev] = p;
+  }
+  *out = cache[dev];
+  return CSA2_OK;
+}
+
 extern "C" {
 
 int csa2_version(void) { return 100; }
@@ -207,6 +235,22 @@ int csa2_index_topk(int mode, int B, int T, int H_I, const void* q_idx, const fl
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_topk_select(scores, stride, n_visible, (int)Q, n_stride, K, out_idx,
                                         out_scores, status, st));
+}
+
+int csa2_index_topk_noalloc(int mode, int B, int T, int H_I, const void* q_idx,
+                            const float* w_idx, const void* z, int64_t n_stride,
+                            const int32_t* n_visible, int K, const int32_t* prev_idx,
+                            int32_t* out_idx, float* out_scores, void* stream) {
+  // REUSE touches no scratch; the other modes run csa2_index_topk's own validation
+  // and kernels on the static scratch, which rejects more than 2^21 scores with
+  // CSA2_ERR_WORKSPACE before launching anything
+  void* scratch = nullptr;
+  if (mode != CSA2_MODE_REUSE) {
+    const int s = static_scratch(&scratch);
+    if (s != CSA2_OK) return s;
+  }
+  return csa2_index_topk(mode, B, T, H_I, q_idx, w_idx, z, n_stride, n_visible, K, prev_idx,
+                         out_idx, out_scores, scratch, scratch ? kStaticScratchBytes : 0, stream);
 }
 
 int csa2_sparse_decode(int B, int T, int H, const void* q, const uint8_t* kv_codes,
