@@ -18,10 +18,13 @@
 // 128x64 O^T accumulators live in TMEM.
 //
 // Warp roles (288 threads):
-//   warps 0-7  workers. Thread (warp w, lane) owns key row / TMEM lane
-//              32*(w%4)+lane and head half w/4: it dequantises half of its key
-//              row (FP4 gather prefetched one tile ahead in registers, or bf16
-//              rows landed by TMA), and runs the softmax for 32 heads of it:
+//   warps 0-7  workers. Warp w stages key rows 16w .. 16w+15 of each tile: the
+//              FP4 gather (prefetched one tile ahead in registers) is laid out
+//              so that one warp load reads 8 rows x 64 contiguous bytes, and
+//              each lane dequantises the pieces it loaded; bf16 window rows
+//              are landed by TMA and converted in place. For the softmax,
+//              thread (warp w, lane) owns key row / TMEM lane 32*(w%4)+lane
+//              and head half w/4, and runs the softmax for 32 heads of it:
 //              a lazy running max per head (rescale only when a score exceeds
 //              it by 2^8), p written as fp16 P^T over the rope chunk of C once
 //              the S^T product has read it.
@@ -141,10 +144,11 @@ template <bool kMax>
 __device__ __forceinline__ float red_op(float a, float b) { return kMax ? fmaxf(a, b) : a + b; }
 
 // Reduce 32 per-thread values (heads h0..h0+31) over the 128 threads of one head
-// half (4 warps, lane quarters 0..3), max or sum, into out[h0 .. h0+31].
+// half (4 warps, lane quarters 0..3), max or sum, into out[h0 .. h0+31] (or added
+// to it with kAcc).
 // Reduce-scatter inside each warp (31 shuffles), then across the 4 warps in
 // shared memory under named barrier `bid`.
-template <bool kMax>
+template <bool kMax, bool kAcc = false>
 __device__ __forceinline__ void reduce32(const float (&v)[32], Misc& ms, float* out, int h0, int lane,
                                          int quarter, int bid) {
   float a[16];
@@ -187,7 +191,7 @@ __device__ __forceinline__ void reduce32(const float (&v)[32], Misc& ms, float* 
     float r = ms.red[0][h0 + lane];
 #pragma unroll
     for (int k = 1; k < 4; ++k) r = red_op<kMax>(r, ms.red[k][h0 + lane]);
-    out[h0 + lane] = r;
+    out[h0 + lane] = kAcc ? out[h0 + lane] + r : r;
   }
   named_sync(bid, 128);
 }
@@ -209,50 +213,43 @@ __device__ __forceinline__ void load_scores16(uint32_t taddr, bool valid, float 
   for (int h = 0; h < 16; ++h) s[h] = valid ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
 }
 
-// Dequantise FP4 blocks [18*HALF, 18*HALF+18) of key row e that fall in chunk
-// group G into C. cw/sw hold the row's code bytes [144*HALF, +144) and the scale
-// bytes from 16*HALF (5 words).
-template <int HALF, int G>
-__device__ __forceinline__ void dequant_group(uint8_t* sC, int e, const uint4 (&cw)[9], const uint32_t (&sw)[5]) {
-  constexpr int g_lo = G < 4 ? 8 * G : 32, g_hi = G < 4 ? 8 * G + 8 : 36;
-  constexpr int h_lo = 18 * HALF, h_hi = 18 * HALF + 18;
-  constexpr int lo = g_lo > h_lo ? g_lo : h_lo, hi_ = g_hi < h_hi ? g_hi : h_hi;
+// Dequantise one 16-byte piece of FP4 codes (elements 32 pc .. 32 pc + 31 of key
+// row `row`, two 16-element blocks) into C: w holds the code bytes, s2 the two
+// scale bytes (block 2 pc in the low byte). The piece fills 16-byte slots
+// 4 (pc & 1) .. +3 of the row in chunk pc / 2.
+__device__ __forceinline__ void dequant_piece(uint8_t* sC, int row, int pc, const uint4& w, uint32_t s2) {
+  uint32_t sh;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sh) : "h"((uint16_t)s2));
+  const uint32_t sa = __byte_perm(sh, 0, 0x1010), sb = __byte_perm(sh, 0, 0x3232);
+  uint32_t hv[16];
+  e2m1x4_to_h2x2(w.x & 0xFFFFu, hv[0], hv[1]);
+  e2m1x4_to_h2x2(w.x >> 16, hv[2], hv[3]);
+  e2m1x4_to_h2x2(w.y & 0xFFFFu, hv[4], hv[5]);
+  e2m1x4_to_h2x2(w.y >> 16, hv[6], hv[7]);
+  e2m1x4_to_h2x2(w.z & 0xFFFFu, hv[8], hv[9]);
+  e2m1x4_to_h2x2(w.z >> 16, hv[10], hv[11]);
+  e2m1x4_to_h2x2(w.w & 0xFFFFu, hv[12], hv[13]);
+  e2m1x4_to_h2x2(w.w >> 16, hv[14], hv[15]);
 #pragma unroll
-  for (int blk = lo; blk < hi_; ++blk) {
-    const int rb = blk - h_lo;                       // block within the half row
-    const uint4 w4 = cw[rb >> 1];
-    const uint32_t clo = (rb & 1) ? w4.z : w4.x, chi = (rb & 1) ? w4.w : w4.y;
-    const int sbyte = blk - 16 * HALF;               // byte within the 5 scale words
-    const uint32_t s2 = e4m3_to_h2((sw[sbyte >> 2] >> (8 * (sbyte & 3))) & 0xFFu);
-    uint32_t hv[8];
-    e2m1x4_to_h2x2(clo & 0xFFFFu, hv[0], hv[1]);
-    e2m1x4_to_h2x2(clo >> 16, hv[2], hv[3]);
-    e2m1x4_to_h2x2(chi & 0xFFFFu, hv[4], hv[5]);
-    e2m1x4_to_h2x2(chi >> 16, hv[6], hv[7]);
+  for (int k = 0; k < 8; ++k) hv[k] = hmul2_u32(hv[k], sa);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) hv[k] = hmul2_u32(hv[k], s2);
-    const int c = blk >> 2, j = (blk & 3) * 2;
-    *reinterpret_cast<uint4*>(sC + cswz(c, e, j)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-    *reinterpret_cast<uint4*>(sC + cswz(c, e, j + 1)) = make_uint4(hv[4], hv[5], hv[6], hv[7]);
-  }
+  for (int k = 8; k < 16; ++k) hv[k] = hmul2_u32(hv[k], sb);
+  const int c = pc >> 1, j = (pc & 1) * 4;
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+    *reinterpret_cast<uint4*>(sC + cswz(c, row, j + s)) =
+        make_uint4(hv[4 * s], hv[4 * s + 1], hv[4 * s + 2], hv[4 * s + 3]);
 }
 
-template <int HALF>
-__device__ __forceinline__ void load_half_row(const uint8_t* cbase, const uint8_t* sbase, int ent,
-                                              uint4 (&cw)[9], uint32_t (&sw)[5]) {
+// One code piece and its two scale bytes of entry `ent` (zeros for ent < 0).
+__device__ __forceinline__ void load_piece(const uint8_t* cbase, const uint8_t* sbase, int ent, int pc,
+                                           uint4& w, uint32_t& s2) {
   if (ent >= 0) {
-    const uint4* cp = reinterpret_cast<const uint4*>(cbase + (int64_t)ent * CSA2_CODE_BYTES) + 9 * HALF;
-    const uint32_t* spt =
-        reinterpret_cast<const uint32_t*>(sbase + (int64_t)ent * CSA2_SCALE_BYTES) + 4 * HALF;
-#pragma unroll
-    for (int k = 0; k < 9; ++k) cw[k] = __ldg(cp + k);
-#pragma unroll
-    for (int k = 0; k < 5; ++k) sw[k] = __ldg(spt + k);
+    w = __ldg(reinterpret_cast<const uint4*>(cbase + (int64_t)ent * CSA2_CODE_BYTES) + pc);
+    s2 = __ldg(reinterpret_cast<const unsigned short*>(sbase + (int64_t)ent * CSA2_SCALE_BYTES) + pc);
   } else {
-#pragma unroll
-    for (int k = 0; k < 9; ++k) cw[k] = make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int k = 0; k < 5; ++k) sw[k] = 0u;
+    w = make_uint4(0, 0, 0, 0);
+    s2 = 0u;
   }
 }
 
@@ -285,10 +282,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kQReady), kWorkers);
-    for (int g = 0; g < 5; ++g) {
-      mbar_init(bar(kChunkFull + g), kWorkers);
-      mbar_init(bar(kGroupFree + g), 1);
-    }
+    mbar_init(bar(kChunkFull), kWorkers);
+    for (int g = 0; g < 5; ++g) mbar_init(bar(kGroupFree + g), 1);
     mbar_init(bar(kSFull), 1);
     mbar_init(bar(kSFull + 1), 1);
     mbar_init(bar(kPFull), kWorkers);
@@ -357,30 +352,42 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     const uint8_t* cbase = nullptr;
     const uint8_t* sbase = nullptr;
     const int32_t* idx_row = nullptr;
-    uint4 cw[9];
-    uint32_t sw[5];
-    int ent = -1, ent_next = -1;
-    // entry index of this thread's key row in tile t (read one tile ahead of its use)
+    // gather layout of warp w (rows 16w .. 16w+15 of a tile): for chunk group g < 4
+    // (code pieces 4g .. 4g+3) lane l takes piece 4g + (l & 3) of rows ra and rb;
+    // for group 4 (pieces 16, 17) piece 16 + (l & 1) of row rc
+    const int ra = 16 * warp + (lane >> 2), rb = ra + 8, rc = 16 * warp + (lane >> 1);
+    uint4 cw[9];       // pieces [2g + k] (g < 4, k: row ra / rb) and [8] (group 4)
+    uint32_t sw[5];    // their scale byte pairs: [g] = row ra | row rb << 16, [4] group 4
+    int ent16 = -1, ent16_next = -1;  // entry of row 16w + lane (lanes < 16), this / next tile
     auto read_idx = [&](int t) -> int {
-      const int p = p_begin + t * kTK + e;
-      int v = (t < ntiles && p < p_end) ? idx_row[p] : -1;
+      const int p = p_begin + t * kTK + 16 * warp + lane;
+      int v = (lane < 16 && t < ntiles && p < p_end) ? idx_row[p] : -1;
       if (v < -1 || v >= fsrc.n_stride) {
         atomicOr(status, CSA2_DEV_BAD_INDEX);
         v = -1;
       }
       return v;
     };
-    auto fetch = [&](int which) {
-      ent = which;
-      if (half == 0) load_half_row<0>(cbase, sbase, ent, cw, sw);
-      else load_half_row<1>(cbase, sbase, ent, cw, sw);
+    auto fetch = [&](int e16) {
+      ent16 = e16;
+      const int ea = __shfl_sync(0xffffffffu, e16, lane >> 2);
+      const int eb = __shfl_sync(0xffffffffu, e16, 8 + (lane >> 2));
+      const int ec = __shfl_sync(0xffffffffu, e16, lane >> 1);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t s0, s1;
+        load_piece(cbase, sbase, ea, 4 * g + (lane & 3), cw[2 * g], s0);
+        load_piece(cbase, sbase, eb, 4 * g + (lane & 3), cw[2 * g + 1], s1);
+        sw[g] = s0 | (s1 << 16);
+      }
+      load_piece(cbase, sbase, ec, 16 + (lane & 1), cw[8], sw[4]);
     };
     if (kFp4) {
       cbase = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
       sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
       idx_row = fsrc.idx + (int64_t)qi * fsrc.K;
       if (ntiles > 0) fetch(read_idx(0));
-      ent_next = read_idx(1);
+      ent16_next = read_idx(1);
     }
     wok = mbar_wait(bar(kQTma), 0);
     if (!wok) fail();
@@ -399,9 +406,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     }
     mbar_arrive(bar(kQReady));
 
-    float l[32];  // running sums of this key row's p, for the 32 heads of this half
-#pragma unroll
-    for (int h = 0; h < 32; ++h) l[h] = 0.f;
+    // running sums of p per head (ms.lsum) are accumulated tile by tile
+    if (quarter == 0) ms.lsum[32 * half + lane] = 0.f;
     int issued_t = -1, waited_t = -1;  // TMA window loads (wt == 0)
 
     for (int t = 0; t < ntiles; ++t) {
@@ -413,24 +419,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         for (int g = 0; g < 5; ++g) {
           if (ok && t > 0 && !mbar_wait(bar(kGroupFree + g), (t - 1) & 1)) { fail(); ok = false; }
           if (ok) {
-            if (g == 0 && half == 0) ms.valid[sb][e] = ent;
-            if (half == 0) {
-              if (g == 0) dequant_group<0, 0>(sC, e, cw, sw);
-              if (g == 1) dequant_group<0, 1>(sC, e, cw, sw);
-              if (g == 2) dequant_group<0, 2>(sC, e, cw, sw);
+            if (g == 0 && lane < 16) ms.valid[sb][16 * warp + lane] = ent16;
+            if (g < 4) {
+              dequant_piece(sC, ra, 4 * g + (lane & 3), cw[2 * g], sw[g] & 0xFFFFu);
+              dequant_piece(sC, rb, 4 * g + (lane & 3), cw[2 * g + 1], sw[g] >> 16);
             } else {
-              if (g == 2) dequant_group<1, 2>(sC, e, cw, sw);
-              if (g == 3) dequant_group<1, 3>(sC, e, cw, sw);
-              if (g == 4) dequant_group<1, 4>(sC, e, cw, sw);
+              dequant_piece(sC, rc, 16 + (lane & 1), cw[8], sw[4]);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(kChunkFull + g));
           }
         }
+        // the whole tile is staged: one release for all 36 S^T MMAs (the issuing
+        // thread then runs them back to back)
+        fence_proxy_async_smem();
+        if (ok) mbar_arrive(bar(kChunkFull));
         wok = ok;
         if (wok && t + 1 < ntiles) {
-          fetch(ent_next);
-          ent_next = read_idx(t + 2);
+          fetch(ent16_next);
+          ent16_next = read_idx(t + 2);
         }
       } else {
         bool ok = wok && !*abort_flag;
@@ -460,16 +465,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
                 *pp = v;
               }
             }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(kChunkFull + g));
           }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(kChunkFull));
         }
         wok = ok;
       }
 
       // ---- softmax of this tile for heads [32*half, 32*half+32)
-      bool got = wok && !*abort_flag && mbar_wait(bar(kSFull + sb), (t >> 1) & 1) &&
-                 mbar_wait(bar(kChunkFull + 4), t & 1);
+      bool got = wok && !*abort_flag && mbar_wait(bar(kSFull + sb), (t >> 1) & 1);
       if (!named_and(bid, 128, got)) { if (e == 0) fail(); wok = false; break; }
       tc_fence_after();
       const bool vld = ms.valid[sb][e] >= 0;
@@ -508,21 +512,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
             ms.alpha[h0 + lane] = mo == mn ? 1.f : exp2f(mo - mn);
           }
           named_sync(bid, 128);
-#pragma unroll
-          for (int h = 0; h < 32; ++h) l[h] *= ms.alpha[h0 + h];
-          for (int i = 0; i < 4; ++i) {
-            uint32_t r[32];
-            const uint32_t ta = tmem + lane_off + kColO + 64 * i + 32 * half;
-            tmem_ld32(ta, r);
+          if (quarter == 0) ms.lsum[h0 + lane] *= ms.alpha[h0 + lane];
+          for (int i = 0; i < 8; ++i) {
+            uint32_t r[16];
+            const uint32_t ta = tmem + lane_off + kColO + 64 * (i >> 1) + 32 * half + 16 * (i & 1);
+            tmem_ld16(ta, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * ms.alpha[h0 + k]);
-            tmem_st32(ta, r);
+            for (int k = 0; k < 16; ++k)
+              r[k] = __float_as_uint(__uint_as_float(r[k]) * ms.alpha[h0 + 16 * (i & 1) + k]);
+            tmem_st16(ta, r);
           }
           tmem_wait_st();
           named_sync(bid, 128);
           if (quarter == 0) ms.mrun[h0 + lane] = fmaxf(ms.mrun[h0 + lane], ms.mnew[h0 + lane]);
           named_sync(bid, 128);
+          // the scores again (S^T of this tile is intact until the QK of tile t+2)
+          load_scores32(s_addr, vld, scale_log2, s);
 #pragma unroll
           for (int h = 0; h < 32; h += 2) {
             const float m0 = ms.mrun[h0 + h], m1 = ms.mrun[h0 + h + 1];
@@ -531,13 +537,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
           }
         }
       }
-      // the sums use the fp16 p that P.V consumes
-#pragma unroll
-      for (int h = 0; h < 32; h += 2) {
-        const float2 pf = __half22float2(*reinterpret_cast<const __half2*>(&pk[h >> 1]));
-        l[h] += pf.x;
-        l[h + 1] += pf.y;
-      }
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         *reinterpret_cast<uint4*>(sC + cswz(8, e, 4 * half + j)) =
@@ -545,6 +544,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kPFull));
+      // the sums use the fp16 p that P.V consumes (while P.V runs)
+      {
+        float pf[32];
+#pragma unroll
+        for (int h = 0; h < 32; h += 2) {
+          const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&pk[h >> 1]));
+          pf[h] = f2.x;
+          pf[h + 1] = f2.y;
+        }
+        reduce32<false, true>(pf, ms, ms.lsum, h0, lane, quarter, bid);
+      }
     }
     if (!kFp4 && wt == 0 && issued_t > waited_t) mbar_wait(bar(kTmaFull), issued_t & 1);
 
@@ -553,7 +563,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       wok = named_and(bid, 128, mbar_wait(bar(kGroupFree + 4), (ntiles - 1) & 1));
       if (!wok && e == 0) fail();
     }
-    reduce32<false>(l, ms, ms.lsum, 32 * half, lane, quarter, bid);
   } else {
     // ======================= MMA issuer =======================
     if (lane == 0) {
@@ -566,22 +575,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         if (*abort_flag) break;
         const int sb = t & 1;
         const uint32_t d_s = tmem + kColS + 64 * sb;
-        for (int g = 0; g < 5 && ok; ++g) {
-          if (!mbar_wait(bar(kChunkFull + g), t & 1)) { fail(); ok = false; break; }
-          tc_fence_after();
-          const int c0 = g < 4 ? 2 * g : 8, nc = g < 4 ? 2 : 1;
-          for (int cc = 0; cc < nc; ++cc) {
-            const int c = c0 + cc;
+        // one wait, then the 36 S^T MMAs back to back: a barrier poll between MMA
+        // batches would let the tensor pipe drain
+        if (!mbar_wait(bar(kChunkFull), t & 1)) { fail(); ok = false; break; }
+        tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = umma_desc_sw128(uC + c * kCChunk + 32 * k);
-              const uint64_t bq = umma_desc_sw128(uQ + c * kQChunk + 32 * k);
-              umma_f16(d_s, a, bq, idesc_qk, (c | k) != 0);
-              issued = true;
-            }
+        for (int c = 0; c < 9; ++c) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = umma_desc_sw128(uC + c * kCChunk + 32 * k);
+            const uint64_t bq = umma_desc_sw128(uQ + c * kQChunk + 32 * k);
+            umma_f16(d_s, a, bq, idesc_qk, (c | k) != 0);
           }
         }
-        if (!ok) break;
+        issued = true;
         umma_commit(bar(kSFull + sb));
         if (!mbar_wait(bar(kPFull), t & 1)) { fail(); ok = false; break; }
         tc_fence_after();
