@@ -4,9 +4,11 @@
 Workload (one "step"): a decode step of a three-layer CSA2 group FULL -> REINDEX ->
 REUSE for 32 sequences at 128K context (32768 compressed entries each), 64 query
 heads, latent 512 + rope 64 in FP4 (E2M1 + E4M3 per 16), indexer 8 x 64 in bf16,
-top-K 2048, sliding window 128. Per layer: csa2_index_topk -> csa2_sparse_decode ->
-csa2_swa_merge (REUSE skips the indexer). The KV caches and keys are resident in HBM
-(written before timing); each timed step re-reads them.
+top-K 2048, sliding window 128. Per layer: csa2_index_topk, then attention over the
+selected entries and the window in one csa2_decode_attention call (or, with
+--attn two-call, csa2_sparse_decode followed by csa2_swa_merge); REUSE skips the
+indexer. The KV caches and keys are resident in HBM (written before timing); each
+timed step re-reads them, and L2 is flushed between steps.
 
 Prints one JSON line (rank 0). --impl reference times the CPU oracle on a bounded
 sample of the same workload instead.
@@ -265,15 +267,22 @@ def run_ours(args):
             calls.append(("index_topk[REUSE]", "reuse",
                           (lambda cur=cur: L.csa2_index_topk(2, cfg.B, cfg.T, 0, None, None, None, 0, None,
                                                              cfg.K, P(cur), P(cur), None, None, 0, sp))))
-        calls.append((f"sparse_decode[{ci.MODE_NAMES[mode]}]", "sparse",
-                      (lambda d=d, cur=cur: L.csa2_sparse_decode(
-                          cfg.B, cfg.T, cfg.H, P(d["q"]), P(codes), P(scales), cfg.N, P(cur), cfg.K, cfg.d_v,
-                          scale, P(d["o"]), P(d["lse"]), wsp, wsn, sp))))
-        calls.append((f"swa_merge[{ci.MODE_NAMES[mode]}]", "swa",
-                      (lambda d=d: L.csa2_swa_merge(
-                          cfg.B, cfg.T, cfg.H, P(d["q"]), P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v,
-                          scale, P(d["o"]), P(d["lse"]), P(d["o"]), P(d["lse"]), wsp, wsn, sp))))
-    launches_per_call = {"index": 2, "reuse": 0, "sparse": 2, "swa": 2}
+        if args.attn == "fused":
+            calls.append((f"decode_attention[{ci.MODE_NAMES[mode]}]", "attn",
+                          (lambda d=d, cur=cur: L.csa2_decode_attention(
+                              cfg.B, cfg.T, cfg.H, P(d["q"]), P(codes), P(scales), cfg.N, P(cur), cfg.K,
+                              P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v, scale, P(d["o"]), P(d["lse"]),
+                              wsp, wsn, sp))))
+        else:
+            calls.append((f"sparse_decode[{ci.MODE_NAMES[mode]}]", "sparse",
+                          (lambda d=d, cur=cur: L.csa2_sparse_decode(
+                              cfg.B, cfg.T, cfg.H, P(d["q"]), P(codes), P(scales), cfg.N, P(cur), cfg.K, cfg.d_v,
+                              scale, P(d["o"]), P(d["lse"]), wsp, wsn, sp))))
+            calls.append((f"swa_merge[{ci.MODE_NAMES[mode]}]", "swa",
+                          (lambda d=d: L.csa2_swa_merge(
+                              cfg.B, cfg.T, cfg.H, P(d["q"]), P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v,
+                              scale, P(d["o"]), P(d["lse"]), P(d["o"]), P(d["lse"]), wsp, wsn, sp))))
+    launches_per_call = {"index": 2, "reuse": 0, "attn": 1, "sparse": 1, "swa": 1}
 
     def cuchk(r):
         err = r[0] if isinstance(r, tuple) else r
@@ -300,8 +309,14 @@ def run_ours(args):
     st, flags = csa2.csa2_read_device_status(ws, stream)
     if st != 0:
         raise RuntimeError(f"device status {st} flags {flags}")
+    # the timed graph has no event nodes between the kernels (each kernel may then
+    # start while its predecessor drains: programmatic dependent launch); a second
+    # graph with an event around every call gives the per-call breakdown
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
+        enqueue_step(record=False)
+    graph_calls = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_calls, stream=stream):
         enqueue_step(record=True)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -309,6 +324,8 @@ def run_ours(args):
         with torch.cuda.stream(stream):
             flush.fill_(1)
             graph.replay()
+            flush.fill_(1)
+            graph_calls.replay()
     torch.cuda.synchronize()
 
     gpu_uuid = None
@@ -324,22 +341,30 @@ def run_ours(args):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    per_call = [[] for _ in calls]
-    step_ms = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):
+        for e0, e1 in ev:
             flush.fill_(1)
+            e0.record(stream)
             graph.replay()
-        stream.synchronize()
-        for i in range(len(calls)):
-            per_call[i].append(cuchk(cu.cuEventElapsedTime(events[i], events[i + 1])))
-        step_ms.append(cuchk(cu.cuEventElapsedTime(events[0], events[-1])))
-    torch.cuda.synchronize()
+            e1.record(stream)
+    stream.synchronize()
     wall = time.perf_counter() - wall0
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
+    # per-call breakdown (separate pass, events between the calls)
+    per_call = [[] for _ in calls]
+    for _ in range(min(args.steps, 200)):
+        with torch.cuda.stream(stream):
+            flush.fill_(1)
+            graph_calls.replay()
+        stream.synchronize()
+        for i in range(len(calls)):
+            per_call[i].append(cuchk(cu.cuEventElapsedTime(events[i], events[i + 1])))
+    torch.cuda.synchronize()
 
     total_s = sum(step_ms) / 1e3
     if world > 1:
@@ -365,6 +390,7 @@ def run_ours(args):
     flops_swa = 2.0 * Q * cfg.H * cfg.W * (576 + cfg.d_v)
     models = {
         "index": ("hbm", Q * cfg.N * KEY_BYTES, "GB/s", peaks["hbm"]),
+        "attn": ("tensor", flops_sparse + flops_swa, "TFLOP/s", peaks["bf16"]),
         "sparse": ("tensor", flops_sparse, "TFLOP/s", peaks["bf16"]),
         "swa": ("tensor", flops_swa, "TFLOP/s", peaks["bf16"]),
     }
@@ -380,8 +406,9 @@ def run_ours(args):
             rows[k] = {"bound": b, "achieved": round(a, 2), "peak": pk, "unit": u, "frac": round(a / pk, 4),
                        "us_per_call": round(tl * 1e6, 2)}
     roofline = {"kernel": {"index": "csa2_index_topk (indexer score + top-K select kernels)",
-                           "sparse": "csa2_sparse_decode (gather/dequant/MMA + combine kernels)",
-                           "swa": "csa2_swa_merge"}[dom],
+                           "attn": "csa2_decode_attention (attn_tc_kernel, FP4 entries + window)",
+                           "sparse": "csa2_sparse_decode (attn_tc_kernel)",
+                           "swa": "csa2_swa_merge (attn_tc_kernel)"}[dom],
                 "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                 "frac": round(achieved / peak, 4), "peak_source": peaks["src"], "traffic": None}
 
@@ -412,6 +439,7 @@ def run_ours(args):
             "frac_of_8tbs": round(bytes_step / (ms_per_step * 1e-3) / 1e9 / TARGET_HBM_GBS, 4),
             "bytes_per_step": bytes_step,
             "roofline": roofline, "roofline_by_call": rows, "calls": breakdown,
+            "calls_note": "per-call means from a separate pass with an event between calls",
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": n_launch,
             "wall_s_timed_loop": round(wall, 3),
             "ced_projection": ced,
@@ -497,11 +525,9 @@ def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bu
                 r = L.csa2_index_topk(d["mode"], cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N,
                                       P(nvis), cfg.K, None, P(cur), None, wsp, wsn, sp)
                 assert r == 0
-            r = L.csa2_sparse_decode(cfg.B, cfg.T, cfg.H, P(d["q"]), P(codes), P(scales), cfg.N, P(cur), cfg.K,
-                                     cfg.d_v, scale, P(d["o"]), P(d["lse"]), wsp, wsn, sp)
-            assert r == 0
-            r = L.csa2_swa_merge(cfg.B, cfg.T, cfg.H, P(d["q"]), P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W,
-                                 cfg.d_v, scale, P(d["o"]), P(d["lse"]), P(d["o"]), P(d["lse"]), wsp, wsn, sp)
+            r = L.csa2_decode_attention(cfg.B, cfg.T, cfg.H, P(d["q"]), P(codes), P(scales), cfg.N, P(cur),
+                                        cfg.K, P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v, scale,
+                                        P(d["o"]), P(d["lse"]), wsp, wsn, sp)
             assert r == 0
         with torch.cuda.stream(stream):
             for h, dd in host_out:
@@ -538,6 +564,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ced", action="store_true")
+    ap.add_argument("--attn", choices=["fused", "two-call"], default="fused",
+                    help="attention per layer: one csa2_decode_attention call, or sparse_decode + swa_merge")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

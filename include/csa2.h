@@ -190,6 +190,24 @@ CSA2_API int csa2_swa_merge(int B, int T, int H, const void* q,
                    int d_v, float softmax_scale, const float* o_g, const float* lse_g,
                    float* o_out, float* lse_out, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * csa2_decode_attention - both attention branches of a decode step in one call:
+ * one softmax over the union of the selected FP4 entries (as csa2_sparse_decode)
+ * and the window rows (as csa2_swa_merge), which equals csa2_sparse_decode
+ * followed by csa2_swa_merge (the log-sum-exp merge of the two branches is the
+ * softmax over both key sets; CSA2 sparse + sliding-window attention, blog repost).
+ * Arguments as in those two calls; o: fp32 [B][T][H][d_v], lse: fp32 [B][T][H]
+ * (nullable). Limits: H % 16 == 0, H <= 64, d_v == 512, K <= 4096, n_win <= 256.
+ * An empty selection and an empty window give O = 0 and LSE = -inf. ws: the
+ * 256-byte status header is enough.
+ */
+CSA2_API int csa2_decode_attention(int B, int T, int H, const void* q,
+                   const uint8_t* kv_codes, const uint8_t* kv_scales, int64_t n_stride,
+                   const int32_t* idx, int K, const void* swa_kv, int64_t s_stride,
+                   const int32_t* win_start, const int32_t* win_len, int n_win, int d_v,
+                   float softmax_scale, float* o, float* lse, void* ws, size_t ws_bytes,
+                   void* stream);
+
 /* Workspace bytes that cover every call above with these or smaller sizes: a
  * 256-byte header (the device status word) plus the fp32 indexer scores of
  * csa2_index_topk ([B*T][n_max rounded up to 1024]). The attention calls need

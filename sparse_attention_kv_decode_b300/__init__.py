@@ -60,6 +60,8 @@ def _lib():
     L.csa2_index_topk.argtypes = [i32, i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, vp, vp, vp, sz, vp]
     L.csa2_index_topk_noalloc.argtypes = [i32, i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, vp, vp, vp]
     L.csa2_sparse_decode.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, vp, vp, vp, sz, vp]
+    L.csa2_decode_attention.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, i64, vp, vp, i32, i32, f32,
+                                        vp, vp, vp, sz, vp]
     L.csa2_swa_merge.argtypes = [i32, i32, i32, vp, vp, i64, vp, vp, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp]
     L.csa2_workspace_bytes.argtypes = [i32, i32, i32, i64, i32]
     L.csa2_workspace_bytes.restype = sz
@@ -323,13 +325,57 @@ def csa2_swa_merge(q: torch.Tensor, swa_kv: torch.Tensor, win_start: torch.Tenso
     return o_out, lse_out
 
 
+def csa2_decode_attention(q: torch.Tensor, kv_codes: torch.Tensor, kv_scales: torch.Tensor, idx: torch.Tensor,
+                          swa_kv: torch.Tensor, win_start: torch.Tensor, win_len: torch.Tensor, n_win: int,
+                          softmax_scale: float = 1.0 / math.sqrt(D_KV), d_v: int = D_LATENT,
+                          o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          ws: Optional[torch.Tensor] = None, stream=None):
+    """Both branches in one softmax: q [B, T, H, 576] bf16 over the selected FP4 entries
+    (kv_codes [B, N, 288], kv_scales [B, N, 36], idx [B, T, K]) and the window rows of
+    swa_kv [B, S, 576] -> (O [B, T, H, d_v] fp32, LSE [B, T, H] fp32)."""
+    L = _lib()
+    _dev(q, "q", _B16)
+    B, T, H, _ = q.shape
+    _dev(kv_codes, "kv_codes", (torch.uint8,))
+    N = kv_codes.shape[1]
+    _dev(kv_codes, "kv_codes", (torch.uint8,), (B, N, CODE_BYTES))
+    _dev(kv_scales, "kv_scales", (torch.uint8,), (B, N, SCALE_BYTES))
+    _dev(idx, "idx", (torch.int32,))
+    K = idx.shape[2]
+    _dev(idx, "idx", (torch.int32,), (B, T, K))
+    _dev(swa_kv, "swa_kv", _B16)
+    S = swa_kv.shape[1]
+    _dev(swa_kv, "swa_kv", _B16, (B, S, D_KV))
+    _dev(win_start, "win_start", (torch.int32,), (B * T,))
+    _dev(win_len, "win_len", (torch.int32,), (B * T,))
+    if o is None:
+        o = torch.empty((B, T, H, d_v), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+    _dev(o, "o", (torch.float32,), (B, T, H, d_v))
+    _dev(lse, "lse", (torch.float32,), (B, T, H))
+    if ws is None:
+        ws = csa2_workspace(B, T, H, 0, K, device=q.device, stream=stream)
+    _check(L.csa2_decode_attention(B, T, H, _ptr(q), _ptr(kv_codes), _ptr(kv_scales), N, _ptr(idx), K,
+                                   _ptr(swa_kv), S, _ptr(win_start), _ptr(win_len), n_win, d_v,
+                                   float(softmax_scale), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "csa2_decode_attention")
+    return o, lse
+
+
 def decode_layer(mode: int, q: torch.Tensor, kv_codes: torch.Tensor, kv_scales: torch.Tensor,
                  swa_kv: torch.Tensor, win_start: torch.Tensor, win_len: torch.Tensor, n_win: int, K: int,
                  q_idx=None, w_idx=None, z=None, n_visible=None, prev_idx=None, ws=None, out_idx=None,
-                 softmax_scale: float = 1.0 / math.sqrt(D_KV), stream=None):
-    """One CSA2 layer: index_topk (by mode) -> sparse_decode -> swa_merge. Returns (O, LSE, idx)."""
+                 softmax_scale: float = 1.0 / math.sqrt(D_KV), fused: bool = True, stream=None):
+    """One CSA2 layer: index_topk (by mode), then attention over the selected entries and
+    the window: one csa2_decode_attention call (fused), or csa2_sparse_decode followed by
+    csa2_swa_merge. Returns (O, LSE, idx)."""
     idx = csa2_index_topk(mode, q_idx, w_idx, z, n_visible, K, prev_idx=prev_idx, out_idx=out_idx, ws=ws,
                           stream=stream)
+    if fused:
+        o, lse = csa2_decode_attention(q, kv_codes, kv_scales, idx, swa_kv, win_start, win_len, n_win,
+                                       softmax_scale, ws=ws, stream=stream)
+        return o, lse, idx
     o_g, lse_g = csa2_sparse_decode(q, kv_codes, kv_scales, idx, softmax_scale, ws=ws, stream=stream)
     o, lse = csa2_swa_merge(q, swa_kv, win_start, win_len, n_win, o_g, lse_g, softmax_scale, o_out=o_g,
                             lse_out=lse_g, ws=ws, stream=stream)

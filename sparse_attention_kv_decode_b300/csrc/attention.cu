@@ -204,14 +204,6 @@ __device__ __forceinline__ void load_scores32(uint32_t taddr, bool valid, float 
 #pragma unroll
   for (int h = 0; h < 32; ++h) s[h] = valid ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
 }
-// Same for 16 heads.
-__device__ __forceinline__ void load_scores16(uint32_t taddr, bool valid, float scale_log2, float (&s)[16]) {
-  uint32_t r[16];
-  tmem_ld16(taddr, r);
-  tmem_wait_ld();
-#pragma unroll
-  for (int h = 0; h < 16; ++h) s[h] = valid ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
-}
 
 // Dequantise one 16-byte piece of FP4 codes (elements 32 pc .. 32 pc + 31 of key
 // row `row`, two 16-element blocks) into C: w holds the code bytes, s2 the two
@@ -260,7 +252,12 @@ __device__ __forceinline__ void allow_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <bool kFp4>
+// Kernel kinds: FP4 entries only (global branch), window rows only (the window
+// branch, merged with an external global branch by log-sum-exp), or both key sets
+// in one softmax (the window rows are the first tiles of the last split).
+enum Kind { kSparse = 0, kWindow = 1, kFused = 2 };
+
+template <int kKind>
 __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, Fp4Src fsrc, RowSrc rsrc,
     const __grid_constant__ CUtensorMap tm_rows, int T, int H, float scale_log2, int split_len,
@@ -314,12 +311,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
   // reads global memory before it has completed.
   grid_dependency_wait();
 
-  // key range of this CTA
-  int p_begin, p_end, row_base = 0;
+  constexpr bool kFp4 = kKind != kWindow;   // FP4 entry tiles
+  constexpr bool kRows = kKind != kSparse;  // bf16 window row tiles
+  // key ranges of this CTA: window rows [r_begin, r_end) (tiles 0 .. nt_r-1), then
+  // FP4 entries [p_begin, p_end) of the index list (tiles nt_r ..)
+  int p_begin = 0, p_end = 0, r_begin = 0, r_end = 0, row_base = 0;
   if (kFp4) {
     p_begin = sp * split_len;
     p_end = min(p_begin + split_len, fsrc.K);
-  } else {
+  }
+  if (kRows) {
     int ws = rsrc.win_start[qi], wl = rsrc.win_len[qi];
     if (wl > rsrc.n_win) wl = rsrc.n_win;
     if (ws < 0 || wl < 0 || (int64_t)ws + wl > rsrc.s_stride) {
@@ -328,11 +329,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       if (ws < 0) { wl += ws; ws = 0; if (wl < 0) wl = 0; }
       if ((int64_t)ws + wl > rsrc.s_stride) wl = (int)(rsrc.s_stride > ws ? rsrc.s_stride - ws : 0);
     }
-    p_begin = sp * split_len;
-    p_end = min(p_begin + split_len, wl);
+    if (kKind == kWindow) {
+      r_begin = sp * split_len;
+      r_end = min(r_begin + split_len, wl);
+    } else if (sp == (int)nsplit - 1) {
+      r_end = wl;
+    }
     row_base = (int)((int64_t)b * rsrc.s_stride + ws);
   }
-  const int ntiles = p_end > p_begin ? (p_end - p_begin + kTK - 1) / kTK : 0;
+  const int nt_r = r_end > r_begin ? (r_end - r_begin + kTK - 1) / kTK : 0;
+  const int nt_f = p_end > p_begin ? (p_end - p_begin + kTK - 1) / kTK : 0;
+  const int ntiles = nt_r + nt_f;
 
   if (warp < 8) {
     // ======================= workers: loads / dequant + softmax =======================
@@ -344,9 +351,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     bool wok = true;                          // pipeline state (uniform within a head half)
     // Q: nine 64x64 swizzled TMA boxes (rows qi*H ..), converted to fp16 in place;
     // rows past H belong to other queries (or are zero) and feed unused heads.
+    int issued_t = -1, waited_t = -1;  // window tiles loaded by TMA (wt == 0)
     if (wt == 0) {
       mbar_arrive_expect_tx(bar(kQTma), 9 * kQChunk);
       for (int c = 0; c < 9; ++c) tma_load_2d(uQ + c * kQChunk, &tm_q, 64 * c, qi * H, bar(kQTma));
+      // the first window tile goes to the still empty tile buffer right away
+      if (kRows && nt_r > 0) {
+        mbar_arrive_expect_tx(bar(kTmaFull), 9 * kCChunk);
+        for (int c = 0; c < 9; ++c)
+          tma_load_2d(uC + c * kCChunk, &tm_rows, 64 * c, row_base + r_begin, bar(kTmaFull));
+        issued_t = 0;
+      }
     }
     // the FP4 gather of tile 0 is issued before the Q conversion so the two overlap
     const uint8_t* cbase = nullptr;
@@ -359,9 +374,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     uint4 cw[9];       // pieces [2g + k] (g < 4, k: row ra / rb) and [8] (group 4)
     uint32_t sw[5];    // their scale byte pairs: [g] = row ra | row rb << 16, [4] group 4
     int ent16 = -1, ent16_next = -1;  // entry of row 16w + lane (lanes < 16), this / next tile
-    auto read_idx = [&](int t) -> int {
-      const int p = p_begin + t * kTK + 16 * warp + lane;
-      int v = (lane < 16 && t < ntiles && p < p_end) ? idx_row[p] : -1;
+    auto read_idx = [&](int tf) -> int {  // tf: FP4 tile
+      const int p = p_begin + tf * kTK + 16 * warp + lane;
+      int v = (lane < 16 && tf < nt_f && p < p_end) ? idx_row[p] : -1;
       if (v < -1 || v >= fsrc.n_stride) {
         atomicOr(status, CSA2_DEV_BAD_INDEX);
         v = -1;
@@ -386,7 +401,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       cbase = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
       sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
       idx_row = fsrc.idx + (int64_t)qi * fsrc.K;
-      if (ntiles > 0) fetch(read_idx(0));
+      if (nt_f > 0) fetch(read_idx(0));
       ent16_next = read_idx(1);
     }
     wok = mbar_wait(bar(kQTma), 0);
@@ -408,12 +423,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
 
     // running sums of p per head (ms.lsum) are accumulated tile by tile
     if (quarter == 0) ms.lsum[32 * half + lane] = 0.f;
-    int issued_t = -1, waited_t = -1;  // TMA window loads (wt == 0)
 
     for (int t = 0; t < ntiles; ++t) {
       const int sb = t & 1;
       // ---- stage the tile into C (group by group, as P.V of tile t-1 releases it)
-      if (kFp4) {
+      const bool row_tile = kRows && t < nt_r;
+      if (kFp4 && !row_tile) {
+        const int tf = t - nt_r;
         bool ok = wok && !*abort_flag;
 #pragma unroll
         for (int g = 0; g < 5; ++g) {
@@ -433,23 +449,24 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         fence_proxy_async_smem();
         if (ok) mbar_arrive(bar(kChunkFull));
         wok = ok;
-        if (wok && t + 1 < ntiles) {
+        if (wok && tf + 1 < nt_f) {
           fetch(ent16_next);
-          ent16_next = read_idx(t + 2);
+          ent16_next = read_idx(tf + 2);
         }
-      } else {
+      } else if (kRows) {
         bool ok = wok && !*abort_flag;
         if (ok && t > 0 && !mbar_wait(bar(kGroupFree + 4), (t - 1) & 1)) { fail(); ok = false; }
-        if (ok && wt == 0) {
+        if (ok && wt == 0 && issued_t < t) {
           mbar_arrive_expect_tx(bar(kTmaFull), 9 * kCChunk);
           for (int c = 0; c < 9; ++c)
-            tma_load_2d(uC + c * kCChunk, &tm_rows, 64 * c, row_base + p_begin + t * kTK, bar(kTmaFull));
+            tma_load_2d(uC + c * kCChunk, &tm_rows, 64 * c, row_base + r_begin + t * kTK, bar(kTmaFull));
           issued_t = t;
         }
-        if (ok && half == 0) ms.valid[sb][e] = (p_begin + t * kTK + e < p_end) ? 1 : -1;
+        if (ok && half == 0) ms.valid[sb][e] = (r_begin + t * kTK + e < r_end) ? 1 : -1;
         if (ok && !mbar_wait(bar(kTmaFull), t & 1)) { fail(); ok = false; }
         if (ok && wt == 0) waited_t = t;
         if (ok) {
+          const bool row_ok = r_begin + t * kTK + e < r_end;
           // bf16 -> fp16 in place; half 0 converts the first 36 pieces of row e, half 1 the rest
           for (int g = 0; g < 5; ++g) {
             const int c0 = g < 4 ? 2 * g : 8, nc = g < 4 ? 2 : 1;
@@ -462,6 +479,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
                 uint4 v = *pp;
                 v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
                 v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
+                // rows past the window are zeroed: their p is 0, and 0 * NaN would not be
+                if (!row_ok) v = make_uint4(0, 0, 0, 0);
                 *pp = v;
               }
             }
@@ -556,7 +575,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         reduce32<false, true>(pf, ms, ms.lsum, h0, lane, quarter, bid);
       }
     }
-    if (!kFp4 && wt == 0 && issued_t > waited_t) mbar_wait(bar(kTmaFull), issued_t & 1);
+    if (kRows && wt == 0 && issued_t > waited_t) mbar_wait(bar(kTmaFull), issued_t & 1);
 
     // ---- wait for the last P.V, then the sums per head
     if (wok && ntiles > 0) {
@@ -748,15 +767,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
 
 // Launch the (split, query) grid as clusters of nsplit CTAs (a power of two <= 16),
 // allowing programmatic dependent launch after the preceding kernel.
-template <bool kFp4>
+template <int kKind>
 static cudaError_t launch_tc(const CUtensorMap& tq, const Fp4Src& f, const RowSrc& r,
                              const CUtensorMap& trows, int Q, int T, int H, float scale_log2,
                              int nsplit, int split_len, const OutArgs& out, uint32_t* status,
                              cudaStream_t st) {
-  cudaError_t e = set_attr_once(kFp4 ? 2 : 3, (const void*)attn_tc_kernel<kFp4>,
+  constexpr int kSlotSmem = kKind == kSparse ? 2 : (kKind == kWindow ? 3 : 9);
+  constexpr int kSlotCluster = kKind == kSparse ? 7 : (kKind == kWindow ? 8 : 10);
+  cudaError_t e = set_attr_once(kSlotSmem, (const void*)attn_tc_kernel<kKind>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTC);
   if (e != cudaSuccess) return e;
-  e = set_attr_once(kFp4 ? 7 : 8, (const void*)attn_tc_kernel<kFp4>,
+  e = set_attr_once(kSlotCluster, (const void*)attn_tc_kernel<kKind>,
                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -773,7 +794,7 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const Fp4Src& f, const RowSr
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kFp4>, tq, f, r, trows, T, H, scale_log2, split_len,
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<kKind>, tq, f, r, trows, T, H, scale_log2, split_len,
                             out, status);
 }
 
@@ -792,7 +813,7 @@ cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t
   memset(&dummy, 0, sizeof(dummy));
   if (!encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64)) return cudaErrorInvalidValue;
   OutArgs out{o_g, lse_g, nullptr, nullptr};
-  return launch_tc<true>(tq, f, r, dummy, Q, T, H, scale_log2, nsplit, split_len, out, status, st);
+  return launch_tc<kSparse>(tq, f, r, dummy, Q, T, H, scale_log2, nsplit, split_len, out, status, st);
 }
 
 cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa,
@@ -812,7 +833,28 @@ cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa
   Fp4Src f{nullptr, nullptr, 0, nullptr, 0};
   RowSrc r{s_stride, win_start, win_len, n_win};
   OutArgs out{o_out, lse_out, o_g, lse_g};
-  return launch_tc<false>(tq, f, r, tm, Q, T, H, scale_log2, nsplit, kTK, out, status, st);
+  return launch_tc<kWindow>(tq, f, r, tm, Q, T, H, scale_log2, nsplit, kTK, out, status, st);
+}
+
+cudaError_t launch_decode_attn(int B, int T, int H, const void* q, const uint8_t* codes,
+                               const uint8_t* scales, int64_t n_stride, const int32_t* idx, int K,
+                               const void* swa, int64_t s_stride, const int32_t* win_start,
+                               const int32_t* win_len, int n_win, float scale_log2, float* o,
+                               float* lse, int nsplit, uint32_t* status, cudaStream_t st) {
+  const int Q = B * T;
+  if (Q == 0) return cudaSuccess;
+  if (nsplit < 1 || nsplit > kMaxSplitsTC || (nsplit & (nsplit - 1))) return cudaErrorInvalidValue;
+  int split_len = (K + nsplit - 1) / nsplit;
+  split_len = (split_len + kTK - 1) / kTK * kTK;
+  Fp4Src f{codes, scales, n_stride, idx, K};
+  RowSrc r{s_stride, win_start, win_len, n_win};
+  CUtensorMap tq, tm;
+  memset(&tm, 0, sizeof(tm));
+  if (!encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64)) return cudaErrorInvalidValue;
+  if (s_stride > 0 && !encode_tensor_map_2d_bf16(&tm, swa, CSA2_D_KV, (uint64_t)B * s_stride, 64, kTK))
+    return cudaErrorInvalidValue;
+  OutArgs out{o, lse, nullptr, nullptr};
+  return launch_tc<kFused>(tq, f, r, tm, Q, T, H, scale_log2, nsplit, split_len, out, status, st);
 }
 
 }  // namespace csa2

@@ -301,4 +301,32 @@ int csa2_swa_merge(int B, int T, int H, const void* q, const void* swa_kv, int64
                                       (cudaStream_t)stream));
 }
 
+int csa2_decode_attention(int B, int T, int H, const void* q, const uint8_t* kv_codes,
+                          const uint8_t* kv_scales, int64_t n_stride, const int32_t* idx, int K,
+                          const void* swa_kv, int64_t s_stride, const int32_t* win_start,
+                          const int32_t* win_len, int n_win, int d_v, float softmax_scale, float* o,
+                          float* lse, void* ws, size_t ws_bytes, void* stream) {
+  CHECK_ARG(B >= 0 && T >= 0 && H >= 1 && K >= 1 && n_stride >= 0 && s_stride >= 0 && n_win >= 0);
+  CHECK_ARG(softmax_scale == softmax_scale);
+  if (H % 16 != 0 || H > 64 || d_v != CSA2_D_LATENT || K > kMaxK || n_win > kMaxWin)
+    return CSA2_ERR_UNSUPPORTED;
+  const int64_t Q = (int64_t)B * T;
+  if (Q == 0) return CSA2_OK;
+  CHECK_ARG(q && idx && o && win_start && win_len);
+  CHECK_ARG(n_stride == 0 || (kv_codes && kv_scales));
+  CHECK_ARG(s_stride == 0 || swa_kv != nullptr);
+  CHECK_ARG(aligned(q, 16) && aligned(kv_codes, 16) && aligned(kv_scales, 4) && aligned(idx, 4) &&
+            aligned(swa_kv, 16) && aligned(win_start, 4) && aligned(win_len, 4) && aligned(o, 16) &&
+            aligned(lse, 4));
+  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
+  CHECK_ARG(aligned(ws, 256));
+  if (ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
+  const int nsplit = attn_splits(Q, K, device_sm_count());
+  uint32_t* status = static_cast<uint32_t*>(ws);
+  const float scale_log2 = softmax_scale * 1.4426950408889634074f;
+  return cuda_status(launch_decode_attn(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K, swa_kv,
+                                        s_stride, win_start, win_len, n_win, scale_log2, o, lse,
+                                        nsplit, status, (cudaStream_t)stream));
+}
+
 }  // extern "C"

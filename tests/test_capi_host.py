@@ -110,3 +110,28 @@ def test_workspace_size_monotone(L):
     assert a == 256 + 32 * 32768 * 4                    # header + fp32 scores
     assert L.csa2_workspace_bytes(1, 1, 64, 0, 2048) == 256
     assert L.csa2_workspace_bytes(-1, 1, 64, 10, 10) == 0
+
+
+def test_decode_attention_validation(L):
+    r = L.csa2_decode_attention
+    f = ctypes.c_float(0.04)
+    args = [1, 1, 64, FAKE, FAKE, FAKE, 1024, FAKE, 128, FAKE, 128, FAKE, FAKE, 128, 512, f, FAKE, FAKE, FAKE,
+            1 << 30, None]
+
+    def call(**kw):
+        a = list(args)
+        for k, v in kw.items():
+            a[int(k[1:])] = v
+        return r(*a)
+
+    assert call(a2=20) == 2                       # heads not a multiple of 16
+    assert call(a13=300) == 2                     # window longer than 256
+    assert call(a8=5000) == 2                     # K above 4096
+    assert call(a14=576) == 2                     # d_v must be 512
+    assert call(a3=None) == 1                     # q missing
+    assert call(a9=None) == 1                     # window rows missing with s_stride > 0
+    assert call(a3=FAKE + 8) == 1                 # q not 16-byte aligned
+    assert call(a15=ctypes.c_float(float("nan"))) == 1
+    assert call(a18=None, a19=0) == 3             # no workspace
+    assert call(a19=128) == 3                     # workspace below the status header
+    assert call(a0=0) == 0                        # empty batch: nothing to do

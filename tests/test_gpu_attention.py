@@ -1,4 +1,5 @@
-"""Sparse decode + SWA merge parity against the FP64 oracle (max-abs 2e-3, rel-L2 1e-3).
+"""Sparse decode + SWA merge parity against the FP64 oracle (max-abs 2e-3, rel-L2 1e-3),
+through the two separate calls and through the one fused call (csa2_decode_attention).
 
 Ref: "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression": sparse attention
 over the whole context combined with a sliding-window branch (blog repost), the CSA2
@@ -34,7 +35,7 @@ def _oracle_query(q_bits_bt, rows_of, idx, swa_bits_b, ws, wl, cfg):
     return og, lg, O, L
 
 
-def _run_group(cfg, inp, sample=None):
+def _run_group(cfg, inp, sample=None, fused=True):
     """Run every layer of the group on the GPU; compare (sampled) queries with the oracle."""
     B, T = cfg.B, cfg.T
     ws = csa2.csa2_workspace(B, T, cfg.H, cfg.N, cfg.K, device=DEV)
@@ -55,7 +56,7 @@ def _run_group(cfg, inp, sample=None):
             kw = dict(q_idx=to_dev_bf16(L.q_idx, DEV), w_idx=to_dev(L.w_idx, DEV), z=to_dev_bf16(L.z, DEV),
                       n_visible=nvis)
         o, lse, idx = csa2.decode_layer(L.mode, qd, codes, scales, to_dev_bf16(L.swa, DEV), wst, wln, cfg.W,
-                                        cfg.K, prev_idx=prev, ws=ws, **kw)
+                                        cfg.K, prev_idx=prev, ws=ws, fused=fused, **kw)
         torch.cuda.synchronize()
         st, flags = csa2.csa2_read_device_status(ws)
         assert st == 0, (st, flags)
@@ -99,27 +100,31 @@ def _run_group(cfg, inp, sample=None):
     return results
 
 
-def test_tiny_config_layer():
-    _run_group(ci.TINY, ci.make_decode_inputs(ci.TINY))
+@pytest.mark.parametrize("fused", [True, False])
+def test_tiny_config_layer(fused):
+    _run_group(ci.TINY, ci.make_decode_inputs(ci.TINY), fused=fused)
 
 
-def test_scaled_group_full_reindex_reuse():
+@pytest.mark.parametrize("fused", [True, False])
+def test_scaled_group_full_reindex_reuse(fused):
     cfg = ci.scaled(ci.DECODE_128K, B=3, N=4096, K=512)
-    _run_group(cfg, ci.make_decode_inputs(cfg))
+    _run_group(cfg, ci.make_decode_inputs(cfg), fused=fused)
 
 
-@pytest.mark.parametrize("H,K,W", [(16, 200, 100), (32, 1000, 1), (48, 64, 256), (64, 130, 0)])
-def test_ragged_shapes(H, K, W):
-    cfg = ci.scaled(ci.DECODE_128K, B=2, N=1500, H=H, K=K, W=max(W, 1), modes=(ci.FULL, ci.REUSE))
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("H,K,W", [(16, 200, 100), (32, 1000, 1), (48, 64, 256), (64, 130, 0), (64, 2048, 200)])
+def test_ragged_shapes(H, K, W, fused):
+    cfg = ci.scaled(ci.DECODE_128K, B=2, N=2500, H=H, K=K, W=max(W, 1), modes=(ci.FULL, ci.REUSE))
     inp = ci.make_decode_inputs(cfg)
     if W == 0:
         inp.win_len[:] = 0
-    _run_group(cfg, inp)
+    _run_group(cfg, inp, fused=fused)
 
 
-def test_prefill_like_many_queries_causal():
+@pytest.mark.parametrize("fused", [True, False])
+def test_prefill_like_many_queries_causal(fused):
     cfg = ci.scaled(ci.PREFILL_CHUNK, T=37, N=1200, K=256, W=16)
-    _run_group(cfg, ci.make_decode_inputs(cfg))
+    _run_group(cfg, ci.make_decode_inputs(cfg), fused=fused)
 
 
 def test_global_equals_dense_when_k_covers_all():
@@ -158,6 +163,59 @@ def test_empty_selection_and_pure_swa():
     assert torch.all(o2 == 0) and torch.all(torch.isneginf(lse2))
 
 
+def test_fused_empty_branches():
+    """One call over an empty selection and/or an empty window."""
+    cfg = ci.scaled(ci.TINY, N=64, K=64, H=16, W=32)
+    inp = ci.make_decode_inputs(cfg)
+    L = inp.layers[0]
+    codes, scales = _cache(L.X)
+    q = to_dev_bf16(L.q, DEV)
+    swa = to_dev_bf16(L.swa, DEV)
+    wst = to_dev(inp.win_start, DEV)
+    none = torch.full((1, 1, 64), -1, dtype=torch.int32, device=DEV)
+    allk = torch.arange(64, dtype=torch.int32, device=DEV).reshape(1, 1, 64)
+    zero = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, lse = csa2.csa2_decode_attention(q, codes, scales, none, swa, wst, to_dev(inp.win_len, DEV), cfg.W,
+                                        cfg.softmax_scale)
+    torch.cuda.synchronize()
+    O, LSE = attention.swa_branch(f64(L.q[0, 0]), f64(L.swa[0]), 0, cfg.W, 512, cfg.softmax_scale)
+    check_attention(o[0, 0].cpu().numpy(), O, "window only")
+    check_lse(lse[0, 0].cpu().numpy(), LSE, "window only")
+    o, lse = csa2.csa2_decode_attention(q, codes, scales, allk, swa, wst, zero, cfg.W, cfg.softmax_scale)
+    torch.cuda.synchronize()
+    rows = fp4.decode(*fp4.encode(L.X[0]))
+    O, LSE = attention.attend(f64(L.q[0, 0]), rows, 512, cfg.softmax_scale)
+    check_attention(o[0, 0].cpu().numpy(), O, "entries only")
+    check_lse(lse[0, 0].cpu().numpy(), LSE, "entries only")
+    o, lse = csa2.csa2_decode_attention(q, codes, scales, none, swa, wst, zero, cfg.W, cfg.softmax_scale)
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_fused_window_rows_past_the_window_are_ignored():
+    """NaN rows right after the window (inside the same 128-row tile) must not leak into O."""
+    cfg = ci.scaled(ci.TINY, N=64, K=64, H=16, W=40)
+    inp = ci.make_decode_inputs(cfg)
+    L = inp.layers[0]
+    codes, scales = _cache(L.X)
+    S = 128
+    swa_bits = np.full((1, S, 576), 0x7FC0, dtype=np.uint16)   # bf16 NaN after the 40 window rows
+    swa_bits[0, :40] = L.swa[0, :40]
+    idx = torch.arange(64, dtype=torch.int32, device=DEV).reshape(1, 1, 64)
+    o, lse = csa2.csa2_decode_attention(to_dev_bf16(L.q, DEV), codes, scales, idx, to_dev_bf16(swa_bits, DEV),
+                                        torch.zeros(1, dtype=torch.int32, device=DEV),
+                                        torch.tensor([40], dtype=torch.int32, device=DEV), cfg.W,
+                                        cfg.softmax_scale)
+    torch.cuda.synchronize()
+    assert S > 40
+    rows = fp4.decode(*fp4.encode(L.X[0]))
+    og, lg = attention.attend(f64(L.q[0, 0]), rows, 512, cfg.softmax_scale)
+    os_, ls = attention.swa_branch(f64(L.q[0, 0]), f64(L.swa[0]), 0, 40, 512, cfg.softmax_scale)
+    O, LSE = attention.merge(og, lg, os_, ls)
+    check_attention(o[0, 0].cpu().numpy(), O, "fused, NaN past window")
+    check_lse(lse[0, 0].cpu().numpy(), LSE, "fused, NaN past window")
+
+
 def test_device_checks_flag_bad_index_and_window():
     cfg = ci.scaled(ci.TINY, N=64, K=64, H=16, W=32)
     inp = ci.make_decode_inputs(cfg)
@@ -185,9 +243,14 @@ def test_device_checks_flag_bad_index_and_window():
 
 def test_full_size_decode_128k_group_sampled():
     """The bench workload: 32 x 32768 entries, 64 heads, K = 2048, FULL -> REINDEX -> REUSE,
-    in the bench's launch configuration; 3 sequences checked against the oracle."""
+    in the bench's launch configuration (fused attention); 3 sequences checked against the oracle."""
     cfg = ci.DECODE_128K
     _run_group(cfg, ci.make_decode_inputs(cfg), sample=[0, 17, 31])
+
+
+def test_full_size_decode_128k_two_calls_sampled():
+    cfg = ci.DECODE_128K
+    _run_group(cfg, ci.make_decode_inputs(cfg), sample=[5], fused=False)
 
 
 def test_deterministic_outputs():
