@@ -131,15 +131,21 @@ CSA2_API int csa2_index_topk(int mode, int B, int T, int H_I,
  *
  * Not part of the method (the pages describe no such call): the same selection
  * as csa2_index_topk (same arguments, kernels and results), with its scratch in
- * a fixed 8 MiB + 256 B device array inside this library, so the call allocates
- * nothing and needs no workspace.
- * Limit: B * T * (n_stride rounded up to 1024) <= 2^21 scores (e.g. 32 queries
- *   over 65,536 entries); larger calls return CSA2_ERR_WORKSPACE and launch
- *   nothing. REUSE has no limit (it uses no scratch).
+ * a fixed device array inside this library (256 B header + 64 KiB of per-query
+ * score ranges + 8 MiB of scores), so the call allocates nothing and needs no
+ * workspace.
+ * Limit: csa2_workspace_bytes(B, T, *, n_stride, K) <= 256 B + 64 KiB + 8 MiB,
+ *   i.e. at most 2^21 padded scores (B * T * (n_stride rounded up to 1024), e.g.
+ *   32 queries over 65,536 entries) and 8192 queries; larger calls return
+ *   CSA2_ERR_WORKSPACE and launch nothing. REUSE has no limit (it uses no
+ *   scratch).
  * Set-up: the first FULL/REINDEX call on each device looks up the array's
  *   address (cudaGetSymbolAddress, which may load the module); make that first
  *   call before any stream capture. A failed lookup returns CSA2_ERR_CUDA.
- * Nothing has to start at zero: the scores are written before they are read.
+ * Starting values: the array is zero when the module loads, which is the state
+ *   the per-query score-range words must start in; each call leaves them zero
+ *   again (the selection is exact from any start, a non-zero leftover only
+ *   costs it an extra round). The scores are written before they are read.
  *   Device-check bits (CSA2_DEV_*) are recorded in the array's status word and
  *   are not reported; use csa2_index_topk with a workspace to read them.
  * One scratch per device: calls that may overlap on a device (two streams, two
@@ -209,12 +215,14 @@ CSA2_API int csa2_decode_attention(int B, int T, int H, const void* q,
                    void* stream);
 
 /* Workspace bytes that cover every call above with these or smaller sizes: a
- * 256-byte header (the device status word) plus the fp32 indexer scores of
- * csa2_index_topk ([B*T][n_max rounded up to 1024]). The attention calls need
+ * 256-byte header (the device status word), then for csa2_index_topk two uint32
+ * score-range words per query (B*T*8 bytes rounded up to 256) and the fp32
+ * indexer scores ([B*T][n_max rounded up to 1024]). The attention calls need
  * only the header. One workspace serves one stream at a time. */
 CSA2_API size_t csa2_workspace_bytes(int B, int T, int H, int64_t n_max, int K);
 
-/* Zero the workspace's status word and counters (once after allocation). */
+/* Zero the whole workspace (status word and score-range words) once after
+ * allocation; the calls keep the range words at zero between calls. */
 CSA2_API int csa2_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /*

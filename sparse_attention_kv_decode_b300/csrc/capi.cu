@@ -99,10 +99,11 @@ static int cuda_status(cudaError_t e) {
   return CSA2_ERR_CUDA;
 }
 
-// Scratch of csa2_index_topk_noalloc: the 256-byte status header, then room for
-// 2^21 fp32 indexer scores (8 MiB), e.g. 32 queries over 65,536 entries or
-// 4 queries over 262,144. It is part of the module image (zero at load).
-constexpr size_t kStaticScratchBytes = kWsHeader + (size_t(1) << 23);
+// Scratch of csa2_index_topk_noalloc: the 256-byte status header, the score
+// range words of up to 8192 queries (64 KiB), then room for 2^21 fp32 indexer
+// scores (8 MiB), e.g. 32 queries over 65,536 entries or 4 queries over 262,144.
+// It is part of the module image (zero at load).
+constexpr size_t kStaticScratchBytes = kWsHeader + 65536 + (size_t(1) << 23);
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 // Device address of g_static_scratch for the current device, looked up once per
@@ -150,12 +151,12 @@ size_t csa2_workspace_bytes(int B, int T, int H, int64_t n_max, int K) {
   if (B < 0 || T < 0 || H < 0 || n_max < 0 || K < 0) return 0;
   (void)H; (void)K;
   const int64_t Q = (int64_t)B * T;
-  return kWsHeader + scores_bytes(Q, n_max);
+  return kWsHeader + range_bytes(Q) + scores_bytes(Q, n_max);
 }
 
 int csa2_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   CHECK_ARG(ws != nullptr && ws_bytes >= kWsHeader && aligned(ws, 256));
-  return cuda_status(cudaMemsetAsync(ws, 0, kWsHeader, (cudaStream_t)stream));
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream));
 }
 
 int csa2_read_device_status(void* ws, void* stream, uint32_t* flags) {
@@ -225,16 +226,17 @@ int csa2_index_topk(int mode, int B, int T, int H_I, const void* q_idx, const fl
             aligned(n_visible, 4) && aligned(out_scores, 4));
   if (ws == nullptr) return CSA2_ERR_WORKSPACE;
   CHECK_ARG(aligned(ws, 256));
-  if (ws_bytes < kWsHeader + scores_bytes(Q, n_stride)) return CSA2_ERR_WORKSPACE;
+  if (ws_bytes < kWsHeader + range_bytes(Q) + scores_bytes(Q, n_stride)) return CSA2_ERR_WORKSPACE;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
-  float* scores = reinterpret_cast<float*>(wsb + kWsHeader);
+  uint32_t* range = reinterpret_cast<uint32_t*>(wsb + kWsHeader);
+  float* scores = reinterpret_cast<float*>(wsb + kWsHeader + range_bytes(Q));
   uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
   const int64_t stride = score_pad(n_stride);
   cudaError_t e = launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores,
-                                     stride, status, st);
+                                     stride, range, status, st);
   if (e != cudaSuccess) return cuda_status(e);
-  return cuda_status(launch_topk_select(scores, stride, n_visible, (int)Q, n_stride, K, out_idx,
-                                        out_scores, status, st));
+  return cuda_status(launch_topk_select(scores, stride, n_visible, (int)Q, n_stride, K, range,
+                                        out_idx, out_scores, status, st));
 }
 
 int csa2_index_topk_noalloc(int mode, int B, int T, int H_I, const void* q_idx,

@@ -32,6 +32,10 @@ inline int64_t score_pad(int64_t n) { return (n + kScoreTile - 1) / kScoreTile *
 int attn_splits(int64_t Q, int K, int n_sm);
 
 
+// Per-query score range words (two uint32 per query) that the scoring kernel
+// leaves for the selection; they sit right after the header, at a fixed offset
+// per query, and the selection sets them back to zero.
+inline size_t range_bytes(int64_t Q) { return ((size_t)Q * 8 + 255) / 256 * 256; }
 inline size_t scores_bytes(int64_t Q, int64_t n_stride) {
   return (size_t)Q * (size_t)score_pad(n_stride) * 4;
 }
@@ -52,12 +56,12 @@ bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inne
 cudaError_t launch_encode_quant(const void* h, int h_dtype, int64_t rows, uint8_t* codes,
                                 uint8_t* scales, cudaStream_t st);
 cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void* z,
-                               int64_t n_stride, const int32_t* n_visible, int B, int T,
-                               int H_I, float* scores, int64_t score_stride, uint32_t* status,
-                               cudaStream_t st);
-cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
-                               int Q, int64_t n_stride, int K, int32_t* out_idx, float* out_scores,
+                               int64_t n_stride, const int32_t* n_visible, int B, int T, int H_I,
+                               float* scores, int64_t score_stride, uint32_t* range,
                                uint32_t* status, cudaStream_t st);
+cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
+                               int Q, int64_t n_stride, int K, uint32_t* range, int32_t* out_idx,
+                               float* out_scores, uint32_t* status, cudaStream_t st);
 cudaError_t launch_copy_idx(const int32_t* src, int32_t* dst, int64_t n, cudaStream_t st);
 cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t* codes,
                                const uint8_t* scales, int64_t n_stride, const int32_t* idx,

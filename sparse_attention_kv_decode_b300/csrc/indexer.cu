@@ -62,6 +62,15 @@ __device__ __forceinline__ void load_q_frag(const uint16_t* q_idx, const float* 
   }
 }
 
+// Order-preserving map of fp32 to uint32 (no NaN); key 0 is never produced.
+__device__ __forceinline__ uint32_t f2key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 __device__ __forceinline__ int clamp_nvis(const int32_t* n_visible, int qi, int64_t n_stride) {
   int v = n_visible[qi];
   return v < 0 ? 0 : (v > n_stride ? (int)n_stride : v);
@@ -71,7 +80,8 @@ template <int NT>
 __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
     const uint16_t* __restrict__ q_idx, const float* __restrict__ w_idx,
     const uint16_t* __restrict__ z, int64_t n_stride, const int32_t* __restrict__ n_visible, int T,
-    int H_I, int Q, float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ status) {
+    int H_I, int Q, float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ range,
+    uint32_t* __restrict__ status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar_full = sbase + kScoreStages * kStageBytes;
@@ -137,6 +147,7 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
   uint32_t qa[NT][8];
   float wv[NT][2];
   int cur_q = -1;
+  uint32_t rmax = 0u, rmin_inv = 0u;  // score range of the current query seen by this warp
   int cons_n = 0;
   for (int gs = gs_begin; gs < gs_end; ++gs) {
     int qi;
@@ -150,6 +161,12 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
       break;
     }
     if (qi != cur_q) {
+      if (cur_q >= 0 && lane == 0 && rmax != 0u) {
+        atomicMax(range + 2 * cur_q, rmin_inv);
+        atomicMax(range + 2 * cur_q + 1, rmax);
+      }
+      rmax = 0u;
+      rmin_inv = 0u;
       load_q_frag<NT>(q_idx, w_idx, qi, H_I, g, tig, qa, wv);
       cur_q = qi;
     }
@@ -178,13 +195,23 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 1);
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 2);
       float* srow = scores + (int64_t)qi * score_stride + key0;
-      if (tig == 0 && r0 + g < keys) srow[r0 + g] = pg;
-      if (tig == 1 && r0 + g + 8 < keys) srow[r0 + g + 8] = pg8;
+      const bool ok0 = tig == 0 && r0 + g < keys, ok1 = tig == 1 && r0 + g + 8 < keys;
+      if (ok0) srow[r0 + g] = pg;
+      if (ok1) srow[r0 + g + 8] = pg8;
+      // the query's score range (for the selection's first histogram), kept per warp
+      // and flushed once per query
+      const uint32_t kk = ok0 ? f2key(pg) : (ok1 ? f2key(pg8) : 0u);
+      rmax = max(rmax, __reduce_max_sync(0xffffffffu, kk));
+      rmin_inv = max(rmin_inv, __reduce_max_sync(0xffffffffu, (ok0 || ok1) ? ~kk : 0u));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
     ++cons_n;
     if (threadIdx.x == 0 && ok) produce_next();
+  }
+  if (cur_q >= 0 && lane == 0 && rmax != 0u) {
+    atomicMax(range + 2 * cur_q, rmin_inv);
+    atomicMax(range + 2 * cur_q + 1, rmax);
   }
   // drain: copies in flight must land before the CTA exits
   if (threadIdx.x == 0) {
@@ -196,8 +223,8 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
 
 cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void* z,
                                int64_t n_stride, const int32_t* n_visible, int B, int T, int H_I,
-                               float* scores, int64_t score_stride, uint32_t* status,
-                               cudaStream_t st) {
+                               float* scores, int64_t score_stride, uint32_t* range,
+                               uint32_t* status, cudaStream_t st) {
   const int Q = B * T;
   if (n_stride == 0 || Q == 0) return cudaSuccess;
   const int64_t total = (int64_t)Q * ((n_stride + kStageKeys - 1) / kStageKeys);
@@ -213,13 +240,13 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
                       cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
     if (e != cudaSuccess) return e;
     index_score_kernel<1><<<(unsigned)grid, kScoreThreads, kScoreSmem, st>>>(
-        qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores, score_stride, status);
+        qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores, score_stride, range, status);
   } else {
     e = set_attr_once(6, (const void*)index_score_kernel<2>,
                       cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
     if (e != cudaSuccess) return e;
     index_score_kernel<2><<<(unsigned)grid, kScoreThreads, kScoreSmem, st>>>(
-        qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores, score_stride, status);
+        qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores, score_stride, range, status);
   }
   return cudaGetLastError();
 }
@@ -227,12 +254,23 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
 // ---------------------------------------------------------------------------
 // Top-K selection: one cluster of C CTAs per query
 // ---------------------------------------------------------------------------
-// CTA r of the cluster owns the visible entries [r*slice, (r+1)*slice) and keeps
-// their scores in shared memory. Every exchange is a push: before a cluster
-// barrier each CTA writes its record into slot r of every peer's receive
-// buffer (distributed shared memory stores, no remote loads), so after the
-// barrier all reads are local and no CTA touches a peer once it has passed
-// the last barrier.
+// CTA r of the cluster owns the visible entries [r*slice, (r+1)*slice) (slice a
+// multiple of 4) and lands their scores in shared memory with one bulk copy.
+// Every exchange is a push: before a cluster barrier each CTA writes its record
+// into slot r of every peer's receive buffer (distributed shared memory stores,
+// no remote loads), so after the barrier all reads are local and no CTA touches
+// a peer once it has passed the last barrier.
+//
+// Fast path (two barriers). The scoring kernel left the query's score range
+// [lo, hi] in the workspace; each CTA bins its scores into kNB monotone bins of
+// that range and pushes the 16-bit histogram. After the barrier every CTA knows
+// all histograms, hence the bin b* holding the K-th score, how many entries each
+// CTA has above it, and how many candidates (bin b*) each CTA holds. If they are
+// at most kCandCap, each CTA pushes its candidates; after the second barrier
+// every CTA ranks all candidates by (score desc, index asc), so it knows how
+// many each CTA contributes, i.e. its own output offset, with no further
+// exchange.
+// General path (range missing, or too many candidates in b*): rounds of
 //   round 0  min / max / count of the surviving candidates (+ the candidate
 //            list itself when small enough) -> every CTA knows the range
 //   round 1  histogram of the candidates over kNB monotone bins of that range
@@ -243,11 +281,11 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
 //            when they all tie, the lowest indices win
 //   output   selected counts are pushed, each CTA writes its selected indices
 //            at its prefix offset (ascending by construction).
-// The bin map floor((s - lo) * kNB / (hi - lo)) is monotone in s, so bins
-// never reorder scores; equal scores always share a bin.
-constexpr int kSelThreads = 512;
+// The bin map floor((s - lo) * kNB / (hi - lo)) (clamped) is monotone in s, so
+// bins never reorder scores; equal scores always share a bin.
+constexpr int kSelThreads = 1024;
 constexpr int kNBMax = 2048;        // histogram bins per refinement round (small clusters)
-constexpr int kNBMin = 512;         // (clusters of more than 4 CTAs)
+constexpr int kNBMin = 1024;        // (clusters of more than 4 CTAs)
 constexpr int kCandCap = 512;       // candidates resolved exactly by ranking
 constexpr int kMaxLevels = 12;
 constexpr int kMaxCluster = 16;
@@ -261,18 +299,21 @@ struct SelRec {
 struct SelShared {
   SelRec rec_in[kMaxCluster];           // pushed candidate statistics
   int sel_in[kMaxCluster];              // pushed selected counts
+  int above_r[kMaxCluster];             // entries above b* per CTA (fast path, pushed)
+  int cand_sel[kMaxCluster];            // selected candidates per CTA (fast path)
   uint32_t hist_local[kNBMax];
   int scan[kSelThreads / 32];
   float red_f[2][kSelThreads / 32];
   int red_i[kSelThreads / 32];
-  int bstar, above, cand_n;
+  int bstar, above, cand_n, my_above;
+  uint64_t bar_load;
   float cand_s[kCandCap];               // own candidates (compacted)
   int cand_i[kCandCap];
 };
 // Regions after the header start at a 128-byte boundary (the histogram pushes
 // are 16-byte vector stores).
 constexpr size_t kSelHdr = (sizeof(SelShared) + 127) & ~size_t(127);
-// followed in dynamic shared memory by: uint32_t hist_in[C][NB] (pushed histograms),
+// followed in dynamic shared memory by: uint16_t hist_in[C][NB] (pushed histograms),
 // float cand_in_s[C][kCandCap], int cand_in_i[C][kCandCap], float sc[slice_cap],
 // uint8_t state[slice_cap]
 
@@ -326,9 +367,144 @@ __device__ __forceinline__ void cluster_barrier() {
                    : "memory");
 }
 
+// Histogram of this CTA's surviving candidates over [lo, hi] into sh.hist_local,
+// pushed as 16-bit counts into slot r of every peer's hist_in.
+__device__ __forceinline__ void build_push_hist(SelShared& sh, uint16_t* hist_in, const float* sc,
+                                                const uint8_t* state, int my_len, float lo, float scl,
+                                                int NB, uint32_t C, uint32_t r) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < NB; i += kSelThreads) sh.hist_local[i] = 0u;
+  __syncthreads();
+  // loads first, 8 per thread in flight, then the atomics
+  for (int e0 = tid; e0 < my_len; e0 += 8 * kSelThreads) {
+    float v[8];
+    uint8_t s[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = e0 + k * kSelThreads;
+      v[k] = e < my_len ? sc[e] : 0.f;
+      s[k] = e < my_len ? state[e] : 1;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (s[k] == 0) atomicAdd(&sh.hist_local[bin_of(v[k], lo, scl, NB)], 1u);
+  }
+  __syncthreads();
+  for (int j = tid; j < (int)C * (NB / 8); j += kSelThreads) {
+    const int peer = j / (NB / 8), o8 = j % (NB / 8);
+    const uint32_t* h = &sh.hist_local[8 * o8];
+    const uint4 v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                               h[6] | (h[7] << 16));
+    st_remote_v4(&hist_in[r * NB + 8 * o8], peer, v);
+  }
+}
+
+// Suffix counts of the summed histograms: the bin b* with above < remaining <=
+// above + count(b*) goes to sh.bstar / sh.above (thread t owns bins from the top).
+__device__ __forceinline__ void find_bstar(SelShared& sh, const uint16_t* hist_in, int NB, uint32_t C,
+                                           int remaining) {
+  const int tid = threadIdx.x;
+  const int per = NB / kSelThreads;
+  const int btop = NB - 1 - per * tid;
+  uint32_t hs[kNBMax / kSelThreads];
+  int mine = 0;
+#pragma unroll
+  for (int k = 0; k < kNBMax / kSelThreads; ++k) {
+    uint32_t h = 0;
+    if (k < per)
+      for (int rr = 0; rr < (int)C; ++rr) h += hist_in[rr * NB + btop - k];
+    hs[k] = h;
+    mine += (int)h;
+  }
+  int total;
+  int above = block_excl_scan(mine, sh.scan, total);
+#pragma unroll
+  for (int k = 0; k < kNBMax / kSelThreads; ++k) {
+    if (k < per) {
+      const int h = (int)hs[k];
+      if (above < remaining && remaining <= above + h) {
+        sh.bstar = btop - k;
+        sh.above = above;
+      }
+      above += h;
+    }
+  }
+  __syncthreads();
+}
+
+// One round of the general path: min / max / count of this CTA's surviving
+// candidates (and the candidates themselves when few) pushed to every peer,
+// then a cluster barrier. Returns the cluster-wide range and count, and the
+// number of survivors in lower-ranked CTAs.
+__device__ __noinline__ void stats_round(SelShared& sh, float* cand_in_s, int* cand_in_i, const float* sc,
+                                         const uint8_t* state, int my0, int my_len, uint32_t C, uint32_t r,
+                                         float& glo, float& ghi, int& gcnt, int& pre_cnt, int& mine_cnt) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float lo = INFINITY, hi = -INFINITY;
+  int cnt = 0;
+  for (int e = tid; e < my_len; e += kSelThreads)
+    if (state[e] == 0) {
+      const float v = sc[e];
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+      ++cnt;
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  }
+  if (lane == 0) {
+    sh.red_f[0][warp] = lo;
+    sh.red_f[1][warp] = hi;
+    sh.red_i[warp] = cnt;
+  }
+  if (tid == 0) sh.cand_n = 0;
+  __syncthreads();
+  lo = INFINITY; hi = -INFINITY; cnt = 0;
+#pragma unroll 1
+  for (int w = 0; w < kSelThreads / 32; ++w) {
+    lo = fminf(lo, sh.red_f[0][w]);
+    hi = fmaxf(hi, sh.red_f[1][w]);
+    cnt += sh.red_i[w];
+  }
+  mine_cnt = cnt;
+  if (cnt <= kCandCap) {
+    for (int e = tid; e < my_len; e += kSelThreads)
+      if (state[e] == 0) {
+        const int p = atomicAdd(&sh.cand_n, 1);
+        sh.cand_s[p] = sc[e];
+        sh.cand_i[p] = my0 + e;
+      }
+  }
+  __syncthreads();
+  if (tid < (int)C)
+    st_remote_v4(&sh.rec_in[r], tid, make_uint4(__float_as_uint(lo), __float_as_uint(hi), (uint32_t)cnt, 0u));
+  if (cnt <= kCandCap) {
+    for (int j = tid; j < (int)C * cnt; j += kSelThreads) {
+      const int peer = j / cnt, k = j % cnt;
+      st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_s[r * kCandCap + k]), peer, __float_as_uint(sh.cand_s[k]));
+      st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_i[r * kCandCap + k]), peer, (uint32_t)sh.cand_i[k]);
+    }
+  }
+  cluster_barrier();
+  glo = INFINITY; ghi = -INFINITY; gcnt = 0; pre_cnt = 0;
+#pragma unroll 1
+  for (int rr = 0; rr < (int)C; ++rr) {
+    const SelRec v = sh.rec_in[rr];
+    if (v.cnt > 0) {
+      glo = fminf(glo, v.lo);
+      ghi = fmaxf(ghi, v.hi);
+    }
+    if (rr < (int)r) pre_cnt += v.cnt;
+    gcnt += v.cnt;
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ n_visible,
-    int64_t n_stride, int K, int slice_cap, int32_t* __restrict__ out_idx,
+    int64_t n_stride, int K, int slice_cap, uint32_t* __restrict__ range, int32_t* __restrict__ out_idx,
     float* __restrict__ out_scores, uint32_t* __restrict__ status) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
@@ -336,122 +512,193 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   const int NB = C <= 4 ? kNBMax : kNBMin;
-  uint32_t* hist_in = reinterpret_cast<uint32_t*>(smem_raw + kSelHdr);
+  uint16_t* hist_in = reinterpret_cast<uint16_t*>(smem_raw + kSelHdr);
   float* cand_in_s = reinterpret_cast<float*>(hist_in + C * NB);
   int* cand_in_i = reinterpret_cast<int*>(cand_in_s + C * kCandCap);
   float* sc = reinterpret_cast<float*>(cand_in_i + C * kCandCap);
   uint8_t* state = reinterpret_cast<uint8_t*>(sc + slice_cap);
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int qi = blockIdx.y;
+  if (tid == 0) {
+    mbar_init(smem_u32(&sh.bar_load), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int nvis = n_visible[qi];
   nvis = nvis < 0 ? 0 : (nvis > n_stride ? (int)n_stride : nvis);
-  const int slice = (nvis + (int)C - 1) / (int)C;
+  const int slice = (((nvis + (int)C - 1) / (int)C) + 3) & ~3;
   const int my0 = (int)r * slice;
   int my_len = nvis - my0;
   my_len = my_len < 0 ? 0 : (my_len > slice ? slice : my_len);
   const int need = nvis < K ? nvis : K;
   int32_t* out = out_idx + (int64_t)qi * K;
   float* outs = out_scores ? out_scores + (int64_t)qi * K : nullptr;
-  const float* srow = scores + (int64_t)qi * score_stride + my0;
 
-  // batched loads (8 in flight per thread) so their latencies overlap
-  for (int e0 = 0; e0 < my_len; e0 += 8 * kSelThreads) {
-    float v[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int e = e0 + k * kSelThreads + tid;
-      v[k] = e < my_len ? srow[e] : 0.f;
+  // this CTA's scores: one bulk copy (16-byte aligned start, length rounded up to 16 bytes)
+  bool loaded = true;
+  if (my_len > 0) {
+    const uint32_t bytes = (uint32_t)(((my_len + 3) & ~3) * 4);
+    if (tid == 0) {
+      mbar_arrive_expect_tx(smem_u32(&sh.bar_load), bytes);
+      bulk_g2s(smem_u32(sc), scores + (int64_t)qi * score_stride + my0, bytes, smem_u32(&sh.bar_load));
     }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int e = e0 + k * kSelThreads + tid;
-      if (e < my_len) {
-        sc[e] = v[k];
-        state[e] = (nvis <= K) ? 1 : 0;
-      }
-    }
+    loaded = mbar_wait(smem_u32(&sh.bar_load), 0);
   }
+  // the score range left by the scoring kernel (read by every CTA before the first barrier)
+  const uint32_t kminv = range[2 * qi], kmax = range[2 * qi + 1];
+  const float rlo = key2f(~kminv), rhi = key2f(kmax);
+  const bool have_range = kmax != 0u && rlo < rhi && isfinite(rlo) && isfinite(rhi);
+  if (!__syncthreads_and(loaded)) {
+    if (tid == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+    my_len = 0;  // score nothing; the selection below still completes
+  }
+  const uint8_t init = nvis <= K ? 1 : 0;
+  for (int e = tid; e < my_len; e += kSelThreads) state[e] = init;
+  if (tid < kMaxCluster) {
+    sh.above_r[tid] = 0;
+    sh.cand_sel[tid] = 0;
+  }
+  if (tid == 0) sh.my_above = 0;
   __syncthreads();
 
-  if (nvis > K) {
-    int remaining = need;
-    for (int level = 0;; ++level) {
-      // ---- round 0: statistics (and small lists) of the surviving candidates
-      float lo = INFINITY, hi = -INFINITY;
-      int cnt = 0;
-      for (int e = tid; e < my_len; e += kSelThreads)
-        if (state[e] == 0) {
-          const float v = sc[e];
-          lo = fminf(lo, v);
-          hi = fmaxf(hi, v);
-          ++cnt;
-        }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  bool settled = false;     // output offsets known without the final exchange
+  int off_fast = 0, total_fast = 0;
+  if (nvis <= K) {
+    // everything visible is selected: CTA r's offset is the visible entries before its slice
+    settled = true;
+    off_fast = my0 < nvis ? my0 : nvis;
+    total_fast = nvis;
+    if (r == 0 && tid == 0) {
+      range[2 * qi] = 0u;
+      range[2 * qi + 1] = 0u;
+    }
+  } else {
+    int rem = need;
+    int level = 0;
+    bool done = false;
+    if (have_range) {
+      // ---- fast path: histogram of the known range, then the b* candidates
+      const float scl = (float)NB / (rhi - rlo);
+      build_push_hist(sh, hist_in, sc, state, my_len, rlo, scl, NB, C, r);
+      cluster_barrier();
+      if (r == 0 && tid == 0) {
+        range[2 * qi] = 0u;
+        range[2 * qi + 1] = 0u;
       }
-      if ((tid & 31) == 0) {
-        sh.red_f[0][tid >> 5] = lo;
-        sh.red_f[1][tid >> 5] = hi;
-        sh.red_i[tid >> 5] = cnt;
-      }
+      find_bstar(sh, hist_in, NB, C, rem);
+      const int bstar = sh.bstar;
+      rem -= sh.above;
+      level = 1;
+      int cand_tot = 0;
+#pragma unroll 1
+      for (int rr = 0; rr < (int)C; ++rr) cand_tot += hist_in[rr * NB + bstar];
       if (tid == 0) sh.cand_n = 0;
       __syncthreads();
-      SelRec mine;
-      mine.lo = INFINITY; mine.hi = -INFINITY; mine.cnt = 0; mine.pad = 0;
-      for (int w = 0; w < kSelThreads / 32; ++w) {
-        mine.lo = fminf(mine.lo, sh.red_f[0][w]);
-        mine.hi = fmaxf(mine.hi, sh.red_f[1][w]);
-        mine.cnt += sh.red_i[w];
-      }
-      if (mine.cnt <= kCandCap) {
-        for (int e = tid; e < my_len; e += kSelThreads)
-          if (state[e] == 0) {
-            const int p = atomicAdd(&sh.cand_n, 1);
-            sh.cand_s[p] = sc[e];
-            sh.cand_i[p] = my0 + e;
+      // classify (all entries are candidates at this point), count the ones above b*
+      // and collect the b* ones
+      int n_above = 0;
+      for (int e0 = tid; e0 < my_len; e0 += 8 * kSelThreads) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int e = e0 + k * kSelThreads;
+          v[k] = e < my_len ? sc[e] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int e = e0 + k * kSelThreads;
+          if (e < my_len) {
+            const int bi = bin_of(v[k], rlo, scl, NB);
+            state[e] = bi > bstar ? 1 : (bi < bstar ? 2 : 0);
+            n_above += bi > bstar;
+            if (bi == bstar && cand_tot <= kCandCap) {
+              const int p = atomicAdd(&sh.cand_n, 1);
+              sh.cand_s[p] = v[k];
+              sh.cand_i[p] = my0 + e;
+            }
           }
+        }
       }
+      n_above = __reduce_add_sync(0xffffffffu, n_above);
+      if (lane == 0 && n_above) atomicAdd(&sh.my_above, n_above);
       __syncthreads();
-      if (tid < (int)C)
-        st_remote_v4(&sh.rec_in[r], tid,
-                     make_uint4(__float_as_uint(mine.lo), __float_as_uint(mine.hi), (uint32_t)mine.cnt, 0u));
-      if (mine.cnt <= kCandCap) {
-        for (int j = tid; j < (int)C * mine.cnt; j += kSelThreads) {
-          const int peer = j / mine.cnt, k = j % mine.cnt;
+      if (cand_tot <= kCandCap) {
+        // push own candidates (their number, hist_in[r][b*], is known to every peer)
+        // and own count above b*
+        if (tid < (int)C) st_remote_u32(reinterpret_cast<uint32_t*>(&sh.above_r[r]), tid, (uint32_t)sh.my_above);
+        const int mine = sh.cand_n;
+        for (int j = tid; j < (int)C * mine; j += kSelThreads) {
+          const int peer = j / mine, k = j % mine;
           st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_s[r * kCandCap + k]), peer,
                         __float_as_uint(sh.cand_s[k]));
-          st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_i[r * kCandCap + k]), peer,
-                        (uint32_t)sh.cand_i[k]);
+          st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_i[r * kCandCap + k]), peer, (uint32_t)sh.cand_i[k]);
         }
-      }
-      cluster_barrier();
-      float glo = INFINITY, ghi = -INFINITY;
-      int gcnt = 0, pre_cnt = 0;
-      for (int rr = 0; rr < (int)C; ++rr) {
-        const SelRec v = sh.rec_in[rr];
-        if (v.cnt > 0) {
-          glo = fminf(glo, v.lo);
-          ghi = fmaxf(ghi, v.hi);
+        cluster_barrier();
+        // rank every candidate of every CTA (one warp per candidate, the lanes split
+        // the comparisons): own ones set the state, all of them the per-CTA counts
+        {
+          int cnt_r[kMaxCluster];
+          int tot = 0;
+#pragma unroll 1
+          for (int rr = 0; rr < (int)C; ++rr) {
+            cnt_r[rr] = hist_in[rr * NB + bstar];
+            tot += cnt_r[rr];
+          }
+          const int warp = tid >> 5;
+          for (int j = warp; j < tot; j += kSelThreads / 32) {
+            int rr = 0, k = j;
+            while (k >= cnt_r[rr]) { k -= cnt_r[rr]; ++rr; }
+            const float s = cand_in_s[rr * kCandCap + k];
+            const int i = cand_in_i[rr * kCandCap + k];
+            int rank = 0;
+            for (int c = lane; c < tot; c += 32) {
+              int r2 = 0, k2 = c;
+              while (k2 >= cnt_r[r2]) { k2 -= cnt_r[r2]; ++r2; }
+              const float t = cand_in_s[r2 * kCandCap + k2];
+              const int ti = cand_in_i[r2 * kCandCap + k2];
+              rank += (t > s) || (t == s && ti < i);
+            }
+            rank = __reduce_add_sync(0xffffffffu, rank);
+            if (lane == 0) {
+              const bool take = rank < rem;
+              if (take) atomicAdd(&sh.cand_sel[rr], 1);
+              if (rr == (int)r) state[i - my0] = take ? 1 : 2;
+            }
+          }
         }
-        if (rr < (int)r) pre_cnt += v.cnt;
-        gcnt += v.cnt;
+        __syncthreads();
+#pragma unroll 1
+        for (int rr = 0; rr < (int)C; ++rr) {
+          const int v = sh.above_r[rr] + sh.cand_sel[rr];
+          if (rr < (int)r) off_fast += v;
+          total_fast += v;
+        }
+        settled = true;
+        done = true;
       }
-      if (remaining >= gcnt) {
+    }
+    // ---- general path (no usable range, or too many candidates in b*)
+    while (!done) {
+      float glo, ghi;
+      int gcnt, pre_cnt, mine_cnt;
+      stats_round(sh, cand_in_s, cand_in_i, sc, state, my0, my_len, C, r, glo, ghi, gcnt, pre_cnt, mine_cnt);
+      if (level == 0 && r == 0 && tid == 0) {
+        range[2 * qi] = 0u;
+        range[2 * qi + 1] = 0u;
+      }
+      if (rem >= gcnt) {
         for (int e = tid; e < my_len; e += kSelThreads)
           if (state[e] == 0) state[e] = 1;
-        __syncthreads();
         break;
       }
       if (gcnt <= kCandCap) {
-        // exact: rank own candidates among all, by (score desc, index asc)
-        for (int j = tid; j < mine.cnt; j += kSelThreads) {
+        for (int j = tid; j < mine_cnt; j += kSelThreads) {
           const float s = sh.cand_s[j];
           const int i = sh.cand_i[j];
           int rank = 0;
+#pragma unroll 1
           for (int rr = 0; rr < (int)C; ++rr) {
             const int n = sh.rec_in[rr].cnt;
             const float* cs = cand_in_s + rr * kCandCap;
@@ -461,9 +708,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
               rank += (t > s) || (t == s && ci[c] < i);
             }
           }
-          state[i - my0] = rank < remaining ? 1 : 2;
+          state[i - my0] = rank < rem ? 1 : 2;
         }
-        __syncthreads();
         break;
       }
       if (glo == ghi || level == kMaxLevels - 1) {
@@ -477,78 +723,55 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
         int ord = block_excl_scan(c, sh.scan, total) + pre_cnt;
         for (int e = e0; e < e1; ++e)
           if (state[e] == 0) {
-            state[e] = ord < remaining ? 1 : 2;
+            state[e] = ord < rem ? 1 : 2;
             ++ord;
           }
-        __syncthreads();
         break;
       }
-      // ---- round 1: histogram refinement over [glo, ghi]
-      const float scl = (float)NB / (ghi - glo);
-      for (int i = tid; i < NB; i += kSelThreads) sh.hist_local[i] = 0u;
-      __syncthreads();
-      for (int e = tid; e < my_len; e += kSelThreads)
-        if (state[e] == 0) atomicAdd(&sh.hist_local[bin_of(sc[e], glo, scl, NB)], 1u);
-      __syncthreads();
-      for (int j = tid; j < (int)C * (NB / 4); j += kSelThreads) {
-        const int peer = j / (NB / 4), q4 = j % (NB / 4);
-        st_remote_v4(&hist_in[r * NB + 4 * q4], peer, *reinterpret_cast<const uint4*>(&sh.hist_local[4 * q4]));
-      }
+      const float scl2 = (float)NB / (ghi - glo);
+      build_push_hist(sh, hist_in, sc, state, my_len, glo, scl2, NB, C, r);
       cluster_barrier();
-      {
-        // thread t owns bins NB-1-per*t .. NB-per*(t+1) (per = NB/kSelThreads): suffix counts from the top
-        const int per = NB / kSelThreads;
-        const int btop = NB - 1 - per * tid;
-        uint32_t hs[kNBMax / kSelThreads];
-        int mine = 0;
-#pragma unroll
-        for (int k = 0; k < kNBMax / kSelThreads; ++k) {
-          uint32_t h = 0;
-          if (k < per)
-            for (int rr = 0; rr < (int)C; ++rr) h += hist_in[rr * NB + btop - k];
-          hs[k] = h;
-          mine += (int)h;
-        }
-        int total;
-        int above = block_excl_scan(mine, sh.scan, total);
-#pragma unroll
-        for (int k = 0; k < kNBMax / kSelThreads; ++k) {
-          if (k < per) {
-            const int h = (int)hs[k];
-            if (above < remaining && remaining <= above + h) {
-              sh.bstar = btop - k;
-              sh.above = above;
-            }
-            above += h;
-          }
-        }
-      }
-      __syncthreads();
-      const int bstar = sh.bstar;
-      remaining -= sh.above;
+      find_bstar(sh, hist_in, NB, C, rem);
+      const int bs = sh.bstar;
+      rem -= sh.above;
       for (int e = tid; e < my_len; e += kSelThreads)
         if (state[e] == 0) {
-          const int bi = bin_of(sc[e], glo, scl, NB);
-          state[e] = bi > bstar ? 1 : (bi < bstar ? 2 : 0);
+          const int bi = bin_of(sc[e], glo, scl2, NB);
+          state[e] = bi > bs ? 1 : (bi < bs ? 2 : 0);
         }
       __syncthreads();
+      ++level;
     }
+    __syncthreads();
   }
 
-  // ---- ordered output
-  const int chunk = (my_len + kSelThreads - 1) / kSelThreads;
+  // ---- ordered output (thread t owns a contiguous chunk of 16 entries, or more)
+  const int chunk = ((my_len + kSelThreads - 1) / kSelThreads + 15) & ~15;
   const int e0 = tid * chunk, e1 = min(e0 + chunk, my_len);
   int c = 0;
-  for (int e = e0; e < e1; ++e) c += state[e] == 1;
+  for (int e = e0; e < e1; e += 16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(state + e);  // state[] is padded to slice_cap
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        c += (e + 4 * q + b < e1) && ((ww[q] >> (8 * b)) & 0xFFu) == 1u;
+  }
   int my_sel;
   int pos = block_excl_scan(c, sh.scan, my_sel);
-  if (tid < (int)C) st_remote_u32(reinterpret_cast<uint32_t*>(&sh.sel_in[r]), tid, (uint32_t)my_sel);
-  cluster_barrier();
-  int offset = 0, total_sel = 0;
-  for (int rr = 0; rr < (int)C; ++rr) {
-    const int v = sh.sel_in[rr];
-    if (rr < (int)r) offset += v;
-    total_sel += v;
+  int offset = off_fast, total_sel = total_fast;
+  if (!settled) {
+    if (tid < (int)C) st_remote_u32(reinterpret_cast<uint32_t*>(&sh.sel_in[r]), tid, (uint32_t)my_sel);
+    cluster_barrier();
+    offset = 0;
+    total_sel = 0;
+#pragma unroll 1
+    for (int rr = 0; rr < (int)C; ++rr) {
+      const int v = sh.sel_in[rr];
+      if (rr < (int)r) offset += v;
+      total_sel += v;
+    }
   }
   pos += offset;
   for (int e = e0; e < e1; ++e)
@@ -574,15 +797,15 @@ static int select_cluster_size(int64_t n_stride) {
 }
 
 cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
-                               int Q, int64_t n_stride, int K, int32_t* out_idx, float* out_scores,
-                               uint32_t* status, cudaStream_t st) {
+                               int Q, int64_t n_stride, int K, uint32_t* range, int32_t* out_idx,
+                               float* out_scores, uint32_t* status, cudaStream_t st) {
   static_assert(kNBMax % kSelThreads == 0 && kNBMin % kSelThreads == 0, "bins per thread");
   if (Q == 0) return cudaSuccess;
   const int C = select_cluster_size(n_stride);
   const int NB = C <= 4 ? kNBMax : kNBMin;
   int slice_cap = (int)((n_stride + C - 1) / C);
   slice_cap = (slice_cap + 15) & ~15;
-  const size_t smem = kSelHdr + (size_t)C * NB * 4 + (size_t)C * kCandCap * 8 +
+  const size_t smem = kSelHdr + (size_t)C * NB * 2 + (size_t)C * kCandCap * 8 +
                       (size_t)slice_cap * 5;
   if (smem > kSelSmemMax) return cudaErrorInvalidValue;
   cudaError_t e = set_attr_once(0, (const void*)topk_select_kernel,
@@ -596,15 +819,17 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
   cfg.blockDim = dim3(kSelThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, score_stride, n_visible, n_stride, K,
-                            slice_cap, out_idx, out_scores, status);
+                            slice_cap, range, out_idx, out_scores, status);
 }
 
 __global__ void copy_idx_kernel(const int32_t* __restrict__ src, int32_t* __restrict__ dst,

@@ -107,8 +107,8 @@ def test_workspace_size_monotone(L):
     b = L.csa2_workspace_bytes(32, 1, 64, 65536, 2048)
     c = L.csa2_workspace_bytes(64, 1, 64, 65536, 2048)
     assert 256 < a <= b <= c
-    assert a == 256 + 32 * 32768 * 4                    # header + fp32 scores
-    assert L.csa2_workspace_bytes(1, 1, 64, 0, 2048) == 256
+    assert a == 256 + 256 + 32 * 32768 * 4              # header + range words + fp32 scores
+    assert L.csa2_workspace_bytes(1, 1, 64, 0, 2048) == 512
     assert L.csa2_workspace_bytes(-1, 1, 64, 10, 10) == 0
 
 
