@@ -231,8 +231,16 @@ __device__ __forceinline__ void quant_block16(const float* v, uint32_t& lo, uint
 }
 
 // ---- mbarrier and bulk-copy helpers (shared by the TMA-fed kernels)
-// Bound on the polls of one mbarrier wait (with back-off, a few seconds).
-constexpr uint32_t kMbarWaitLimit = 1u << 25;
+// Bound on one mbarrier wait: wall time (the global nanosecond timer), checked
+// every few hundred polls, so a stalled pipeline turns into an error status
+// within about a second instead of spinning.
+constexpr uint64_t kMbarWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ void mbar_init(uint32_t a, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count) : "memory");
@@ -256,11 +264,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
 }
 // Bounded wait for the completion of the phase with the given parity.
 __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
-  for (uint32_t i = 0; i < kMbarWaitLimit; ++i) {
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
-    if (i > 256) __nanosleep(64);
+    if (i > 64) __nanosleep(64);
+    if ((i & 255) == 0 && global_ns() - t0 > kMbarWaitNs) return false;
   }
-  return false;
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,

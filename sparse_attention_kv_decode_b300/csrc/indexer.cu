@@ -8,8 +8,7 @@
 //
 // Scoring (HBM-bound: 128 B of keys per entry, ~8 FLOP per key byte) runs on
 // the tensor cores through m16n8k16 bf16 MMAs with 16 keys as M and 8 indexer
-// heads as N; each thread streams two 16-byte pieces of a key row, so a warp
-// reads 2 KB contiguous per tile. Selection runs in one thread-block cluster
+// heads as N, fed by plain 16-byte loads. Selection runs in one thread-block cluster
 // per query: every CTA keeps its slice of scores in shared memory and the
 // cluster agrees on the K-th score through a few histogram rounds exchanged
 // over distributed shared memory (no global atomics, no spin waits).
@@ -20,24 +19,22 @@ namespace csa2 {
 // ---------------------------------------------------------------------------
 // Scoring
 // ---------------------------------------------------------------------------
-// A persistent kernel streams the keys through a ring of shared-memory stages
-// filled by bulk copies (one 16 KB stage = 128 keys of one query), so each SM
-// keeps ~200 KB of key reads in flight with a single issuing thread. The stages
-// of all queries form one list; each CTA takes a contiguous, balanced range of
-// it, so it stays on one query (and one stretch of keys) for many stages.
-//
-// Each consumer warp scores 16 keys of a stage with four m16n8k16 bf16 MMAs per
-// group of 8 indexer heads. Thread (g = lane/4, tig = lane%4) takes, for key
-// rows g and g+8, the 16-byte pieces at byte offsets 16*tig and 64+16*tig; the
-// MMA's k-slots are assigned to channels so that these words are exactly the
-// A fragment, and the B fragment (indexer query of head g) is read from the
-// same offsets: the contraction order is a permutation of the 64 channels,
-// which leaves each dot product unchanged.
-constexpr int kStageKeys = 128;
-constexpr int kStageBytes = kStageKeys * CSA2_D_IDX * 2;  // 16 KB
-constexpr int kScoreStages = 4;
-constexpr int kScoreThreads = 256;
-constexpr int kScoreSmem = kScoreStages * kStageBytes + 2 * kScoreStages * 8;
+// The scoring is a pure stream over the keys (4 MiB per query at 128K context),
+// so it is written for memory-level parallelism with nothing to synchronise:
+// every warp owns a contiguous, balanced run of 16-key groups (a query at a
+// time) and loads each group's MMA fragments straight from global memory into
+// registers, kScoreUnroll groups (8 x 16-byte loads per thread) in flight. A
+// group is scored with four m16n8k16 bf16 MMAs per 8 indexer heads: thread
+// (g = lane/4, tig = lane%4) holds, for key rows g and g+8, the 16-byte pieces
+// at byte offsets 16*tig and 64+16*tig; the MMA's k-slots are assigned to
+// channels so that these words are exactly the A fragment, and the B fragment
+// (the indexer query of head g) is read from the same offsets: the contraction
+// order is a permutation of the 64 channels, which leaves each dot product
+// unchanged.
+constexpr int kScoreThreads = 512;
+constexpr int kScoreCtasPerSm = 2;
+constexpr int kScoreUnroll = 2;
+constexpr int kGroupKeys = 16;
 
 template <int NT>
 __device__ __forceinline__ void load_q_frag(const uint16_t* q_idx, const float* w_idx, int qi,
@@ -77,115 +74,73 @@ __device__ __forceinline__ int clamp_nvis(const int32_t* n_visible, int qi, int6
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
+__global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_kernel(
     const uint16_t* __restrict__ q_idx, const float* __restrict__ w_idx,
     const uint16_t* __restrict__ z, int64_t n_stride, const int32_t* __restrict__ n_visible, int T,
-    int H_I, int Q, float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ range,
-    uint32_t* __restrict__ status) {
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + kScoreStages * kStageBytes;
-  const uint32_t bar_empty = bar_full + kScoreStages * 8;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int H_I, int Q, float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ range) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
-  const int stages_per_q = (int)((n_stride + kStageKeys - 1) / kStageKeys);
-  const int total = Q * stages_per_q;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kScoreStages; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kScoreThreads / 32);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-
-  // the CTA's work list: global stage ids blockIdx.x, +gridDim.x, ... that hold visible keys
-  auto stage_keys = [&](int gs, int& qi, int64_t& key0) -> int {
-    qi = gs / stages_per_q;
-    key0 = (int64_t)(gs - qi * stages_per_q) * kStageKeys;
-    const int nv = clamp_nvis(n_visible, qi, n_stride);
-    const int64_t k = nv - key0;
-    return k <= 0 ? 0 : (k > kStageKeys ? kStageKeys : (int)k);
-  };
-
-  const int gs_begin = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
-  const int gs_end = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
-  bool ok = true;
-  int prod_gs = gs_begin;     // next stage id the producer will consider
-  int prod_n = 0;             // stages produced so far (ring position)
-  auto produce_next = [&]() {
-    while (prod_gs < gs_end) {
-      int qi;
-      int64_t key0;
-      const int keys = stage_keys(prod_gs, qi, key0);
-      const int gs = prod_gs;
-      prod_gs += 1;
-      if (keys == 0) continue;
-      const int slot = prod_n % kScoreStages;
-      if (prod_n >= kScoreStages) {
-        if (!mbar_wait(bar_empty + 8 * slot, ((prod_n / kScoreStages) - 1) & 1)) {
-          atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
-          ok = false;
-          prod_gs = gs_end;
-          return;
-        }
-      }
-      const int b = qi / T;
-      const uint16_t* src = z + ((int64_t)b * n_stride + key0) * CSA2_D_IDX;
-      const uint32_t bytes = (uint32_t)keys * CSA2_D_IDX * 2;
-      mbar_arrive_expect_tx(bar_full + 8 * slot, bytes);
-      bulk_g2s(sbase + slot * kStageBytes, src, bytes, bar_full + 8 * slot);
-      ++prod_n;
-      (void)gs;
-      return;
-    }
-  };
-  if (threadIdx.x == 0)
-    for (int i = 0; i < kScoreStages; ++i) produce_next();
+  const int gpq = (int)((n_stride + kGroupKeys - 1) / kGroupKeys);   // groups per query
+  const int64_t total = (int64_t)Q * gpq;
+  const int64_t nwarps = (int64_t)gridDim.x * (kScoreThreads / 32);
+  const int64_t wid = (int64_t)blockIdx.x * (kScoreThreads / 32) + (threadIdx.x >> 5);
+  const int64_t w_begin = total * wid / nwarps, w_end = total * (wid + 1) / nwarps;
 
   uint32_t qa[NT][8];
   float wv[NT][2];
-  int cur_q = -1;
+  int cur_q = -1, nv = 0;
   uint32_t rmax = 0u, rmin_inv = 0u;  // score range of the current query seen by this warp
-  int cons_n = 0;
-  for (int gs = gs_begin; gs < gs_end; ++gs) {
-    int qi;
-    int64_t key0;
-    const int keys = stage_keys(gs, qi, key0);
-    if (keys == 0) continue;
-    const int slot = cons_n % kScoreStages;
-    const bool ready = mbar_wait(bar_full + 8 * slot, (cons_n / kScoreStages) & 1);
-    if (!__all_sync(0xffffffffu, ready)) {
-      if (lane == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
-      break;
-    }
-    if (qi != cur_q) {
-      if (cur_q >= 0 && lane == 0 && rmax != 0u) {
-        atomicMax(range + 2 * cur_q, rmin_inv);
-        atomicMax(range + 2 * cur_q + 1, rmax);
+  for (int64_t g0 = w_begin; g0 < w_end; g0 += kScoreUnroll) {
+    // fragments of up to kScoreUnroll groups (all loads issued before any use)
+    uint4 v[kScoreUnroll][4];
+    int qg[kScoreUnroll], key0g[kScoreUnroll];
+#pragma unroll
+    for (int u = 0; u < kScoreUnroll; ++u) {
+      const int64_t gi = g0 + u;
+      const int qi = (int)(gi / gpq);
+      const int key0 = (int)(gi - (int64_t)qi * gpq) * kGroupKeys;
+      qg[u] = gi < w_end ? qi : -1;
+      key0g[u] = key0;
+      if (gi < w_end && qi != cur_q) {
+        // a new query: flush the range of the previous one, load its indexer rows
+        if (cur_q >= 0 && lane == 0 && rmax != 0u) {
+          atomicMax(range + 2 * cur_q, rmin_inv);
+          atomicMax(range + 2 * cur_q + 1, rmax);
+        }
+        rmax = 0u;
+        rmin_inv = 0u;
+        load_q_frag<NT>(q_idx, w_idx, qi, H_I, g, tig, qa, wv);
+        nv = clamp_nvis(n_visible, qi, n_stride);
+        cur_q = qi;
       }
-      rmax = 0u;
-      rmin_inv = 0u;
-      load_q_frag<NT>(q_idx, w_idx, qi, H_I, g, tig, qa, wv);
-      cur_q = qi;
+      const int b = qi / T;
+      const int ra = key0 + g, rb = ra + 8;
+      const uint16_t* zb = z + (int64_t)b * n_stride * CSA2_D_IDX;
+      const bool oka = gi < w_end && ra < nv, okb = gi < w_end && rb < nv;
+      const uint4* pa = reinterpret_cast<const uint4*>(zb + (int64_t)ra * CSA2_D_IDX);
+      const uint4* pb = reinterpret_cast<const uint4*>(zb + (int64_t)rb * CSA2_D_IDX);
+      v[u][0] = oka ? pa[tig] : make_uint4(0, 0, 0, 0);
+      v[u][1] = oka ? pa[4 + tig] : make_uint4(0, 0, 0, 0);
+      v[u][2] = okb ? pb[tig] : make_uint4(0, 0, 0, 0);
+      v[u][3] = okb ? pb[4 + tig] : make_uint4(0, 0, 0, 0);
     }
-    const int r0 = warp * 16;
-    if (r0 < keys) {
-      const uint8_t* st = smem + slot * kStageBytes;
-      const uint4 v0 = *reinterpret_cast<const uint4*>(st + (r0 + g) * 128 + 16 * tig);
-      const uint4 v1 = *reinterpret_cast<const uint4*>(st + (r0 + g) * 128 + 64 + 16 * tig);
-      const uint4 v2 = *reinterpret_cast<const uint4*>(st + (r0 + g + 8) * 128 + 16 * tig);
-      const uint4 v3 = *reinterpret_cast<const uint4*>(st + (r0 + g + 8) * 128 + 64 + 16 * tig);
-      const uint32_t ra[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
-                               v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+    for (int u = 0; u < kScoreUnroll; ++u) {
+      if (qg[u] < 0) continue;
+      const int qi = qg[u], key0 = key0g[u];
+      if (key0 >= nv && qi == cur_q) continue;   // past the visible keys
+      const uint32_t ra_[16] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y,
+                                v[u][1].z, v[u][1].w, v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w,
+                                v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
       float pg = 0.f, pg8 = 0.f;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          mma_bf16(acc, ra[2 * j], ra[8 + 2 * j], ra[2 * j + 1], ra[8 + 2 * j + 1], qa[nt][2 * j],
+          mma_bf16(acc, ra_[2 * j], ra_[8 + 2 * j], ra_[2 * j + 1], ra_[8 + 2 * j + 1], qa[nt][2 * j],
                    qa[nt][2 * j + 1]);
         pg += wv[nt][0] * fmaxf(acc[0], 0.f) + wv[nt][1] * fmaxf(acc[1], 0.f);
         pg8 += wv[nt][0] * fmaxf(acc[2], 0.f) + wv[nt][1] * fmaxf(acc[3], 0.f);
@@ -195,29 +150,17 @@ __global__ void __launch_bounds__(kScoreThreads) index_score_kernel(
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 1);
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 2);
       float* srow = scores + (int64_t)qi * score_stride + key0;
-      const bool ok0 = tig == 0 && r0 + g < keys, ok1 = tig == 1 && r0 + g + 8 < keys;
-      if (ok0) srow[r0 + g] = pg;
-      if (ok1) srow[r0 + g + 8] = pg8;
-      // the query's score range (for the selection's first histogram), kept per warp
-      // and flushed once per query
+      const bool ok0 = tig == 0 && key0 + g < nv, ok1 = tig == 1 && key0 + g + 8 < nv;
+      if (ok0) srow[g] = pg;
+      if (ok1) srow[g + 8] = pg8;
       const uint32_t kk = ok0 ? f2key(pg) : (ok1 ? f2key(pg8) : 0u);
       rmax = max(rmax, __reduce_max_sync(0xffffffffu, kk));
       rmin_inv = max(rmin_inv, __reduce_max_sync(0xffffffffu, (ok0 || ok1) ? ~kk : 0u));
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-    ++cons_n;
-    if (threadIdx.x == 0 && ok) produce_next();
   }
   if (cur_q >= 0 && lane == 0 && rmax != 0u) {
     atomicMax(range + 2 * cur_q, rmin_inv);
     atomicMax(range + 2 * cur_q + 1, rmax);
-  }
-  // drain: copies in flight must land before the CTA exits
-  if (threadIdx.x == 0) {
-    const int first = prod_n > kScoreStages ? prod_n - kScoreStages : 0;
-    for (int n = first; n < prod_n; ++n)
-      mbar_wait(bar_full + 8 * (n % kScoreStages), (n / kScoreStages) & 1);
   }
 }
 
@@ -225,30 +168,30 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
                                int64_t n_stride, const int32_t* n_visible, int B, int T, int H_I,
                                float* scores, int64_t score_stride, uint32_t* range,
                                uint32_t* status, cudaStream_t st) {
+  (void)status;
   const int Q = B * T;
   if (n_stride == 0 || Q == 0) return cudaSuccess;
-  const int64_t total = (int64_t)Q * ((n_stride + kStageKeys - 1) / kStageKeys);
-  if (total > INT32_MAX / 2) return cudaErrorInvalidValue;
-  const int n_sm = device_sm_count();
-  int64_t grid = (int64_t)n_sm * 3;
-  if (grid > total) grid = total;
+  const int64_t total = (int64_t)Q * ((n_stride + kGroupKeys - 1) / kGroupKeys);
+  const int64_t warps = (int64_t)device_sm_count() * kScoreCtasPerSm * (kScoreThreads / 32);
+  int64_t grid = (int64_t)device_sm_count() * kScoreCtasPerSm;
+  if (total < warps) grid = (total + kScoreThreads / 32 - 1) / (kScoreThreads / 32);
   auto qp = static_cast<const uint16_t*>(q_idx);
   auto zp = static_cast<const uint16_t*>(z);
-  cudaError_t e;
-  if (H_I <= 8) {
-    e = set_attr_once(5, (const void*)index_score_kernel<1>,
-                      cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
-    if (e != cudaSuccess) return e;
-    index_score_kernel<1><<<(unsigned)grid, kScoreThreads, kScoreSmem, st>>>(
-        qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores, score_stride, range, status);
-  } else {
-    e = set_attr_once(6, (const void*)index_score_kernel<2>,
-                      cudaFuncAttributeMaxDynamicSharedMemorySize, kScoreSmem);
-    if (e != cudaSuccess) return e;
-    index_score_kernel<2><<<(unsigned)grid, kScoreThreads, kScoreSmem, st>>>(
-        qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores, score_stride, range, status);
-  }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kScoreThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (H_I <= 8)
+    return cudaLaunchKernelEx(&cfg, index_score_kernel<1>, qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores,
+                              score_stride, range);
+  return cudaLaunchKernelEx(&cfg, index_score_kernel<2>, qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores,
+                            score_stride, range);
 }
 
 // ---------------------------------------------------------------------------
