@@ -55,7 +55,7 @@ constexpr int kTmemCols = 512;
 constexpr int kColS = 0;                 // S^T buffers at columns [0, 64) and [64, 128)
 constexpr int kColO = 128;               // O^T M-tile i at columns [128 + 64 i, +64)
 constexpr float kRescale = 8.0f;         // lazy-max slack, log2 units (factor 256)
-constexpr int kMiscBytes = 4096;
+constexpr int kMiscBytes = 6144;
 constexpr int kSmemTC = 1024 + kQBytes + kCBytes + kMiscBytes;
 constexpr int kMaxSplitsTC = 16;
 // merge buffers inside the (finished) tile buffer
@@ -66,7 +66,7 @@ static_assert(kRecvBytes + kMaxSplitsTC * 2 * 64 * 4 <= kCBytes, "merge buffers 
 
 // mbarrier slots (8 bytes each)
 enum Bar { kQReady = 0, kChunkFull = 1, kGroupFree = 6, kSFull = 11, kPFull = 13, kTmaFull = 14,
-           kDrain = 15, kQTma = 16, kNumBars = 17 };
+           kDrain = 15, kQTma = 16, kRecv = 17, kNumBars = 18 };
 
 struct Misc {
   uint64_t bars[kNumBars];
@@ -79,6 +79,7 @@ struct Misc {
   float alpha[64];
   float lsum[64];
   float red[4][64];
+  float ml_in[4][2][64];   // (max, sum) per head pushed by each split (merge of <= 4 splits)
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc area");
 static_assert(offsetof(Misc, tmem_base) % 16 == 0, "TMEM address slot alignment");
@@ -287,6 +288,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     mbar_init(bar(kTmaFull), 1);
     mbar_init(bar(kDrain), 1);
     mbar_init(bar(kQTma), 1);
+    mbar_init(bar(kRecv), 1);
     ms.abort_flag = 0;
     ms.vote[0][0] = ms.vote[0][1] = ms.vote[1][0] = ms.vote[1][1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -634,6 +636,152 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
   allow_dependents();
   __syncthreads();
   const bool has = ntiles > 0 && !*abort_flag;
+  if (nsplit <= 4) {
+    // CTA o owns value dims [o*Dn, (o+1)*Dn) (whole 128-dim M-tiles). Each split
+    // scales its O^T rows by its own weight and ships the peers' rows with one bulk
+    // shared-to-shared copy per peer (staged in padded rows); the owner adds them to
+    // its own M-tiles read from TMEM.
+    constexpr float kLn2 = 0.69314718055994530942f, kLog2e = 1.4426950408889634074f;
+    const int Dn = kDV / (int)nsplit, tiles_own = Dn / 128;
+    const uint32_t slice_bytes = (uint32_t)Dn * kRecvStride * 4;
+    auto recv_slot = [&](int j) { return reinterpret_cast<float*>(sC + (size_t)j * slice_bytes); };
+    auto staging = [&](int k) {
+      return reinterpret_cast<float*>(k < 2 ? sQ + (size_t)k * slice_bytes : sC + (size_t)3 * slice_bytes);
+    };
+    const int tid = threadIdx.x;
+    if (tid < 64) {
+      const float m = has ? ms.mrun[tid] : -INFINITY;
+      const float s = has ? ms.lsum[tid] : 0.f;
+      for (uint32_t p = 0; p < nsplit; ++p) {
+        st_cluster_f32(map_rank(smem_u32(&ms.ml_in[sp][0][tid]), p), m);
+        st_cluster_f32(map_rank(smem_u32(&ms.ml_in[sp][1][tid]), p), s);
+      }
+    }
+    if (tid == 0 && nsplit > 1) mbar_arrive_expect_tx(bar(kRecv), (nsplit - 1) * slice_bytes);
+    // (max, sum) of every split visible; every CTA past its last P.V, so the tile and
+    // Q buffers of all of them may be reused
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    if (tid < 64) {
+      float M = -INFINITY;
+      for (uint32_t s = 0; s < nsplit; ++s) M = fmaxf(M, ms.ml_in[s][0][tid]);
+      float mext = -INFINITY;
+      if (out.o_ext) {
+        mext = out.lse_ext[(int64_t)qi * H + (tid < H ? tid : 0)] * kLog2e;
+        M = fmaxf(M, mext);
+      }
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float L = 0.f;
+      for (uint32_t s = 0; s < nsplit; ++s) {
+        const float ls = ms.ml_in[s][1][tid];
+        L += ls > 0.f ? ls * exp2f(ms.ml_in[s][0][tid] - Mu) : 0.f;
+      }
+      const float wext = (out.o_ext && mext != -INFINITY) ? exp2f(mext - Mu) : 0.f;
+      L += wext;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const float lown = ms.ml_in[sp][1][tid];
+      ms.mnew[tid] = lown > 0.f ? exp2f(ms.ml_in[sp][0][tid] - Mu) * inv : 0.f;   // weight of this split
+      ms.alpha[tid] = wext * inv;                                                  // weight of the external branch
+      if (sp == 0 && out.lse && tid < H)
+        out.lse[(int64_t)qi * H + tid] = L > 0.f ? (Mu + log2f(L)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    const int quarter = warp & 3, half = warp >> 2;
+    const int e = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    if (warp < 8 && nsplit > 1) {
+      // scaled rows of the peers' M-tiles -> staging (padded rows, conflict-free)
+      for (int i = 0; i < 4; ++i) {
+        const int o = i / tiles_own;
+        if (o == sp) continue;
+        uint32_t r[32];
+        if (has) {
+          tmem_ld32(tmem + lane_off + kColO + 64 * i + 32 * half, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = 0u;
+        }
+        const int k_st = (o - sp - 1 + (int)nsplit) % (int)nsplit;
+        float* dst = staging(k_st) + (size_t)(128 * i + e - o * Dn) * kRecvStride + 32 * half;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int h = 32 * half + 4 * k;
+          *reinterpret_cast<float4*>(dst + 4 * k) =
+              make_float4(__uint_as_float(r[4 * k]) * ms.mnew[h], __uint_as_float(r[4 * k + 1]) * ms.mnew[h + 1],
+                          __uint_as_float(r[4 * k + 2]) * ms.mnew[h + 2], __uint_as_float(r[4 * k + 3]) * ms.mnew[h + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    __syncthreads();
+    if (tid == 0)
+      for (int o = 0; o < (int)nsplit; ++o) {
+        if (o == sp) continue;
+        const int k_st = (o - sp - 1 + (int)nsplit) % (int)nsplit;  // slot of this split at the owner
+        asm volatile(
+            "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                map_rank(smem_u32(recv_slot(k_st)), (uint32_t)o)),
+            "r"(smem_u32(staging(k_st))), "r"(slice_bytes), "r"(map_rank(bar(kRecv), (uint32_t)o))
+            : "memory");
+      }
+    bool got = true;
+    if (nsplit > 1) got = mbar_wait(bar(kRecv), 0);
+    if (!__syncthreads_and(got)) {
+      if (tid == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+    } else if (warp < 8) {
+      // own M-tiles: this split's rows from TMEM plus the received rows, plus the
+      // external branch; each head's output row is written by consecutive lanes
+      float* o = out.o + (int64_t)qi * H * kDV;
+      const float* oe = out.o_ext ? out.o_ext + (int64_t)qi * H * kDV : nullptr;
+      for (int j = 0; j < tiles_own; ++j) {
+        const int i = sp * tiles_own + j;
+        const int dl = 128 * j + e, d = 128 * i + e;
+        uint32_t r[32];
+        if (has) {
+          tmem_ld32(tmem + lane_off + kColO + 64 * i + 32 * half, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = 0u;
+        }
+        float acc[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[k] = __uint_as_float(r[k]) * ms.mnew[32 * half + k];
+        for (int s = 0; s + 1 < (int)nsplit; ++s) {
+          const float* src = recv_slot(s) + (size_t)dl * kRecvStride + 32 * half;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 v = *reinterpret_cast<const float4*>(src + 4 * k);
+            acc[4 * k] += v.x; acc[4 * k + 1] += v.y; acc[4 * k + 2] += v.z; acc[4 * k + 3] += v.w;
+          }
+        }
+        if (oe) {
+          // all 32 loads issued before the first use
+          float ev[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int h = 32 * half + k;
+            ev[k] = h < H ? __ldcs(oe + (int64_t)h * kDV + d) : 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float w = ms.alpha[32 * half + k];
+            if (w > 0.f) acc[k] += w * ev[k];
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int h = 32 * half + k;
+          if (h < H) o[(int64_t)h * kDV + d] = acc[k];
+        }
+      }
+    }
+    // no CTA leaves while a peer may still copy out of (or into) it
+    tc_fence_before();
+    cluster_sync_all();
+  } else {
   const int Dn = kDV / (int)nsplit;  // value dims owned by each CTA
   float* recv = reinterpret_cast<float*>(sC);                     // [src][dl][kRecvStride]
   float* ml = reinterpret_cast<float*>(sC + kMlOffset);           // [src][2][64]
@@ -752,6 +900,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       }
     }
   }
+  }  // nsplit > 4
 
   tc_fence_before();
   __syncthreads();
