@@ -59,6 +59,21 @@ def load_peaks():
     return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
 
 
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None when the
+    kernel's source has changed since that capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        rec = json.load(open(p))[kernel]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest() != rec["sha256"]:
+            return None
+        return int(rec["bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
@@ -410,7 +425,10 @@ def run_ours(args):
                            "sparse": "csa2_sparse_decode (attn_tc_kernel)",
                            "swa": "csa2_swa_merge (attn_tc_kernel)"}[dom],
                 "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "peak_source": peaks["src"], "traffic": None}
+                "frac": round(achieved / peak, 4), "peak_source": peaks["src"],
+                "traffic": ncu_traffic({"index": "index_score_kernel<1>", "attn": "attn_tc_kernel<2>",
+                                        "sparse": "attn_tc_kernel<0>", "swa": "attn_tc_kernel<1>"}[dom]),
+                "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"}
 
     ced = None
     if not args.no_ced:
@@ -489,7 +507,7 @@ def run_ced(args, torch, csa2, dev, peaks):
             "value": round(tf, 1), "unit": "TFLOP/s", "ms_per_launch": round(t * 1e3, 4), "launches": n,
             "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peaks["bf16"], "unit": "TFLOP/s",
                          "frac": round(tf / peaks["bf16"], 4), "peak_source": peaks["src"] + " bf16 burst",
-                         "frac_of_sustained": round(tf / peaks["bf16_sus"], 4), "traffic": None}}
+                         "frac_of_sustained": round(tf / peaks["bf16_sus"], 4), "traffic": ncu_traffic("ced_proj_kernel")}}
 
 
 def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs, ws, world, dev):
