@@ -17,7 +17,7 @@
 // same 128-byte-swizzled shared-memory tile. S^T (two buffers) and the four
 // 128x64 O^T accumulators live in TMEM.
 //
-// Warp roles (288 threads):
+// Warp roles (320 threads):
 //   warps 0-7  workers. Warp w stages key rows 16w .. 16w+15 of each tile: the
 //              FP4 gather (prefetched one tile ahead in registers) is laid out
 //              so that one warp load reads 8 rows x 64 contiguous bytes, and
@@ -29,6 +29,8 @@
 //              it by 2^8), p written as fp16 P^T over the rope chunk of C once
 //              the S^T product has read it.
 //   warp 8     TMEM allocation and the single-thread MMA issuer.
+//   warp 9     requests every entry the split gathers after its first tile into
+//              L2 at the start (the register prefetch runs only one tile ahead).
 // The splits of one query form a thread-block cluster. After the last P.V each
 // CTA pushes its (max, sum) per head and its unnormalised O^T rows to the CTA
 // that owns those value dims (distributed shared memory stores into the freed
@@ -50,7 +52,7 @@ constexpr int kCChunk = kTK * 128;       // 128 keys x 64 dims fp16
 constexpr int kQBytes = 9 * kQChunk;
 constexpr int kCBytes = 9 * kCChunk;
 constexpr int kWorkers = 256;
-constexpr int kThreadsTC = kWorkers + 32;
+constexpr int kThreadsTC = kWorkers + 64;   // + MMA warp + L2 prefetch warp
 constexpr int kTmemCols = 512;
 constexpr int kColS = 0;                 // S^T buffers at columns [0, 64) and [64, 128)
 constexpr int kColO = 128;               // O^T M-tile i at columns [128 + 64 i, +64)
@@ -59,7 +61,7 @@ constexpr int kMiscBytes = 6144;
 constexpr int kSmemTC = 1024 + kQBytes + kCBytes + kMiscBytes;
 constexpr int kMaxSplitsTC = 16;
 // merge buffers inside the (finished) tile buffer
-constexpr int kRecvStride = 68;          // floats per received O^T row (64 heads + pad)
+constexpr int kRecvStride = 68;          // floats per received O^T row (64 heads + pad), > 4 splits
 constexpr int kRecvBytes = kDV * kRecvStride * 4;                    // 139,264
 constexpr int kMlOffset = kRecvBytes;                                // [split][2][64] floats
 static_assert(kRecvBytes + kMaxSplitsTC * 2 * 64 * 4 <= kCBytes, "merge buffers fit the tile");
@@ -72,17 +74,21 @@ struct Misc {
   uint64_t bars[kNumBars];
   alignas(16) uint32_t tmem_base;
   int abort_flag;
-  int vote[2][2];          // [head half][tile parity]
   int valid[2][kTK];       // key validity of the tile, by tile parity
-  float mrun[64];          // running max per head (log2 domain)
-  float mnew[64];
-  float alpha[64];
-  float lsum[64];
-  float red[4][64];
-  float ml_in[4][2][64];   // (max, sum) per head pushed by each split (merge of <= 4 splits)
+  // per-head arrays, read as 16-byte vectors
+  alignas(16) float mrun[64];   // running max per head (log2 domain)
+  alignas(16) float mnew[64];
+  alignas(16) float alpha[64];
+  alignas(16) float lsum[64];
+  alignas(16) float red[4][64];
+  alignas(16) float ml_in[4][2][64];   // (max, sum) per head pushed by each split (merge of <= 4 splits)
 };
 static_assert(sizeof(Misc) <= kMiscBytes, "misc area");
 static_assert(offsetof(Misc, tmem_base) % 16 == 0, "TMEM address slot alignment");
+static_assert(offsetof(Misc, mrun) % 16 == 0 && offsetof(Misc, ml_in) % 16 == 0 &&
+                  offsetof(Misc, alpha) % 16 == 0 && offsetof(Misc, mnew) % 16 == 0,
+              "vector reads of the per-head arrays");
+static_assert((kQBytes + kCBytes) % 16 == 0, "Misc placement");
 
 struct Fp4Src {
   const uint8_t* codes;   // [B][n_stride][288]
@@ -115,12 +121,46 @@ __device__ __forceinline__ bool named_and(int id, int n, bool v) {
       : "memory");
   return r != 0;
 }
+// OR of a predicate over the `n` threads of named barrier `id` (all get the result).
+__device__ __forceinline__ bool named_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+// 2^x with the SFU's approximation (relative error ~2^-22; 2^-inf = 0): p is
+// stored as fp16, whose rounding (2^-11) dominates.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// 2-D TMA load delivered to the same shared-memory offset (data and mbarrier
+// transaction bytes) of every CTA of the cluster in `mask`.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               uint32_t mbar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar), "h"(mask)
+      : "memory");
 }
 __device__ __forceinline__ uint32_t map_rank(uint32_t local, uint32_t rank) {
   uint32_t r;
@@ -246,6 +286,15 @@ __device__ __forceinline__ void load_piece(const uint8_t* cbase, const uint8_t* 
   }
 }
 
+// Requests into L2 (no data returned): `bytes` from a 16-byte aligned address (a
+// multiple of 16), or the line holding one address.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -290,7 +339,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     mbar_init(bar(kQTma), 1);
     mbar_init(bar(kRecv), 1);
     ms.abort_flag = 0;
-    ms.vote[0][0] = ms.vote[0][1] = ms.vote[1][0] = ms.vote[1][1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 8) {
@@ -303,6 +351,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the splits of a query share one Q load (multicast): every CTA's barriers must be
+  // initialised before a peer's copy lands, so the cluster meets once before it
+  if (nsplit > 1) cluster_arrive();
   const uint32_t tmem = ms.tmem_base;
   volatile int* abort_flag = &ms.abort_flag;
   auto fail = [&]() {
@@ -312,6 +363,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
   // Inputs may be written by the preceding kernel in the stream: nothing below
   // reads global memory before it has completed.
   grid_dependency_wait();
+  if (nsplit > 1) cluster_wait();
 
   constexpr bool kFp4 = kKind != kWindow;   // FP4 entry tiles
   constexpr bool kRows = kKind != kSparse;  // bf16 window row tiles
@@ -356,7 +408,13 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     int issued_t = -1, waited_t = -1;  // window tiles loaded by TMA (wt == 0)
     if (wt == 0) {
       mbar_arrive_expect_tx(bar(kQTma), 9 * kQChunk);
-      for (int c = 0; c < 9; ++c) tma_load_2d(uQ + c * kQChunk, &tm_q, 64 * c, qi * H, bar(kQTma));
+      if (nsplit > 1) {
+        // split sp loads chunks sp, sp + nsplit, .. for every CTA of the cluster
+        for (int c = sp; c < 9; c += (int)nsplit)
+          tma_load_2d_mc(uQ + c * kQChunk, &tm_q, 64 * c, qi * H, bar(kQTma), (uint16_t)((1u << nsplit) - 1u));
+      } else {
+        for (int c = 0; c < 9; ++c) tma_load_2d(uQ + c * kQChunk, &tm_q, 64 * c, qi * H, bar(kQTma));
+      }
       // the first window tile goes to the still empty tile buffer right away
       if (kRows && nt_r > 0) {
         mbar_arrive_expect_tx(bar(kTmaFull), 9 * kCChunk);
@@ -503,22 +561,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       float s[32];
       load_scores32(s_addr, vld, scale_log2, s);
       if (t == 0) reduce32<true>(s, ms, ms.mrun, h0, lane, quarter, bid);
-      // P^T row of this key for the 32 heads: exp2(s - m) in fp16, over the rope chunk
+      // P^T row of this key for the 32 heads: 2^(s - m) in fp16, over the rope chunk
       uint32_t pk[16];
       bool need = false;
 #pragma unroll
-      for (int h = 0; h < 32; h += 2) {
-        const float m0 = ms.mrun[h0 + h], m1 = ms.mrun[h0 + h + 1];
-        need |= (s[h] > m0 + kRescale) | (s[h + 1] > m1 + kRescale);
-        pk[h >> 1] = pack_h2(exp2f(s[h] - (m0 == -INFINITY ? 0.f : m0)),
-                             exp2f(s[h + 1] - (m1 == -INFINITY ? 0.f : m1)));
+      for (int h = 0; h < 32; h += 4) {
+        const float4 m4 = *reinterpret_cast<const float4*>(&ms.mrun[h0 + h]);
+        const float m[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) need |= s[h + k] > m[k] + kRescale;
+        pk[h >> 1] = pack_h2(ex2_approx(s[h] - (m[0] == -INFINITY ? 0.f : m[0])),
+                             ex2_approx(s[h + 1] - (m[1] == -INFINITY ? 0.f : m[1])));
+        pk[(h >> 1) + 1] = pack_h2(ex2_approx(s[h + 2] - (m[2] == -INFINITY ? 0.f : m[2])),
+                                   ex2_approx(s[h + 3] - (m[3] == -INFINITY ? 0.f : m[3])));
       }
       if (t > 0) {
-        if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(&ms.vote[half][sb], 1);
-        named_sync(bid, 128);
-        const bool rescale = ms.vote[half][sb] != 0;
-        named_sync(bid, 128);
-        if (e == 0) ms.vote[half][sb] = 0;
+        // one barrier: does any key of this head half exceed its running max by 2^8?
+        const bool rescale = named_or(bid, 128, need);
         if (rescale) {
           reduce32<true>(s, ms, ms.mnew, h0, lane, quarter, bid);
           // O^T must be final for tile t-1 before it is rescaled
@@ -553,8 +612,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
 #pragma unroll
           for (int h = 0; h < 32; h += 2) {
             const float m0 = ms.mrun[h0 + h], m1 = ms.mrun[h0 + h + 1];
-            pk[h >> 1] = pack_h2(exp2f(s[h] - (m0 == -INFINITY ? 0.f : m0)),
-                                 exp2f(s[h + 1] - (m1 == -INFINITY ? 0.f : m1)));
+            pk[h >> 1] = pack_h2(ex2_approx(s[h] - (m0 == -INFINITY ? 0.f : m0)),
+                                 ex2_approx(s[h + 1] - (m1 == -INFINITY ? 0.f : m1)));
           }
         }
       }
@@ -584,7 +643,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       wok = named_and(bid, 128, mbar_wait(bar(kGroupFree + 4), (ntiles - 1) & 1));
       if (!wok && e == 0) fail();
     }
-  } else {
+  } else if (warp == 8) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_f16(kTK, 64, 0, 0, 0, 0);
@@ -630,6 +689,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       }
     }
     __syncwarp();
+  } else if (kFp4) {
+    // ======================= L2 prefetch of the gathered entries =======================
+    // Each tile's FP4 gather is issued one tile ahead into registers; from a cold L2 its
+    // latency is longer than the tile's S^T product, so every entry this split gathers
+    // after its first tile is requested into L2 once, up front.
+    const uint8_t* cb = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
+    const uint8_t* sb = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
+    const int32_t* ir = fsrc.idx + (int64_t)qi * fsrc.K;
+    for (int p = p_begin + kTK + lane; p < p_end; p += 32) {
+      const int ent = ir[p];
+      if (ent >= 0 && ent < fsrc.n_stride) {
+        prefetch_l2_bulk(cb + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
+        const uint8_t* s0 = sb + (int64_t)ent * CSA2_SCALE_BYTES;
+        prefetch_l2(s0);
+        prefetch_l2(s0 + CSA2_SCALE_BYTES - 1);
+      }
+    }
   }
 
   // ======================= merge the splits of this query =======================
@@ -638,17 +714,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
   const bool has = ntiles > 0 && !*abort_flag;
   if (nsplit <= 4) {
     // CTA o owns value dims [o*Dn, (o+1)*Dn) (whole 128-dim M-tiles). Each split
-    // scales its O^T rows by its own weight and ships the peers' rows with one bulk
-    // shared-to-shared copy per peer (staged in padded rows); the owner adds them to
-    // its own M-tiles read from TMEM.
+    // stages its raw O^T rows of the peers' M-tiles (rows of 64 heads, 16-byte pieces
+    // swizzled by row) while the slower splits finish, and ships each peer's slice
+    // with one bulk shared-to-shared copy; the owner weights every split's rows by
+    // exp2(m_s - M) / L and adds them to its own M-tiles read from TMEM.
     constexpr float kLn2 = 0.69314718055994530942f, kLog2e = 1.4426950408889634074f;
     const int Dn = kDV / (int)nsplit, tiles_own = Dn / 128;
-    const uint32_t slice_bytes = (uint32_t)Dn * kRecvStride * 4;
+    const uint32_t slice_bytes = (uint32_t)Dn * 64 * 4;
     auto recv_slot = [&](int j) { return reinterpret_cast<float*>(sC + (size_t)j * slice_bytes); };
     auto staging = [&](int k) {
       return reinterpret_cast<float*>(k < 2 ? sQ + (size_t)k * slice_bytes : sC + (size_t)3 * slice_bytes);
     };
+    // float offset of 16-byte piece j (0..15) of row r in a slice
+    auto piece = [](int r, int j) { return r * 64 + ((j ^ (r & 7)) << 2); };
     const int tid = threadIdx.x;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int e = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     if (tid < 64) {
       const float m = has ? ms.mrun[tid] : -INFINITY;
       const float s = has ? ms.lsum[tid] : 0.f;
@@ -658,40 +740,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       }
     }
     if (tid == 0 && nsplit > 1) mbar_arrive_expect_tx(bar(kRecv), (nsplit - 1) * slice_bytes);
-    // (max, sum) of every split visible; every CTA past its last P.V, so the tile and
-    // Q buffers of all of them may be reused
-    tc_fence_before();
-    cluster_sync_all();
-    tc_fence_after();
-    if (tid < 64) {
-      float M = -INFINITY;
-      for (uint32_t s = 0; s < nsplit; ++s) M = fmaxf(M, ms.ml_in[s][0][tid]);
-      float mext = -INFINITY;
-      if (out.o_ext) {
-        mext = out.lse_ext[(int64_t)qi * H + (tid < H ? tid : 0)] * kLog2e;
-        M = fmaxf(M, mext);
-      }
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float L = 0.f;
-      for (uint32_t s = 0; s < nsplit; ++s) {
-        const float ls = ms.ml_in[s][1][tid];
-        L += ls > 0.f ? ls * exp2f(ms.ml_in[s][0][tid] - Mu) : 0.f;
-      }
-      const float wext = (out.o_ext && mext != -INFINITY) ? exp2f(mext - Mu) : 0.f;
-      L += wext;
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const float lown = ms.ml_in[sp][1][tid];
-      ms.mnew[tid] = lown > 0.f ? exp2f(ms.ml_in[sp][0][tid] - Mu) * inv : 0.f;   // weight of this split
-      ms.alpha[tid] = wext * inv;                                                  // weight of the external branch
-      if (sp == 0 && out.lse && tid < H)
-        out.lse[(int64_t)qi * H + tid] = L > 0.f ? (Mu + log2f(L)) * kLn2 : -INFINITY;
-    }
-    __syncthreads();
-    const int quarter = warp & 3, half = warp >> 2;
-    const int e = quarter * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // this CTA is past its last P.V: its own Q and tile buffers are free for staging
     if (warp < 8 && nsplit > 1) {
-      // scaled rows of the peers' M-tiles -> staging (padded rows, conflict-free)
       for (int i = 0; i < 4; ++i) {
         const int o = i / tiles_own;
         if (o == sp) continue;
@@ -704,18 +754,20 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
           for (int k = 0; k < 32; ++k) r[k] = 0u;
         }
         const int k_st = (o - sp - 1 + (int)nsplit) % (int)nsplit;
-        float* dst = staging(k_st) + (size_t)(128 * i + e - o * Dn) * kRecvStride + 32 * half;
+        float* dst = staging(k_st);
+        const int row = 128 * i + e - o * Dn;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int h = 32 * half + 4 * k;
-          *reinterpret_cast<float4*>(dst + 4 * k) =
-              make_float4(__uint_as_float(r[4 * k]) * ms.mnew[h], __uint_as_float(r[4 * k + 1]) * ms.mnew[h + 1],
-                          __uint_as_float(r[4 * k + 2]) * ms.mnew[h + 2], __uint_as_float(r[4 * k + 3]) * ms.mnew[h + 3]);
-        }
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<uint4*>(dst + piece(row, 8 * half + k)) =
+              make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
       }
       fence_proxy_async_smem();
     }
-    __syncthreads();
+    // (max, sum) of every split visible; every CTA past its last P.V, so the tile
+    // buffers of all of them may be written
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
     if (tid == 0)
       for (int o = 0; o < (int)nsplit; ++o) {
         if (o == sp) continue;
@@ -726,13 +778,41 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
             "r"(smem_u32(staging(k_st))), "r"(slice_bytes), "r"(map_rank(bar(kRecv), (uint32_t)o))
             : "memory");
       }
+    // weights per (split, head) overwrite the pushed maxima; the external branch's in alpha
+    if (tid >= 32 && tid < 96) {
+      const int h = tid - 32;
+      float M = -INFINITY;
+      for (uint32_t s = 0; s < nsplit; ++s) M = fmaxf(M, ms.ml_in[s][0][h]);
+      float mext = -INFINITY;
+      if (out.o_ext) {
+        mext = out.lse_ext[(int64_t)qi * H + (h < H ? h : 0)] * kLog2e;
+        M = fmaxf(M, mext);
+      }
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float L = 0.f;
+      for (uint32_t s = 0; s < nsplit; ++s) {
+        const float ls = ms.ml_in[s][1][h];
+        L += ls > 0.f ? ls * exp2f(ms.ml_in[s][0][h] - Mu) : 0.f;
+      }
+      const float wext = (out.o_ext && mext != -INFINITY) ? exp2f(mext - Mu) : 0.f;
+      L += wext;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (uint32_t s = 0; s < nsplit; ++s) {
+        const float ls = ms.ml_in[s][1][h];
+        ms.ml_in[s][0][h] = ls > 0.f ? exp2f(ms.ml_in[s][0][h] - Mu) * inv : 0.f;
+      }
+      ms.alpha[h] = wext * inv;
+      if (sp == 0 && out.lse && h < H)
+        out.lse[(int64_t)qi * H + h] = L > 0.f ? (Mu + log2f(L)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
     bool got = true;
     if (nsplit > 1) got = mbar_wait(bar(kRecv), 0);
     if (!__syncthreads_and(got)) {
       if (tid == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
     } else if (warp < 8) {
-      // own M-tiles: this split's rows from TMEM plus the received rows, plus the
-      // external branch; each head's output row is written by consecutive lanes
+      // own M-tiles: every split's rows times its weight, plus the external branch;
+      // each head's output row is written by consecutive lanes
       float* o = out.o + (int64_t)qi * H * kDV;
       const float* oe = out.o_ext ? out.o_ext + (int64_t)qi * H * kDV : nullptr;
       for (int j = 0; j < tiles_own; ++j) {
@@ -748,16 +828,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         }
         float acc[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) acc[k] = __uint_as_float(r[k]) * ms.mnew[32 * half + k];
+        for (int k = 0; k < 32; k += 4) {
+          const float4 w = *reinterpret_cast<const float4*>(&ms.ml_in[sp][0][32 * half + k]);
+          acc[k] = __uint_as_float(r[k]) * w.x;
+          acc[k + 1] = __uint_as_float(r[k + 1]) * w.y;
+          acc[k + 2] = __uint_as_float(r[k + 2]) * w.z;
+          acc[k + 3] = __uint_as_float(r[k + 3]) * w.w;
+        }
         for (int s = 0; s + 1 < (int)nsplit; ++s) {
-          const float* src = recv_slot(s) + (size_t)dl * kRecvStride + 32 * half;
+          const int src_sp = (sp - s - 1 + (int)nsplit) % (int)nsplit;  // sender of slot s
+          const float* src = recv_slot(s);
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const float4 v = *reinterpret_cast<const float4*>(src + 4 * k);
-            acc[4 * k] += v.x; acc[4 * k + 1] += v.y; acc[4 * k + 2] += v.z; acc[4 * k + 3] += v.w;
+            const float4 v = *reinterpret_cast<const float4*>(src + piece(dl, 8 * half + k));
+            const float4 w = *reinterpret_cast<const float4*>(&ms.ml_in[src_sp][0][32 * half + 4 * k]);
+            acc[4 * k] += w.x * v.x; acc[4 * k + 1] += w.y * v.y;
+            acc[4 * k + 2] += w.z * v.z; acc[4 * k + 3] += w.w * v.w;
           }
         }
-        if (oe) {
+        if (kKind == kWindow && oe) {
           // all 32 loads issued before the first use
           float ev[32];
 #pragma unroll
