@@ -4,10 +4,11 @@
 Workload (one "step"): a decode step of a three-layer CSA2 group FULL -> REINDEX ->
 REUSE for 32 sequences at 128K context (32768 compressed entries each), 64 query
 heads, latent 512 + rope 64 in FP4 (E2M1 + E4M3 per 16), indexer 8 x 64 in bf16,
-top-K 2048, sliding window 128. Per layer: csa2_index_topk, then attention over the
-selected entries and the window in one csa2_decode_attention call (or, with
---attn two-call, csa2_sparse_decode followed by csa2_swa_merge); REUSE skips the
-indexer. The KV caches and keys are resident in HBM (written before timing); each
+top-K 2048, sliding window 128. Per layer one csa2_decode_layer call: the top-K
+selection (which also requests the selected FP4 rows into L2), then the attention over
+the selected entries and the window (csa2_decode_attention); REUSE skips the indexer.
+--attn fused times csa2_index_topk + csa2_decode_attention instead, --attn two-call
+csa2_index_topk + csa2_sparse_decode + csa2_swa_merge. The KV caches and keys are resident in HBM (written before timing); each
 timed step re-reads them, and L2 is flushed between steps.
 
 Prints one JSON line (rank 0). --impl reference times the CPU oracle on a bounded
@@ -267,22 +268,41 @@ def run_ours(args):
     P = lambda t: t.data_ptr()
     wsp, wsn = P(ws), ws.numel()
 
-    # the step as a list of (name, kind, thunk) C-ABI calls on `stream`
-    calls = []
+    # the step as a list of (name, kind, thunk) C-ABI calls on `stream`: `calls` for the
+    # per-call breakdown, `step_calls` for the timed step (with --attn layer one
+    # csa2_decode_layer per layer, which is csa2_index_topk_prefetch + csa2_decode_attention)
+    calls, step_calls = [], []
     cur = None
+    layer = args.attn == "layer"
     for li, d in enumerate(dl):
         mode = d["mode"]
         if mode != ci.REUSE:
             cur = idx_bufs[li % 2]
-            calls.append((f"index_topk[{ci.MODE_NAMES[mode]}]", "index",
-                          (lambda d=d, cur=cur, mode=mode: L.csa2_index_topk(
-                              mode, cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N, P(nvis),
-                              cfg.K, None, P(cur), None, wsp, wsn, sp))))
+            if layer:
+                calls.append((f"index_topk_prefetch[{ci.MODE_NAMES[mode]}]", "index",
+                              (lambda d=d, cur=cur, mode=mode: L.csa2_index_topk_prefetch(
+                                  mode, cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N, P(nvis),
+                                  cfg.K, None, P(cur), None, P(codes), P(scales), wsp, wsn, sp))))
+            else:
+                calls.append((f"index_topk[{ci.MODE_NAMES[mode]}]", "index",
+                              (lambda d=d, cur=cur, mode=mode: L.csa2_index_topk(
+                                  mode, cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N, P(nvis),
+                                  cfg.K, None, P(cur), None, wsp, wsn, sp))))
         else:
             calls.append(("index_topk[REUSE]", "reuse",
                           (lambda cur=cur: L.csa2_index_topk(2, cfg.B, cfg.T, 0, None, None, None, 0, None,
                                                              cfg.K, P(cur), P(cur), None, None, 0, sp))))
-        if args.attn == "fused":
+        if layer:
+            step_calls.append((f"decode_layer[{ci.MODE_NAMES[mode]}]", "layer",
+                               (lambda d=d, cur=cur, mode=mode: L.csa2_decode_layer(
+                                   mode, cfg.B, cfg.T, cfg.H, cfg.H_I, P(d["q"]),
+                                   P(d["q_idx"]) if mode != ci.REUSE else None,
+                                   P(d["w"]) if mode != ci.REUSE else None,
+                                   P(d["z"]) if mode != ci.REUSE else None, P(codes), P(scales), cfg.N,
+                                   P(nvis) if mode != ci.REUSE else None, cfg.K,
+                                   P(cur) if mode == ci.REUSE else None, P(cur), P(d["swa"]), cfg.S, P(wst),
+                                   P(wln), cfg.W, cfg.d_v, scale, P(d["o"]), P(d["lse"]), wsp, wsn, sp))))
+        if args.attn in ("fused", "layer"):
             calls.append((f"decode_attention[{ci.MODE_NAMES[mode]}]", "attn",
                           (lambda d=d, cur=cur: L.csa2_decode_attention(
                               cfg.B, cfg.T, cfg.H, P(d["q"]), P(codes), P(scales), cfg.N, P(cur), cfg.K,
@@ -297,6 +317,8 @@ def run_ours(args):
                           (lambda d=d: L.csa2_swa_merge(
                               cfg.B, cfg.T, cfg.H, P(d["q"]), P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v,
                               scale, P(d["o"]), P(d["lse"]), P(d["o"]), P(d["lse"]), wsp, wsn, sp))))
+    if not layer:
+        step_calls = calls
     launches_per_call = {"index": 2, "reuse": 0, "attn": 1, "sparse": 1, "swa": 1}
 
     def cuchk(r):
@@ -308,7 +330,7 @@ def run_ours(args):
     events = [cuchk(cu.cuEventCreate(0)) for _ in range(len(calls) + 1)]
 
     def enqueue_step(record=True):
-        for i, (name, _, fn) in enumerate(calls):
+        for i, (name, _, fn) in enumerate(calls if record else step_calls):
             if record:
                 cuchk(cu.cuEventRecordWithFlags(events[i], sp, cu.CUevent_record_flags.CU_EVENT_RECORD_EXTERNAL))
             st = fn()
@@ -538,14 +560,15 @@ def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bu
                 dd.copy_(h, non_blocking=True)
         cur = None
         for li, d in enumerate(dl):
-            if d["mode"] != ci.REUSE:
+            reuse = d["mode"] == ci.REUSE
+            if not reuse:
                 cur = idx_bufs[li % 2]
-                r = L.csa2_index_topk(d["mode"], cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N,
-                                      P(nvis), cfg.K, None, P(cur), None, wsp, wsn, sp)
-                assert r == 0
-            r = L.csa2_decode_attention(cfg.B, cfg.T, cfg.H, P(d["q"]), P(codes), P(scales), cfg.N, P(cur),
-                                        cfg.K, P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v, scale,
-                                        P(d["o"]), P(d["lse"]), wsp, wsn, sp)
+            r = L.csa2_decode_layer(d["mode"], cfg.B, cfg.T, cfg.H, cfg.H_I, P(d["q"]),
+                                    None if reuse else P(d["q_idx"]), None if reuse else P(d["w"]),
+                                    None if reuse else P(d["z"]), P(codes), P(scales), cfg.N,
+                                    None if reuse else P(nvis), cfg.K, P(cur) if reuse else None, P(cur),
+                                    P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v, scale, P(d["o"]),
+                                    P(d["lse"]), wsp, wsn, sp)
             assert r == 0
         with torch.cuda.stream(stream):
             for h, dd in host_out:
@@ -582,8 +605,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ced", action="store_true")
-    ap.add_argument("--attn", choices=["fused", "two-call"], default="fused",
-                    help="attention per layer: one csa2_decode_attention call, or sparse_decode + swa_merge")
+    ap.add_argument("--attn", choices=["layer", "fused", "two-call"], default="layer",
+                    help="per layer: one csa2_decode_layer call (selection that prefetches the selected rows "
+                         "into L2, then the attention); csa2_index_topk + csa2_decode_attention; or "
+                         "csa2_index_topk + csa2_sparse_decode + csa2_swa_merge")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -127,6 +127,22 @@ CSA2_API int csa2_index_topk(int mode, int B, int T, int H_I,
                     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * csa2_index_topk_prefetch - csa2_index_topk whose selection also requests the FP4
+ * rows (kv_codes [B][n_stride][288], kv_scales [B][n_stride][36], the cache the
+ * attention that follows gathers from) of the entries it selects into L2.
+ *
+ * Not in the pages: a scheduling aid with the same results as csa2_index_topk;
+ * the attention's gathers then find the rows in L2. kv_codes 16-byte aligned;
+ * both may be null only in REUSE mode (which prefetches nothing).
+ */
+CSA2_API int csa2_index_topk_prefetch(int mode, int B, int T, int H_I,
+                    const void* q_idx, const float* w_idx,
+                    const void* z, int64_t n_stride, const int32_t* n_visible,
+                    int K, const int32_t* prev_idx, int32_t* out_idx, float* out_scores,
+                    const uint8_t* kv_codes, const uint8_t* kv_scales,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/*
  * csa2_index_topk_noalloc - csa2_index_topk without a caller workspace.
  *
  * Not part of the method (the pages describe no such call): the same selection
@@ -213,6 +229,27 @@ CSA2_API int csa2_decode_attention(int B, int T, int H, const void* q,
                    const int32_t* win_start, const int32_t* win_len, int n_win, int d_v,
                    float softmax_scale, float* o, float* lse, void* ws, size_t ws_bytes,
                    void* stream);
+
+/*
+ * csa2_decode_layer - one CSA2 decode layer: csa2_index_topk followed by
+ * csa2_decode_attention over the selection it writes (CSA2 global attention with
+ * its indexer and top-K, picx.dev summary; the sliding-window branch, blog repost).
+ *
+ * Equals csa2_index_topk_prefetch followed by csa2_decode_attention with the same
+ * arguments (out_scores not written): out_idx [B][T][K] receives the selection
+ * (REUSE: a copy of prev_idx), then o and lse the attention over it. kv_codes /
+ * kv_scales and z share n_stride (one entry per compressed position).
+ * Limits and argument rules: those of both calls. Both are checked before
+ * anything is launched. ws: csa2_workspace_bytes(B, T, H, n_stride, K) bytes
+ * prepared by csa2_workspace_init (REUSE: the header).
+ */
+CSA2_API int csa2_decode_layer(int mode, int B, int T, int H, int H_I, const void* q,
+                   const void* q_idx, const float* w_idx, const void* z,
+                   const uint8_t* kv_codes, const uint8_t* kv_scales, int64_t n_stride,
+                   const int32_t* n_visible, int K, const int32_t* prev_idx, int32_t* out_idx,
+                   const void* swa_kv, int64_t s_stride, const int32_t* win_start,
+                   const int32_t* win_len, int n_win, int d_v, float softmax_scale, float* o,
+                   float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /* Workspace bytes that cover every call above with these or smaller sizes: a
  * 256-byte header (the device status word), then for csa2_index_topk two uint32

@@ -62,6 +62,10 @@ def _lib():
     L.csa2_sparse_decode.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, vp, vp, vp, sz, vp]
     L.csa2_decode_attention.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, i64, vp, vp, i32, i32, f32,
                                         vp, vp, vp, sz, vp]
+    L.csa2_index_topk_prefetch.argtypes = [i32, i32, i32, i32, vp, vp, vp, i64, vp, i32, vp, vp, vp, vp, vp,
+                                           vp, sz, vp]
+    L.csa2_decode_layer.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, i32, vp, vp,
+                                    vp, i64, vp, vp, i32, i32, f32, vp, vp, vp, sz, vp]
     L.csa2_swa_merge.argtypes = [i32, i32, i32, vp, vp, i64, vp, vp, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp]
     L.csa2_workspace_bytes.argtypes = [i32, i32, i32, i64, i32]
     L.csa2_workspace_bytes.restype = sz
@@ -72,7 +76,8 @@ def _lib():
     L.csa2_version.argtypes = []
     L.csa2_last_cuda_error.argtypes = []
     L.csa2_last_cuda_error.restype = ctypes.c_char_p
-    for fn in ("csa2_encode_kv", "csa2_index_topk", "csa2_sparse_decode", "csa2_swa_merge",
+    for fn in ("csa2_encode_kv", "csa2_index_topk", "csa2_index_topk_prefetch", "csa2_sparse_decode",
+               "csa2_swa_merge", "csa2_decode_layer",
                "csa2_workspace_init", "csa2_read_device_status", "csa2_version"):
         getattr(L, fn).restype = ctypes.c_int
     _LIB = L
@@ -363,19 +368,69 @@ def csa2_decode_attention(q: torch.Tensor, kv_codes: torch.Tensor, kv_scales: to
     return o, lse
 
 
+def csa2_decode_layer(mode: int, q: torch.Tensor, kv_codes: torch.Tensor, kv_scales: torch.Tensor,
+                      swa_kv: torch.Tensor, win_start: torch.Tensor, win_len: torch.Tensor, n_win: int, K: int,
+                      q_idx=None, w_idx=None, z=None, n_visible=None, prev_idx=None, out_idx=None,
+                      softmax_scale: float = 1.0 / math.sqrt(D_KV), d_v: int = D_LATENT,
+                      o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      ws: Optional[torch.Tensor] = None, stream=None):
+    """One CSA2 decode layer in one call: the top-K selection of `mode` (as csa2_index_topk)
+    and the attention over it and the window (as csa2_decode_attention). Returns
+    (O [B, T, H, d_v] fp32, LSE [B, T, H] fp32, idx [B, T, K] int32)."""
+    L = _lib()
+    _dev(q, "q", _B16)
+    B, T, H, _ = q.shape
+    _dev(kv_codes, "kv_codes", (torch.uint8,))
+    N = kv_codes.shape[1]
+    _dev(kv_codes, "kv_codes", (torch.uint8,), (B, N, CODE_BYTES))
+    _dev(kv_scales, "kv_scales", (torch.uint8,), (B, N, SCALE_BYTES))
+    _dev(swa_kv, "swa_kv", _B16)
+    S = swa_kv.shape[1]
+    _dev(swa_kv, "swa_kv", _B16, (B, S, D_KV))
+    _dev(win_start, "win_start", (torch.int32,), (B * T,))
+    _dev(win_len, "win_len", (torch.int32,), (B * T,))
+    H_I = 0
+    if mode == REUSE:
+        if prev_idx is None:
+            raise ValueError("REUSE needs prev_idx")
+        _dev(prev_idx, "prev_idx", (torch.int32,), (B, T, K))
+    else:
+        _dev(q_idx, "q_idx", _B16)
+        H_I = q_idx.shape[2]
+        _dev(q_idx, "q_idx", _B16, (B, T, H_I, D_IDX))
+        _dev(w_idx, "w_idx", (torch.float32,), (B, T, H_I))
+        _dev(z, "z", _B16, (B, N, D_IDX))
+        _dev(n_visible, "n_visible", (torch.int32,), (B * T,))
+    if out_idx is None:
+        out_idx = torch.empty((B, T, K), dtype=torch.int32, device=q.device)
+    _dev(out_idx, "out_idx", (torch.int32,), (B, T, K))
+    if o is None:
+        o = torch.empty((B, T, H, d_v), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+    _dev(o, "o", (torch.float32,), (B, T, H, d_v))
+    _dev(lse, "lse", (torch.float32,), (B, T, H))
+    if ws is None:
+        ws = csa2_workspace(B, T, H, N if mode != REUSE else 0, K, device=q.device, stream=stream)
+    _check(L.csa2_decode_layer(mode, B, T, H, H_I, _ptr(q), _ptr(q_idx), _ptr(w_idx), _ptr(z), _ptr(kv_codes),
+                               _ptr(kv_scales), N, _ptr(n_visible), K, _ptr(prev_idx), _ptr(out_idx), _ptr(swa_kv),
+                               S, _ptr(win_start), _ptr(win_len), n_win, d_v, float(softmax_scale), _ptr(o),
+                               _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "csa2_decode_layer")
+    return o, lse, out_idx
+
+
 def decode_layer(mode: int, q: torch.Tensor, kv_codes: torch.Tensor, kv_scales: torch.Tensor,
                  swa_kv: torch.Tensor, win_start: torch.Tensor, win_len: torch.Tensor, n_win: int, K: int,
                  q_idx=None, w_idx=None, z=None, n_visible=None, prev_idx=None, ws=None, out_idx=None,
                  softmax_scale: float = 1.0 / math.sqrt(D_KV), fused: bool = True, stream=None):
-    """One CSA2 layer: index_topk (by mode), then attention over the selected entries and
-    the window: one csa2_decode_attention call (fused), or csa2_sparse_decode followed by
-    csa2_swa_merge. Returns (O, LSE, idx)."""
+    """One CSA2 layer: one csa2_decode_layer call (fused), or csa2_index_topk (by mode)
+    followed by csa2_sparse_decode and csa2_swa_merge. Returns (O, LSE, idx)."""
+    if fused:
+        return csa2_decode_layer(mode, q, kv_codes, kv_scales, swa_kv, win_start, win_len, n_win, K,
+                                 q_idx=q_idx, w_idx=w_idx, z=z, n_visible=n_visible, prev_idx=prev_idx,
+                                 out_idx=out_idx, softmax_scale=softmax_scale, ws=ws, stream=stream)
     idx = csa2_index_topk(mode, q_idx, w_idx, z, n_visible, K, prev_idx=prev_idx, out_idx=out_idx, ws=ws,
                           stream=stream)
-    if fused:
-        o, lse = csa2_decode_attention(q, kv_codes, kv_scales, idx, swa_kv, win_start, win_len, n_win,
-                                       softmax_scale, ws=ws, stream=stream)
-        return o, lse, idx
     o_g, lse_g = csa2_sparse_decode(q, kv_codes, kv_scales, idx, softmax_scale, ws=ws, stream=stream)
     o, lse = csa2_swa_merge(q, swa_kv, win_start, win_len, n_win, o_g, lse_g, softmax_scale, o_out=o_g,
                             lse_out=lse_g, ws=ws, stream=stream)

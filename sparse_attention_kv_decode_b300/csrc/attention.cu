@@ -66,7 +66,8 @@ constexpr int kRecvBytes = kDV * kRecvStride * 4;                    // 139,264
 constexpr int kMlOffset = kRecvBytes;                                // [split][2][64] floats
 static_assert(kRecvBytes + kMaxSplitsTC * 2 * 64 * 4 <= kCBytes, "merge buffers fit the tile");
 
-// mbarrier slots (8 bytes each)
+// mbarrier slots (8 bytes each); kChunkFull: chunks 0-5 of the tile staged,
+// kChunkFull + 1: chunks 6-8
 enum Bar { kQReady = 0, kChunkFull = 1, kGroupFree = 6, kSFull = 11, kPFull = 13, kTmaFull = 14,
            kDrain = 15, kQTma = 16, kRecv = 17, kNumBars = 18 };
 
@@ -286,15 +287,6 @@ __device__ __forceinline__ void load_piece(const uint8_t* cbase, const uint8_t* 
   }
 }
 
-// Requests into L2 (no data returned): `bytes` from a 16-byte aligned address (a
-// multiple of 16), or the line holding one address.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
-}
-
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -330,6 +322,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
   if (threadIdx.x == 0) {
     mbar_init(bar(kQReady), kWorkers);
     mbar_init(bar(kChunkFull), kWorkers);
+    mbar_init(bar(kChunkFull + 1), kWorkers);
     for (int g = 0; g < 5; ++g) mbar_init(bar(kGroupFree + g), 1);
     mbar_init(bar(kSFull), 1);
     mbar_init(bar(kSFull + 1), 1);
@@ -503,11 +496,16 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
               dequant_piece(sC, rc, 16 + (lane & 1), cw[8], sw[4]);
             }
           }
+          // chunks 0-5 are released as soon as they are staged: the S^T product of
+          // this tile starts on them while the last two groups wait for the end of the
+          // previous P.V
+          if (g == 2) {
+            fence_proxy_async_smem();
+            if (ok) mbar_arrive(bar(kChunkFull));
+          }
         }
-        // the whole tile is staged: one release for all 36 S^T MMAs (the issuing
-        // thread then runs them back to back)
         fence_proxy_async_smem();
-        if (ok) mbar_arrive(bar(kChunkFull));
+        if (ok) mbar_arrive(bar(kChunkFull + 1));
         wok = ok;
         if (wok && tf + 1 < nt_f) {
           fetch(ent16_next);
@@ -547,6 +545,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
           }
           fence_proxy_async_smem();
           mbar_arrive(bar(kChunkFull));
+          mbar_arrive(bar(kChunkFull + 1));
         }
         wok = ok;
       }
@@ -655,17 +654,30 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         if (*abort_flag) break;
         const int sb = t & 1;
         const uint32_t d_s = tmem + kColS + 64 * sb;
-        // one wait, then the 36 S^T MMAs back to back: a barrier poll between MMA
-        // batches would let the tensor pipe drain
+        // two waits (chunks 0-5, then 6-8), each followed by its MMAs back to back: a
+        // barrier poll costs the tensor pipe a few hundred cycles, so there is no
+        // finer release
         if (!mbar_wait(bar(kChunkFull), t & 1)) { fail(); ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 9; ++c) {
+        for (int c = 0; c < 6; ++c) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t a = umma_desc_sw128(uC + c * kCChunk + 32 * k);
             const uint64_t bq = umma_desc_sw128(uQ + c * kQChunk + 32 * k);
             umma_f16(d_s, a, bq, idesc_qk, (c | k) != 0);
+          }
+        }
+        issued = true;
+        if (!mbar_wait(bar(kChunkFull + 1), t & 1)) { fail(); ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 6; c < 9; ++c) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t a = umma_desc_sw128(uC + c * kCChunk + 32 * k);
+            const uint64_t bq = umma_desc_sw128(uQ + c * kQChunk + 32 * k);
+            umma_f16(d_s, a, bq, idesc_qk, 1u);
           }
         }
         issued = true;
@@ -697,13 +709,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     const uint8_t* cb = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
     const uint8_t* sb = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
     const int32_t* ir = fsrc.idx + (int64_t)qi * fsrc.K;
-    for (int p = p_begin + kTK + lane; p < p_end; p += 32) {
-      const int ent = ir[p];
-      if (ent >= 0 && ent < fsrc.n_stride) {
-        prefetch_l2_bulk(cb + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
-        const uint8_t* s0 = sb + (int64_t)ent * CSA2_SCALE_BYTES;
-        prefetch_l2(s0);
-        prefetch_l2(s0 + CSA2_SCALE_BYTES - 1);
+    // eight index loads in flight per lane before their requests go out
+    constexpr int kBatch = 8;
+    for (int p0 = p_begin + kTK; p0 < p_end; p0 += 32 * kBatch) {
+      int ent[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int p = p0 + 32 * k + lane;
+        ent[k] = p < p_end ? ir[p] : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (ent[k] >= 0 && ent[k] < fsrc.n_stride) {
+          prefetch_l2_bulk(cb + (int64_t)ent[k] * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
+          const uint8_t* s0 = sb + (int64_t)ent[k] * CSA2_SCALE_BYTES;
+          prefetch_l2(s0);
+          prefetch_l2(s0 + CSA2_SCALE_BYTES - 1);
+        }
       }
     }
   }

@@ -202,10 +202,54 @@ int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_model, const 
                                         z_out, static_cast<uint32_t*>(ws), st));
 }
 
-int csa2_index_topk(int mode, int B, int T, int H_I, const void* q_idx, const float* w_idx,
-                    const void* z, int64_t n_stride, const int32_t* n_visible, int K,
-                    const int32_t* prev_idx, int32_t* out_idx, float* out_scores, void* ws,
-                    size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+// Argument checks of csa2_decode_attention (CSA2_OK also for an empty batch).
+static int check_decode_attention(int B, int T, int H, const void* q, const uint8_t* kv_codes,
+                                  const uint8_t* kv_scales, int64_t n_stride, const int32_t* idx,
+                                  int K, const void* swa_kv, int64_t s_stride,
+                                  const int32_t* win_start, const int32_t* win_len, int n_win,
+                                  int d_v, float softmax_scale, float* o, float* lse, void* ws,
+                                  size_t ws_bytes) {
+  CHECK_ARG(B >= 0 && T >= 0 && H >= 1 && K >= 1 && n_stride >= 0 && s_stride >= 0 && n_win >= 0);
+  CHECK_ARG(softmax_scale == softmax_scale);
+  if (H % 16 != 0 || H > 64 || d_v != CSA2_D_LATENT || K > kMaxK || n_win > kMaxWin)
+    return CSA2_ERR_UNSUPPORTED;
+  const int64_t Q = (int64_t)B * T;
+  if (Q == 0) return CSA2_OK;
+  CHECK_ARG(q && idx && o && win_start && win_len);
+  CHECK_ARG(n_stride == 0 || (kv_codes && kv_scales));
+  CHECK_ARG(s_stride == 0 || swa_kv != nullptr);
+  CHECK_ARG(aligned(q, 16) && aligned(kv_codes, 16) && aligned(kv_scales, 4) && aligned(idx, 4) &&
+            aligned(swa_kv, 16) && aligned(win_start, 4) && aligned(win_len, 4) && aligned(o, 16) &&
+            aligned(lse, 4));
+  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
+  CHECK_ARG(aligned(ws, 256));
+  if (ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
+  return CSA2_OK;
+}
+
+static int decode_attention_launch(int B, int T, int H, const void* q, const uint8_t* kv_codes,
+                                   const uint8_t* kv_scales, int64_t n_stride, const int32_t* idx,
+                                   int K, const void* swa_kv, int64_t s_stride,
+                                   const int32_t* win_start, const int32_t* win_len, int n_win,
+                                   float softmax_scale, float* o, float* lse, void* ws,
+                                   void* stream) {
+  const int nsplit = attn_splits((int64_t)B * T, K, device_sm_count());
+  uint32_t* status = static_cast<uint32_t*>(ws);
+  const float scale_log2 = softmax_scale * 1.4426950408889634074f;
+  return cuda_status(launch_decode_attn(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K, swa_kv,
+                                        s_stride, win_start, win_len, n_win, scale_log2, o, lse,
+                                        nsplit, status, (cudaStream_t)stream));
+}
+
+// csa2_index_topk; pf_codes / pf_scales (nullable) name the FP4 cache whose rows of the
+// selected entries the selection requests into L2
+static int index_topk_impl(int mode, int B, int T, int H_I, const void* q_idx, const float* w_idx,
+                           const void* z, int64_t n_stride, const int32_t* n_visible, int K,
+                           const int32_t* prev_idx, int32_t* out_idx, float* out_scores, void* ws,
+                           size_t ws_bytes, void* stream, const uint8_t* pf_codes,
+                           const uint8_t* pf_scales) {
   CHECK_ARG(mode == CSA2_MODE_FULL || mode == CSA2_MODE_REINDEX || mode == CSA2_MODE_REUSE);
   CHECK_ARG(B >= 0 && T >= 0 && K >= 1);
   if (K > kMaxK) return CSA2_ERR_UNSUPPORTED;
@@ -236,7 +280,28 @@ int csa2_index_topk(int mode, int B, int T, int H_I, const void* q_idx, const fl
                                      stride, range, status, st);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_topk_select(scores, stride, n_visible, (int)Q, n_stride, K, range,
-                                        out_idx, out_scores, status, st));
+                                        out_idx, out_scores, status, st, pf_codes, pf_scales, T));
+}
+
+extern "C" {
+
+int csa2_index_topk(int mode, int B, int T, int H_I, const void* q_idx, const float* w_idx,
+                    const void* z, int64_t n_stride, const int32_t* n_visible, int K,
+                    const int32_t* prev_idx, int32_t* out_idx, float* out_scores, void* ws,
+                    size_t ws_bytes, void* stream) {
+  return index_topk_impl(mode, B, T, H_I, q_idx, w_idx, z, n_stride, n_visible, K, prev_idx,
+                         out_idx, out_scores, ws, ws_bytes, stream, nullptr, nullptr);
+}
+
+int csa2_index_topk_prefetch(int mode, int B, int T, int H_I, const void* q_idx, const float* w_idx,
+                             const void* z, int64_t n_stride, const int32_t* n_visible, int K,
+                             const int32_t* prev_idx, int32_t* out_idx, float* out_scores,
+                             const uint8_t* kv_codes, const uint8_t* kv_scales, void* ws,
+                             size_t ws_bytes, void* stream) {
+  CHECK_ARG(mode == CSA2_MODE_REUSE || n_stride == 0 || (kv_codes && kv_scales));
+  CHECK_ARG(aligned(kv_codes, 16));
+  return index_topk_impl(mode, B, T, H_I, q_idx, w_idx, z, n_stride, n_visible, K, prev_idx,
+                         out_idx, out_scores, ws, ws_bytes, stream, kv_codes, kv_scales);
 }
 
 int csa2_index_topk_noalloc(int mode, int B, int T, int H_I, const void* q_idx,
@@ -308,27 +373,32 @@ int csa2_decode_attention(int B, int T, int H, const void* q, const uint8_t* kv_
                           const void* swa_kv, int64_t s_stride, const int32_t* win_start,
                           const int32_t* win_len, int n_win, int d_v, float softmax_scale, float* o,
                           float* lse, void* ws, size_t ws_bytes, void* stream) {
-  CHECK_ARG(B >= 0 && T >= 0 && H >= 1 && K >= 1 && n_stride >= 0 && s_stride >= 0 && n_win >= 0);
-  CHECK_ARG(softmax_scale == softmax_scale);
-  if (H % 16 != 0 || H > 64 || d_v != CSA2_D_LATENT || K > kMaxK || n_win > kMaxWin)
-    return CSA2_ERR_UNSUPPORTED;
-  const int64_t Q = (int64_t)B * T;
-  if (Q == 0) return CSA2_OK;
-  CHECK_ARG(q && idx && o && win_start && win_len);
-  CHECK_ARG(n_stride == 0 || (kv_codes && kv_scales));
-  CHECK_ARG(s_stride == 0 || swa_kv != nullptr);
-  CHECK_ARG(aligned(q, 16) && aligned(kv_codes, 16) && aligned(kv_scales, 4) && aligned(idx, 4) &&
-            aligned(swa_kv, 16) && aligned(win_start, 4) && aligned(win_len, 4) && aligned(o, 16) &&
-            aligned(lse, 4));
-  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
-  CHECK_ARG(aligned(ws, 256));
-  if (ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
-  const int nsplit = attn_splits(Q, K, device_sm_count());
-  uint32_t* status = static_cast<uint32_t*>(ws);
-  const float scale_log2 = softmax_scale * 1.4426950408889634074f;
-  return cuda_status(launch_decode_attn(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K, swa_kv,
-                                        s_stride, win_start, win_len, n_win, scale_log2, o, lse,
-                                        nsplit, status, (cudaStream_t)stream));
+  const int s = check_decode_attention(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K, swa_kv,
+                                       s_stride, win_start, win_len, n_win, d_v, softmax_scale, o,
+                                       lse, ws, ws_bytes);
+  if (s != CSA2_OK || (int64_t)B * T == 0) return s;
+  return decode_attention_launch(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K, swa_kv, s_stride,
+                                 win_start, win_len, n_win, softmax_scale, o, lse, ws, stream);
+}
+
+int csa2_decode_layer(int mode, int B, int T, int H, int H_I, const void* q, const void* q_idx,
+                      const float* w_idx, const void* z, const uint8_t* kv_codes,
+                      const uint8_t* kv_scales, int64_t n_stride, const int32_t* n_visible, int K,
+                      const int32_t* prev_idx, int32_t* out_idx, const void* swa_kv,
+                      int64_t s_stride, const int32_t* win_start, const int32_t* win_len,
+                      int n_win, int d_v, float softmax_scale, float* o, float* lse, void* ws,
+                      size_t ws_bytes, void* stream) {
+  // both halves are validated before either launches
+  int s = check_decode_attention(B, T, H, q, kv_codes, kv_scales, n_stride, out_idx, K, swa_kv,
+                                 s_stride, win_start, win_len, n_win, d_v, softmax_scale, o, lse,
+                                 ws, ws_bytes);
+  if (s != CSA2_OK) return s;
+  s = index_topk_impl(mode, B, T, H_I, q_idx, w_idx, z, n_stride, n_visible, K, prev_idx, out_idx,
+                      nullptr, ws, ws_bytes, stream, kv_codes, kv_scales);
+  if (s != CSA2_OK || (int64_t)B * T == 0) return s;
+  return decode_attention_launch(B, T, H, q, kv_codes, kv_scales, n_stride, out_idx, K, swa_kv,
+                                 s_stride, win_start, win_len, n_win, softmax_scale, o, lse, ws,
+                                 stream);
 }
 
 }  // extern "C"

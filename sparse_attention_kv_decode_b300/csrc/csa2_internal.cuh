@@ -59,9 +59,13 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
                                int64_t n_stride, const int32_t* n_visible, int B, int T, int H_I,
                                float* scores, int64_t score_stride, uint32_t* range,
                                uint32_t* status, cudaStream_t st);
+// pf_codes / pf_scales (nullable): FP4 cache whose rows of the selected entries are
+// requested into L2 as they are written (batch b = query / T, rows of n_stride)
 cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
                                int Q, int64_t n_stride, int K, uint32_t* range, int32_t* out_idx,
-                               float* out_scores, uint32_t* status, cudaStream_t st);
+                               float* out_scores, uint32_t* status, cudaStream_t st,
+                               const uint8_t* pf_codes = nullptr, const uint8_t* pf_scales = nullptr,
+                               int T = 1);
 cudaError_t launch_copy_idx(const int32_t* src, int32_t* dst, int64_t n, cudaStream_t st);
 cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t* codes,
                                const uint8_t* scales, int64_t n_stride, const int32_t* idx,
@@ -273,6 +277,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
   }
 }
 
+// Requests into L2 (no data returned): `bytes` from a 16-byte aligned address (a
+// multiple of 16), or the line holding one address.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t mbar) {
   asm volatile(
@@ -403,6 +416,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

@@ -448,7 +448,8 @@ __device__ __noinline__ void stats_round(SelShared& sh, float* cand_in_s, int* c
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ n_visible,
     int64_t n_stride, int K, int slice_cap, uint32_t* __restrict__ range, int32_t* __restrict__ out_idx,
-    float* __restrict__ out_scores, uint32_t* __restrict__ status) {
+    float* __restrict__ out_scores, uint32_t* __restrict__ status, const uint8_t* __restrict__ pf_codes,
+    const uint8_t* __restrict__ pf_scales, int T) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
   uint32_t C, r;
@@ -717,11 +718,21 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     }
   }
   pos += offset;
+  // the FP4 rows of the selected entries are requested into L2 for the attention that
+  // gathers them next
+  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * n_stride * CSA2_CODE_BYTES : nullptr;
+  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * n_stride * CSA2_SCALE_BYTES : nullptr;
   for (int e = e0; e < e1; ++e)
     if (state[e] == 1) {
       if (pos < K) {
-        out[pos] = my0 + e;
+        const int ent = my0 + e;
+        out[pos] = ent;
         if (outs) outs[pos] = sc[e];
+        if (pfc) {
+          prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
+          prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES);
+          prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES + CSA2_SCALE_BYTES - 1);
+        }
       }
       ++pos;
     }
@@ -741,7 +752,8 @@ static int select_cluster_size(int64_t n_stride) {
 
 cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
                                int Q, int64_t n_stride, int K, uint32_t* range, int32_t* out_idx,
-                               float* out_scores, uint32_t* status, cudaStream_t st) {
+                               float* out_scores, uint32_t* status, cudaStream_t st,
+                               const uint8_t* pf_codes, const uint8_t* pf_scales, int T) {
   static_assert(kNBMax % kSelThreads == 0 && kNBMin % kSelThreads == 0, "bins per thread");
   if (Q == 0) return cudaSuccess;
   const int C = select_cluster_size(n_stride);
@@ -772,7 +784,8 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, score_stride, n_visible, n_stride, K,
-                            slice_cap, range, out_idx, out_scores, status);
+                            slice_cap, range, out_idx, out_scores, status, pf_codes, pf_scales,
+                            T < 1 ? 1 : T);
 }
 
 __global__ void copy_idx_kernel(const int32_t* __restrict__ src, int32_t* __restrict__ dst,

@@ -135,3 +135,34 @@ def test_decode_attention_validation(L):
     assert call(a18=None, a19=0) == 3             # no workspace
     assert call(a19=128) == 3                     # workspace below the status header
     assert call(a0=0) == 0                        # empty batch: nothing to do
+
+
+def test_decode_layer_validation(L):
+    """Both halves of csa2_decode_layer are checked before anything launches (no GPU)."""
+    r = L.csa2_decode_layer
+    f = ctypes.c_float(0.04)
+    # mode, B, T, H, H_I, q, q_idx, w_idx, z, codes, scales, N, n_visible, K, prev, out_idx,
+    # swa, S, win_start, win_len, n_win, d_v, scale, o, lse, ws, ws_bytes, stream
+    args = [0, 1, 1, 64, 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, 128, None, FAKE,
+            FAKE, 128, FAKE, FAKE, 128, 512, f, FAKE, FAKE, FAKE, 1 << 30, None]
+
+    def call(**kw):
+        a = list(args)
+        for k, v in kw.items():
+            a[int(k[1:])] = v
+        return r(*a)
+
+    assert call(a3=20) == 2                       # attention: heads not a multiple of 16
+    assert call(a20=300) == 2                     # attention: window longer than 256
+    assert call(a21=576) == 2                     # attention: d_v must be 512
+    assert call(a13=5000) == 2                    # K above 4096
+    assert call(a4=17) == 2                       # selection: more than 16 indexer heads
+    assert call(a0=7) == 1                        # unknown mode
+    assert call(a5=None) == 1                     # q missing
+    assert call(a6=None) == 1                     # q_idx missing (FULL)
+    assert call(a15=None) == 1                    # out_idx missing
+    assert call(a0=2, a14=None) == 1              # REUSE without prev_idx
+    assert call(a22=ctypes.c_float(float("nan"))) == 1
+    assert call(a25=None, a26=0) == 3             # no workspace
+    assert call(a26=4096) == 3                    # workspace without room for the scores
+    assert call(a1=0) == 0                        # empty batch: nothing to do

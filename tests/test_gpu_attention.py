@@ -1,5 +1,6 @@
 """Sparse decode + SWA merge parity against the FP64 oracle (max-abs 2e-3, rel-L2 1e-3),
-through the two separate calls and through the one fused call (csa2_decode_attention).
+through the separate calls (csa2_index_topk, csa2_sparse_decode, csa2_swa_merge) and
+through the one-layer call (csa2_decode_layer: the selection, then csa2_decode_attention).
 
 Ref: "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression": sparse attention
 over the whole context combined with a sliding-window branch (blog repost), the CSA2
@@ -260,3 +261,34 @@ def test_deterministic_outputs():
     b = _run_group(cfg, inp)
     for (_, oa, la, ia), (_, ob, lb, ib) in zip(a, b):
         assert np.array_equal(oa, ob) and np.array_equal(la, lb) and np.array_equal(ia, ib)
+
+
+def test_decode_layer_equals_topk_then_attention():
+    """csa2_decode_layer (whose selection also requests the selected FP4 rows into L2) writes
+    exactly what csa2_index_topk followed by csa2_decode_attention writes."""
+    cfg = ci.scaled(ci.DECODE_128K, B=4, N=4096, K=512)
+    inp = ci.make_decode_inputs(cfg)
+    B, T = cfg.B, cfg.T
+    ws = csa2.csa2_workspace(B, T, cfg.H, cfg.N, cfg.K, device=DEV)
+    nvis = to_dev(inp.n_visible, DEV)
+    wst, wln = to_dev(inp.win_start, DEV), to_dev(inp.win_len, DEV)
+    prev = None
+    codes = scales = None
+    for L in inp.layers:
+        if L.mode == ci.FULL:
+            codes, scales = _cache(L.X)
+        qd, swa = to_dev_bf16(L.q, DEV), to_dev_bf16(L.swa, DEV)
+        kw = {}
+        if L.mode != ci.REUSE:
+            kw = dict(q_idx=to_dev_bf16(L.q_idx, DEV), w_idx=to_dev(L.w_idx, DEV), z=to_dev_bf16(L.z, DEV),
+                      n_visible=nvis)
+        o1, l1, i1 = csa2.csa2_decode_layer(L.mode, qd, codes, scales, swa, wst, wln, cfg.W, cfg.K,
+                                            prev_idx=prev, ws=ws, **kw)
+        i2 = csa2.csa2_index_topk(L.mode, kw.get("q_idx"), kw.get("w_idx"), kw.get("z"), kw.get("n_visible"),
+                                  cfg.K, prev_idx=prev, out_idx=torch.empty_like(i1), ws=ws)
+        o2, l2 = csa2.csa2_decode_attention(qd, codes, scales, i2, swa, wst, wln, cfg.W, ws=ws)
+        torch.cuda.synchronize()
+        assert csa2.csa2_read_device_status(ws)[0] == 0
+        assert torch.equal(i1, i2)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+        prev = i1
