@@ -7,9 +7,15 @@
 // bf16.
 //
 // One persistent, warp-specialised tcgen05 GEMM over the concatenated output
-// columns of every layer ([576 kv | 64 z] per layer, 640 per layer):
-//   warp 0      TMA producer: H tile 128x64 and four 64-row weight boxes per
-//               k-block into a 4-stage shared-memory ring (128-byte swizzle)
+// columns of every layer ([576 kv | 64 z] per layer, 640 per layer). The CTAs run
+// in pairs (clusters of 2) on the row tiles 2i and 2i+1 of the same column tile:
+// each loads half of the weight boxes and multicasts them to both, so the weight
+// lines that many SMs read at the same moment leave L2 once per pair (those
+// shared reads, not the H tiles, were what held the tensor pipe back):
+//   warp 0      TMA producer: own H tile 128x64 and two of the four 64-row weight
+//               boxes per k-block (multicast to the pair) into a 4-stage
+//               shared-memory ring (128-byte swizzle); a stage is refilled once
+//               the MMAs of both CTAs have released it
 //   warp 1      TMEM allocation and the MMA issuer: tcgen05.mma kind::f16,
 //               M=128, N=256, K=16, fp32 accumulators in TMEM, double-buffered
 //               (2 x 256 columns) so the epilogue of one tile overlaps the
@@ -34,20 +40,43 @@ constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
 constexpr int kSegPerLayer = 10;                // 9 kv segments (576) + 1 z segment (64)
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
-constexpr int kGroupM = 16;                     // m-tiles per raster group
+constexpr int kGroupM = 8;                      // m-tile pairs per raster group
 constexpr size_t kSmemBytes = kStages * kStageBytes + 1024 + 256;
 
+// Work item t of a pair: m-tile pair mp (row tiles 2mp, 2mp+1) x column tile n,
+// m-pairs fastest inside groups of kGroupM pairs.
 struct TileMap {
-  int m_tiles, n_tiles, total;
-  __device__ __forceinline__ void coords(int t, int& m, int& n) const {
+  int m_pairs, n_tiles, total;
+  __device__ __forceinline__ void coords(int t, int rank, int& m, int& n) const {
     const int per_group = kGroupM * n_tiles;
     const int grp = t / per_group;
     const int in = t - grp * per_group;
-    const int gm = min(kGroupM, m_tiles - grp * kGroupM);
+    const int gm = min(kGroupM, m_pairs - grp * kGroupM);
     n = in / gm;
-    m = grp * kGroupM + in % gm;
+    m = 2 * (grp * kGroupM + in % gm) + rank;
   }
 };
+
+__device__ __forceinline__ void cluster_sync_pair() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// arrive on the same mbarrier of both CTAs of the pair once the MMAs issued so far complete
+__device__ __forceinline__ void umma_commit_pair(uint32_t mbar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          mbar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar), "h"((uint16_t)3)
+      : "memory");
+}
 
 __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmWkv,
@@ -68,16 +97,19 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_segs = n_layers * kSegPerLayer;
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
   TileMap tm;
-  tm.m_tiles = (rows + kBM - 1) / kBM;
+  tm.m_pairs = ((rows + kBM - 1) / kBM + 1) / 2;
   tm.n_tiles = (n_segs + 3) / 4;
-  tm.total = tm.m_tiles * tm.n_tiles;
+  tm.total = tm.m_pairs * tm.n_tiles;
   const int kblocks = d_model / kBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 2);   // released by the MMAs of both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_tfull + 8 * a, 1);
@@ -97,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // both CTAs' barriers exist before the pair's first multicast or remote arrive
+  cluster_sync_pair();
   const uint32_t tmem = *tmem_holder;
 
   if (warp == 0) {
@@ -107,9 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < tm.total && !*abort_flag; t += gridDim.x) {
+      for (int t = pair; t < tm.total && !*abort_flag; t += n_pairs) {
         int m, n;
-        tm.coords(t, m, n);
+        tm.coords(t, (int)rank, m, n);
         int nseg = n_segs - 4 * n;
         nseg = nseg > 4 ? 4 : nseg;
         const uint32_t bytes = kABytes + nseg * kSegBytes;
@@ -124,14 +158,16 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
           armed[stage] = true;
           armed_phase[stage] = phase;
           const uint32_t sa = sbase + stage * kStageBytes;
+          // rows past the matrix (an odd last pair) read as zeros
           tma_load_2d(sa, &tmA, kb * kBK, m * kBM, fb);
-          for (int s = 0; s < nseg; ++s) {
+          // weight boxes s of this CTA's parity, into the same stage of both CTAs
+          for (int s = (int)rank; s < nseg; s += 2) {
             const int g = 4 * n + s, l = g / kSegPerLayer, sl = g % kSegPerLayer;
             const uint32_t sb = sa + kABytes + s * kSegBytes;
             if (sl < 9)
-              tma_load_2d(sb, &tmWkv, kb * kBK, l * CSA2_D_KV + sl * 64, fb);
+              tma_load_2d_pair(sb, &tmWkv, kb * kBK, l * CSA2_D_KV + sl * 64, fb);
             else
-              tma_load_2d(sb, &tmWz, kb * kBK, l * CSA2_D_IDX, fb);
+              tma_load_2d_pair(sb, &tmWz, kb * kBK, l * CSA2_D_IDX, fb);
           }
           if (++stage == kStages) stage = 0, phase ^= 1;
         }
@@ -147,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool issued = false;
-      for (int t = blockIdx.x; t < tm.total && !*abort_flag; t += gridDim.x) {
+      for (int t = pair; t < tm.total && !*abort_flag; t += n_pairs) {
         if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1)) {
           atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
           *abort_flag = 1;
@@ -170,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
           for (int k = 0; k < kBK / 16; ++k)
             umma_bf16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), idesc,
                       (kb | k) != 0);
-          umma_commit(bar_empty + 8 * stage);
+          umma_commit_pair(bar_empty + 8 * stage);
           issued = true;
           if (++stage == kStages) stage = 0, phase ^= 1;
         }
@@ -189,10 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
     const int r_in = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < tm.total; t += gridDim.x) {
+    for (int t = pair; t < tm.total; t += n_pairs) {
       if (*abort_flag) break;
       int m, n;
-      tm.coords(t, m, n);
+      tm.coords(t, (int)rank, m, n);
       bool ok = mbar_wait(bar_tfull + 8 * acc, acc_phase);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -258,6 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
                  "r"(kTmemCols)
                  : "memory");
   }
+  // the peer's multicasts into this CTA and its releases of this CTA's stages have
+  // landed before either CTA exits
+  cluster_sync_pair();
 }
 
 }  // namespace
@@ -275,15 +314,25 @@ cudaError_t launch_ced_project(const void* h, int64_t rows, int d_model, const v
   cudaError_t e = set_attr_once(4, (const void*)ced_proj_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t m_tiles = (rows + kBM - 1) / kBM;
+  const int64_t m_pairs = ((rows + kBM - 1) / kBM + 1) / 2;
   const int64_t n_tiles = ((int64_t)n_layers * kSegPerLayer + 3) / 4;
-  const int64_t total = m_tiles * n_tiles;
-  const int n_sm = device_sm_count();
-  const int grid = (int)(total < n_sm ? total : n_sm);
-  ced_proj_kernel<<<grid, kThreads, kSmemBytes, st>>>(ta, tkv, tz, (int)rows, d_model, n_layers,
-                                                      codes, scales,
-                                                      static_cast<uint16_t*>(z_out), status);
-  return cudaGetLastError();
+  const int64_t total = m_pairs * n_tiles;
+  const int n_pairs_max = device_sm_count() / 2;
+  const int grid = 2 * (int)(total < n_pairs_max ? total : n_pairs_max);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ced_proj_kernel, ta, tkv, tz, (int)rows, d_model, n_layers, codes,
+                            scales, static_cast<uint16_t*>(z_out), status);
 }
 
 }  // namespace csa2
