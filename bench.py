@@ -533,33 +533,59 @@ def run_ced(args, torch, csa2, dev, peaks):
 
 
 def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs, ws, world, dev):
-    """Same step through the C ABI with host buffers: per step, H2D of the step's queries
-    (pinned) and D2H of every layer's output; no graph, one ctypes call per ABI call."""
-    stream = torch.cuda.Stream(device=dev)
-    sp = stream.cuda_stream
+    """Same step through the C ABI with host buffers, as a serving loop runs it: per step,
+    H2D of the step's queries from pinned memory and D2H of every layer's output, no graph,
+    one ctypes call per layer. The copies run on their own streams with two sets of device
+    I/O buffers, so step i+1's upload and step i-1's download overlap step i's kernels."""
+    comp = torch.cuda.Stream(device=dev)
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
+    sp = comp.cuda_stream
     scale = ctypes.c_float(cfg.softmax_scale)
     P = lambda t: t.data_ptr()
-    host_in, host_out = [], []
     h2d = d2h = 0
-    for d in dl:
-        for k in ("q", "q_idx", "w"):
-            if k in d:
-                h = torch.empty(d[k].shape, dtype=d[k].dtype, pin_memory=True)
-                h.copy_(d[k].cpu())
-                host_in.append((h, d[k]))
-                h2d += h.numel() * h.element_size()
-        for k in ("o", "lse"):
-            h = torch.empty(d[k].shape, dtype=d[k].dtype, pin_memory=True)
-            host_out.append((h, d[k]))
-            d2h += h.numel() * h.element_size()
+    sets = []   # per buffer set: [(host, device) inputs], [(host, device) outputs], per-layer dicts
+    for sidx in range(2):
+        ins, outs, layers = [], [], []
+        for d in dl:
+            dd = dict(d)
+            for k in ("q", "q_idx", "w", "o", "lse"):
+                if k in d:
+                    dd[k] = d[k] if sidx == 0 else torch.empty_like(d[k])
+            for k in ("q", "q_idx", "w"):
+                if k in dd:
+                    h = torch.empty(dd[k].shape, dtype=dd[k].dtype, pin_memory=True)
+                    h.copy_(d[k].cpu())
+                    ins.append((h, dd[k]))
+                    if sidx == 0:
+                        h2d += h.numel() * h.element_size()
+            for k in ("o", "lse"):
+                h = torch.empty(dd[k].shape, dtype=dd[k].dtype, pin_memory=True)
+                outs.append((h, dd[k]))
+                if sidx == 0:
+                    d2h += h.numel() * h.element_size()
+            layers.append(dd)
+        sets.append((ins, outs, layers))
     wsp, wsn = P(ws), ws.numel()
+    ev = lambda: torch.cuda.Event()
+    # per set: inputs landed / kernels done / outputs copied out
+    up_done, comp_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    started = [False, False]
 
-    def step():
-        with torch.cuda.stream(stream):
-            for h, dd in host_in:
+    def step(i):
+        s = i & 1
+        ins, outs, layers = sets[s]
+        with torch.cuda.stream(up):
+            if started[s]:
+                up.wait_event(comp_done[s])      # the kernels of step i-2 have read this set's inputs
+            for h, dd in ins:
                 dd.copy_(h, non_blocking=True)
+            up_done[s].record(up)
+        comp.wait_event(up_done[s])
+        if started[s]:
+            comp.wait_event(down_done[s])        # step i-2's outputs have left this set
         cur = None
-        for li, d in enumerate(dl):
+        for li, d in enumerate(layers):
             reuse = d["mode"] == ci.REUSE
             if not reuse:
                 cur = idx_bufs[li % 2]
@@ -570,30 +596,40 @@ def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bu
                                     P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v, scale, P(d["o"]),
                                     P(d["lse"]), wsp, wsn, sp)
             assert r == 0
-        with torch.cuda.stream(stream):
-            for h, dd in host_out:
+        comp_done[s].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(comp_done[s])
+            for h, dd in outs:
                 h.copy_(dd, non_blocking=True)
+            down_done[s].record(down)
+        started[s] = True
 
-    for _ in range(max(3, args.warmup // 4)):
-        step()
-    stream.synchronize()
+    for i in range(max(3, args.warmup // 4)):
+        step(i)
+    torch.cuda.synchronize(dev)
     n = max(10, args.steps // 10)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
-    e0.record(stream)
-    for _ in range(n):
-        step()
-    e1.record(stream)
-    stream.synchronize()
+    # the timed region starts before the first upload and ends after the last download
+    e0.record(up)
+    comp.wait_stream(up)
+    down.wait_stream(up)
+    for i in range(n):
+        step(i)
+    down.wait_stream(comp)
+    e1.record(down)
+    torch.cuda.synchronize(dev)
     total = e0.elapsed_time(e1) / 1e3
     if world > 1:
         t = torch.tensor([total], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total = float(t.item())
     return {"value": world * n / total, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n, "note": "C-ABI calls without a graph; pinned host inputs/outputs copied every step"}
+            "steps": n, "note": "csa2_decode_layer calls without a graph; pinned host inputs and outputs copied "
+                                "every step on copy streams, two device I/O buffer sets (upload of step i+1 and "
+                                "download of step i-1 overlap step i)"}
 
 
 def main():
