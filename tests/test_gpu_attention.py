@@ -36,8 +36,9 @@ def _oracle_query(q_bits_bt, rows_of, idx, swa_bits_b, ws, wl, cfg):
     return og, lg, O, L
 
 
-def _run_group(cfg, inp, sample=None, fused=True):
-    """Run every layer of the group on the GPU; compare (sampled) queries with the oracle."""
+def _run_group(cfg, inp, sample=None, fused=True, t_sample=None):
+    """Run every layer of the group on the GPU; compare (sampled) sequences and query tokens
+    with the oracle."""
     B, T = cfg.B, cfg.T
     ws = csa2.csa2_workspace(B, T, cfg.H, cfg.N, cfg.K, device=DEV)
     nvis = to_dev(inp.n_visible, DEV)
@@ -70,6 +71,7 @@ def _run_group(cfg, inp, sample=None, fused=True):
         prev = idx
 
     bs = range(B) if sample is None else sample
+    ts = list(range(T)) if t_sample is None else list(t_sample)
     X = kv_host["X"]
     for b in bs:
         cache_rows = {}
@@ -88,8 +90,8 @@ def _run_group(cfg, inp, sample=None, fused=True):
 
         for (L, o, lse, idx_h) in results:
             if L.mode != ci.REUSE:
-                I = indexer.scores(f64(L.q_idx[b]), L.w_idx[b], f64(L.z[b]))
-            for t in range(T):
+                I = dict(zip(ts, indexer.scores(f64(L.q_idx[b][ts]), L.w_idx[b][ts], f64(L.z[b]))))
+            for t in ts:
                 qi = b * T + t
                 if L.mode != ci.REUSE:
                     want = indexer.topk(I[t], inp.n_visible[qi], cfg.K)
@@ -247,6 +249,21 @@ def test_full_size_decode_128k_group_sampled():
     in the bench's launch configuration (fused attention); 3 sequences checked against the oracle."""
     cfg = ci.DECODE_128K
     _run_group(cfg, ci.make_decode_inputs(cfg), sample=[0, 17, 31])
+
+
+def test_full_size_decode_1m_sampled():
+    """4 sequences over 262,144 entries each (1M tokens at 4:1), K = 2048, one FULL layer: the
+    four queries split 16 ways (16-CTA clusters, the merge for more than four splits);
+    sequences 0 and 3 checked against the oracle."""
+    cfg = ci.DECODE_1M
+    _run_group(cfg, ci.make_decode_inputs(cfg), sample=[0, 3])
+
+
+def test_full_size_prefill_chunk_sampled():
+    """4096 query tokens of one sequence over 32768 entries with causal visibility, K = 2048,
+    window 128 (the prefill-chunk workload); first, middle and last tokens checked."""
+    cfg = ci.PREFILL_CHUNK
+    _run_group(cfg, ci.make_decode_inputs(cfg), t_sample=[0, 1, 777, 2048, 4095])
 
 
 def test_full_size_decode_128k_two_calls_sampled():
