@@ -689,21 +689,29 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     __syncthreads();
   }
 
-  // ---- ordered output (thread t owns a contiguous chunk of 16 entries, or more)
-  const int chunk = ((my_len + kSelThreads - 1) / kSelThreads + 15) & ~15;
-  const int e0 = tid * chunk, e1 = min(e0 + chunk, my_len);
-  int c = 0;
-  for (int e = e0; e < e1; e += 16) {
-    const uint4 w = *reinterpret_cast<const uint4*>(state + e);  // state[] is padded to slice_cap
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-        c += (e + 4 * q + b < e1) && ((ww[q] >> (8 * b)) & 0xFFu) == 1u;
+  // ---- ordered output: warp w owns a contiguous run of entries, compacted 32 at a time
+  // with ballots (a count pass, one scan of the 32 warp counts, a write pass)
+  const int warp = tid >> 5;
+  constexpr int kWarps = kSelThreads / 32;
+  const int per_warp = ((my_len + kWarps - 1) / kWarps + 31) & ~31;
+  const int wb = warp * per_warp, we = min(wb + per_warp, my_len);
+  int wc = 0;
+  for (int e0 = wb; e0 < we; e0 += 32) {
+    const int e = e0 + lane;
+    wc += __popc(__ballot_sync(0xffffffffu, e < we && state[e] == 1));
   }
-  int my_sel;
-  int pos = block_excl_scan(c, sh.scan, my_sel);
+  __syncthreads();   // sh.scan is free (any earlier use is complete)
+  if (lane == 0) sh.scan[warp] = wc;
+  __syncthreads();
+  const int wcnt = sh.scan[lane];
+  int incl = wcnt;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += t;
+  }
+  const int my_sel = __shfl_sync(0xffffffffu, incl, 31);
+  int pos = __shfl_sync(0xffffffffu, incl - wcnt, warp);
   int offset = off_fast, total_sel = total_fast;
   if (!settled) {
     if (tid < (int)C) st_remote_u32(reinterpret_cast<uint32_t*>(&sh.sel_in[r]), tid, (uint32_t)my_sel);
@@ -722,20 +730,23 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   // gathers them next
   const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * n_stride * CSA2_CODE_BYTES : nullptr;
   const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * n_stride * CSA2_SCALE_BYTES : nullptr;
-  for (int e = e0; e < e1; ++e)
-    if (state[e] == 1) {
-      if (pos < K) {
-        const int ent = my0 + e;
-        out[pos] = ent;
-        if (outs) outs[pos] = sc[e];
-        if (pfc) {
-          prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
-          prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES);
-          prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES + CSA2_SCALE_BYTES - 1);
-        }
+  for (int e0 = wb; e0 < we; e0 += 32) {
+    const int e = e0 + lane;
+    const bool take = e < we && state[e] == 1;
+    const uint32_t bal = __ballot_sync(0xffffffffu, take);
+    const int p = pos + __popc(bal & ((1u << lane) - 1u));
+    if (take && p < K) {
+      const int ent = my0 + e;
+      out[p] = ent;
+      if (outs) outs[p] = sc[e];
+      if (pfc) {
+        prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
+        prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES);
+        prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES + CSA2_SCALE_BYTES - 1);
       }
-      ++pos;
     }
+    pos += __popc(bal);
+  }
   if (r == C - 1)
     for (int p = total_sel + tid; p < K; p += kSelThreads) {
       out[p] = -1;
