@@ -79,6 +79,18 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def aggregate_over_ranks(total_s: float, steps: int, world: int, device=None):
+    """Every rank times its own replica of the workload (no collective on the data path);
+    the job's time is the slowest rank's, and its value is world x steps / that time.
+    Returns (seconds, whole-job steps/s)."""
+    if world > 1:
+        import torch
+        t = torch.tensor([total_s], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    return total_s, world * steps / total_s
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
@@ -403,13 +415,8 @@ def run_ours(args):
             per_call[i].append(cuchk(cu.cuEventElapsedTime(events[i], events[i + 1])))
     torch.cuda.synchronize()
 
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s, value = aggregate_over_ranks(sum(step_ms) / 1e3, args.steps, world, dev)
     ms_per_step = total_s * 1e3 / args.steps
-    value = world * args.steps / total_s
     peaks = load_peaks()
     bytes_step = algorithmic_bytes_per_step(cfg)
 
@@ -621,12 +628,8 @@ def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bu
     down.wait_stream(comp)
     e1.record(down)
     torch.cuda.synchronize(dev)
-    total = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total = float(t.item())
-    return {"value": world * n / total, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+    total, value = aggregate_over_ranks(e0.elapsed_time(e1) / 1e3, n, world, dev)
+    return {"value": value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "note": "csa2_decode_layer calls without a graph; pinned host inputs and outputs copied "
                                 "every step on copy streams, two device I/O buffer sets (upload of step i+1 and "
                                 "download of step i-1 overlap step i)"}

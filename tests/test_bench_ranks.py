@@ -1,0 +1,59 @@
+"""Multi-rank host logic of bench.py on CPU (gloo, world size 2, no GPU).
+
+The decode sequences are independent, so `bench.py --gpus N` runs one replica of the
+workload per rank with no collective on the data path; the job's time is the slowest
+rank's and its value is N x steps / that time. Only rank 0 prints.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    r, lr, w = bench.dist_env()
+    # rank k timed 1 + k seconds for its 100 steps
+    total, value = bench.aggregate_over_ranks(1.0 + rank, 100, w)
+    q.put((rank, r, lr, w, total, value))
+    dist.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29400 + os.getpid() % 500
+    ps = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    got = sorted(q.get(timeout=180) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, r, lr, w, total, value in got:
+        assert (r, lr, w) == (rank, rank, 2)
+        assert total == 2.0                    # the slower rank's time
+        assert value == pytest.approx(2 * 100 / 2.0)
+
+
+def test_single_rank_is_unchanged():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.aggregate_over_ranks(0.5, 10, 1) == (0.5, 20.0)
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
