@@ -484,6 +484,7 @@ def run_ours(args):
             "config": config_block(),
             "hbm_gbs_step": round(bytes_step / (ms_per_step * 1e-3) / 1e9, 1),
             "frac_of_8tbs": round(bytes_step / (ms_per_step * 1e-3) / 1e9 / TARGET_HBM_GBS, 4),
+            "frac_of_measured_hbm": round(bytes_step / (ms_per_step * 1e-3) / 1e9 / peaks["hbm"], 4),
             "bytes_per_step": bytes_step,
             "roofline": roofline, "roofline_by_call": rows, "calls": breakdown,
             "calls_note": "per-call means from a separate pass with an event between calls",
