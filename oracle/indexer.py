@@ -6,12 +6,21 @@ Attention 2: a FULL layer computes its own indexer K and top-K indices, a
 REINDEX layer computes fresh top-K indices, a REUSE layer takes the preceding
 layer's indices unchanged.
 
+Hierarchical Sparse Indexer (same summary, Methodology / 3): the first FULL
+layer's selection builds a candidate pool of at most 2,048 blocks x 8
+positions that bounds the search of the REINDEX layers after it.
+
 Readings (the page names the indexer but prints no formula):
   * score I[n] = sum_h w[h] * max(0, q[h] . z[n]) over H_I indexer heads, with
     a per-query weight vector w (the multi-head ReLU scalar score);
   * top-K keeps the K largest scores among the visible entries n < n_visible;
     equal scores go to the lower index; the result is listed in ascending
-    index order and padded with -1 when fewer than K entries are visible.
+    index order and padded with -1 when fewer than K entries are visible;
+  * a pool block is an aligned run of 8 compressed positions (8b .. 8b+7); the
+    pool of a query is the union of the blocks that hold an entry of the FULL
+    layer's selection for that query (at most K blocks, 8K positions), and a
+    REINDEX layer given that selection ranks only the pool's visible positions
+    with its own indexer query and keys, under the same top-K rules.
 """
 from __future__ import annotations
 
@@ -46,12 +55,38 @@ def kth_score(score_row: np.ndarray, n_visible: int, K: int) -> float:
     return float(s[K - 1])
 
 
+POOL_BLOCK = 8   # positions per block of the candidate pool
+
+
+def candidate_pool(full_idx: np.ndarray, block: int = POOL_BLOCK) -> np.ndarray:
+    """Positions of the candidate pool built from one query's FULL-layer selection
+    full_idx [K] (-1 padded): every position of every aligned block that holds a selected
+    entry, ascending (int64)."""
+    sel = np.asarray(full_idx, dtype=np.int64)
+    sel = sel[sel >= 0]
+    blocks = np.unique(sel // block)
+    return (blocks[:, None] * block + np.arange(block)[None, :]).reshape(-1)
+
+
+def topk_in_pool(score_row: np.ndarray, n_visible: int, K: int, pool: np.ndarray) -> np.ndarray:
+    """topk restricted to the pool's visible positions (int32 [K], ascending, -1 padded)."""
+    pool = np.asarray(pool, dtype=np.int64)
+    cand = pool[pool < int(n_visible)]
+    s = np.asarray(score_row, dtype=np.float64)[cand]
+    order = np.lexsort((cand, -s))                     # score desc, then position asc
+    take = np.sort(cand[order[: min(K, cand.size)]])
+    out = np.full(K, -1, dtype=np.int32)
+    out[: take.size] = take
+    return out
+
+
 def index_topk(mode: int, q_idx, w_idx, z, n_visible, K: int, prev_idx=None):
     """One sequence's indices for a layer of the given mode (0 FULL, 1 REINDEX, 2 REUSE).
 
     FULL and REINDEX compute the same thing from their own query and keys (the
     difference between them is which main KV the attention reads); REUSE
-    returns the preceding layer's indices.
+    returns the preceding layer's indices. REINDEX given prev_idx (the first FULL
+    layer's selection, [T, K]) searches only each query's candidate pool.
     """
     if mode == 2:
         if prev_idx is None:
@@ -59,4 +94,6 @@ def index_topk(mode: int, q_idx, w_idx, z, n_visible, K: int, prev_idx=None):
         return np.array(prev_idx, dtype=np.int32, copy=True)
     I = scores(q_idx, w_idx, z)
     T = I.shape[0]
+    if mode == 1 and prev_idx is not None:
+        return np.stack([topk_in_pool(I[t], n_visible[t], K, candidate_pool(prev_idx[t])) for t in range(T)])
     return np.stack([topk(I[t], n_visible[t], K) for t in range(T)])

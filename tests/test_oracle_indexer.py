@@ -75,3 +75,87 @@ def test_kth_score():
     s = np.array([5.0, 1.0, 3.0, 4.0])
     assert indexer.kth_score(s, 4, 2) == 4.0
     assert indexer.kth_score(s, 4, 4) == -np.inf
+
+
+# ---- Hierarchical Sparse Indexer (picx.dev summary, Methodology / 3): the first FULL
+# layer's selection builds a candidate pool of aligned 8-position blocks that bounds the
+# search of the REINDEX layers after it.
+
+def test_candidate_pool_of_a_known_selection():
+    """Entries 3, 5 (block 0), 17 (block 2), 100 (block 12) and padding: three blocks."""
+    pool = indexer.candidate_pool(np.array([3, 5, 17, 100, -1, -1]))
+    want = np.concatenate([np.arange(0, 8), np.arange(16, 24), np.arange(96, 104)])
+    assert np.array_equal(pool, want)
+    assert indexer.candidate_pool(np.full(4, -1)).size == 0
+
+
+def test_pool_covering_every_entry_gives_the_full_top_k():
+    """When the FULL selection touches every block, the pool is every position and the
+    REINDEX result equals the unrestricted top-K (same rules, same ties)."""
+    rng = np.random.default_rng(3)
+    N, K = 96, 40
+    s = np.round(rng.standard_normal(N), 1)            # coarse values: many ties
+    full_sel = np.arange(0, N, 8) + rng.integers(0, 8, size=N // 8)
+    full_idx = np.full(K, -1)
+    full_idx[: full_sel.size] = np.sort(full_sel)
+    pool = indexer.candidate_pool(full_idx)
+    assert np.array_equal(pool, np.arange(N))
+    for nv in (N, 61, 7):
+        assert np.array_equal(indexer.topk_in_pool(s, nv, K, pool), indexer.topk(s, nv, K))
+
+
+def test_pool_top_k_matches_brute_force_and_stays_in_the_pool():
+    """Brute force: walk the pool's visible positions, keep the best with a strict
+    comparison (ties to the lower position), K times."""
+    rng = np.random.default_rng(4)
+    N, K = 200, 12
+    for trial in range(20):
+        s = np.round(rng.standard_normal(N), 1)
+        full_idx = np.sort(rng.choice(N, size=9, replace=False))
+        pool = indexer.candidate_pool(full_idx)
+        nv = int(rng.integers(1, N + 1))
+        got = indexer.topk_in_pool(s, nv, K, pool)
+        alive = [int(p) for p in pool if p < nv]
+        chosen = []
+        for _ in range(min(K, len(alive))):
+            best = alive[0]
+            for i in alive[1:]:
+                if s[i] > s[best]:
+                    best = i
+            chosen.append(best)
+            alive.remove(best)
+        want = sorted(chosen) + [-1] * (K - len(chosen))
+        assert got.tolist() == want, trial
+        sel = got[got >= 0]
+        assert np.all(np.isin(sel, pool)) and np.all(sel < nv)
+
+
+def test_pool_size_bound_and_k_covering_the_pool():
+    """At most 8 positions per selected entry; with K at least the pool's visible size the
+    whole visible pool is selected."""
+    rng = np.random.default_rng(5)
+    full_idx = np.sort(rng.choice(10_000, size=2048, replace=False))
+    pool = indexer.candidate_pool(full_idx)
+    assert pool.size <= 8 * 2048 and np.all(np.diff(pool) > 0)
+    s = rng.standard_normal(10_000)
+    nv = 9_000
+    vis = pool[pool < nv]
+    got = indexer.topk_in_pool(s, nv, vis.size + 5, pool)
+    assert np.array_equal(got[: vis.size], vis) and np.all(got[vis.size:] == -1)
+
+
+def test_reindex_with_the_full_selection_searches_its_pool():
+    """index_topk(REINDEX, prev_idx = the FULL selection) = per-query top-K over the pool of
+    that query's FULL selection; without prev_idx REINDEX scans every visible entry."""
+    rng = np.random.default_rng(6)
+    T, H_I, N, K = 3, 2, 256, 16
+    q = rng.standard_normal((T, H_I, 64)); w = np.abs(rng.standard_normal((T, H_I)))
+    z = rng.standard_normal((N, 64)); nv = np.array([256, 200, 31])
+    full = indexer.index_topk(0, q, w, z, nv, K)
+    q2 = rng.standard_normal((T, H_I, 64)); z2 = rng.standard_normal((N, 64))
+    got = indexer.index_topk(1, q2, w, z2, nv, K, prev_idx=full)
+    I = indexer.scores(q2, w, z2)
+    for t in range(T):
+        assert np.array_equal(got[t], indexer.topk_in_pool(I[t], nv[t], K, indexer.candidate_pool(full[t])))
+    assert np.array_equal(indexer.index_topk(1, q2, w, z2, nv, K),
+                          np.stack([indexer.topk(I[t], nv[t], K) for t in range(T)]))
