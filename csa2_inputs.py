@@ -18,8 +18,8 @@ from typing import Dict, List, Optional, Tuple
 
 import numpy as np
 
-FULL, REINDEX, REUSE = 0, 1, 2
-MODE_NAMES = {FULL: "FULL", REINDEX: "REINDEX", REUSE: "REUSE"}
+FULL, REINDEX, REUSE, REINDEX_POOL = 0, 1, 2, 3
+MODE_NAMES = {FULL: "FULL", REINDEX: "REINDEX", REUSE: "REUSE", REINDEX_POOL: "REINDEX_POOL"}
 
 D_LATENT = 512
 D_ROPE = 64

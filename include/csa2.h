@@ -55,7 +55,8 @@ typedef enum {
   CSA2_ERR_DEVICE_CHECK = 6   /* a device-side bounds check fired              */
 } csa2_status;
 
-typedef enum { CSA2_MODE_FULL = 0, CSA2_MODE_REINDEX = 1, CSA2_MODE_REUSE = 2 } csa2_mode;
+typedef enum { CSA2_MODE_FULL = 0, CSA2_MODE_REINDEX = 1, CSA2_MODE_REUSE = 2,
+               CSA2_MODE_REINDEX_POOL = 3 } csa2_mode;
 typedef enum { CSA2_F32 = 0, CSA2_BF16 = 1 } csa2_dtype;
 
 /* Fixed dimensions of the format. */
@@ -117,6 +118,14 @@ CSA2_API int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_mode
  * Limits: 1 <= H_I <= 16, 1 <= K <= 4096, n_stride <= 262144 (1M tokens at 4:1).
  * REUSE: copies prev_idx [B][T][K] to out_idx (nothing to do when they are
  *   the same pointer); q_idx, w_idx, z, n_visible and out_scores are ignored.
+ * REINDEX_POOL: REINDEX restricted to the candidate pool of the Hierarchical Sparse
+ *   Indexer (picx.dev summary, Methodology / 3): prev_idx [B][T][K] is the first FULL
+ *   layer's selection (as written by this call: ascending, -1 padded), and query (b,t)
+ *   ranks only the positions of the aligned 8-entry blocks holding one of its entries
+ *   (at most 8K positions), below n_visible, under the same rules; the cost no longer
+ *   grows with n_stride. A prev_idx that is not ascending or holds an index outside
+ *   [-1, n_stride) sets CSA2_DEV_BAD_INDEX. The block reading is this library's
+ *   (the page gives "2,048 blocks x 8 positions").
  * ws: at least csa2_workspace_bytes(B, T, *, n_stride, K) bytes, prepared
  * once by csa2_workspace_init.
  */

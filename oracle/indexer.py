@@ -81,12 +81,13 @@ def topk_in_pool(score_row: np.ndarray, n_visible: int, K: int, pool: np.ndarray
 
 
 def index_topk(mode: int, q_idx, w_idx, z, n_visible, K: int, prev_idx=None):
-    """One sequence's indices for a layer of the given mode (0 FULL, 1 REINDEX, 2 REUSE).
+    """One sequence's indices for a layer of the given mode (0 FULL, 1 REINDEX, 2 REUSE,
+    3 REINDEX over the candidate pool of prev_idx).
 
     FULL and REINDEX compute the same thing from their own query and keys (the
     difference between them is which main KV the attention reads); REUSE
-    returns the preceding layer's indices. REINDEX given prev_idx (the first FULL
-    layer's selection, [T, K]) searches only each query's candidate pool.
+    returns the preceding layer's indices. The pool mode takes prev_idx as the first FULL
+    layer's selection ([T, K]) and searches only each query's candidate pool.
     """
     if mode == 2:
         if prev_idx is None:
@@ -94,6 +95,8 @@ def index_topk(mode: int, q_idx, w_idx, z, n_visible, K: int, prev_idx=None):
         return np.array(prev_idx, dtype=np.int32, copy=True)
     I = scores(q_idx, w_idx, z)
     T = I.shape[0]
-    if mode == 1 and prev_idx is not None:
+    if mode == 3:
+        if prev_idx is None:
+            raise ValueError("the pool mode needs the FULL layer's selection")
         return np.stack([topk_in_pool(I[t], n_visible[t], K, candidate_pool(prev_idx[t])) for t in range(T)])
     return np.stack([topk(I[t], n_visible[t], K) for t in range(T)])

@@ -27,7 +27,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libcsa2.so")
 
-FULL, REINDEX, REUSE = 0, 1, 2
+FULL, REINDEX, REUSE, REINDEX_POOL = 0, 1, 2, 3
 F32, BF16 = 0, 1
 D_KV, D_LATENT, D_IDX = 576, 512, 64
 CODE_BYTES, SCALE_BYTES = 288, 36
@@ -223,6 +223,10 @@ def csa2_index_topk(mode: int, q_idx: Optional[torch.Tensor], w_idx: Optional[to
     if z.shape != (B_, N, D_IDX):
         raise ValueError("z must be [B, N, 64]")
     _dev(n_visible, "n_visible", (torch.int32,), (B_ * T_,))
+    if mode == REINDEX_POOL:
+        if prev_idx is None:
+            raise ValueError("REINDEX_POOL needs the FULL layer's selection as prev_idx")
+        _dev(prev_idx, "prev_idx", (torch.int32,), (B_, T_, K))
     if out_idx is None:
         out_idx = torch.empty((B_, T_, K), dtype=torch.int32, device=q_idx.device)
     _dev(out_idx, "out_idx", (torch.int32,), (B_, T_, K))
@@ -390,11 +394,11 @@ def csa2_decode_layer(mode: int, q: torch.Tensor, kv_codes: torch.Tensor, kv_sca
     _dev(win_start, "win_start", (torch.int32,), (B * T,))
     _dev(win_len, "win_len", (torch.int32,), (B * T,))
     H_I = 0
-    if mode == REUSE:
+    if mode in (REUSE, REINDEX_POOL):
         if prev_idx is None:
-            raise ValueError("REUSE needs prev_idx")
+            raise ValueError("REUSE and REINDEX_POOL need prev_idx")
         _dev(prev_idx, "prev_idx", (torch.int32,), (B, T, K))
-    else:
+    if mode != REUSE:
         _dev(q_idx, "q_idx", _B16)
         H_I = q_idx.shape[2]
         _dev(q_idx, "q_idx", _B16, (B, T, H_I, D_IDX))

@@ -151,7 +151,7 @@ size_t csa2_workspace_bytes(int B, int T, int H, int64_t n_max, int K) {
   if (B < 0 || T < 0 || H < 0 || n_max < 0 || K < 0) return 0;
   (void)H; (void)K;
   const int64_t Q = (int64_t)B * T;
-  return kWsHeader + range_bytes(Q) + scores_bytes(Q, n_max);
+  return kWsHeader + range_bytes(Q) + scores_bytes(Q, n_max) + pool_bytes(Q, K);
 }
 
 int csa2_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -250,7 +250,8 @@ static int index_topk_impl(int mode, int B, int T, int H_I, const void* q_idx, c
                            const int32_t* prev_idx, int32_t* out_idx, float* out_scores, void* ws,
                            size_t ws_bytes, void* stream, const uint8_t* pf_codes,
                            const uint8_t* pf_scales) {
-  CHECK_ARG(mode == CSA2_MODE_FULL || mode == CSA2_MODE_REINDEX || mode == CSA2_MODE_REUSE);
+  CHECK_ARG(mode == CSA2_MODE_FULL || mode == CSA2_MODE_REINDEX || mode == CSA2_MODE_REUSE ||
+            mode == CSA2_MODE_REINDEX_POOL);
   CHECK_ARG(B >= 0 && T >= 0 && K >= 1);
   if (K > kMaxK) return CSA2_ERR_UNSUPPORTED;
   const int64_t Q = (int64_t)B * T;
@@ -267,14 +268,34 @@ static int index_topk_impl(int mode, int B, int T, int H_I, const void* q_idx, c
   CHECK_ARG(q_idx && w_idx && n_visible && out_idx);
   CHECK_ARG(n_stride == 0 || z != nullptr);
   CHECK_ARG(aligned(q_idx, 16) && aligned(z, 16) && aligned(w_idx, 4) && aligned(out_idx, 4) &&
-            aligned(n_visible, 4) && aligned(out_scores, 4));
+            aligned(n_visible, 4) && aligned(out_scores, 4) && aligned(prev_idx, 4));
+  // REINDEX_POOL searches only the candidate pool of prev_idx (the first FULL layer's selection)
+  const bool pooled = mode == CSA2_MODE_REINDEX_POOL;
+  CHECK_ARG(!pooled || prev_idx != nullptr);
   if (ws == nullptr) return CSA2_ERR_WORKSPACE;
   CHECK_ARG(aligned(ws, 256));
-  if (ws_bytes < kWsHeader + range_bytes(Q) + scores_bytes(Q, n_stride)) return CSA2_ERR_WORKSPACE;
+  const size_t after_scores = kWsHeader + range_bytes(Q) + scores_bytes(Q, n_stride);
+  if (ws_bytes < after_scores + (pooled ? pool_bytes(Q, K) : 0)) return CSA2_ERR_WORKSPACE;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   uint32_t* range = reinterpret_cast<uint32_t*>(wsb + kWsHeader);
   float* scores = reinterpret_cast<float*>(wsb + kWsHeader + range_bytes(Q));
   uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
+  if (pooled) {
+    // at most K blocks x 8 positions, and no more than the (8-aligned) cache rows
+    int32_t* blocks = reinterpret_cast<int32_t*>(wsb + after_scores);
+    int32_t* pool_nv = reinterpret_cast<int32_t*>(wsb + after_scores + ((size_t)Q * K * 4 + 255) / 256 * 256);
+    const int64_t n8 = (n_stride + 7) / 8 * 8;
+    const int64_t pcap = (int64_t)8 * K < n8 ? (int64_t)8 * K : n8;
+    const int64_t pstride = score_pad(pcap);
+    cudaError_t e = launch_pool_build(prev_idx, (int)Q, K, n_visible, n_stride, blocks, pool_nv, status, st);
+    if (e == cudaSuccess)
+      e = launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores, pstride, range,
+                             status, st, blocks, pool_nv, K);
+    if (e != cudaSuccess) return cuda_status(e);
+    return cuda_status(launch_topk_select(scores, pstride, pool_nv, (int)Q, pcap, K, range, out_idx,
+                                          out_scores, status, st, pf_codes, pf_scales, T, n_stride,
+                                          blocks, K));
+  }
   const int64_t stride = score_pad(n_stride);
   cudaError_t e = launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores,
                                      stride, range, status, st);

@@ -36,6 +36,10 @@ int attn_splits(int64_t Q, int K, int n_sm);
 // leaves for the selection; they sit right after the header, at a fixed offset
 // per query, and the selection sets them back to zero.
 inline size_t range_bytes(int64_t Q) { return ((size_t)Q * 8 + 255) / 256 * 256; }
+// candidate pool of a REINDEX call: block ids [Q][K] and the visible count per query
+inline size_t pool_bytes(int64_t Q, int K) {
+  return ((size_t)Q * K * 4 + 255) / 256 * 256 + ((size_t)Q * 4 + 255) / 256 * 256;
+}
 inline size_t scores_bytes(int64_t Q, int64_t n_stride) {
   return (size_t)Q * (size_t)score_pad(n_stride) * 4;
 }
@@ -55,17 +59,25 @@ bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inne
 // Kernel launchers (return cudaError_t of the launch).
 cudaError_t launch_encode_quant(const void* h, int h_dtype, int64_t rows, uint8_t* codes,
                                 uint8_t* scales, cudaStream_t st);
+// pool / pool_nv / pool_stride (nullable): score the positions of a candidate pool
+// (ascending block ids [Q][pool_stride], visible positions per query) instead of 0..n-1
 cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void* z,
                                int64_t n_stride, const int32_t* n_visible, int B, int T, int H_I,
                                float* scores, int64_t score_stride, uint32_t* range,
-                               uint32_t* status, cudaStream_t st);
+                               uint32_t* status, cudaStream_t st, const int32_t* pool = nullptr,
+                               const int32_t* pool_nv = nullptr, int pool_stride = 0);
 // pf_codes / pf_scales (nullable): FP4 cache whose rows of the selected entries are
 // requested into L2 as they are written (batch b = query / T, rows of n_stride)
 cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
                                int Q, int64_t n_stride, int K, uint32_t* range, int32_t* out_idx,
                                float* out_scores, uint32_t* status, cudaStream_t st,
                                const uint8_t* pf_codes = nullptr, const uint8_t* pf_scales = nullptr,
-                               int T = 1);
+                               int T = 1, int64_t kv_stride = -1, const int32_t* pool = nullptr,
+                               int pool_stride = 0);
+// Candidate pool of the Hierarchical Sparse Indexer from a selection sel [Q][K]:
+// ascending block ids blocks [Q][K] and the number of pool positions below n_visible
+cudaError_t launch_pool_build(const int32_t* sel, int Q, int K, const int32_t* n_visible, int64_t n_stride,
+                              int32_t* blocks, int32_t* pool_nv, uint32_t* status, cudaStream_t st);
 cudaError_t launch_copy_idx(const int32_t* src, int32_t* dst, int64_t n, cudaStream_t st);
 cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t* codes,
                                const uint8_t* scales, int64_t n_stride, const int32_t* idx,

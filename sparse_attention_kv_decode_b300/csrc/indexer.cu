@@ -73,16 +73,24 @@ __device__ __forceinline__ int clamp_nvis(const int32_t* n_visible, int qi, int6
   return v < 0 ? 0 : (v > n_stride ? (int)n_stride : v);
 }
 
+// With a candidate pool (pool != nullptr: per query the ascending block ids [pool_stride]
+// of the pool and, in pool_nv, its number of visible positions) a query's positions are
+// the pool's, 8 per block: group j covers pool blocks 2j and 2j+1, i.e. key rows g of the
+// MMA from the first block and rows g+8 from the second, and its scores land at pool
+// positions 16j .. 16j+15.
 template <int NT>
 __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_kernel(
     const uint16_t* __restrict__ q_idx, const float* __restrict__ w_idx,
     const uint16_t* __restrict__ z, int64_t n_stride, const int32_t* __restrict__ n_visible, int T,
-    int H_I, int Q, float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ range) {
+    int H_I, int Q, float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ range,
+    const int32_t* __restrict__ pool, const int32_t* __restrict__ pool_nv, int pool_stride) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
-  const int gpq = (int)((n_stride + kGroupKeys - 1) / kGroupKeys);   // groups per query
+  const bool pooled = pool != nullptr;
+  const int64_t npos = pooled ? 8 * (int64_t)pool_stride : n_stride;   // positions per query
+  const int gpq = (int)((npos + kGroupKeys - 1) / kGroupKeys);           // groups per query
   const int64_t total = (int64_t)Q * gpq;
   const int64_t nwarps = (int64_t)gridDim.x * (kScoreThreads / 32);
   const int64_t wid = (int64_t)blockIdx.x * (kScoreThreads / 32) + (threadIdx.x >> 5);
@@ -95,7 +103,7 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
   for (int64_t g0 = w_begin; g0 < w_end; g0 += kScoreUnroll) {
     // fragments of up to kScoreUnroll groups (all loads issued before any use)
     uint4 v[kScoreUnroll][4];
-    int qg[kScoreUnroll], key0g[kScoreUnroll];
+    int qg[kScoreUnroll], key0g[kScoreUnroll], okg[kScoreUnroll];
 #pragma unroll
     for (int u = 0; u < kScoreUnroll; ++u) {
       const int64_t gi = g0 + u;
@@ -112,13 +120,22 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
         rmax = 0u;
         rmin_inv = 0u;
         load_q_frag<NT>(q_idx, w_idx, qi, H_I, g, tig, qa, wv);
-        nv = clamp_nvis(n_visible, qi, n_stride);
+        nv = pooled ? min(max(pool_nv[qi], 0), 8 * pool_stride) : clamp_nvis(n_visible, qi, n_stride);
         cur_q = qi;
       }
       const int b = qi / T;
-      const int ra = key0 + g, rb = ra + 8;
+      // positions key0 + g and key0 + 8 + g; their key rows (pool: the blocks' entries)
+      bool oka = gi < w_end && key0 + g < nv, okb = gi < w_end && key0 + 8 + g < nv;
+      int64_t ra = key0 + g, rb = ra + 8;
+      if (pooled) {
+        const int32_t* blk = pool + (int64_t)qi * pool_stride + (key0 >> 3);
+        ra = oka ? (int64_t)blk[0] * 8 + g : 0;
+        rb = okb ? (int64_t)blk[1] * 8 + g : 0;
+        oka = oka && ra >= 0 && ra < n_stride;
+        okb = okb && rb >= 0 && rb < n_stride;
+      }
+      okg[u] = (oka ? 1 : 0) | (okb ? 2 : 0);
       const uint16_t* zb = z + (int64_t)b * n_stride * CSA2_D_IDX;
-      const bool oka = gi < w_end && ra < nv, okb = gi < w_end && rb < nv;
       const uint4* pa = reinterpret_cast<const uint4*>(zb + (int64_t)ra * CSA2_D_IDX);
       const uint4* pb = reinterpret_cast<const uint4*>(zb + (int64_t)rb * CSA2_D_IDX);
       v[u][0] = oka ? pa[tig] : make_uint4(0, 0, 0, 0);
@@ -150,7 +167,7 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 1);
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 2);
       float* srow = scores + (int64_t)qi * score_stride + key0;
-      const bool ok0 = tig == 0 && key0 + g < nv, ok1 = tig == 1 && key0 + g + 8 < nv;
+      const bool ok0 = tig == 0 && (okg[u] & 1), ok1 = tig == 1 && (okg[u] & 2);
       if (ok0) srow[g] = pg;
       if (ok1) srow[g + 8] = pg8;
       const uint32_t kk = ok0 ? f2key(pg) : (ok1 ? f2key(pg8) : 0u);
@@ -167,11 +184,13 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
 cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void* z,
                                int64_t n_stride, const int32_t* n_visible, int B, int T, int H_I,
                                float* scores, int64_t score_stride, uint32_t* range,
-                               uint32_t* status, cudaStream_t st) {
+                               uint32_t* status, cudaStream_t st, const int32_t* pool,
+                               const int32_t* pool_nv, int pool_stride) {
   (void)status;
   const int Q = B * T;
   if (n_stride == 0 || Q == 0) return cudaSuccess;
-  const int64_t total = (int64_t)Q * ((n_stride + kGroupKeys - 1) / kGroupKeys);
+  const int64_t npos = pool ? 8 * (int64_t)pool_stride : n_stride;
+  const int64_t total = (int64_t)Q * ((npos + kGroupKeys - 1) / kGroupKeys);
   const int64_t warps = (int64_t)device_sm_count() * kScoreCtasPerSm * (kScoreThreads / 32);
   int64_t grid = (int64_t)device_sm_count() * kScoreCtasPerSm;
   if (total < warps) grid = (total + kScoreThreads / 32 - 1) / (kScoreThreads / 32);
@@ -189,9 +208,9 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
   cfg.numAttrs = 1;
   if (H_I <= 8)
     return cudaLaunchKernelEx(&cfg, index_score_kernel<1>, qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores,
-                              score_stride, range);
+                              score_stride, range, pool, pool_nv, pool_stride);
   return cudaLaunchKernelEx(&cfg, index_score_kernel<2>, qp, w_idx, zp, n_stride, n_visible, T, H_I, Q, scores,
-                            score_stride, range);
+                            score_stride, range, pool, pool_nv, pool_stride);
 }
 
 // ---------------------------------------------------------------------------
@@ -292,6 +311,76 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scan, int& total) {
   __syncthreads();
   return pre;
 }
+
+// ---------------------------------------------------------------------------
+// Candidate pool of the Hierarchical Sparse Indexer ("DeepSeek-V4.1-Flash", picx.dev
+// summary, Methodology / 3): the aligned 8-position blocks that hold an entry of the
+// first FULL layer's selection bound the search of the REINDEX layers after it.
+// ---------------------------------------------------------------------------
+// One CTA per query over its (ascending, -1 padded) selection sel [K]: a new block
+// starts wherever an entry's block differs from the previous entry's; the block ids are
+// compacted in order into blocks [K] and pool_nv gets the number of pool positions below
+// n_visible. A selection that is not ascending or holds an index outside [-1, n_stride)
+// sets CSA2_DEV_BAD_INDEX.
+constexpr int kPoolPerThread = (kMaxK + kSelThreads - 1) / kSelThreads;
+
+__global__ void __launch_bounds__(kSelThreads) pool_build_kernel(
+    const int32_t* __restrict__ sel, int K, const int32_t* __restrict__ n_visible, int64_t n_stride,
+    int32_t* __restrict__ blocks, int32_t* __restrict__ pool_nv, uint32_t* __restrict__ status) {
+  __shared__ int scan[kSelThreads / 32];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int qi = blockIdx.x, tid = threadIdx.x;
+  const int32_t* s = sel + (int64_t)qi * K;
+  const int per = (K + kSelThreads - 1) / kSelThreads;
+  const int i0 = tid * per;
+  const int nvis = clamp_nvis(n_visible, qi, n_stride);
+  int prev = (i0 > 0 && i0 - 1 < K) ? s[i0 - 1] : -1;
+  if (prev < -1 || prev >= n_stride) prev = -1;
+  int mine[kPoolPerThread];
+  int cnt = 0, vis = 0;
+  bool bad = false;
+#pragma unroll
+  for (int k = 0; k < kPoolPerThread; ++k) {
+    if (k >= per) break;
+    const int i = i0 + k;
+    int v = i < K ? s[i] : -1;
+    if (v < -1 || v >= n_stride) { bad = true; v = -1; }
+    if (v >= 0) {
+      if (prev >= 0 && v < prev) bad = true;
+      if (prev < 0 || (v >> 3) != (prev >> 3)) {
+        mine[cnt++] = v >> 3;
+        vis += min(max(nvis - 8 * (v >> 3), 0), 8);
+      }
+      prev = v;
+    }
+  }
+  int total;
+  const int off = block_excl_scan(cnt, scan, total);
+#pragma unroll
+  for (int k = 0; k < kPoolPerThread; ++k)
+    if (k < cnt) blocks[(int64_t)qi * K + off + k] = mine[k];
+  int vis_total;
+  block_excl_scan(vis, scan, vis_total);
+  if (tid == 0) pool_nv[qi] = vis_total;
+  if (bad) atomicOr(status, CSA2_DEV_BAD_INDEX);
+}
+
+cudaError_t launch_pool_build(const int32_t* sel, int Q, int K, const int32_t* n_visible, int64_t n_stride,
+                              int32_t* blocks, int32_t* pool_nv, uint32_t* status, cudaStream_t st) {
+  if (Q == 0) return cudaSuccess;
+  if (K > kMaxK) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)Q);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pool_build_kernel, sel, K, n_visible, n_stride, blocks, pool_nv, status);
+}
+
 
 __device__ __forceinline__ void st_remote_u32(uint32_t* local_addr, int rank, uint32_t v) {
   uint32_t la = smem_u32(local_addr), ra;
@@ -449,7 +538,8 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ n_visible,
     int64_t n_stride, int K, int slice_cap, uint32_t* __restrict__ range, int32_t* __restrict__ out_idx,
     float* __restrict__ out_scores, uint32_t* __restrict__ status, const uint8_t* __restrict__ pf_codes,
-    const uint8_t* __restrict__ pf_scales, int T) {
+    const uint8_t* __restrict__ pf_scales, int T, int64_t kv_stride, const int32_t* __restrict__ pool,
+    int pool_stride) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
   uint32_t C, r;
@@ -728,18 +818,21 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   pos += offset;
   // the FP4 rows of the selected entries are requested into L2 for the attention that
   // gathers them next
-  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * n_stride * CSA2_CODE_BYTES : nullptr;
-  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * n_stride * CSA2_SCALE_BYTES : nullptr;
+  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * kv_stride * CSA2_CODE_BYTES : nullptr;
+  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * kv_stride * CSA2_SCALE_BYTES : nullptr;
+  // with a candidate pool the positions are the pool's: position j is entry
+  // block[j / 8] * 8 + j % 8
+  const int32_t* pblk = pool ? pool + (int64_t)qi * pool_stride : nullptr;
   for (int e0 = wb; e0 < we; e0 += 32) {
     const int e = e0 + lane;
     const bool take = e < we && state[e] == 1;
     const uint32_t bal = __ballot_sync(0xffffffffu, take);
     const int p = pos + __popc(bal & ((1u << lane) - 1u));
     if (take && p < K) {
-      const int ent = my0 + e;
+      const int ent = pblk ? pblk[(my0 + e) >> 3] * 8 + ((my0 + e) & 7) : my0 + e;
       out[p] = ent;
       if (outs) outs[p] = sc[e];
-      if (pfc) {
+      if (pfc && ent >= 0 && ent < kv_stride) {
         prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
         prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES);
         prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES + CSA2_SCALE_BYTES - 1);
@@ -764,7 +857,8 @@ static int select_cluster_size(int64_t n_stride) {
 cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
                                int Q, int64_t n_stride, int K, uint32_t* range, int32_t* out_idx,
                                float* out_scores, uint32_t* status, cudaStream_t st,
-                               const uint8_t* pf_codes, const uint8_t* pf_scales, int T) {
+                               const uint8_t* pf_codes, const uint8_t* pf_scales, int T,
+                               int64_t kv_stride, const int32_t* pool, int pool_stride) {
   static_assert(kNBMax % kSelThreads == 0 && kNBMin % kSelThreads == 0, "bins per thread");
   if (Q == 0) return cudaSuccess;
   const int C = select_cluster_size(n_stride);
@@ -796,7 +890,7 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, score_stride, n_visible, n_stride, K,
                             slice_cap, range, out_idx, out_scores, status, pf_codes, pf_scales,
-                            T < 1 ? 1 : T);
+                            T < 1 ? 1 : T, kv_stride < 0 ? n_stride : kv_stride, pool, pool_stride);
 }
 
 __global__ void copy_idx_kernel(const int32_t* __restrict__ src, int32_t* __restrict__ dst,

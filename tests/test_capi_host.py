@@ -107,8 +107,10 @@ def test_workspace_size_monotone(L):
     b = L.csa2_workspace_bytes(32, 1, 64, 65536, 2048)
     c = L.csa2_workspace_bytes(64, 1, 64, 65536, 2048)
     assert 256 < a <= b <= c
-    assert a == 256 + 256 + 32 * 32768 * 4              # header + range words + fp32 scores
-    assert L.csa2_workspace_bytes(1, 1, 64, 0, 2048) == 512
+    # header + range words + fp32 scores + the candidate pool of a REINDEX call (block ids
+    # [Q][K] and one visible count per query)
+    assert a == 256 + 256 + 32 * 32768 * 4 + 32 * 2048 * 4 + 256
+    assert L.csa2_workspace_bytes(1, 1, 64, 0, 2048) == 512 + 2048 * 4 + 256
     assert L.csa2_workspace_bytes(-1, 1, 64, 10, 10) == 0
 
 

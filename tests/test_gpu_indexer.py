@@ -136,3 +136,110 @@ def test_deterministic_repeat():
     a, _ = _run(L.q_idx, L.w_idx, L.z, inp.n_visible, cfg.K)
     b, _ = _run(L.q_idx, L.w_idx, L.z, inp.n_visible, cfg.K)
     assert np.array_equal(a, b)
+
+
+# ---- REINDEX over the candidate pool (Hierarchical Sparse Indexer, picx.dev summary,
+# Methodology / 3): the pool is built from the GPU's own FULL selection, and the oracle
+# ranks the same pool's visible positions.
+
+def _check_pool(L_full, L_re, nvis, K, exact=False):
+    B, T = L_re.q_idx.shape[:2]
+    dev = "cuda"
+    full, _ = _run(L_full.q_idx, L_full.w_idx, L_full.z, nvis, K, with_scores=False)
+    out_s = torch.empty((B, T, K), dtype=torch.float32, device=dev)
+    got = csa2.csa2_index_topk(csa2.REINDEX_POOL, to_dev_bf16(L_re.q_idx, dev), to_dev(L_re.w_idx, dev),
+                               to_dev_bf16(L_re.z, dev), to_dev(nvis.astype(np.int32), dev), K,
+                               prev_idx=torch.from_numpy(full).to(dev), out_scores=out_s)
+    torch.cuda.synchronize()
+    got, gs = got.cpu().numpy(), out_s.cpu().numpy()
+    ndiff = 0
+    for b in range(B):
+        I = indexer.scores(f64(L_re.q_idx[b]), L_re.w_idx[b], f64(L_re.z[b]))
+        for t in range(T):
+            nv = int(nvis[b * T + t])
+            pool = indexer.candidate_pool(full[b, t])
+            vis = pool[pool < nv]
+            want = indexer.topk_in_pool(I[t], nv, K, pool)
+            g = got[b, t][got[b, t] >= 0]
+            assert np.all(np.diff(g) > 0) and g.size == min(K, vis.size)
+            assert np.all(got[b, t][g.size:] == -1)
+            assert np.all(np.isin(g, vis)), "selected outside the pool"
+            if exact:
+                assert np.array_equal(got[b, t], want)
+            else:
+                s = np.sort(I[t][vis])[::-1]
+                kth = s[K - 1] if K <= s.size else -np.inf
+                diff = np.setxor1d(g, want[want >= 0])
+                if diff.size:
+                    bad = diff[np.abs(I[t][diff] - kth) > 1e-6 * abs(kth)]
+                    assert bad.size == 0, f"{bad.size} pool-set differences outside the tie band"
+                ndiff += diff.size
+            np.testing.assert_allclose(gs[b, t, :g.size], I[t][g], rtol=2e-5, atol=2e-5)
+    return ndiff
+
+
+@pytest.mark.parametrize("N,K", [(4096, 256), (3001, 300), (20000, 1024)])
+def test_reindex_pool_scaled(N, K):
+    cfg = ci.scaled(ci.DECODE_128K, B=3, N=N, H=16, K=K, W=8, modes=(ci.FULL, ci.REINDEX))
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    _check_pool(inp.layers[0], inp.layers[1], inp.n_visible, K)
+
+
+def test_reindex_pool_causal_ragged():
+    """Several query tokens per sequence with ragged visibility (partial last blocks, fewer
+    visible pool positions than K, a single visible entry)."""
+    cfg = ci.scaled(ci.PREFILL_CHUNK, B=2, T=6, N=3000, H=16, K=200, W=8, modes=(ci.FULL, ci.REINDEX))
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    nvis = np.array([1, 7, 9, 200, 1603, 3000, 2999, 8, 16, 17, 640, 2048], dtype=np.int32)
+    _check_pool(inp.layers[0], inp.layers[1], nvis, cfg.K)
+
+
+def test_reindex_pool_exact_ties():
+    """Integer data: exact scores and ties, so the pool selection must equal the oracle's."""
+    rng = np.random.default_rng(31)
+    B, T, N, H_I, K = 2, 2, 9000, 8, 700
+
+    class L:
+        pass
+    Lf, Lr = L(), L()
+    for Lx in (Lf, Lr):
+        Lx.q_idx = ci.bf16_bits(rng.integers(-2, 3, (B, T, H_I, 64)).astype(np.float32))
+        Lx.w_idx = rng.integers(0, 3, (B, T, H_I)).astype(np.float32)
+        Lx.z = ci.bf16_bits(rng.integers(-1, 2, (B, N, 64)).astype(np.float32))
+    _check_pool(Lf, Lr, np.array([N, 7000, 5555, 4321], dtype=np.int32), K, exact=True)
+
+
+def test_reindex_pool_full_size_128k():
+    """32 sequences x 32768 entries, K = 2048: REINDEX ranks at most 16,384 pool positions."""
+    cfg = ci.scaled(ci.DECODE_128K, modes=(ci.FULL, ci.REINDEX))
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    _check_pool(inp.layers[0], inp.layers[1], inp.n_visible, cfg.K)
+
+
+def test_reindex_pool_full_size_1m():
+    """4 sequences x 262144 entries: the pool keeps REINDEX at <= 16,384 positions."""
+    cfg = ci.scaled(ci.DECODE_1M, modes=(ci.FULL, ci.REINDEX))
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    _check_pool(inp.layers[0], inp.layers[1], inp.n_visible, cfg.K)
+
+
+def test_reindex_pool_flags_a_selection_out_of_order():
+    """prev_idx that is not ascending, or holds an index past the cache, sets the device
+    bad-index bit; the call still completes with in-range indices."""
+    rng = np.random.default_rng(32)
+    B, T, N, H_I, K = 1, 2, 2048, 8, 64
+    q = ci.bf16_bits(rng.standard_normal((B, T, H_I, 64), dtype=np.float32))
+    w = np.abs(rng.standard_normal((B, T, H_I), dtype=np.float32))
+    z = ci.bf16_bits(rng.standard_normal((B, N, 64), dtype=np.float32))
+    prev = np.sort(rng.choice(N, size=(B, T, K)), axis=-1).astype(np.int32)
+    prev[0, 0, 5], prev[0, 0, 6] = prev[0, 0, 6] + 1, prev[0, 0, 5]   # out of order
+    prev[0, 1, -1] = N + 100                                           # past the cache
+    dev = "cuda"
+    ws = csa2.csa2_workspace(B, T, 0, N, K, device=dev)
+    got = csa2.csa2_index_topk(csa2.REINDEX_POOL, to_dev_bf16(q, dev), to_dev(w, dev), to_dev_bf16(z, dev),
+                               to_dev(np.full(B * T, N, np.int32), dev), K, prev_idx=torch.from_numpy(prev).to(dev),
+                               ws=ws)
+    st, flags = csa2.csa2_read_device_status(ws)
+    assert flags & csa2.DEV_BAD_INDEX
+    g = got.cpu().numpy()
+    assert np.all((g == -1) | ((g >= 0) & (g < N)))

@@ -144,18 +144,19 @@ def test_pool_size_bound_and_k_covering_the_pool():
     assert np.array_equal(got[: vis.size], vis) and np.all(got[vis.size:] == -1)
 
 
-def test_reindex_with_the_full_selection_searches_its_pool():
-    """index_topk(REINDEX, prev_idx = the FULL selection) = per-query top-K over the pool of
-    that query's FULL selection; without prev_idx REINDEX scans every visible entry."""
+def test_reindex_pool_mode_searches_the_full_selection_pool():
+    """index_topk(REINDEX_POOL, prev_idx = the FULL selection) = per-query top-K over the pool
+    of that query's FULL selection; plain REINDEX scans every visible entry, prev_idx or not."""
     rng = np.random.default_rng(6)
     T, H_I, N, K = 3, 2, 256, 16
     q = rng.standard_normal((T, H_I, 64)); w = np.abs(rng.standard_normal((T, H_I)))
     z = rng.standard_normal((N, 64)); nv = np.array([256, 200, 31])
     full = indexer.index_topk(0, q, w, z, nv, K)
     q2 = rng.standard_normal((T, H_I, 64)); z2 = rng.standard_normal((N, 64))
-    got = indexer.index_topk(1, q2, w, z2, nv, K, prev_idx=full)
+    got = indexer.index_topk(3, q2, w, z2, nv, K, prev_idx=full)
     I = indexer.scores(q2, w, z2)
     for t in range(T):
         assert np.array_equal(got[t], indexer.topk_in_pool(I[t], nv[t], K, indexer.candidate_pool(full[t])))
-    assert np.array_equal(indexer.index_topk(1, q2, w, z2, nv, K),
-                          np.stack([indexer.topk(I[t], nv[t], K) for t in range(T)]))
+    full_scan = np.stack([indexer.topk(I[t], nv[t], K) for t in range(T)])
+    assert np.array_equal(indexer.index_topk(1, q2, w, z2, nv, K), full_scan)
+    assert np.array_equal(indexer.index_topk(1, q2, w, z2, nv, K, prev_idx=full), full_scan)
