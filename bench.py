@@ -459,6 +459,13 @@ def run_ours(args):
                                         "sparse": "attn_tc_kernel<0>", "swa": "attn_tc_kernel<1>"}[dom]),
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"}
 
+    pool = None
+    if not args.no_pool:
+        try:
+            pool = run_pool_indexer(args, torch, L, cfg, dl, codes, scales, nvis, idx_bufs, ws, dev, peaks, stream,
+                                    flush)
+        except Exception as ex:  # reported, not hidden
+            pool = {"error": repr(ex)}
     ced = None
     if not args.no_ced:
         try:
@@ -491,11 +498,88 @@ def run_ours(args):
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": n_launch,
             "wall_s_timed_loop": round(wall, 3),
             "ced_projection": ced,
+            "hierarchical_indexer": pool,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def run_pool_indexer(args, torch, L, cfg, dl, codes, scales, nvis, idx_bufs, ws, dev, peaks, stream, flush):
+    """The REINDEX layer's selection two ways on the same inputs: the full scan
+    (CSA2_MODE_REINDEX) and the hierarchical indexer (CSA2_MODE_REINDEX_POOL), which scores
+    only the aligned 8-position blocks of the FULL layer's selection. Device time per call
+    (CUDA graph of the one call, events on its stream, L2 flushed between replays) and the
+    pool's key bytes as an HBM roofline."""
+    li_full = next((i for i, d in enumerate(dl) if d["mode"] == ci.FULL), None)
+    li_re = next((i for i, d in enumerate(dl) if d["mode"] == ci.REINDEX), None)
+    if li_full is None or li_re is None:
+        return None
+    d = dl[li_re]
+    full_sel = idx_bufs[li_full % 2].clone()
+    outs = [torch.empty_like(full_sel) for _ in range(2)]
+    sp = stream.cuda_stream
+    P = lambda t: t.data_ptr()
+    pf = args.attn == "layer"
+
+    def call(mode, prev, out):
+        if pf:
+            return L.csa2_index_topk_prefetch(mode, cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N,
+                                              P(nvis), cfg.K, prev, P(out), None, P(codes), P(scales),
+                                              P(ws), ws.numel(), sp)
+        return L.csa2_index_topk(mode, cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N, P(nvis),
+                                 cfg.K, prev, P(out), None, P(ws), ws.numel(), sp)
+
+    variants = [("REINDEX", lambda: call(ci.REINDEX, None, outs[0])),
+                ("REINDEX_POOL", lambda: call(ci.REINDEX_POOL, P(full_sel), outs[1]))]
+    times = {}
+    for name, fn in variants:
+        with torch.cuda.stream(stream):
+            if fn() != 0:
+                raise RuntimeError(f"index_topk[{name}] failed")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        ts = []
+        n = min(args.steps, 200)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n + 3)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+        stream.synchronize()
+        ts = [e0.elapsed_time(e1) for e0, e1 in evs[3:]]
+        times[name] = statistics.mean(ts) * 1e-3
+    from sparse_attention_kv_decode_b300 import csa2_read_device_status
+    st, flags = csa2_read_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags}")
+
+    # pool size per query from the FULL selection: distinct 8-position blocks, visible positions in them
+    sel = full_sel.reshape(-1, cfg.K).cpu().numpy()
+    nv = nvis.reshape(-1).cpu().numpy().astype(np.int64)
+    pooled = 0
+    for r in range(sel.shape[0]):
+        blk = np.unique(sel[r][sel[r] >= 0] >> 3).astype(np.int64)
+        pooled += int(np.clip(nv[r] - 8 * blk, 0, 8).sum())
+    Q = cfg.B * cfg.T
+    full_bytes = Q * cfg.N * KEY_BYTES
+    pool_bytes = pooled * KEY_BYTES
+    t_full, t_pool = times["REINDEX"], times["REINDEX_POOL"]
+    a_full = full_bytes / t_full / 1e9
+    a_pool = pool_bytes / t_pool / 1e9
+    return {"call": "csa2_index_topk_prefetch" if pf else "csa2_index_topk",
+            "reindex_us": round(t_full * 1e6, 2), "reindex_pool_us": round(t_pool * 1e6, 2),
+            "speedup": round(t_full / t_pool, 3),
+            "pool_positions_mean": round(pooled / Q, 1), "positions_full_scan": cfg.N,
+            "reindex_key_gbs": round(a_full, 1), "reindex_pool_key_gbs": round(a_pool, 1),
+            "reindex_pool_frac": round(a_pool / peaks["hbm"], 4), "peak_gbs": peaks["hbm"],
+            "launches": {"REINDEX": 2, "REINDEX_POOL": 3},
+            "note": "pool = aligned 8-position blocks holding an entry of the FULL layer's selection; "
+                    "bytes = pooled visible positions x 128-byte keys"}
 
 
 def run_ced(args, torch, csa2, dev, peaks):
@@ -645,6 +729,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ced", action="store_true")
+    ap.add_argument("--no-pool", action="store_true", help="skip the REINDEX vs REINDEX_POOL indexer timing")
     ap.add_argument("--attn", choices=["layer", "fused", "two-call"], default="layer",
                     help="per layer: one csa2_decode_layer call (selection that prefetches the selected rows "
                          "into L2, then the attention); csa2_index_topk + csa2_decode_attention; or "
