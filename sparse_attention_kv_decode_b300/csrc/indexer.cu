@@ -100,8 +100,11 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
   float wv[NT][2];
   int cur_q = -1, nv = 0;
   uint32_t rmax = 0u, rmin_inv = 0u;  // score range of the current query seen by this warp
-  for (int64_t g0 = w_begin; g0 < w_end; g0 += kScoreUnroll) {
-    // fragments of up to kScoreUnroll groups (all loads issued before any use)
+  for (int64_t g0 = w_begin; g0 < w_end;) {
+    // fragments of up to kScoreUnroll groups (all loads issued before any use); a batch
+    // ends at a query boundary, since the indexer rows in registers are one query's
+    const int64_t q_end = (g0 / gpq + 1) * gpq;
+    const int nb = (int)min((int64_t)kScoreUnroll, min(w_end, q_end) - g0);
     uint4 v[kScoreUnroll][4];
     int qg[kScoreUnroll], key0g[kScoreUnroll], okg[kScoreUnroll];
 #pragma unroll
@@ -109,9 +112,9 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
       const int64_t gi = g0 + u;
       const int qi = (int)(gi / gpq);
       const int key0 = (int)(gi - (int64_t)qi * gpq) * kGroupKeys;
-      qg[u] = gi < w_end ? qi : -1;
+      qg[u] = u < nb ? qi : -1;
       key0g[u] = key0;
-      if (gi < w_end && qi != cur_q) {
+      if (u == 0 && qi != cur_q) {
         // a new query: flush the range of the previous one, load its indexer rows
         if (cur_q >= 0 && lane == 0 && rmax != 0u) {
           atomicMax(range + 2 * cur_q, rmin_inv);
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
       }
       const int b = qi / T;
       // positions key0 + g and key0 + 8 + g; their key rows (pool: the blocks' entries)
-      bool oka = gi < w_end && key0 + g < nv, okb = gi < w_end && key0 + 8 + g < nv;
+      bool oka = u < nb && key0 + g < nv, okb = u < nb && key0 + 8 + g < nv;
       int64_t ra = key0 + g, rb = ra + 8;
       if (pooled) {
         const int32_t* blk = pool + (int64_t)qi * pool_stride + (key0 >> 3);
@@ -147,7 +150,7 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
     for (int u = 0; u < kScoreUnroll; ++u) {
       if (qg[u] < 0) continue;
       const int qi = qg[u], key0 = key0g[u];
-      if (key0 >= nv && qi == cur_q) continue;   // past the visible keys
+      if (key0 >= nv) continue;   // past the visible keys (qi is the current query)
       const uint32_t ra_[16] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y,
                                 v[u][1].z, v[u][1].w, v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w,
                                 v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
       rmax = max(rmax, __reduce_max_sync(0xffffffffu, kk));
       rmin_inv = max(rmin_inv, __reduce_max_sync(0xffffffffu, (ok0 || ok1) ? ~kk : 0u));
     }
+    g0 += nb;
   }
   if (cur_q >= 0 && lane == 0 && rmax != 0u) {
     atomicMax(range + 2 * cur_q, rmin_inv);
@@ -847,10 +851,14 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     }
 }
 
-static int select_cluster_size(int64_t n_stride) {
+// CTAs per query: enough for at most 8192 scores each; while the grid stays within one
+// CTA per SM, more (slices of at least 2048), since the selection's phases scale with
+// the slice, not with the cluster.
+static int select_cluster_size(int64_t n_stride, int Q) {
   int64_t per = (n_stride + 8191) / 8192;
   int c = 1;
   while (c < per && c < kMaxCluster) c <<= 1;
+  while (c < kMaxCluster && (int64_t)Q * 2 * c <= device_sm_count() && n_stride >= (int64_t)4096 * c) c <<= 1;
   return c;
 }
 
@@ -861,7 +869,7 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
                                int64_t kv_stride, const int32_t* pool, int pool_stride) {
   static_assert(kNBMax % kSelThreads == 0 && kNBMin % kSelThreads == 0, "bins per thread");
   if (Q == 0) return cudaSuccess;
-  const int C = select_cluster_size(n_stride);
+  const int C = select_cluster_size(n_stride, Q);
   const int NB = C <= 4 ? kNBMax : kNBMin;
   int slice_cap = (int)((n_stride + C - 1) / C);
   slice_cap = (slice_cap + 15) & ~15;

@@ -129,6 +129,18 @@ def test_reuse_copies_and_aliases():
     assert torch.equal(same, prev)
 
 
+@pytest.mark.parametrize("B,N", [(6, 20000), (3, 40000), (33, 4099)])
+def test_warp_runs_across_query_boundaries(B, N):
+    """All entries visible, at sizes where a scoring warp's run of key groups ends inside
+    one query and continues in the next (the groups are split evenly over 148 x 32 warps,
+    not per query): every query's last groups must be scored with that query's indexer
+    rows."""
+    cfg = ci.scaled(ci.DECODE_128K, B=B, N=N, H=16, K=256, W=8, modes=(ci.FULL,))
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    L = inp.layers[0]
+    _check_all(L.q_idx, L.w_idx, L.z, np.full(B, N, np.int32), cfg.K)
+
+
 def test_deterministic_repeat():
     cfg = ci.scaled(ci.DECODE_128K, B=4, N=8192, K=1024, modes=(ci.FULL,))
     inp = ci.make_decode_inputs(cfg, with_x=False)
@@ -192,6 +204,14 @@ def test_reindex_pool_causal_ragged():
     inp = ci.make_decode_inputs(cfg, with_x=False)
     nvis = np.array([1, 7, 9, 200, 1603, 3000, 2999, 8, 16, 17, 640, 2048], dtype=np.int32)
     _check_pool(inp.layers[0], inp.layers[1], nvis, cfg.K)
+
+
+def test_reindex_pool_many_query_tokens():
+    """2100 query tokens of one sequence over a short cache (640 entries, pools of one to
+    eight blocks per token, causal): warp runs of the pooled scoring cross many queries."""
+    cfg = ci.scaled(ci.PREFILL_CHUNK, B=1, T=2100, N=640, H=16, K=64, W=8, modes=(ci.FULL, ci.REINDEX))
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    _check_pool(inp.layers[0], inp.layers[1], inp.n_visible, cfg.K)
 
 
 def test_reindex_pool_exact_ties():
