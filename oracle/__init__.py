@@ -17,9 +17,10 @@ Modules:
   attention  sparse MQA over selected entries, sliding window, LSE merge
   ced        CED projection C_l = H W_l^KV, Z_l = H W_l^Z with the FP4 cache write
   decode     one CSA2 layer group (FULL / REINDEX / REUSE) end to end
+  append     decode-time cache append (window ring, one FP4 entry every 4 tokens)
 
 Parity status: every function is pinned by tests under tests/test_oracle_*.py
 to values the pages or the mathematics fix; the only unpinned item is
 whole-model behaviour (it needs trained weights), which is out of scope.
 """
-from . import fp4, indexer, attention, ced, decode  # noqa: F401
+from . import fp4, indexer, attention, ced, decode, append  # noqa: F401
