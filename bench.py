@@ -466,6 +466,12 @@ def run_ours(args):
                                     flush)
         except Exception as ex:  # reported, not hidden
             pool = {"error": repr(ex)}
+    app = None
+    if not args.no_pool:
+        try:
+            app = run_cache_append(args, torch, csa2, cfg, dev, stream, flush)
+        except Exception as ex:  # reported, not hidden
+            app = {"error": repr(ex)}
     ced = None
     if not args.no_ced:
         try:
@@ -499,6 +505,7 @@ def run_ours(args):
             "wall_s_timed_loop": round(wall, 3),
             "ced_projection": ced,
             "hierarchical_indexer": pool,
+            "cache_append": app,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -580,6 +587,57 @@ def run_pool_indexer(args, torch, L, cfg, dl, codes, scales, nvis, idx_bufs, ws,
             "launches": {"REINDEX": 2, "REINDEX_POOL": 3},
             "note": "pool = aligned 8-position blocks holding an entry of the FULL layer's selection; "
                     "bytes = pooled visible positions x 128-byte keys"}
+
+
+def run_cache_append(args, torch, csa2, cfg, dev, stream, flush):
+    """csa2_cache_append for the bench's sequences: the FULL layer's append of one token
+    (window ring row, the FP4 entry the token completes, its indexer key, n_visible and
+    the window bounds), CUDA graph of the one call, L2 flushed between replays. Every
+    sequence sits at a token that completes an entry (the costlier of the two kinds of
+    step); n_tokens is not advanced so that each replay does the same work."""
+    B, N, W = cfg.B, cfg.N, cfg.W
+    g = torch.Generator(device=dev).manual_seed(7)
+    swa = torch.zeros((B, 2 * W, 576), dtype=torch.bfloat16, device=dev)
+    codes = torch.zeros((B, N, 288), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((B, N, 36), dtype=torch.uint8, device=dev)
+    z = torch.zeros((B, N, 64), dtype=torch.bfloat16, device=dev)
+    row = torch.randn((B, 576), generator=g, device=dev).to(torch.bfloat16)
+    ent = torch.randn((B, 576), generator=g, device=dev)
+    zk = torch.randn((B, 64), generator=g, device=dev).to(torch.bfloat16)
+    n_tok = torch.full((B,), 4 * (N // 2) - 1, dtype=torch.int32, device=dev)
+    nvis, wst, wln = (torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(3))
+    ws = csa2.csa2_workspace(B, 1, 1, 0, 1, device=dev)
+
+    def call():
+        csa2.csa2_cache_append(n_tok, swa_row=row, swa_kv=swa, n_win=W, entry_kv=ent, entry_z=zk, kv_codes=codes,
+                               kv_scales=scales, z=z, n_visible=nvis, win_start=wst, win_len=wln, advance=False,
+                               ws=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        call()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call()
+    n = min(args.steps, 200)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n + 3)]
+    with torch.cuda.stream(stream):
+        for e0, e1 in evs:
+            flush.fill_(1)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+    stream.synchronize()
+    us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs[3:]) * 1e3
+    st, flags = csa2.csa2_read_device_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags}")
+    # per sequence: window row in + 2 rows out, fp32 entry in + 288 + 36 B out, key in + out,
+    # n_tokens in, n_visible / win_start / win_len out
+    bytes_call = B * (1152 * 3 + 2304 + 324 + 128 * 2 + 4 + 12)
+    return {"call": "csa2_cache_append", "sequences": B, "us": round(us, 2), "bytes": bytes_call,
+            "gbs": round(bytes_call / (us * 1e-6) / 1e9, 2), "launches": 1,
+            "note": "one token per sequence completing an FP4 entry; a few KB per sequence, launch-bound"}
 
 
 def run_ced(args, torch, csa2, dev, peaks):
@@ -729,7 +787,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ced", action="store_true")
-    ap.add_argument("--no-pool", action="store_true", help="skip the REINDEX vs REINDEX_POOL indexer timing")
+    ap.add_argument("--no-pool", action="store_true",
+                    help="skip the side measurements (REINDEX vs REINDEX_POOL, csa2_cache_append)")
     ap.add_argument("--attn", choices=["layer", "fused", "two-call"], default="layer",
                     help="per layer: one csa2_decode_layer call (selection that prefetches the selected rows "
                          "into L2, then the attention); csa2_index_topk + csa2_decode_attention; or "

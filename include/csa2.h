@@ -260,6 +260,45 @@ CSA2_API int csa2_decode_layer(int mode, int B, int T, int H, int H_I, const voi
                    const int32_t* win_len, int n_win, int d_v, float softmax_scale, float* o,
                    float* lse, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * csa2_cache_append - decode-time cache append: one new token per sequence b
+ * (the sliding window covers the most recent n_win tokens, blog repost; one
+ * compressed entry per four tokens, wesearch.press card; FP4 entries, picx.dev
+ * summary, Methodology / 5).
+ *
+ * The new token of sequence b has position p = n_tokens[b] (0-based; p < 0: the
+ * sequence is idle and nothing is written for it). For each active b:
+ *  - window: swa_row [B][576] bf16 is copied to rows p % n_win and
+ *    p % n_win + n_win of swa_kv [B][s_stride][576] (a ring of n_win slots kept
+ *    twice, s_stride >= 2 * n_win), so that after the call the last
+ *    len = min(p + 1, n_win) tokens, oldest first, are the rows
+ *    [win_start[b], win_start[b] + len) with win_start[b] = (p + 1 - len) % n_win
+ *    and win_len[b] = len, the window arguments of csa2_swa_merge /
+ *    csa2_decode_attention / csa2_decode_layer (T = 1);
+ *  - entry: when (p + 1) % ratio == 0 the token completes entry
+ *    e = (p + 1) / ratio - 1: entry_kv [B][576] (entry_dtype fp32 or bf16; how
+ *    tokens become an entry is the caller's) is quantised as csa2_encode_kv (a)
+ *    into kv_codes [B][n_stride][288] / kv_scales [B][n_stride][36] row e, and
+ *    entry_z [B][64] bf16 is copied to z [B][n_stride][64] row e; an entry past
+ *    the cache (e >= n_stride) is skipped and sets CSA2_DEV_BAD_INDEX;
+ *  - n_visible[b] = (p + 1) / ratio (the entries visible to this token);
+ *  - advance != 0: n_tokens[b] = p + 1 afterwards (call it with advance on the
+ *    last of a step's per-layer appends).
+ * Every output part is optional: swa_row == NULL skips the window rows,
+ * entry_kv / entry_z == NULL skip those writes, n_visible / (win_start, win_len)
+ * == NULL skip those outputs (win_start and win_len come together). ratio >= 1.
+ * Alignment: 16 bytes for swa_row, swa_kv, entry_kv, entry_z, z; 8 for kv_codes.
+ * ws: the 256-byte status header (csa2_workspace_init). The call waits for the
+ * preceding kernel on the stream before writing (a ring row it replaces may
+ * still be read by the previous step's attention).
+ */
+CSA2_API int csa2_cache_append(int B, int32_t* n_tokens, int advance, int ratio,
+                   const void* swa_row, void* swa_kv, int64_t s_stride, int n_win,
+                   const void* entry_kv, int entry_dtype, const void* entry_z,
+                   uint8_t* kv_codes, uint8_t* kv_scales, void* z, int64_t n_stride,
+                   int32_t* n_visible, int32_t* win_start, int32_t* win_len,
+                   void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes that cover every call above with these or smaller sizes: a
  * 256-byte header (the device status word), then for csa2_index_topk two uint32
  * score-range words per query (B*T*8 bytes rounded up to 256) and the fp32

@@ -67,6 +67,8 @@ def _lib():
     L.csa2_decode_layer.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, i64, vp, i32, vp, vp,
                                     vp, i64, vp, vp, i32, i32, f32, vp, vp, vp, sz, vp]
     L.csa2_swa_merge.argtypes = [i32, i32, i32, vp, vp, i64, vp, vp, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp]
+    L.csa2_cache_append.argtypes = [i32, vp, i32, i32, vp, vp, i64, i32, vp, i32, vp, vp, vp, vp, i64, vp, vp,
+                                    vp, vp, sz, vp]
     L.csa2_workspace_bytes.argtypes = [i32, i32, i32, i64, i32]
     L.csa2_workspace_bytes.restype = sz
     L.csa2_workspace_init.argtypes = [vp, sz, vp]
@@ -77,7 +79,7 @@ def _lib():
     L.csa2_last_cuda_error.argtypes = []
     L.csa2_last_cuda_error.restype = ctypes.c_char_p
     for fn in ("csa2_encode_kv", "csa2_index_topk", "csa2_index_topk_prefetch", "csa2_sparse_decode",
-               "csa2_swa_merge", "csa2_decode_layer",
+               "csa2_swa_merge", "csa2_decode_layer", "csa2_cache_append",
                "csa2_workspace_init", "csa2_read_device_status", "csa2_version"):
         getattr(L, fn).restype = ctypes.c_int
     _LIB = L
@@ -421,6 +423,61 @@ def csa2_decode_layer(mode: int, q: torch.Tensor, kv_codes: torch.Tensor, kv_sca
                                S, _ptr(win_start), _ptr(win_len), n_win, d_v, float(softmax_scale), _ptr(o),
                                _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "csa2_decode_layer")
     return o, lse, out_idx
+
+
+def csa2_cache_append(n_tokens: torch.Tensor, swa_row: Optional[torch.Tensor] = None,
+                      swa_kv: Optional[torch.Tensor] = None, n_win: Optional[int] = None,
+                      entry_kv: Optional[torch.Tensor] = None, entry_z: Optional[torch.Tensor] = None,
+                      kv_codes: Optional[torch.Tensor] = None, kv_scales: Optional[torch.Tensor] = None,
+                      z: Optional[torch.Tensor] = None, n_visible: Optional[torch.Tensor] = None,
+                      win_start: Optional[torch.Tensor] = None, win_len: Optional[torch.Tensor] = None,
+                      ratio: int = 4, advance: bool = True, ws: Optional[torch.Tensor] = None, stream=None):
+    """Append one token per sequence, in place: n_tokens [B] int32 (the new token's
+    position; < 0 = idle), swa_row [B, 576] bf16 into the mirrored window ring swa_kv
+    [B, S >= 2 n_win, 576] (n_win defaults to S // 2), and every ratio-th token the
+    compressed entry entry_kv [B, 576] (fp32/bf16, FP4-encoded into kv_codes [B, N, 288]
+    / kv_scales [B, N, 36]) and its key entry_z [B, 64] (into z [B, N, 64]); writes
+    n_visible, win_start, win_len [B] int32 when given; advance increments n_tokens."""
+    L = _lib()
+    _dev(n_tokens, "n_tokens", (torch.int32,))
+    B = n_tokens.numel()
+    _dev(n_tokens, "n_tokens", (torch.int32,), (B,))
+    S = 0
+    if swa_kv is not None:
+        _dev(swa_kv, "swa_kv", _B16)
+        S = swa_kv.shape[1]
+        _dev(swa_kv, "swa_kv", _B16, (B, S, D_KV))
+        if n_win is None:
+            n_win = S // 2
+    if swa_row is not None:
+        _dev(swa_row, "swa_row", _B16, (B, D_KV))
+    N = 0
+    if kv_codes is not None:
+        _dev(kv_codes, "kv_codes", (torch.uint8,))
+        N = kv_codes.shape[1]
+        _dev(kv_codes, "kv_codes", (torch.uint8,), (B, N, CODE_BYTES))
+    if kv_scales is not None:
+        _dev(kv_scales, "kv_scales", (torch.uint8,), (B, N, SCALE_BYTES))
+    if z is not None:
+        _dev(z, "z", _B16)
+        if kv_codes is None:
+            N = z.shape[1]
+        _dev(z, "z", _B16, (B, N, D_IDX))
+    dt = F32
+    if entry_kv is not None:
+        _dev(entry_kv, "entry_kv", (torch.float32,) + _B16, (B, D_KV))
+        dt = F32 if entry_kv.dtype == torch.float32 else BF16
+    if entry_z is not None:
+        _dev(entry_z, "entry_z", _B16, (B, D_IDX))
+    for t, name in ((n_visible, "n_visible"), (win_start, "win_start"), (win_len, "win_len")):
+        if t is not None:
+            _dev(t, name, (torch.int32,), (B,))
+    if ws is None:
+        ws = csa2_workspace(B, 1, 1, 0, 1, device=n_tokens.device, stream=stream)
+    _check(L.csa2_cache_append(B, _ptr(n_tokens), 1 if advance else 0, int(ratio), _ptr(swa_row), _ptr(swa_kv), S,
+                               int(n_win or 0), _ptr(entry_kv), dt, _ptr(entry_z), _ptr(kv_codes), _ptr(kv_scales),
+                               _ptr(z), N, _ptr(n_visible), _ptr(win_start), _ptr(win_len), _ptr(ws), ws.numel(),
+                               _stream(stream)), "csa2_cache_append")
 
 
 def decode_layer(mode: int, q: torch.Tensor, kv_codes: torch.Tensor, kv_scales: torch.Tensor,

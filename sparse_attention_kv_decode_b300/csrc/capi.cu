@@ -202,6 +202,34 @@ int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_model, const 
                                         z_out, static_cast<uint32_t*>(ws), st));
 }
 
+int csa2_cache_append(int B, int32_t* n_tokens, int advance, int ratio, const void* swa_row, void* swa_kv,
+                      int64_t s_stride, int n_win, const void* entry_kv, int entry_dtype, const void* entry_z,
+                      uint8_t* kv_codes, uint8_t* kv_scales, void* z, int64_t n_stride, int32_t* n_visible,
+                      int32_t* win_start, int32_t* win_len, void* ws, size_t ws_bytes, void* stream) {
+  CHECK_ARG(B >= 0 && ratio >= 1 && n_stride >= 0 && s_stride >= 0 && n_win >= 0);
+  CHECK_ARG((win_start == nullptr) == (win_len == nullptr));
+  if (swa_row != nullptr || win_start != nullptr) CHECK_ARG(n_win >= 1);
+  if (swa_row != nullptr) {
+    CHECK_ARG(swa_kv != nullptr && s_stride >= 2 * (int64_t)n_win);
+    CHECK_ARG(aligned(swa_row, 16) && aligned(swa_kv, 16));
+  }
+  if (entry_kv != nullptr) {
+    CHECK_ARG(entry_dtype == CSA2_F32 || entry_dtype == CSA2_BF16);
+    CHECK_ARG(kv_codes != nullptr && kv_scales != nullptr);
+    CHECK_ARG(aligned(entry_kv, 16) && aligned(kv_codes, 8));
+  }
+  if (entry_z != nullptr) CHECK_ARG(z != nullptr && aligned(entry_z, 16) && aligned(z, 16));
+  if (B == 0) return CSA2_OK;
+  CHECK_ARG(n_tokens != nullptr);
+  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
+  CHECK_ARG(aligned(ws, 256));
+  if (ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
+  return cuda_status(launch_cache_append(B, n_tokens, advance, ratio, swa_row, swa_kv, s_stride, n_win, entry_kv,
+                                         entry_dtype, entry_z, kv_codes, kv_scales, z, n_stride, n_visible,
+                                         win_start, win_len, static_cast<uint32_t*>(ws),
+                                         (cudaStream_t)stream));
+}
+
 }  // extern "C"
 
 // Argument checks of csa2_decode_attention (CSA2_OK also for an empty batch).

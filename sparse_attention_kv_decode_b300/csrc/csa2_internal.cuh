@@ -57,6 +57,11 @@ bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inne
                                uint32_t box_inner, uint32_t box_outer);
 
 // Kernel launchers (return cudaError_t of the launch).
+cudaError_t launch_cache_append(int B, int32_t* n_tokens, int advance, int ratio, const void* swa_row,
+                                void* swa_kv, int64_t s_stride, int n_win, const void* entry_kv,
+                                int entry_dtype, const void* entry_z, uint8_t* codes, uint8_t* scales,
+                                void* z, int64_t n_stride, int32_t* n_visible, int32_t* win_start,
+                                int32_t* win_len, uint32_t* status, cudaStream_t st);
 cudaError_t launch_encode_quant(const void* h, int h_dtype, int64_t rows, uint8_t* codes,
                                 uint8_t* scales, cudaStream_t st);
 // pool / pool_nv / pool_stride (nullable): score the positions of a candidate pool

@@ -168,3 +168,34 @@ def test_decode_layer_validation(L):
     assert call(a25=None, a26=0) == 3             # no workspace
     assert call(a26=4096) == 3                    # workspace without room for the scores
     assert call(a1=0) == 0                        # empty batch: nothing to do
+
+
+def test_cache_append_validation(L):
+    """csa2_cache_append rejects bad arguments before launching (no GPU)."""
+    r = L.csa2_cache_append
+    # B, n_tokens, advance, ratio, swa_row, swa_kv, S, n_win, entry_kv, entry_dtype, entry_z,
+    # codes, scales, z, N, n_visible, win_start, win_len, ws, ws_bytes, stream
+    args = [4, FAKE, 1, 4, FAKE, FAKE, 256, 128, FAKE, 0, FAKE, FAKE, FAKE, FAKE, 1024, FAKE, FAKE, FAKE,
+            FAKE, 1 << 20, None]
+
+    def call(**kw):
+        a = list(args)
+        for k, v in kw.items():
+            a[int(k[1:])] = v
+        return r(*a)
+
+    assert call(a3=0) == 1                        # ratio below 1
+    assert call(a6=255) == 1                      # ring store shorter than 2 * n_win
+    assert call(a7=0) == 1                        # a window row without a window
+    assert call(a4=None, a7=0) == 1               # window bounds requested without a window
+    assert call(a17=None) == 1                    # win_start without win_len
+    assert call(a5=None) == 1                     # window row without a store
+    assert call(a4=FAKE + 8) == 1                 # misaligned window row
+    assert call(a9=5) == 1                        # unknown entry dtype
+    assert call(a11=None) == 1                    # entry without codes
+    assert call(a13=None) == 1                    # key without z
+    assert call(a1=None) == 1                     # n_tokens missing
+    assert call(a18=None, a19=0) == 3             # no workspace (status word)
+    assert call(a19=64) == 3                      # workspace smaller than the header
+    assert call(a0=0) == 0                        # empty batch: nothing to do
+    assert call(a0=0, a1=None) == 0
