@@ -472,6 +472,13 @@ def run_ours(args):
             app = run_cache_append(args, torch, csa2, cfg, dev, stream, flush)
         except Exception as ex:  # reported, not hidden
             app = {"error": repr(ex)}
+    variants = None
+    if not args.no_pool:
+        try:
+            variants = run_step_variants(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs,
+                                         ws, stream, flush)
+        except Exception as ex:  # reported, not hidden
+            variants = {"error": repr(ex)}
     ced = None
     if not args.no_ced:
         try:
@@ -506,6 +513,7 @@ def run_ours(args):
             "ced_projection": ced,
             "hierarchical_indexer": pool,
             "cache_append": app,
+            "step_variants": variants,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -638,6 +646,89 @@ def run_cache_append(args, torch, csa2, cfg, dev, stream, flush):
     return {"call": "csa2_cache_append", "sequences": B, "us": round(us, 2), "bytes": bytes_call,
             "gbs": round(bytes_call / (us * 1e-6) / 1e9, 2), "launches": 1,
             "note": "one token per sequence completing an FP4 entry; a few KB per sequence, launch-bound"}
+
+
+def run_step_variants(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs, ws, stream, flush):
+    """The timed decode step in two more forms, each as one CUDA graph timed like the step:
+    (1) step_with_pool: the REINDEX layer ranks only the FULL layer's candidate pool
+        (CSA2_MODE_REINDEX_POOL); (2) step_with_append: before each layer its cache append of
+        the step's token (FULL: window row, the FP4 entry the token completes and its key;
+        REINDEX: window row and key; REUSE: window row), the layers reading n_visible and
+        the window bounds the appends write. The token is 4N-1, the last one of the cache, so
+        the layers see the same N entries and W window rows as the step; n_tokens is not
+        advanced, so every replay does the same work."""
+    P = lambda t: t.data_ptr() if t is not None else None
+    sp = stream.cuda_stream
+    scale = ctypes.c_float(cfg.softmax_scale)
+    wsp, wsn = P(ws), ws.numel()
+    B, W = cfg.B, cfg.W
+
+    def layer(d, mode, prev, out, nv, ws_, wl_, swa, s_stride):
+        reuse = mode == ci.REUSE
+        return L.csa2_decode_layer(mode, cfg.B, cfg.T, cfg.H, cfg.H_I, P(d["q"]),
+                                   None if reuse else P(d["q_idx"]), None if reuse else P(d["w"]),
+                                   None if reuse else P(d["z"]), P(codes), P(scales), cfg.N,
+                                   None if reuse else P(nv), cfg.K, P(prev), P(out), P(swa), s_stride,
+                                   P(ws_), P(wl_), W, cfg.d_v, scale, P(d["o"]), P(d["lse"]), wsp, wsn, sp)
+
+    def timed(thunks):
+        with torch.cuda.stream(stream):
+            for fn in thunks:
+                if fn() != 0:
+                    raise RuntimeError("step variant call failed")
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for fn in thunks:
+                fn()
+        n = min(args.steps, 500)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n + 3)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+        stream.synchronize()
+        st, flags = csa2.csa2_read_device_status(ws, stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} flags {flags}")
+        us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs[3:]) * 1e3
+        return {"us_per_step": round(us, 2), "steps_per_s": round(1e6 / us, 1)}
+
+    modes = [d["mode"] for d in dl]
+    out = {}
+    if modes == [ci.FULL, ci.REINDEX, ci.REUSE]:
+        full_sel, re_sel = idx_bufs[0], idx_bufs[1]
+        thunks = [lambda: layer(dl[0], ci.FULL, None, full_sel, nvis, wst, wln, dl[0]["swa"], cfg.S),
+                  lambda: layer(dl[1], ci.REINDEX_POOL, full_sel, re_sel, nvis, wst, wln, dl[1]["swa"], cfg.S),
+                  lambda: layer(dl[2], ci.REUSE, re_sel, re_sel, nvis, wst, wln, dl[2]["swa"], cfg.S)]
+        out["step_with_pool"] = dict(timed(thunks), launches=3 + 3 + 1,
+                                     note="FULL -> REINDEX_POOL -> REUSE, csa2_decode_layer per layer")
+
+        g = torch.Generator(device=stream.device).manual_seed(11)
+        rings = [torch.zeros((B, 2 * W, 576), dtype=torch.bfloat16, device=stream.device) for _ in dl]
+        rows = [torch.randn((B, 576), generator=g, device=stream.device).to(torch.bfloat16) for _ in dl]
+        ent = torch.randn((B, 576), generator=g, device=stream.device)
+        keys = [torch.randn((B, 64), generator=g, device=stream.device).to(torch.bfloat16) for _ in dl]
+        n_tok = torch.full((B,), 4 * cfg.N - 1, dtype=torch.int32, device=stream.device)
+        a_nv, a_ws, a_wl = (torch.zeros(B, dtype=torch.int32, device=stream.device) for _ in range(3))
+
+        def app(li, with_entry, with_key):
+            return L.csa2_cache_append(B, P(n_tok), 0, 4, P(rows[li]), P(rings[li]), 2 * W, W,
+                                       P(ent) if with_entry else None, csa2.F32,
+                                       P(keys[li]) if with_key else None, P(codes), P(scales),
+                                       P(dl[li]["z"]) if with_key else None, cfg.N, P(a_nv), P(a_ws), P(a_wl),
+                                       wsp, wsn, sp)
+        thunks = [lambda: app(0, True, True),
+                  lambda: layer(dl[0], ci.FULL, None, full_sel, a_nv, a_ws, a_wl, rings[0], 2 * W),
+                  lambda: app(1, False, True),
+                  lambda: layer(dl[1], ci.REINDEX, None, re_sel, a_nv, a_ws, a_wl, rings[1], 2 * W),
+                  lambda: app(2, False, False),
+                  lambda: layer(dl[2], ci.REUSE, re_sel, re_sel, a_nv, a_ws, a_wl, rings[2], 2 * W)]
+        out["step_with_append"] = dict(timed(thunks), launches=3 + 2 + 2 + 1,
+                                       note="csa2_cache_append before each csa2_decode_layer (token 4N-1)")
+    return out
 
 
 def run_ced(args, torch, csa2, dev, peaks):

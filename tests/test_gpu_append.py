@@ -153,3 +153,88 @@ def test_decode_after_appends_attends_over_the_token_history():
         Ow, lw = attention.attend(f64(q[b, 0]), keys, 512, tau)
         check_attention(o[b, 0], Ow, f"sequence {b}")
         check_lse(lse[b, 0], lw, f"sequence {b}")
+
+
+def test_serving_loop_in_a_cuda_graph():
+    """One decode step captured once and replayed per token: csa2_cache_append (advancing
+    n_tokens on the device) then csa2_decode_layer(FULL) with the n_visible and window
+    bounds the append wrote. K covers every entry, so each token's output is one softmax
+    over all entries completed so far and its last n_win tokens."""
+    rng = np.random.default_rng(45)
+    B, H, H_I, n_win, N, steps = 2, 16, 8, 16, 16, 40
+    K = N
+    tau = 1.0 / math.sqrt(576)
+    dev = DEV
+    swa = torch.zeros((B, 2 * n_win, 576), dtype=torch.bfloat16, device=dev)
+    codes = torch.zeros((B, N, 288), dtype=torch.uint8, device=dev)
+    scales = torch.zeros((B, N, 36), dtype=torch.uint8, device=dev)
+    z = torch.zeros((B, N, 64), dtype=torch.bfloat16, device=dev)
+    nvis, wst, wln = (torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(3))
+    n_tok = torch.tensor([0, 9], dtype=torch.int32, device=dev)     # sequence 1 starts 9 tokens in
+    # static per-step inputs, refilled before each replay
+    row_in = torch.zeros((B, 576), dtype=torch.bfloat16, device=dev)
+    ent_in = torch.zeros((B, 576), dtype=torch.float32, device=dev)
+    key_in = torch.zeros((B, 64), dtype=torch.bfloat16, device=dev)
+    q_in = torch.zeros((B, 1, H, 576), dtype=torch.bfloat16, device=dev)
+    qi_in = torch.zeros((B, 1, H_I, 64), dtype=torch.bfloat16, device=dev)
+    w_in = torch.ones((B, 1, H_I), dtype=torch.float32, device=dev)
+    idx = torch.empty((B, 1, K), dtype=torch.int32, device=dev)
+    o = torch.empty((B, 1, H, 512), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, 1, H), dtype=torch.float32, device=dev)
+    ws = csa2.csa2_workspace(B, 1, H, N, K, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        csa2.csa2_cache_append(n_tok, swa_row=row_in, swa_kv=swa, n_win=n_win, entry_kv=ent_in, entry_z=key_in,
+                               kv_codes=codes, kv_scales=scales, z=z, n_visible=nvis, win_start=wst, win_len=wln,
+                               ws=ws, stream=stream)
+        csa2.csa2_decode_layer(csa2.FULL, q_in, codes, scales, swa, wst, wln, n_win, K, q_idx=qi_in, w_idx=w_in,
+                               z=z, n_visible=nvis, out_idx=idx, o=o, lse=lse, softmax_scale=tau, ws=ws,
+                               stream=stream)
+
+    hist_rows, hist_ent = [[], []], [[], []]
+    # sequence 1's first 9 tokens: its history before the loop (written by plain appends)
+    with torch.cuda.stream(stream):
+        pre = torch.tensor([-1, 0], dtype=torch.int32, device=dev)
+        for _ in range(9):
+            r = ci.bf16_bits(rng.standard_normal((B, 576), dtype=np.float32))
+            e = rng.standard_normal((B, 576), dtype=np.float32)
+            csa2.csa2_cache_append(pre, swa_row=to_dev_bf16(r, dev), swa_kv=swa, n_win=n_win, entry_kv=to_dev(e, dev),
+                                   kv_codes=codes, kv_scales=scales, ws=ws, stream=stream)
+            hist_rows[1].append(r[1])
+            if len(hist_rows[1]) % 4 == 0:
+                hist_ent[1].append(e[1])
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        step()                                   # warm (sets kernel attributes)
+    stream.synchronize()
+    # the warm step consumed one token per sequence: restart from the same state
+    with torch.cuda.stream(stream):
+        n_tok.copy_(torch.tensor([0, 9], dtype=torch.int32, device=dev))
+    stream.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for t in range(steps):
+        r = ci.bf16_bits(rng.standard_normal((B, 576), dtype=np.float32))
+        e = rng.standard_normal((B, 576), dtype=np.float32)
+        q = ci.bf16_bits(rng.standard_normal((B, 1, H, 576), dtype=np.float32))
+        with torch.cuda.stream(stream):   # inputs and replay on the graph's stream, in order
+            row_in.copy_(to_dev_bf16(r, dev))
+            ent_in.copy_(to_dev(e, dev))
+            q_in.copy_(to_dev_bf16(q, dev))
+            graph.replay()
+        stream.synchronize()
+        for b in range(B):
+            hist_rows[b].append(r[b])
+            if len(hist_rows[b]) % 4 == 0:
+                hist_ent[b].append(e[b])
+            keys = [f64(np.array(hist_rows[b][-n_win:]))]
+            if hist_ent[b]:
+                c, s = fp4.encode(np.array(hist_ent[b], np.float32))
+                keys.insert(0, fp4.decode(c, s))
+            Ow, lw = attention.attend(f64(q[b, 0]), np.concatenate(keys), 512, tau)
+            check_attention(o[b, 0].cpu().numpy(), Ow, f"token {t} sequence {b}")
+            check_lse(lse[b, 0].cpu().numpy(), lw, f"token {t} sequence {b}")
+    assert _host(n_tok).tolist() == [steps, 9 + steps]
+    assert csa2.csa2_read_device_status(ws) == (0, 0)
