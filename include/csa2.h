@@ -299,6 +299,19 @@ CSA2_API int csa2_cache_append(int B, int32_t* n_tokens, int advance, int ratio,
                    int32_t* n_visible, int32_t* win_start, int32_t* win_len,
                    void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * csa2_check_bounded_wait - self-check of the failure path of the kernels' waits.
+ *
+ * Every mbarrier wait inside the kernels gives up after one second of wall time,
+ * sets CSA2_DEV_PIPELINE_TIMEOUT in the workspace status word, drains what it
+ * started and returns (no kernel traps or spins). This call runs that path on
+ * purpose: one CTA waits, through the same wait routine, on an mbarrier that
+ * nothing arrives on, for limit_ns nanoseconds (1000 <= limit_ns <= 1e9), then sets
+ * the bit and returns. Afterwards csa2_read_device_status reports CSA2_ERR_TIMEOUT
+ * with that bit, and the context stays usable. ws: the 256-byte status header.
+ */
+CSA2_API int csa2_check_bounded_wait(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes that cover every call above with these or smaller sizes: a
  * 256-byte header (the device status word), then for csa2_index_topk two uint32
  * score-range words per query (B*T*8 bytes rounded up to 256) and the fp32

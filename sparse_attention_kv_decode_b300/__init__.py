@@ -69,6 +69,7 @@ def _lib():
     L.csa2_swa_merge.argtypes = [i32, i32, i32, vp, vp, i64, vp, vp, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp]
     L.csa2_cache_append.argtypes = [i32, vp, i32, i32, vp, vp, i64, i32, vp, i32, vp, vp, vp, vp, i64, vp, vp,
                                     vp, vp, sz, vp]
+    L.csa2_check_bounded_wait.argtypes = [i64, vp, sz, vp]
     L.csa2_workspace_bytes.argtypes = [i32, i32, i32, i64, i32]
     L.csa2_workspace_bytes.restype = sz
     L.csa2_workspace_init.argtypes = [vp, sz, vp]
@@ -79,7 +80,7 @@ def _lib():
     L.csa2_last_cuda_error.argtypes = []
     L.csa2_last_cuda_error.restype = ctypes.c_char_p
     for fn in ("csa2_encode_kv", "csa2_index_topk", "csa2_index_topk_prefetch", "csa2_sparse_decode",
-               "csa2_swa_merge", "csa2_decode_layer", "csa2_cache_append",
+               "csa2_swa_merge", "csa2_decode_layer", "csa2_cache_append", "csa2_check_bounded_wait",
                "csa2_workspace_init", "csa2_read_device_status", "csa2_version"):
         getattr(L, fn).restype = ctypes.c_int
     _LIB = L
@@ -478,6 +479,13 @@ def csa2_cache_append(n_tokens: torch.Tensor, swa_row: Optional[torch.Tensor] = 
                                int(n_win or 0), _ptr(entry_kv), dt, _ptr(entry_z), _ptr(kv_codes), _ptr(kv_scales),
                                _ptr(z), N, _ptr(n_visible), _ptr(win_start), _ptr(win_len), _ptr(ws), ws.numel(),
                                _stream(stream)), "csa2_cache_append")
+
+
+def csa2_check_bounded_wait(limit_ns: int, ws: torch.Tensor, stream=None) -> None:
+    """Run the kernels' wait-timeout path on purpose (a wait on an mbarrier nothing
+    arrives on, bounded by limit_ns); read the result with csa2_read_device_status."""
+    _check(_lib().csa2_check_bounded_wait(int(limit_ns), _ptr(ws), ws.numel(), _stream(stream)),
+           "csa2_check_bounded_wait")
 
 
 def decode_layer(mode: int, q: torch.Tensor, kv_codes: torch.Tensor, kv_scales: torch.Tensor,

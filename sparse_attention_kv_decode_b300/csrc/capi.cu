@@ -202,6 +202,14 @@ int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_model, const 
                                         z_out, static_cast<uint32_t*>(ws), st));
 }
 
+int csa2_check_bounded_wait(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream) {
+  CHECK_ARG(limit_ns >= 1000 && limit_ns <= (int64_t)kMbarWaitNs);
+  if (ws == nullptr) return CSA2_ERR_WORKSPACE;
+  CHECK_ARG(aligned(ws, 256));
+  if (ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
+  return cuda_status(launch_wait_check((uint64_t)limit_ns, static_cast<uint32_t*>(ws), (cudaStream_t)stream));
+}
+
 int csa2_cache_append(int B, int32_t* n_tokens, int advance, int ratio, const void* swa_row, void* swa_kv,
                       int64_t s_stride, int n_win, const void* entry_kv, int entry_dtype, const void* entry_z,
                       uint8_t* kv_codes, uint8_t* kv_scales, void* z, int64_t n_stride, int32_t* n_visible,

@@ -57,6 +57,7 @@ bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inne
                                uint32_t box_inner, uint32_t box_outer);
 
 // Kernel launchers (return cudaError_t of the launch).
+cudaError_t launch_wait_check(uint64_t limit_ns, uint32_t* status, cudaStream_t st);
 cudaError_t launch_cache_append(int B, int32_t* n_tokens, int advance, int ratio, const void* swa_row,
                                 void* swa_kv, int64_t s_stride, int n_win, const void* entry_kv,
                                 int entry_dtype, const void* entry_z, uint8_t* codes, uint8_t* scales,
@@ -284,13 +285,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t a, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the completion of the phase with the given parity.
-__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t a, uint32_t parity, uint64_t limit_ns = kMbarWaitNs) {
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(a, parity)) return true;
     if (i > 64) __nanosleep(64);
-    if ((i & 255) == 0 && global_ns() - t0 > kMbarWaitNs) return false;
+    if ((i & 255) == 0 && global_ns() - t0 > limit_ns) return false;
   }
 }
 

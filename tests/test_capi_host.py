@@ -199,3 +199,11 @@ def test_cache_append_validation(L):
     assert call(a19=64) == 3                      # workspace smaller than the header
     assert call(a0=0) == 0                        # empty batch: nothing to do
     assert call(a0=0, a1=None) == 0
+
+
+def test_check_bounded_wait_validation(L):
+    r = L.csa2_check_bounded_wait
+    assert r(999, FAKE, 1 << 20, None) == 1            # bound below a microsecond
+    assert r(2_000_000_000, FAKE, 1 << 20, None) == 1  # above the kernels' own one-second bound
+    assert r(1_000_000, None, 0, None) == 3            # no workspace (status word)
+    assert r(1_000_000, FAKE, 64, None) == 3           # workspace smaller than the header
