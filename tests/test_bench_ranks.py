@@ -57,3 +57,14 @@ def test_reference_arm_other_ranks_exit_quietly():
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_step_bytes_are_the_stated_algorithmic_bytes():
+    """Per sequence and layer: indexer keys (N x 128 B, FULL and REINDEX), K selected FP4
+    entries (324 B each) and the window (W x 576 x 2 B): 346,292,224 B for 32 sequences at
+    32768 entries, K = 2048, W = 128, FULL -> REINDEX -> REUSE."""
+    import bench
+    import csa2_inputs as ci
+    cfg = ci.DECODE_128K
+    per_seq = 2 * cfg.N * 128 + 3 * (cfg.K * 324 + cfg.W * 576 * 2)
+    assert bench.algorithmic_bytes_per_step(cfg) == per_seq * cfg.B == 346_292_224
