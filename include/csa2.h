@@ -158,7 +158,10 @@ CSA2_API int csa2_index_topk_prefetch(int mode, int B, int T, int H_I,
  * as csa2_index_topk (same arguments, kernels and results), with its scratch in
  * a fixed device array inside this library (256 B header + 64 KiB of per-query
  * score ranges + 8 MiB of scores), so the call allocates nothing and needs no
- * workspace.
+ * workspace. It is for callers that cannot allocate device memory for one: a
+ * serving engine that reserves all free device memory for its own KV pool at
+ * start-up, or a plug-in that receives tensors from a host framework but no
+ * allocator. Every GPU that loads the library holds the array until exit.
  * Limit: csa2_workspace_bytes(B, T, *, n_stride, K) <= 256 B + 64 KiB + 8 MiB,
  *   i.e. at most 2^21 padded scores (B * T * (n_stride rounded up to 1024), e.g.
  *   32 queries over 65,536 entries) and 8192 queries; larger calls return

@@ -1,8 +1,11 @@
 """csa2_index_topk_noalloc: csa2_index_topk on the library's fixed device scratch.
 
-The call allocates nothing and takes no workspace; it must return what the
-workspace call returns for the same inputs, call after call (the scratch keeps
-whatever the previous call left in it).
+The call allocates nothing and takes no workspace, for callers that cannot allocate
+device memory (an engine that has reserved all of it for its own KV pool, a plug-in
+given tensors but no allocator). It must return what the workspace call returns for
+the same inputs, call after call (the scratch keeps whatever the previous call left in
+it). The file is collected last, and it also passes when run alone in a fresh process
+(then its first call does the per-device set-up).
 
 Ref: "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression", picx.dev summary,
 Methodology / 2. CSA2 (the indexer's top-K of FULL / REINDEX, and REUSE).
