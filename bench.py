@@ -479,6 +479,12 @@ def run_ours(args):
                                          ws, stream, flush)
         except Exception as ex:  # reported, not hidden
             variants = {"error": repr(ex)}
+    others = None
+    if not args.no_configs:
+        try:
+            others = run_other_configs(args, torch, csa2, dev, peaks, flush)
+        except Exception as ex:  # reported, not hidden
+            others = {"error": repr(ex)}
     ced = None
     if not args.no_ced:
         try:
@@ -514,6 +520,7 @@ def run_ours(args):
             "hierarchical_indexer": pool,
             "cache_append": app,
             "step_variants": variants,
+            "other_configs": others,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -731,6 +738,79 @@ def run_step_variants(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, w
     return out
 
 
+def run_other_configs(args, torch, csa2, dev, peaks, flush):
+    """The other decode workloads, one csa2_decode_layer(FULL) call each as a CUDA graph
+    (inputs resident, L2 flushed between replays): 4 sequences at 1M tokens (262,144
+    entries), reported against HBM (keys + selected entries + window), and a 4096-token
+    prefill chunk over 32,768 entries (causal), reported in TFLOP/s (attention over the
+    selected entries and the window, plus the indexer, as stated for that workload)."""
+    out = {}
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    L = csa2.lib()
+    P = lambda t: t.data_ptr() if t is not None else None
+    b16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    for cfg, steps in ((ci.DECODE_1M, min(args.steps, 200)), (ci.PREFILL_CHUNK, min(args.steps, 20))):
+        inp = ci.make_decode_inputs(cfg)
+        Lr = inp.layers[0]
+        X = t32(Lr.X)
+        codes, scales = csa2.csa2_encode_kv(X)
+        del X
+        Lr.X = None
+        q, qi, w, z, swa = b16(Lr.q), b16(Lr.q_idx), t32(Lr.w_idx), b16(Lr.z), b16(Lr.swa)
+        nvis, wst, wln = t32(inp.n_visible), t32(inp.win_start), t32(inp.win_len)
+        idx = torch.empty((cfg.B, cfg.T, cfg.K), dtype=torch.int32, device=dev)
+        o = torch.empty((cfg.B, cfg.T, cfg.H, cfg.d_v), dtype=torch.float32, device=dev)
+        lse = torch.empty((cfg.B, cfg.T, cfg.H), dtype=torch.float32, device=dev)
+        ws = csa2.csa2_workspace(cfg.B, cfg.T, cfg.H, cfg.N, cfg.K, device=dev)
+        scale = ctypes.c_float(cfg.softmax_scale)
+
+        def call():
+            return L.csa2_decode_layer(ci.FULL, cfg.B, cfg.T, cfg.H, cfg.H_I, P(q), P(qi), P(w), P(z), P(codes),
+                                       P(scales), cfg.N, P(nvis), cfg.K, None, P(idx), P(swa), cfg.S, P(wst), P(wln),
+                                       cfg.W, cfg.d_v, scale, P(o), P(lse), P(ws), ws.numel(), sp)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            if call() != 0:
+                raise RuntimeError(f"{cfg.name}: csa2_decode_layer failed")
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps + 3)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+        stream.synchronize()
+        st, flags = csa2.csa2_read_device_status(ws, stream)
+        if st != 0:
+            raise RuntimeError(f"{cfg.name}: device status {st} flags {flags}")
+        us = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs[3:]) * 1e3
+        row = {"sequences": cfg.B, "query_tokens": cfg.T, "entries": cfg.N, "top_k": cfg.K, "n_win": cfg.W,
+               "us_per_call": round(us, 2), "calls_per_s": round(1e6 / us, 1), "timed_calls": steps,
+               "launches_per_call": 3}
+        if cfg.T == 1:
+            byt = algorithmic_bytes_per_step(cfg)
+            gbs = byt / (us * 1e-6) / 1e9
+            row.update(bytes=byt, gbs=round(gbs, 1), frac_of_8tbs=round(gbs / TARGET_HBM_GBS, 4),
+                       frac_of_measured_hbm=round(gbs / peaks["hbm"], 4))
+        else:
+            Qn = cfg.B * cfg.T
+            flop = 2.0 * Qn * cfg.H * (cfg.K + cfg.W) * (576 + cfg.d_v) + 2.0 * Qn * cfg.N * cfg.H_I * 64
+            tf = flop / (us * 1e-6) / 1e12
+            row.update(flop=flop, tflops=round(tf, 1), frac_of_bf16_peak=round(tf / peaks["bf16"], 4),
+                       flop_note="attention over K entries + window (2 Q H (K+W) 1088) + indexer over all "
+                                 "N entries (2 Q N H_I 64), as stated for this workload")
+        out[cfg.name] = row
+        del codes, scales, q, qi, w, z, swa, idx, o, lse, ws, g, inp
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ced(args, torch, csa2, dev, peaks):
     """CED projection, Eq. (1), with the fused FP4 cache write: 32768 x 4096 against
     20 layers x (576 + 64) columns. Timed alone with CUDA events (inputs > L2)."""
@@ -878,6 +958,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-ced", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the 1M-context decode and the prefill-chunk measurements")
     ap.add_argument("--no-pool", action="store_true",
                     help="skip the side measurements (REINDEX vs REINDEX_POOL, csa2_cache_append)")
     ap.add_argument("--attn", choices=["layer", "fused", "two-call"], default="layer",
