@@ -162,11 +162,12 @@ CSA2_API int csa2_index_topk_prefetch(int mode, int B, int T, int H_I,
  * serving engine that reserves all free device memory for its own KV pool at
  * start-up, or a plug-in that receives tensors from a host framework but no
  * allocator. Every GPU that loads the library holds the array until exit.
- * Limit: csa2_workspace_bytes(B, T, *, n_stride, K) <= 256 B + 64 KiB + 8 MiB,
- *   i.e. at most 2^21 padded scores (B * T * (n_stride rounded up to 1024), e.g.
- *   32 queries over 65,536 entries) and 8192 queries; larger calls return
- *   CSA2_ERR_WORKSPACE and launch nothing. REUSE has no limit (it uses no
- *   scratch).
+ * Limit: with Q = B * T, the call needs 256 B + roundup256(8 Q) + 4 Q *
+ *   roundup1024(n_stride) bytes (REINDEX_POOL: plus roundup256(4 Q K) +
+ *   roundup256(4 Q)), at most 256 B + 64 KiB + 8 MiB: FULL / REINDEX take up to
+ *   2^21 padded scores and 8192 queries (e.g. 32 queries over 65,536 entries);
+ *   larger calls return CSA2_ERR_WORKSPACE and launch nothing. REUSE has no
+ *   limit (it uses no scratch).
  * Set-up: the first FULL/REINDEX call on each device looks up the array's
  *   address (cudaGetSymbolAddress, which may load the module); make that first
  *   call before any stream capture. A failed lookup returns CSA2_ERR_CUDA.
