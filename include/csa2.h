@@ -165,7 +165,8 @@ CSA2_API int csa2_index_topk_prefetch(int mode, int B, int T, int H_I,
  * Limit: with Q = B * T, the call needs 256 B + roundup256(8 Q) + 4 Q *
  *   roundup1024(n_stride) bytes (REINDEX_POOL: plus roundup256(4 Q K) +
  *   roundup256(4 Q)), at most 256 B + 64 KiB + 8 MiB: FULL / REINDEX take up to
- *   2^21 padded scores and 8192 queries (e.g. 32 queries over 65,536 entries);
+ *   2^21 padded scores, hence at most 2048 queries (e.g. 32 queries over 65,536
+ *   entries);
  *   larger calls return CSA2_ERR_WORKSPACE and launch nothing. REUSE has no
  *   limit (it uses no scratch).
  * Set-up: the first FULL/REINDEX call on each device looks up the array's
