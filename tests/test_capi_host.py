@@ -207,3 +207,13 @@ def test_check_bounded_wait_validation(L):
     assert r(2_000_000_000, FAKE, 1 << 20, None) == 1  # above the kernels' own one-second bound
     assert r(1_000_000, None, 0, None) == 3            # no workspace (status word)
     assert r(1_000_000, FAKE, 64, None) == 3           # workspace smaller than the header
+
+
+def test_binding_declares_argument_types_for_every_entry_point(L):
+    """Every call of the header has its C signature declared in the binding (ctypes would
+    otherwise pass 64-bit sizes and pointers as C ints)."""
+    for name in declared_symbols():
+        fn = getattr(L, name)
+        if name in ("csa2_version", "csa2_last_cuda_error"):
+            continue
+        assert fn.argtypes is not None, name
