@@ -11,8 +11,10 @@ the selected entries and the window (csa2_decode_attention); REUSE skips the ind
 csa2_index_topk + csa2_sparse_decode + csa2_swa_merge. The KV caches and keys are resident in HBM (written before timing); each
 timed step re-reads them, and L2 is flushed between steps.
 
-Prints one JSON line (rank 0). --impl reference times the CPU oracle on a bounded
-sample of the same workload instead.
+Prints one JSON line. The GPU arm runs on one GPU only (--gpus 1, no torchrun ranks):
+the attention and CED kernels use TMA cluster multicast, which this library runs in
+single-GPU calls only, so more ranks get an "unavailable" line and launch nothing.
+--impl reference times the CPU oracle on the same workload instead (rank 0 only).
 """
 from __future__ import annotations
 
@@ -239,18 +241,27 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+ONE_GPU_ONLY = ("one GPU per process and one process per job: the attention and CED kernels load "
+                "through TMA cluster multicast, which this library runs in single-GPU calls only")
+
+
 def run_ours(args):
+    rank, _, world = dist_env()
+    if world > 1 or args.gpus != 1:
+        # refused before CUDA is touched: no kernel of this library runs under more than one rank
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "n_gpus": max(world, args.gpus), "unavailable": ONE_GPU_ONLY}),
+                  flush=True)
+        print(f"bench.py: --gpus {args.gpus} / WORLD_SIZE {world} refused: {ONE_GPU_ONLY}", file=sys.stderr)
+        return 0
+    world = 1
     import torch
     from cuda.bindings import driver as cu
 
     import sparse_attention_kv_decode_b300 as csa2
 
-    rank, local_rank, world = dist_env()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     L = csa2.lib()
     cfg = CFG
     inp = ci.make_decode_inputs(cfg)
@@ -385,8 +396,6 @@ def run_ours(args):
     except Exception:
         gpu_uuid = None
     clocks = ClockSampler(gpu_uuid)
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
@@ -401,8 +410,6 @@ def run_ours(args):
     stream.synchronize()
     wall = time.perf_counter() - wall0
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-    if world > 1:
-        torch.distributed.barrier()
     clk = clocks.stop()
     # per-call breakdown (separate pass, events between the calls)
     per_call = [[] for _ in calls]
@@ -523,8 +530,6 @@ def run_ours(args):
             "other_configs": others,
         }
         print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
     return 0
 
 
@@ -931,8 +936,6 @@ def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bu
     n = max(10, args.steps // 10)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
     # the timed region starts before the first upload and ends after the last download
     e0.record(up)
     comp.wait_stream(up)

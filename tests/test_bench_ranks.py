@@ -1,8 +1,9 @@
 """Multi-rank host logic of bench.py on CPU (gloo, world size 2, no GPU).
 
-The decode sequences are independent, so `bench.py --gpus N` runs one replica of the
-workload per rank with no collective on the data path; the job's time is the slowest
-rank's and its value is N x steps / that time. Only rank 0 prints.
+The GPU arm runs on one GPU only: under more than one rank (or with --gpus other than 1)
+it prints an "unavailable" line on rank 0 and exits before touching CUDA. The timing rule
+for independent replicas (the job's time is the slowest rank's, its value N x steps / that
+time) is host logic and is checked here with two gloo ranks; only rank 0 prints.
 """
 import os
 import subprocess
@@ -91,3 +92,24 @@ def test_reference_arm_line_has_the_contract_keys():
     e = d["e2e"]
     assert e["value"] == d["value"] and e["unit"] == d["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("env_ranks,gpus", [(None, 2), (("0", "2"), 2), (("1", "2"), 2), (("0", "4"), 1)])
+def test_gpu_arm_refuses_more_than_one_gpu(env_ranks, gpus):
+    """No kernel of the library runs under more than one rank: the GPU arm refuses before
+    importing torch's CUDA runtime, rank 0 prints one "unavailable" line, the others nothing."""
+    import json
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    if env_ranks:
+        env.update(RANK=env_ranks[0], LOCAL_RANK=env_ranks[0], WORLD_SIZE=env_ranks[1])
+    r = subprocess.run([sys.executable, "bench.py", "--gpus", str(gpus), "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "refused" in r.stderr
+    lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    if env_ranks and env_ranks[0] != "0":
+        assert lines == []
+    else:
+        assert len(lines) == 1
+        d = json.loads(lines[0])
+        assert "unavailable" in d and d["n_gpus"] >= 2 and "value" not in d

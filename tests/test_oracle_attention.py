@@ -7,6 +7,7 @@ picx.dev summary, Methodology / 2. CSA2.
 import math
 
 import numpy as np
+import pytest
 
 from oracle import attention, fp4, indexer
 
@@ -96,3 +97,22 @@ def test_padding_entries_are_skipped():
     O, L = attention.sparse_global(q, rows, np.array([1, 4, -1, -1]), 6, 0.5)
     O2, L2 = attention.attend(q, rows[[1, 4]], 6, 0.5)
     assert np.allclose(O, O2) and np.allclose(L, L2)
+
+
+@pytest.mark.parametrize("n_win", [1, 3, 5])
+def test_swa_branch_attends_the_last_n_win_tokens(n_win):
+    """The window of a query at position p is tokens max(0, p+1-n_win) .. p of the raw store
+    (the sliding window of the blog repost, reading R9). Brute force over that token list, at
+    positions whose window starts anywhere in the store, the last one ending at its last row."""
+    rng = np.random.default_rng(40 + n_win)
+    n_tok, D, d_v, tau = 17, 6, 4, 0.4
+    store = rng.standard_normal((n_tok, D))
+    q = rng.standard_normal((2, D))
+    for p in sorted({0, 1, n_win - 1, n_win, n_win + 3, 9, n_tok - 1}):
+        if p < 0:
+            continue
+        window = [store[j].tolist() for j in range(n_tok) if p - n_win < j <= p]
+        length = len(window)
+        O, L = attention.swa_branch(q, store, p + 1 - length, length, d_v, tau)
+        Ob, Lb = _brute(q.tolist(), window, d_v, tau)
+        assert np.allclose(O, Ob, atol=1e-13) and np.allclose(L, Lb, atol=1e-13), f"window of token {p}"
