@@ -71,6 +71,7 @@ typedef enum { CSA2_F32 = 0, CSA2_BF16 = 1 } csa2_dtype;
 #define CSA2_DEV_BAD_WINDOW 0x2u  /* swa_merge window outside [0, s_stride)    */
 #define CSA2_DEV_TOPK_LEVELS 0x4u /* top-K refinement did not settle           */
 #define CSA2_DEV_PIPELINE_TIMEOUT 0x8u /* a bounded mbarrier wait gave up       */
+#define CSA2_DEV_RANGE 0x10u      /* a bf16 query / window value outside fp16 range */
 
 /*
  * csa2_encode_kv - write the FP4 main KV cache.
@@ -127,7 +128,9 @@ CSA2_API int csa2_encode_kv(const void* h, int h_dtype, int64_t rows, int d_mode
  *   [-1, n_stride) sets CSA2_DEV_BAD_INDEX. The block reading is this library's
  *   (the page gives "2,048 blocks x 8 positions").
  * ws: at least csa2_workspace_bytes(B, T, *, n_stride, K) bytes, prepared
- * once by csa2_workspace_init.
+ * once by csa2_workspace_init (REINDEX_POOL needs only 256 + roundup256(8 B T) +
+ * 4 B T P + roundup256(4 B T K) + roundup256(4 B T) bytes, with P =
+ * roundup1024(min(8 K, roundup8(n_stride))) pool positions per query).
  */
 CSA2_API int csa2_index_topk(int mode, int B, int T, int H_I,
                     const void* q_idx, const float* w_idx,
@@ -162,16 +165,20 @@ CSA2_API int csa2_index_topk_prefetch(int mode, int B, int T, int H_I,
  * serving engine that reserves all free device memory for its own KV pool at
  * start-up, or a plug-in that receives tensors from a host framework but no
  * allocator. Every GPU that loads the library holds the array until exit.
- * Limit: with Q = B * T, the call needs 256 B + roundup256(8 Q) + 4 Q *
- *   roundup1024(n_stride) bytes (REINDEX_POOL: plus roundup256(4 Q K) +
- *   roundup256(4 Q)), at most 256 B + 64 KiB + 8 MiB: FULL / REINDEX take up to
- *   2^21 padded scores, hence at most 2048 queries (e.g. 32 queries over 65,536
- *   entries);
- *   larger calls return CSA2_ERR_WORKSPACE and launch nothing. REUSE has no
- *   limit (it uses no scratch).
- * Set-up: the first FULL/REINDEX call on each device looks up the array's
- *   address (cudaGetSymbolAddress, which may load the module); make that first
- *   call before any stream capture. A failed lookup returns CSA2_ERR_CUDA.
+ * Limit: with Q = B * T, FULL / REINDEX need 256 B + roundup256(8 Q) + 4 Q *
+ *   roundup1024(n_stride) bytes, at most 256 B + 64 KiB + 8 MiB: up to 2^21
+ *   padded scores, hence at most 2048 queries (e.g. 32 queries over 65,536
+ *   entries). REINDEX_POOL scores only its pool, P = roundup1024(min(8 K,
+ *   roundup8(n_stride))) positions per query, and needs 256 B + roundup256(8 Q)
+ *   + 4 Q P + roundup256(4 Q K) + roundup256(4 Q) bytes (e.g. 32 queries with
+ *   K = 2048 at any n_stride). Larger calls return CSA2_ERR_WORKSPACE and launch
+ *   nothing. REUSE has no limit (it uses no scratch).
+ * Set-up: every FULL/REINDEX/REINDEX_POOL call made outside a stream capture
+ *   looks up the array's address on the current device (cudaGetSymbolAddress,
+ *   which may load the module; a failed lookup returns CSA2_ERR_CUDA); a call
+ *   inside a capture uses the address found by the last call outside one on
+ *   that device, so make one call on each device before capturing (a capture
+ *   before any returns CSA2_ERR_UNSUPPORTED).
  * Starting values: the array is zero when the module loads, which is the state
  *   the per-query score-range words must start in; each call leaves them zero
  *   again (the selection is exact from any start, a non-zero leftover only
@@ -200,6 +207,11 @@ CSA2_API int csa2_index_topk_noalloc(int mode, int B, int T, int H_I,
  * q: bf16 [B][T][H][576]; idx: int32 [B][T][K]; o_g: fp32 [B][T][H][d_v];
  * lse_g: fp32 [B][T][H]. Limits: H % 16 == 0, H <= 64, d_v == 512, K <= 4096.
  * Indices outside [-1, n_stride) are skipped and set CSA2_DEV_BAD_INDEX.
+ * Range of q: the products run on fp16 tensor cores, so q must be finite with
+ * |q| <= 65504 (every such bf16 value is exact in fp16 down to 2^-14 in
+ * magnitude; smaller ones round to fp16's subnormal grid, an absolute error of at
+ * most 2^-25). A value outside sets CSA2_DEV_RANGE; the outputs of that query are
+ * then undefined. The FP4 entries always fit (|C| <= 6 * 448).
  */
 CSA2_API int csa2_sparse_decode(int B, int T, int H, const void* q,
                        const uint8_t* kv_codes, const uint8_t* kv_scales, int64_t n_stride,
@@ -219,6 +231,8 @@ CSA2_API int csa2_sparse_decode(int B, int T, int H, const void* q,
  * outputs of csa2_sparse_decode); o_out: fp32 [B][T][H][d_v] (may alias
  * o_g); lse_out: fp32 [B][T][H] (nullable, may alias lse_g).
  * A window outside [0, s_stride) is clipped and sets CSA2_DEV_BAD_WINDOW.
+ * Range: q and the window rows must be finite with |x| <= 65504, as in
+ * csa2_sparse_decode (fp16 tensor cores); a value outside sets CSA2_DEV_RANGE.
  */
 CSA2_API int csa2_swa_merge(int B, int T, int H, const void* q,
                    const void* swa_kv, int64_t s_stride,
@@ -235,7 +249,8 @@ CSA2_API int csa2_swa_merge(int B, int T, int H, const void* q,
  * Arguments as in those two calls; o: fp32 [B][T][H][d_v], lse: fp32 [B][T][H]
  * (nullable). Limits: H % 16 == 0, H <= 64, d_v == 512, K <= 4096, n_win <= 256.
  * An empty selection and an empty window give O = 0 and LSE = -inf. ws: the
- * 256-byte status header is enough.
+ * 256-byte status header is enough. q and the window rows: finite, |x| <= 65504
+ * (CSA2_DEV_RANGE otherwise, as in csa2_sparse_decode).
  */
 CSA2_API int csa2_decode_attention(int B, int T, int H, const void* q,
                    const uint8_t* kv_codes, const uint8_t* kv_scales, int64_t n_stride,

@@ -34,7 +34,7 @@ CODE_BYTES, SCALE_BYTES = 288, 36
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3: "CSA2_ERR_WORKSPACE",
           4: "CSA2_ERR_CUDA", 5: "CSA2_ERR_TIMEOUT", 6: "CSA2_ERR_DEVICE_CHECK"}
-DEV_BAD_INDEX, DEV_BAD_WINDOW, DEV_TOPK_LEVELS, DEV_PIPELINE_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+DEV_BAD_INDEX, DEV_BAD_WINDOW, DEV_TOPK_LEVELS, DEV_PIPELINE_TIMEOUT, DEV_RANGE = 0x1, 0x2, 0x4, 0x8, 0x10
 
 _LIB = None
 
@@ -248,7 +248,8 @@ def csa2_index_topk_noalloc(mode: int, q_idx: Optional[torch.Tensor], w_idx: Opt
                             out_idx: torch.Tensor, prev_idx: Optional[torch.Tensor] = None,
                             out_scores: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """csa2_index_topk on the library's fixed device scratch: no workspace, and
-    nothing is allocated (out_idx [B, T, K] int32 is the caller's)."""
+    nothing is allocated (out_idx [B, T, K] int32 is the caller's). REUSE and
+    REINDEX_POOL take prev_idx [B, T, K] int32 (REINDEX_POOL: the FULL layer's selection)."""
     L = _lib()
     _dev(out_idx, "out_idx", (torch.int32,))
     B_, T_, K_ = out_idx.shape
@@ -271,10 +272,16 @@ def csa2_index_topk_noalloc(mode: int, q_idx: Optional[torch.Tensor], w_idx: Opt
     if z.shape != (B_, N, D_IDX):
         raise ValueError("z must be [B, N, 64]")
     _dev(n_visible, "n_visible", (torch.int32,), (B_ * T_,))
+    if mode == REINDEX_POOL:
+        if prev_idx is None:
+            raise ValueError("REINDEX_POOL needs the FULL layer's selection as prev_idx")
+        _dev(prev_idx, "prev_idx", (torch.int32,), (B_, T_, K))
+    else:
+        prev_idx = None
     if out_scores is not None:
         _dev(out_scores, "out_scores", (torch.float32,), (B_, T_, K))
     _check(L.csa2_index_topk_noalloc(mode, B_, T_, H_I, _ptr(q_idx), _ptr(w_idx), _ptr(z), N, _ptr(n_visible), K,
-                                     None, _ptr(out_idx), _ptr(out_scores), _stream(stream)),
+                                     _ptr(prev_idx), _ptr(out_idx), _ptr(out_scores), _stream(stream)),
            "csa2_index_topk_noalloc")
     return out_idx
 

@@ -461,6 +461,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     if (!wok) fail();
     else {
       const int h = wt >> 2;  // 64 rows x 72 pieces: 4 threads per row, 18 pieces each
+      uint32_t nonfinite = 0u;
 #pragma unroll 6
       for (int k = 0; k < 18; ++k) {
         const int pc = (wt & 3) * 18 + k;
@@ -468,8 +469,11 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         uint4 v = *pp;
         v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
         v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
+        nonfinite |= h2_nonfinite(v.x) | h2_nonfinite(v.y) | h2_nonfinite(v.z) | h2_nonfinite(v.w);
         *pp = v;
       }
+      // a query value outside the fp16 range (rows past H are not this query's)
+      if (nonfinite && h < H) atomicOr(status, CSA2_DEV_RANGE);
       fence_proxy_async_smem();
     }
     mbar_arrive(bar(kQReady));
@@ -525,6 +529,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         if (ok && wt == 0) waited_t = t;
         if (ok) {
           const bool row_ok = r_begin + t * kTK + e < r_end;
+          uint32_t nonfinite = 0u;
           // bf16 -> fp16 in place; half 0 converts the first 36 pieces of row e, half 1 the rest
           for (int g = 0; g < 5; ++g) {
             const int c0 = g < 4 ? 2 * g : 8, nc = g < 4 ? 2 : 1;
@@ -537,12 +542,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
                 uint4 v = *pp;
                 v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
                 v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
+                nonfinite |= h2_nonfinite(v.x) | h2_nonfinite(v.y) | h2_nonfinite(v.z) | h2_nonfinite(v.w);
                 // rows past the window are zeroed: their p is 0, and 0 * NaN would not be
                 if (!row_ok) v = make_uint4(0, 0, 0, 0);
                 *pp = v;
               }
             }
           }
+          // a window value outside the fp16 range
+          if (nonfinite && row_ok) atomicOr(status, CSA2_DEV_RANGE);
           fence_proxy_async_smem();
           mbar_arrive(bar(kChunkFull));
           mbar_arrive(bar(kChunkFull + 1));

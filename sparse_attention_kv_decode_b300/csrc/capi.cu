@@ -106,23 +106,30 @@ static int cuda_status(cudaError_t e) {
 constexpr size_t kStaticScratchBytes = kWsHeader + 65536 + (size_t(1) << 23);
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
-// Device address of g_static_scratch for the current device, looked up once per
-// device (the lookup may load this module, so it must not run inside a stream
-// capture for the first time).
-static int static_scratch(void** out) {
+// Device address of g_static_scratch for the current device. Outside a stream
+// capture it is looked up on every call (so a context torn down and created again
+// since the last call gets its own address); inside a capture, where the lookup
+// could load the module, the address of the last call outside one is used, and a
+// capture before any such call is refused.
+static int static_scratch(cudaStream_t st, void** out) {
   static std::mutex mu;
   static void* cache[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_status(e);
   if (dev < 0 || dev >= 64) return CSA2_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return cuda_status(e);
   std::lock_guard<std::mutex> lk(mu);
-  if (cache[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return cuda_status(e);
     if (p == nullptr) return CSA2_ERR_CUDA;
     cache[dev] = p;
+  } else if (cache[dev] == nullptr) {
+    return CSA2_ERR_UNSUPPORTED;
   }
   *out = cache[dev];
   return CSA2_OK;
@@ -310,19 +317,21 @@ static int index_topk_impl(int mode, int B, int T, int H_I, const void* q_idx, c
   CHECK_ARG(!pooled || prev_idx != nullptr);
   if (ws == nullptr) return CSA2_ERR_WORKSPACE;
   CHECK_ARG(aligned(ws, 256));
-  const size_t after_scores = kWsHeader + range_bytes(Q) + scores_bytes(Q, n_stride);
+  // REINDEX_POOL scores at most K blocks x 8 positions per query, and no more than the
+  // (8-aligned) cache rows: its score rows are that long, not n_stride
+  const int64_t n8 = (n_stride + 7) / 8 * 8;
+  const int64_t pcap = (int64_t)8 * K < n8 ? (int64_t)8 * K : n8;
+  const int64_t pstride = score_pad(pcap);
+  const size_t after_scores =
+      kWsHeader + range_bytes(Q) + (pooled ? (size_t)Q * (size_t)pstride * 4 : scores_bytes(Q, n_stride));
   if (ws_bytes < after_scores + (pooled ? pool_bytes(Q, K) : 0)) return CSA2_ERR_WORKSPACE;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   uint32_t* range = reinterpret_cast<uint32_t*>(wsb + kWsHeader);
   float* scores = reinterpret_cast<float*>(wsb + kWsHeader + range_bytes(Q));
   uint32_t* status = reinterpret_cast<uint32_t*>(wsb);
   if (pooled) {
-    // at most K blocks x 8 positions, and no more than the (8-aligned) cache rows
     int32_t* blocks = reinterpret_cast<int32_t*>(wsb + after_scores);
     int32_t* pool_nv = reinterpret_cast<int32_t*>(wsb + after_scores + ((size_t)Q * K * 4 + 255) / 256 * 256);
-    const int64_t n8 = (n_stride + 7) / 8 * 8;
-    const int64_t pcap = (int64_t)8 * K < n8 ? (int64_t)8 * K : n8;
-    const int64_t pstride = score_pad(pcap);
     cudaError_t e = launch_pool_build(prev_idx, (int)Q, K, n_visible, n_stride, blocks, pool_nv, status, st);
     if (e == cudaSuccess)
       e = launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores, pstride, range,
@@ -370,7 +379,7 @@ int csa2_index_topk_noalloc(int mode, int B, int T, int H_I, const void* q_idx,
   // CSA2_ERR_WORKSPACE before launching anything
   void* scratch = nullptr;
   if (mode != CSA2_MODE_REUSE) {
-    const int s = static_scratch(&scratch);
+    const int s = static_scratch((cudaStream_t)stream, &scratch);
     if (s != CSA2_OK) return s;
   }
   return csa2_index_topk(mode, B, T, H_I, q_idx, w_idx, z, n_stride, n_visible, K, prev_idx,

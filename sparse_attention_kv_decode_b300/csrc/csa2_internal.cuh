@@ -231,6 +231,12 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t v) {
   return pack_h2(bf16_lo(v), bf16_hi(v));
 }
+// Non-zero when either fp16 half of h2 is infinite or NaN (all-ones exponent): the
+// bf16 value it came from was outside the fp16 range (or not finite).
+__device__ __forceinline__ uint32_t h2_nonfinite(uint32_t h2) {
+  const uint32_t e = h2 & 0x7C007C00u;
+  return (uint32_t)((e & 0xFFFFu) == 0x7C00u) | (uint32_t)((e >> 16) == 0x7C00u);
+}
 
 // Quantise one 16-value block. Returns the 8 code bytes (as two u32) and the
 // E4M3 scale code.

@@ -309,3 +309,39 @@ def test_decode_layer_equals_topk_then_attention():
         assert torch.equal(i1, i2)
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
         prev = i1
+
+
+def test_range_flag_for_values_outside_fp16():
+    """The products run on fp16 tensor cores: a bf16 query or window value above 65504 in
+    magnitude sets CSA2_DEV_RANGE; 65280 (the largest bf16 value below it) does not."""
+    cfg = ci.scaled(ci.TINY, N=64, K=64, H=16, W=32)
+    inp = ci.make_decode_inputs(cfg)
+    L = inp.layers[0]
+    codes, scales = _cache(L.X)
+    ws = csa2.csa2_workspace(1, 1, 16, 64, 64, device=DEV)
+    idx = torch.arange(64, dtype=torch.int32, device=DEV).reshape(1, 1, 64)
+    wst, wln = to_dev(inp.win_start, DEV), to_dev(inp.win_len, DEV)
+
+    def run(q_bits, swa_bits):
+        csa2.csa2_decode_attention(to_dev_bf16(q_bits, DEV), codes, scales, idx, to_dev_bf16(swa_bits, DEV), wst,
+                                   wln, cfg.W, cfg.softmax_scale, ws=ws)
+        return csa2.csa2_read_device_status(ws)
+
+    big_ok, too_big = np.uint16(0x477F), np.uint16(0x4780)   # 65280 and 65536 as bf16
+    assert run(L.q, L.swa) == (0, 0)
+    q = L.q.copy(); q[0, 0, 3, 100] = big_ok
+    s = L.swa.copy(); s[0, int(inp.win_start[0]), 7] = big_ok | np.uint16(0x8000)
+    assert run(q, s) == (0, 0)
+    q = L.q.copy(); q[0, 0, 15, 575] = too_big
+    st, flags = run(q, L.swa)
+    assert st == 6 and flags == csa2.DEV_RANGE
+    s = L.swa.copy(); s[0, int(inp.win_start[0]) + int(inp.win_len[0]) - 1, 0] = too_big | np.uint16(0x8000)
+    st, flags = run(L.q, s)
+    assert st == 6 and flags == csa2.DEV_RANGE
+    # a row past the window is not part of the call's input
+    end = int(inp.win_start[0]) + int(inp.win_len[0]) - 1
+    wl = torch.tensor([int(inp.win_len[0]) - 1], dtype=torch.int32, device=DEV)
+    s = L.swa.copy(); s[0, end, 0] = too_big
+    csa2.csa2_decode_attention(to_dev_bf16(L.q, DEV), codes, scales, idx, to_dev_bf16(s, DEV), wst, wl, cfg.W,
+                               cfg.softmax_scale, ws=ws)
+    assert csa2.csa2_read_device_status(ws) == (0, 0)

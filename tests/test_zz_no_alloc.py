@@ -81,3 +81,51 @@ def test_rejects_more_scores_than_the_scratch_holds():
     torch.cuda.synchronize()
     # all scores are 0: the K lowest indices win the ties
     assert bool((out == torch.arange(K, dtype=torch.int32, device="cuda")).all())
+
+
+def test_leftover_scores_under_the_range_words_of_a_larger_call():
+    """The per-query range words sit after the header and the scores after them, both
+    placed by the call's own query count: a 32-query call leaves scores where a later
+    64-query call keeps its range words. The selection must stay exact from that start."""
+    N, K = 32768, 2048
+    for B in (32, 64, 32):
+        cfg = ci.scaled(ci.DECODE_128K, B=B, N=N, H=16, K=K, W=8, modes=(ci.FULL,), seed=B)
+        q, w, z, nv = _layer(cfg)
+        want_s = torch.empty((B, 1, K), dtype=torch.float32, device="cuda")
+        want = csa2.csa2_index_topk(csa2.FULL, q, w, z, nv, K, out_scores=want_s)
+        got = torch.full((B, 1, K), -7, dtype=torch.int32, device="cuda")
+        got_s = torch.empty((B, 1, K), dtype=torch.float32, device="cuda")
+        csa2.csa2_index_topk_noalloc(csa2.FULL, q, w, z, nv, K, got, out_scores=got_s)
+        torch.cuda.synchronize()
+        _same(got, want)
+        _same(got_s.view(torch.int32), want_s.view(torch.int32))
+
+
+def test_reindex_pool_matches_workspace_call():
+    """REINDEX_POOL through the fixed scratch: its score rows are pool-sized, so 32 queries
+    with K = 2048 fit at any cache length (here 100,000 entries, where a full scan would not
+    fit). Compared bit for bit with the workspace call, twice in a row."""
+    B, N, K, H_I = 32, 100000, 2048, 8
+    g = torch.Generator(device="cuda").manual_seed(12)
+    q = torch.randn((B, 1, H_I, 64), generator=g, device="cuda").to(torch.bfloat16)
+    w = torch.randn((B, 1, H_I), generator=g, device="cuda").abs()
+    z = torch.randn((B, N, 64), generator=g, device="cuda").to(torch.bfloat16)
+    nv = torch.randint(N // 2, N + 1, (B,), generator=g, device="cuda", dtype=torch.int32)
+    full_sel = csa2.csa2_index_topk(csa2.FULL, q, w, z, nv, K)
+    q2 = torch.randn((B, 1, H_I, 64), generator=g, device="cuda").to(torch.bfloat16)
+    z2 = torch.randn((B, N, 64), generator=g, device="cuda").to(torch.bfloat16)
+    want_s = torch.empty((B, 1, K), dtype=torch.float32, device="cuda")
+    want = csa2.csa2_index_topk(csa2.REINDEX_POOL, q2, w, z2, nv, K, prev_idx=full_sel, out_scores=want_s)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        got = torch.full((B, 1, K), -7, dtype=torch.int32, device="cuda")
+        got_s = torch.empty((B, 1, K), dtype=torch.float32, device="cuda")
+        csa2.csa2_index_topk_noalloc(csa2.REINDEX_POOL, q2, w, z2, nv, K, got, prev_idx=full_sel,
+                                     out_scores=got_s)
+        torch.cuda.synchronize()
+        _same(got, want)
+        _same(got_s.view(torch.int32), want_s.view(torch.int32))
+    # the full scan of the same call does not fit the scratch and is refused
+    with pytest.raises(csa2.Csa2Error) as ex:
+        csa2.csa2_index_topk_noalloc(csa2.REINDEX, q2, w, z2, nv, K, got)
+    assert ex.value.status == 3
