@@ -851,6 +851,321 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     }
 }
 
+// ---------------------------------------------------------------------------
+// Top-K selection, one CTA per query (up to kRowMaxN visible positions)
+// ---------------------------------------------------------------------------
+// The query's scores land in shared memory (a few bulk copies). Selection state is two
+// bitmaps over the positions, one bit per position (word w holds positions 32w ..
+// 32w+31): selected, and still in play.
+//   round 0  thread t visits positions k * kRowThreads + t (conflict-free reads): a
+//            histogram of all scores over kRowBins monotone bins of [lo, hi] (the range
+//            the scoring kernel left, else the scores' min / max); one block scan from
+//            the top gives the bin b* holding the K-th score; a second pass marks the
+//            higher bins selected and b*'s scores in play (one ballot per 32 positions
+//            gives a bitmap word);
+//   round i  the scores in play (few) are binned again over their own min / max;
+//   exact    when at most kRowRankCap scores remain in play, they are listed in shared
+//            memory and each is ranked against all of them by (score desc, position
+//            asc);
+//   ties     when they all tie (min == max), the lowest positions win.
+// The bin map ((s - lo) * (NB-1) / (hi - lo), rounded to an integer by adding 2^23) is
+// monotone in s, so bins never reorder scores and equal scores share a bin. Thread t then
+// owns bitmap word t: one block scan of the per-word counts orders both the tie rule and
+// the output (ascending by position).
+constexpr int kRowThreads = 1024;
+constexpr int kRowBins = 2048;
+constexpr int kRowRankCap = 128;
+constexpr int kRowMaxN = 32 * kRowThreads;
+constexpr int kRowCopies = 8;    // bulk copies that land the scores
+
+struct RowShared {
+  uint32_t hist[kRowBins];
+  uint32_t selw[kRowThreads];    // selected bitmap
+  uint32_t candw[kRowThreads];   // in-play bitmap
+  int scan[kRowThreads / 32];
+  float red[2][kRowThreads / 32];
+  int bstar, above, cand_n;
+  uint32_t rng[2];
+  uint64_t bar_load;
+  float cand_s[kRowRankCap];
+  int cand_i[kRowRankCap];
+};
+
+// Bin of s in [0, kRowBins) for s in [lo, hi], scl = (NB-1) / (hi - lo): (s - lo) * scl
+// is at most NB-1 up to rounding, and adding 2^23 rounds it to an integer held in the
+// low mantissa bits. Each step is monotone in s.
+__device__ __forceinline__ uint32_t row_bin(float s, float lo, float scl) {
+  return __float_as_uint(fmaf(s - lo, scl, 8388608.f)) & (uint32_t)(kRowBins - 1);
+}
+
+// Block-wide min of a and max of b (all threads get them).
+__device__ __forceinline__ void row_minmax(float& a, float& b, RowShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  __syncthreads();   // sh.red may still be read by a previous call
+  if (lane == 0) {
+    sh.red[0][warp] = a;
+    sh.red[1][warp] = b;
+  }
+  __syncthreads();
+  a = sh.red[0][lane];
+  b = sh.red[1][lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+}
+
+// b* of a histogram in sh.hist for the rem-th largest: sets sh.bstar / sh.above.
+__device__ __forceinline__ void row_find_bstar(RowShared& sh, int rem) {
+  const int tid = threadIdx.x;
+  const int b1 = kRowBins - 1 - 2 * tid, b0 = b1 - 1;
+  const int h1 = (int)sh.hist[b1], h0 = (int)sh.hist[b0];
+  int total;
+  const int above = block_excl_scan(h1 + h0, sh.scan, total);
+  if (above < rem && rem <= above + h1) {
+    sh.bstar = b1;
+    sh.above = above;
+  } else if (above + h1 < rem && rem <= above + h1 + h0) {
+    sh.bstar = b0;
+    sh.above = above + h1;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kRowThreads, 1) topk_row_kernel(
+    const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ n_visible,
+    int64_t n_stride, int K, uint32_t* __restrict__ range, int32_t* __restrict__ out_idx,
+    float* __restrict__ out_scores, uint32_t* __restrict__ status, const uint8_t* __restrict__ pf_codes,
+    const uint8_t* __restrict__ pf_scales, int T, int64_t kv_stride, const int32_t* __restrict__ pool,
+    int pool_stride) {
+  extern __shared__ __align__(128) float sv[];   // the query's scores, position order
+  __shared__ RowShared sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int qi = blockIdx.x;
+  if (tid == 0) {
+    mbar_init(smem_u32(&sh.bar_load), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  sh.selw[tid] = 0u;
+  sh.candw[tid] = 0u;
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  int nvis = clamp_nvis(n_visible, qi, n_stride);
+  // 16-byte pieces of the row (a score row is score_stride >= roundup4(nvis) floats)
+  const int n16 = (nvis + 3) >> 2;
+  if (tid == 0) {
+    if (nvis > 0) mbar_arrive_expect_tx(smem_u32(&sh.bar_load), (uint32_t)n16 * 16);
+    // the score range the scoring kernel left (consumed: set back to zero)
+    sh.rng[0] = range[2 * qi];
+    sh.rng[1] = range[2 * qi + 1];
+    range[2 * qi] = 0u;
+    range[2 * qi + 1] = 0u;
+  }
+  __syncthreads();   // expect_tx precedes every copy's completion
+  if (tid < kRowCopies && nvis > 0) {
+    const int per = (n16 + kRowCopies - 1) / kRowCopies;
+    const int a = tid * per, b = min(a + per, n16);
+    if (b > a)
+      bulk_g2s(smem_u32(sv + 4 * a), scores + (int64_t)qi * score_stride + 4 * a, (uint32_t)(b - a) * 16,
+               smem_u32(&sh.bar_load));
+  }
+  // one warp waits for the copies, the others at the barrier
+  const bool loaded = nvis == 0 || tid >= 32 || mbar_wait(smem_u32(&sh.bar_load), 0);
+  if (!__syncthreads_and(loaded)) {
+    if (tid == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+    nvis = 0;   // select nothing; the output below still completes
+  }
+  const int nk = (nvis + kRowThreads - 1) / kRowThreads;
+  if (nvis <= K) {
+    // everything visible is selected: bitmap words of the first nvis positions
+    const int p0 = 32 * tid;
+    const int nmine = min(max(nvis - p0, 0), 32);
+    sh.selw[tid] = nmine >= 32 ? 0xffffffffu : ((1u << nmine) - 1u);
+  } else {
+    int rem = K;
+    float lo = key2f(~sh.rng[0]), hi = key2f(sh.rng[1]);
+    if (!(sh.rng[1] != 0u && lo < hi && isfinite(lo) && isfinite(hi))) {
+      float a = INFINITY, b = -INFINITY;
+      for (int k = 0; k < nk; ++k) {
+        const int p = k * kRowThreads + tid;
+        if (p < nvis) {
+          a = fminf(a, sv[p]);
+          b = fmaxf(b, sv[p]);
+        }
+      }
+      row_minmax(a, b, sh);
+      lo = a;
+      hi = b;
+    }
+    bool done = false;
+    int nplay = nvis;   // positions in play
+    const float scl0 = (float)(kRowBins - 1) / (hi - lo);
+    const bool round0 = lo < hi && scl0 <= 1e30f;
+    if (round0) {
+      // ---- round 0 over every visible position
+      for (int i = tid; i < kRowBins; i += kRowThreads) sh.hist[i] = 0u;
+      __syncthreads();
+#pragma unroll 8
+      for (int k = 0; k < nk; ++k) {
+        const int p = k * kRowThreads + tid;
+        if (p < nvis) atomicAdd(&sh.hist[row_bin(sv[p], lo, scl0)], 1u);
+      }
+      __syncthreads();
+      row_find_bstar(sh, rem);
+      const uint32_t bstar = (uint32_t)sh.bstar;
+      nplay = (int)sh.hist[bstar];
+      rem -= sh.above;
+      // lane k of each warp collects bitmap word k * 32 + warp (positions k * 1024 + 32 warp ..)
+      uint32_t my_sel = 0u, my_cand = 0u;
+#pragma unroll 8
+      for (int k = 0; k < nk; ++k) {
+        const int p = k * kRowThreads + tid;
+        const bool ok = p < nvis;
+        const uint32_t bi = ok ? row_bin(sv[p], lo, scl0) : 0u;
+        const uint32_t bs = __ballot_sync(0xffffffffu, ok && bi > bstar);
+        const uint32_t bc = __ballot_sync(0xffffffffu, ok && bi == bstar);
+        if (lane == k) {
+          my_sel = bs;
+          my_cand = bc;
+        }
+      }
+      if (lane < nk) {
+        sh.selw[lane * 32 + warp] = my_sel;
+        sh.candw[lane * 32 + warp] = my_cand;
+      }
+      __syncthreads();
+      if (nplay == rem) {   // every score of b* is taken
+        sh.selw[tid] |= sh.candw[tid];
+        done = true;
+      }
+    }
+    // ---- later rounds over the positions still in play (thread t: bitmap word t), binned
+    // by their order-preserving integer keys relative to the smallest: each round
+    // divides the key span by 2^11, so single keys are reached in at most three rounds
+    uint32_t cw = sh.candw[tid];
+    if (!round0) {
+      const int nmine = min(max(nvis - 32 * tid, 0), 32);
+      cw = nmine >= 32 ? 0xffffffffu : ((1u << nmine) - 1u);
+    }
+#pragma unroll 1
+    for (int level = 1; !done; ++level) {
+      // invariant: rem >= 1, nplay > rem positions in play, every higher score selected
+      if (nplay <= kRowRankCap) {
+        // exact: list the scores in play, rank each by (score desc, position asc)
+        if (tid == 0) sh.cand_n = 0;
+        __syncthreads();
+        for (uint32_t m = cw; m; m &= m - 1u) {
+          const int p = 32 * tid + __ffs(m) - 1;
+          const int slot = atomicAdd(&sh.cand_n, 1);
+          sh.cand_s[slot] = sv[p];
+          sh.cand_i[slot] = p;
+        }
+        __syncthreads();
+        if (tid < nplay) {
+          const float sc = sh.cand_s[tid];
+          const int i = sh.cand_i[tid];
+          int rank = 0;
+          for (int j = 0; j < nplay; ++j) {
+            const float t = sh.cand_s[j];
+            rank += (t > sc) || (t == sc && sh.cand_i[j] < i);
+          }
+          if (rank < rem) atomicOr(&sh.selw[i >> 5], 1u << (i & 31));
+        }
+        break;
+      }
+      // key range of the scores in play
+      uint32_t ka = 0xffffffffu, kb = 0u;
+      for (uint32_t m = cw; m; m &= m - 1u) {
+        const uint32_t x = f2key(sv[32 * tid + __ffs(m) - 1]);
+        ka = min(ka, x);
+        kb = max(kb, x);
+      }
+      {
+        ka = __reduce_min_sync(0xffffffffu, ka);
+        kb = __reduce_max_sync(0xffffffffu, kb);
+        __syncthreads();   // sh.red may still be read by a previous use
+        if (lane == 0) {
+          sh.red[0][warp] = __uint_as_float(ka);
+          sh.red[1][warp] = __uint_as_float(kb);
+        }
+        __syncthreads();
+        ka = __reduce_min_sync(0xffffffffu, __float_as_uint(sh.red[0][lane]));
+        kb = __reduce_max_sync(0xffffffffu, __float_as_uint(sh.red[1][lane]));
+      }
+      const uint32_t span = kb - ka;
+      if (span == 0u || level >= kMaxLevels) {
+        // all tie (or the search did not settle): lowest positions first
+        if (span != 0u && tid == 0) atomicOr(status, CSA2_DEV_TOPK_LEVELS);
+        const int c = __popc(cw);
+        int total;
+        const int pre = block_excl_scan(c, sh.scan, total);
+        int take = min(max(rem - pre, 0), c);
+        uint32_t t = 0u;
+        for (uint32_t m = cw; take > 0; --take) {
+          t |= m & (~m + 1u);
+          m &= m - 1u;
+        }
+        sh.selw[tid] |= t;
+        break;
+      }
+      const int shift = span < (uint32_t)kRowBins ? 0 : 32 - __clz((int)span) - 11;
+      for (int i = tid; i < kRowBins; i += kRowThreads) sh.hist[i] = 0u;
+      __syncthreads();
+      for (uint32_t m = cw; m; m &= m - 1u)
+        atomicAdd(&sh.hist[(f2key(sv[32 * tid + __ffs(m) - 1]) - ka) >> shift], 1u);
+      __syncthreads();
+      row_find_bstar(sh, rem);
+      const uint32_t bstar = (uint32_t)sh.bstar;
+      nplay = (int)sh.hist[bstar];
+      rem -= sh.above;
+      uint32_t ns = 0u, nc = 0u;
+      for (uint32_t m = cw; m; m &= m - 1u) {
+        const int j = __ffs(m) - 1;
+        const uint32_t bi = (f2key(sv[32 * tid + j]) - ka) >> shift;
+        ns |= (uint32_t)(bi > bstar) << j;
+        nc |= (uint32_t)(bi == bstar) << j;
+      }
+      cw = nc;
+      if (nplay == rem) ns |= nc;
+      sh.selw[tid] |= ns;
+      if (nplay == rem) break;
+      __syncthreads();   // every thread has read sh.hist[b*] and sh.above
+    }
+  }
+  __syncthreads();
+
+  // ---- ordered output: thread t writes the selected positions of bitmap word t
+  const uint32_t sel = sh.selw[tid];
+  int total;
+  int r = block_excl_scan(__popc(sel), sh.scan, total);
+  int32_t* out = out_idx + (int64_t)qi * K;
+  float* outs = out_scores ? out_scores + (int64_t)qi * K : nullptr;
+  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * kv_stride * CSA2_CODE_BYTES : nullptr;
+  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * kv_stride * CSA2_SCALE_BYTES : nullptr;
+  const int32_t* pblk = pool ? pool + (int64_t)qi * pool_stride : nullptr;
+  for (uint32_t m = sel; m && r < K; m &= m - 1u, ++r) {
+    const int pos = 32 * tid + __ffs(m) - 1;
+    const int ent = pblk ? pblk[pos >> 3] * 8 + (pos & 7) : pos;
+    out[r] = ent;
+    if (outs) outs[r] = sv[pos];
+    if (pfc && ent >= 0 && ent < kv_stride) {
+      prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
+      prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES);
+      prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES + CSA2_SCALE_BYTES - 1);
+    }
+  }
+  for (int q = total + tid; q < K; q += kRowThreads) {
+    out[q] = -1;
+    if (outs) outs[q] = __int_as_float(0x7fc00000);
+  }
+}
+
 // CTAs per query: enough for at most 8192 scores each; while the grid stays within one
 // CTA per SM, more (slices of at least 2048), since the selection's phases scale with
 // the slice, not with the cluster.
@@ -868,7 +1183,30 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
                                const uint8_t* pf_codes, const uint8_t* pf_scales, int T,
                                int64_t kv_stride, const int32_t* pool, int pool_stride) {
   static_assert(kNBMax % kSelThreads == 0 && kNBMin % kSelThreads == 0, "bins per thread");
+  static_assert(kRowBins == 2 * kRowThreads, "two bins per thread in the row kernel's scan");
   if (Q == 0) return cudaSuccess;
+  if (n_stride <= kRowMaxN && (int64_t)Q * select_cluster_size(n_stride, Q) > device_sm_count()) {
+    // many queries: one CTA per query, the scores in shared memory (with few queries the
+    // clusters below spread each query over several SMs and finish sooner)
+    const size_t smem = (size_t)((n_stride + 3) & ~3) * 4;
+    cudaError_t e = set_attr_once(5, (const void*)topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kRowMaxN * 4);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)Q);
+    cfg.blockDim = dim3(kRowThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int tt = T < 1 ? 1 : T;
+    const int64_t kvs = kv_stride < 0 ? n_stride : kv_stride;
+    return cudaLaunchKernelEx(&cfg, topk_row_kernel, scores, score_stride, n_visible, n_stride, K, range, out_idx,
+                              out_scores, status, pf_codes, pf_scales, tt, kvs, pool, pool_stride);
+  }
   const int C = select_cluster_size(n_stride, Q);
   const int NB = C <= 4 ? kNBMax : kNBMin;
   int slice_cap = (int)((n_stride + C - 1) / C);

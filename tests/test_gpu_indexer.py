@@ -84,6 +84,28 @@ def test_exact_ties_resolved_to_lower_index():
             assert np.array_equal(got[b, t], indexer.topk(I[t], nvis[b * T + t], K))
 
 
+@pytest.mark.parametrize("levels", [128, 16])
+def test_clustered_scores_need_refinement(levels):
+    """Exact scores (one head, q = e_0, w = 1: the score is z[n, 0]) packed into a narrow band
+    1 + j/128 (j < levels) with one far outlier (2^100): the first histogram round puts the
+    whole band in one bin, the next one bins the band exactly; with 16 levels every level
+    repeats ~375 times, so the K-th score's bin is all ties (lowest positions first)."""
+    B, T, N, H_I, K = 1, 2, 6000, 8, 3000
+    q = np.zeros((B, T, H_I, 64), np.float32)
+    q[..., 0, 0] = 1.0
+    w = np.zeros((B, T, H_I), np.float32)
+    w[..., 0] = 1.0
+    z = np.zeros((B, N, 64), np.float32)
+    z[0, :, 0] = 1.0 + (np.arange(N) % levels) / 128.0
+    z[0, 4321, 0] = 2.0 ** 100
+    zb, qb = ci.bf16_bits(z), ci.bf16_bits(q)
+    nvis = np.array([N, N - 1], np.int32)
+    got, _ = _run(qb, w, zb, nvis, K)
+    I = indexer.scores(f64(qb[0]), w[0], f64(zb[0]))
+    for t in range(T):
+        assert np.array_equal(got[0, t], indexer.topk(I[t], nvis[t], K))
+
+
 def test_all_scores_equal():
     B, T, N, H_I, K = 1, 1, 5000, 8, 777
     q = np.zeros((B, T, H_I, 64), np.uint16)
