@@ -12,7 +12,8 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libcsa2.so")
 BUILD = os.path.join(ROOT, "_build")
-SOURCES = ["capi.cu", "encode.cu", "indexer.cu", "attention.cu", "ced_gemm.cu", "append.cu", "selfcheck.cu"]
+SOURCES = ["capi.cu", "encode.cu", "indexer.cu", "index_gemm.cu", "attention.cu", "ced_gemm.cu", "append.cu",
+           "selfcheck.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

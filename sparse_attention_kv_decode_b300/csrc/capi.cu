@@ -342,8 +342,12 @@ static int index_topk_impl(int mode, int B, int T, int H_I, const void* q_idx, c
                                           blocks, K));
   }
   const int64_t stride = score_pad(n_stride);
-  cudaError_t e = launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores,
-                                     stride, range, status, st);
+  // many query tokens per sequence: the keys x (token, head) GEMM on the tensor cores
+  cudaError_t e = index_gemm_applies(T, H_I)
+                      ? launch_index_gemm(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores, stride, range,
+                                          status, st)
+                      : launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores, stride, range,
+                                           status, st);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_topk_select(scores, stride, n_visible, (int)Q, n_stride, K, range,
                                         out_idx, out_scores, status, st, pf_codes, pf_scales, T));

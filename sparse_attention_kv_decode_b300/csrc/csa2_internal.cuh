@@ -72,6 +72,12 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
                                float* scores, int64_t score_stride, uint32_t* range,
                                uint32_t* status, cudaStream_t st, const int32_t* pool = nullptr,
                                const int32_t* pool_nv = nullptr, int pool_stride = 0);
+// Indexer scoring of T >= 256 / H_I query tokens per sequence as a tcgen05 GEMM (keys x
+// (token, head) tiles); same scores and range words as launch_index_score without a pool.
+bool index_gemm_applies(int T, int H_I);
+cudaError_t launch_index_gemm(const void* q_idx, const float* w_idx, const void* z, int64_t n_stride,
+                              const int32_t* n_visible, int B, int T, int H_I, float* scores,
+                              int64_t score_stride, uint32_t* range, uint32_t* status, cudaStream_t st);
 // pf_codes / pf_scales (nullable): FP4 cache whose rows of the selected entries are
 // requested into L2 as they are written (batch b = query / T, rows of n_stride)
 cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const int32_t* n_visible,
@@ -107,6 +113,16 @@ cudaError_t launch_memset_u32(uint32_t* p, size_t n, cudaStream_t st);
 // Device helpers
 // ---------------------------------------------------------------------------
 #ifdef __CUDACC__
+
+// Order-preserving map of fp32 to uint32 (no NaN); key 0 is never produced. The scoring
+// kernels leave each query's min / max score as keys for the selection.
+__device__ __forceinline__ uint32_t f2key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }

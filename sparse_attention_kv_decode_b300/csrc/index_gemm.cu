@@ -1,0 +1,380 @@
+// Indexer scoring of many query tokens of one sequence on the tensor cores.
+//
+// Ref: "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression", picx.dev
+// summary, Methodology / 2. CSA2 (the indexer ranks every compressed entry for every
+// query token before the top-K) and / 3 (indexer cost grows with the context). The
+// pages give no indexer formula; this library scores
+//   I[t, n] = sum_h w[t, h] * max(0, q[t, h] . z[n])   (h < H_I).
+//
+// With T query tokens of one sequence (a prefill chunk) the dot products form a GEMM:
+// S[n, (t, h)] = z[n] . q[t, h], keys as M (128 per tile), a tile of T_tile = 256 / H_I
+// tokens x H_I heads as N = 256, and the 64 channels as K (four K = 16 steps). The keys
+// are then read once per token tile instead of once per token.
+//   warp 0      TMA producer: the token tile's q rows (32 KB, once per work item) and
+//               one 128-key z box per key tile into a ring of stages (128-byte swizzle)
+//   warp 1      TMEM allocation and the MMA issuer: tcgen05.mma kind::f16, M=128,
+//               N=256, K=16, fp32 accumulators in TMEM, double-buffered (2 x 256
+//               columns) so the epilogue of one key tile overlaps the MMAs of the next
+//   warps 2..9  epilogue: thread = key row (TMEM lane); each warpgroup takes half of
+//               the columns, applies max(0, .), weights the heads by w[t, h] (fp32),
+//               sums them, and stores one fp32 score per (token, key) below the
+//               token's causal limit, plus the token's running min / max score (the
+//               range words the selection starts from).
+// A work item is (sequence, token tile, chunk of key tiles); the key tiles past the
+// token tile's largest visible count are skipped. Every mbarrier wait is bounded.
+#include <cuda.h>
+
+#include "csa2_internal.cuh"
+
+namespace csa2 {
+namespace {
+
+constexpr int kGM = 128;                         // keys per tile
+constexpr int kGN = 256;                         // (token, head) columns per tile
+constexpr int kGStages = 6;
+constexpr int kGZBytes = kGM * CSA2_D_IDX * 2;   // 16 KB
+constexpr int kGQBytes = kGN * CSA2_D_IDX * 2;   // 32 KB
+constexpr int kGEpiWarps = 8;
+constexpr int kGThreads = 64 + 32 * kGEpiWarps;
+constexpr int kGTmemCols = 512;
+constexpr int kGMaxTT = 64;                      // tokens per tile for H_I = 4
+constexpr size_t kGSmem = 1024 + kGQBytes + kGStages * kGZBytes + 4096;
+
+struct GemmShape {
+  int B, T, ntt, nchunks, kpc;
+  int64_t n_stride;
+  __device__ __forceinline__ int total() const { return B * ntt * nchunks; }
+};
+
+template <int HI>
+__device__ __forceinline__ void item_coords(const GemmShape& g, const int32_t* n_visible, int it, int& b,
+                                            int& t0, int& nt, int& kt0, int& kt1) {
+  constexpr int TT = kGN / HI;
+  const int c = it % g.nchunks;
+  const int j = (it / g.nchunks) % g.ntt;
+  b = it / (g.nchunks * g.ntt);
+  t0 = j * TT;
+  nt = min(TT, g.T - t0);
+  int maxnv = 0;
+  for (int t = 0; t < nt; ++t) {
+    int v = n_visible[(int64_t)b * g.T + t0 + t];
+    v = v < 0 ? 0 : (v > g.n_stride ? (int)g.n_stride : v);
+    maxnv = max(maxnv, v);
+  }
+  const int nkt = (maxnv + kGM - 1) / kGM;
+  kt0 = c * g.kpc;
+  kt1 = min(kt0 + g.kpc, nkt);
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// OR of a predicate over the n threads of named barrier id (all of them get the result).
+__device__ __forceinline__ bool named_or(int id, int n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+template <int HI>
+__global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
+    const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_q,
+    const float* __restrict__ w_idx, const int32_t* __restrict__ n_visible, GemmShape g,
+    float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ range,
+    uint32_t* __restrict__ status) {
+  constexpr int TT = kGN / HI;
+  static_assert(TT <= kGMaxTT && kGN % HI == 0 && 32 % HI == 0, "token tile");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sq = smem_u32(smem);
+  const uint32_t sz = sq + kGQBytes;
+  uint8_t* misc = smem + kGQBytes + kGStages * kGZBytes;
+  const uint32_t bar_full = smem_u32(misc);
+  const uint32_t bar_empty = bar_full + 8 * kGStages;
+  const uint32_t bar_tfull = bar_empty + 8 * kGStages;
+  const uint32_t bar_tempty = bar_tfull + 16;
+  const uint32_t bar_qfull = bar_tempty + 16;
+  const uint32_t bar_qempty = bar_qfull + 8;
+  const uint32_t bar_drain = bar_qempty + 8;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 260);
+  float* w_s = reinterpret_cast<float*>(misc + 512);                  // [TT * HI]
+  int* nv_s = reinterpret_cast<int*>(misc + 512 + kGN * 4);           // [TT]
+  uint32_t* rng_s = reinterpret_cast<uint32_t*>(misc + 512 + kGN * 4 + kGMaxTT * 4);  // [TT][2]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, kGEpiWarps);
+    }
+    mbar_init(bar_qfull, 1);
+    mbar_init(bar_qempty, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(kGTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  // inputs may be written by the preceding kernel in the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int total = g.total();
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, qphase = 0;
+      bool armed[kGStages];
+      uint32_t armed_phase[kGStages];
+      for (int s = 0; s < kGStages; ++s) armed[s] = false, armed_phase[s] = 0;
+      bool q_armed = false;
+      uint32_t q_armed_phase = 0;
+      for (int it = blockIdx.x; it < total && !*abort_flag; it += gridDim.x) {
+        int b, t0, nt, kt0, kt1;
+        item_coords<HI>(g, n_visible, it, b, t0, nt, kt0, kt1);
+        if (kt0 >= kt1) continue;
+        // the q tile of the previous item is released by its last MMAs
+        if (!mbar_wait(bar_qempty, qphase ^ 1)) {
+          atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_qfull, kGQBytes);
+        q_armed = true;
+        q_armed_phase = qphase;
+        tma_load_2d(sq, &tm_q, 0, (b * g.T + t0) * HI, bar_qfull);
+        qphase ^= 1;
+        for (int kt = kt0; kt < kt1; ++kt) {
+          if (!mbar_wait(bar_empty + 8 * stage, phase ^ 1)) {
+            atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * stage;
+          mbar_arrive_expect_tx(fb, kGZBytes);
+          armed[stage] = true;
+          armed_phase[stage] = phase;
+          // rows past this sequence's cache belong to the next one (or read as zeros): their
+          // keys are past every token's visible count, so their scores are never stored
+          tma_load_2d(sz + stage * kGZBytes, &tm_z, 0, (int)((int64_t)b * g.n_stride + (int64_t)kt * kGM), fb);
+          if (++stage == kGStages) stage = 0, phase ^= 1;
+        }
+      }
+      // drain: every armed copy has landed before the CTA may exit
+      for (int s = 0; s < kGStages; ++s)
+        if (armed[s]) mbar_wait(bar_full + 8 * s, armed_phase[s]);
+      if (q_armed) mbar_wait(bar_qfull, q_armed_phase);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kGM, kGN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0, qphase = 0;
+      bool issued = false;
+      for (int it = blockIdx.x; it < total && !*abort_flag; it += gridDim.x) {
+        int b, t0, nt, kt0, kt1;
+        item_coords<HI>(g, n_visible, it, b, t0, nt, kt0, kt1);
+        if (kt0 >= kt1) continue;
+        if (!mbar_wait(bar_qfull, qphase)) {
+          atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        qphase ^= 1;
+        tc_fence_after();
+        const uint64_t bd = umma_desc_sw128(sq);
+        bool ok = true;
+        for (int kt = kt0; kt < kt1; ++kt) {
+          if (!mbar_wait(bar_tempty + 8 * acc, acc_phase ^ 1) || !mbar_wait(bar_full + 8 * stage, phase)) {
+            atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = umma_desc_sw128(sz + stage * kGZBytes);
+          const uint32_t d_tmem = tmem + acc * kGN;
+#pragma unroll
+          for (int k = 0; k < CSA2_D_IDX / 16; ++k)
+            umma_bf16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), idesc, k != 0);
+          umma_commit(bar_empty + 8 * stage);
+          umma_commit(bar_tfull + 8 * acc);
+          issued = true;
+          if (++stage == kGStages) stage = 0, phase ^= 1;
+          if (++acc == 2) acc = 0, acc_phase ^= 1;
+        }
+        umma_commit(bar_qempty);
+        if (!ok) break;
+      }
+      if (issued) {
+        umma_commit(bar_drain);
+        mbar_wait(bar_drain, 0);
+      }
+    }
+  } else {
+    // ---------------- epilogue: thread = key row, warpgroup = half of the columns
+    const int ew = warp - 2;                 // 0..7
+    const int quarter = warp & 3;            // TMEM lanes 32 * quarter ..
+    const int half = ew >> 2;                // columns [128 half, 128 half + 128)
+    const int et = threadIdx.x - 64;         // 0..255
+    const int key = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    // The epilogue warps meet at named barrier 1 only at item boundaries, and every one of
+    // them reaches each of those meetings (a warp whose wait gave up skips its remaining
+    // tiles, not the meetings), so the abort decision taken there is the same for all.
+    for (int it = blockIdx.x; it < total; it += gridDim.x) {
+      int b, t0, nt, kt0, kt1;
+      item_coords<HI>(g, n_visible, it, b, t0, nt, kt0, kt1);
+      if (kt0 >= kt1) continue;
+      // also: the previous item's readers of w_s / nv_s / rng_s are done
+      if (named_or(1, 32 * kGEpiWarps, *abort_flag != 0)) break;
+      {
+        const int tl = et / HI;
+        w_s[et] = tl < nt ? w_idx[((int64_t)b * g.T + t0) * HI + et] : 0.f;
+        if (et < TT) {
+          int v = et < nt ? n_visible[(int64_t)b * g.T + t0 + et] : 0;
+          nv_s[et] = v < 0 ? 0 : (v > g.n_stride ? (int)g.n_stride : v);
+          rng_s[2 * et] = 0u;
+          rng_s[2 * et + 1] = 0u;
+        }
+      }
+      named_bar(1, 32 * kGEpiWarps);
+      for (int kt = kt0; kt < kt1; ++kt) {
+        const bool got = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, acc_phase));
+        if (!got) {
+          if (lane == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const int n = kt * kGM + key;
+        const uint32_t tbase = tmem + acc * kGN + ((uint32_t)(quarter * 32) << 16) + 128 * half;
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t r[32];
+          tmem_ld32(tbase + 32 * c4, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int tk = 0; tk < 32 / HI; ++tk) {
+            const int tl = (128 * half + 32 * c4) / HI + tk;
+            const float* wt = w_s + tl * HI;
+            float s = 0.f;
+#pragma unroll
+            for (int h = 0; h < HI; ++h) s = fmaf(wt[h], fmaxf(__uint_as_float(r[tk * HI + h]), 0.f), s);
+            const bool valid = tl < nt && n < nv_s[tl];
+            if (valid) scores[((int64_t)b * g.T + t0 + tl) * score_stride + n] = s;
+            const uint32_t kk = valid ? f2key(s) : 0u;
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, kk);
+            const uint32_t kinv = __reduce_max_sync(0xffffffffu, valid ? ~kk : 0u);
+            if (lane == 0 && kmax != 0u) {
+              atomicMax(&rng_s[2 * tl], kinv);
+              atomicMax(&rng_s[2 * tl + 1], kmax);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+        if (++acc == 2) acc = 0, acc_phase ^= 1;
+      }
+      // the item's score range per token into the range words
+      named_bar(1, 32 * kGEpiWarps);
+      if (et < nt && rng_s[2 * et + 1] != 0u) {
+        atomicMax(range + 2 * ((int64_t)b * g.T + t0 + et), rng_s[2 * et]);
+        atomicMax(range + 2 * ((int64_t)b * g.T + t0 + et) + 1, rng_s[2 * et + 1]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kGTmemCols)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+bool index_gemm_applies(int T, int H_I) {
+  return (H_I == 4 || H_I == 8 || H_I == 16) && T >= kGN / H_I;
+}
+
+cudaError_t launch_index_gemm(const void* q_idx, const float* w_idx, const void* z, int64_t n_stride,
+                              const int32_t* n_visible, int B, int T, int H_I, float* scores,
+                              int64_t score_stride, uint32_t* range, uint32_t* status, cudaStream_t st) {
+  if (B == 0 || T == 0 || n_stride == 0) return cudaSuccess;
+  if (!index_gemm_applies(T, H_I)) return cudaErrorInvalidValue;
+  if ((int64_t)B * n_stride > ((int64_t)1 << 31) - kGM || (int64_t)B * T * H_I > ((int64_t)1 << 31) - kGN)
+    return cudaErrorInvalidValue;
+  CUtensorMap tz, tq;
+  if (!encode_tensor_map_2d_bf16(&tz, z, CSA2_D_IDX, (uint64_t)B * n_stride, CSA2_D_IDX, kGM) ||
+      !encode_tensor_map_2d_bf16(&tq, q_idx, CSA2_D_IDX, (uint64_t)B * T * H_I, CSA2_D_IDX, kGN))
+    return cudaErrorInvalidValue;
+  GemmShape g;
+  g.B = B;
+  g.T = T;
+  g.n_stride = n_stride;
+  const int TT = kGN / H_I;
+  g.ntt = (T + TT - 1) / TT;
+  const int nkt = (int)((n_stride + kGM - 1) / kGM);
+  const int n_sm = device_sm_count();
+  const int64_t base = (int64_t)B * g.ntt;
+  int64_t nch = (4 * (int64_t)n_sm + base - 1) / base;   // about four items per SM
+  if (nch > nkt) nch = nkt;
+  if (nch < 1) nch = 1;
+  g.kpc = (int)((nkt + nch - 1) / nch);
+  g.nchunks = (nkt + g.kpc - 1) / g.kpc;
+  const int64_t total = base * g.nchunks;
+  if (total > ((int64_t)1 << 31) - 1) return cudaErrorInvalidValue;
+  const int grid = (int)(total < n_sm ? total : n_sm);
+  const void* fn = H_I == 4 ? (const void*)index_gemm_kernel<4>
+                   : (H_I == 8 ? (const void*)index_gemm_kernel<8> : (const void*)index_gemm_kernel<16>);
+  const int slot = H_I == 4 ? 11 : (H_I == 8 ? 12 : 13);
+  cudaError_t e = set_attr_once(slot, fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kGThreads);
+  cfg.dynamicSmemBytes = kGSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (H_I == 4)
+    return cudaLaunchKernelEx(&cfg, index_gemm_kernel<4>, tz, tq, w_idx, n_visible, g, scores, score_stride, range,
+                              status);
+  if (H_I == 8)
+    return cudaLaunchKernelEx(&cfg, index_gemm_kernel<8>, tz, tq, w_idx, n_visible, g, scores, score_stride, range,
+                              status);
+  return cudaLaunchKernelEx(&cfg, index_gemm_kernel<16>, tz, tq, w_idx, n_visible, g, scores, score_stride, range,
+                            status);
+}
+
+}  // namespace csa2

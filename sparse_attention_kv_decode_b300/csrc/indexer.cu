@@ -59,15 +59,6 @@ __device__ __forceinline__ void load_q_frag(const uint16_t* q_idx, const float* 
   }
 }
 
-// Order-preserving map of fp32 to uint32 (no NaN); key 0 is never produced.
-__device__ __forceinline__ uint32_t f2key(float f) {
-  const uint32_t b = __float_as_uint(f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key2f(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
 __device__ __forceinline__ int clamp_nvis(const int32_t* n_visible, int qi, int64_t n_stride) {
   int v = n_visible[qi];
   return v < 0 ? 0 : (v > n_stride ? (int)n_stride : v);

@@ -68,6 +68,21 @@ def test_causal_visibility_and_padding():
     _check_all(q, w, z, nvis, K)
 
 
+@pytest.mark.parametrize("B,T,N,H_I,K", [(2, 100, 5000, 8, 512), (1, 40, 3000, 16, 300), (3, 70, 1500, 4, 200),
+                                          (1, 300, 9000, 8, 2048)])
+def test_many_query_tokens_gemm_scoring(B, T, N, H_I, K):
+    """Query tokens in tiles of 256 / H_I scored as one keys x (token, head) GEMM on the
+    tensor cores (a partial last tile, ragged causal limits including 0 and N, key tiles
+    past a tile's largest limit skipped): sets and returned scores match the oracle."""
+    rng = np.random.default_rng(25 + T)
+    q = ci.bf16_bits(rng.standard_normal((B, T, H_I, 64), dtype=np.float32))
+    w = np.abs(rng.standard_normal((B, T, H_I), dtype=np.float32))
+    z = ci.bf16_bits(rng.standard_normal((B, N, 64), dtype=np.float32))
+    nvis = rng.integers(0, N + 1, B * T).astype(np.int32)
+    nvis[0], nvis[-1], nvis[1] = 0, N, N - 1
+    _check_all(q, w, z, nvis, K)
+
+
 def test_exact_ties_resolved_to_lower_index():
     """Small integers make every dot product exact in fp32 and fp64, so scores tie
     exactly and the selection must equal the oracle's with no tolerance."""
