@@ -22,6 +22,7 @@
 //               range words the selection starts from).
 // A work item is (sequence, token tile, chunk of key tiles); the key tiles past the
 // token tile's largest visible count are skipped. Every mbarrier wait is bounded.
+#include <climits>
 #include <cuda.h>
 
 #include "csa2_internal.cuh"
@@ -262,6 +263,17 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
         }
       }
       named_bar(1, 32 * kGEpiWarps);
+      // this thread's tokens are tl0 .. tl0 + kTh - 1 (one half of the tile's columns);
+      // running min / max of their visible scores over the item's key tiles
+      constexpr int kTh = 128 / HI;
+      const int tl0 = 128 * half / HI;
+      float mn[kTh], mx[kTh];
+#pragma unroll
+      for (int i = 0; i < kTh; ++i) mn[i] = INFINITY, mx[i] = -INFINITY;
+      int min_nv = INT_MAX;
+#pragma unroll
+      for (int i = 0; i < kTh; ++i)
+        if (tl0 + i < nt) min_nv = min(min_nv, nv_s[tl0 + i]);
       for (int kt = kt0; kt < kt1; ++kt) {
         const bool got = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, acc_phase));
         if (!got) {
@@ -271,27 +283,32 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
         }
         tc_fence_after();
         const int n = kt * kGM + key;
+        // every token of this half sees every key of the tile (the common case)
+        const bool full = (kt + 1) * kGM <= min_nv;
         const uint32_t tbase = tmem + acc * kGN + ((uint32_t)(quarter * 32) << 16) + 128 * half;
-#pragma unroll 1
+#pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t r[32];
           tmem_ld32(tbase + 32 * c4, r);
           tmem_wait_ld();
 #pragma unroll
           for (int tk = 0; tk < 32 / HI; ++tk) {
-            const int tl = (128 * half + 32 * c4) / HI + tk;
+            const int ti = c4 * (32 / HI) + tk;   // token of this half
+            const int tl = tl0 + ti;
             const float* wt = w_s + tl * HI;
-            float s = 0.f;
+            // two independent partial sums (even / odd heads)
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int h = 0; h < HI; ++h) s = fmaf(wt[h], fmaxf(__uint_as_float(r[tk * HI + h]), 0.f), s);
-            const bool valid = tl < nt && n < nv_s[tl];
-            if (valid) scores[((int64_t)b * g.T + t0 + tl) * score_stride + n] = s;
-            const uint32_t kk = valid ? f2key(s) : 0u;
-            const uint32_t kmax = __reduce_max_sync(0xffffffffu, kk);
-            const uint32_t kinv = __reduce_max_sync(0xffffffffu, valid ? ~kk : 0u);
-            if (lane == 0 && kmax != 0u) {
-              atomicMax(&rng_s[2 * tl], kinv);
-              atomicMax(&rng_s[2 * tl + 1], kmax);
+            for (int h = 0; h < HI; h += 2) {
+              s0 = fmaf(wt[h], fmaxf(__uint_as_float(r[tk * HI + h]), 0.f), s0);
+              s1 = fmaf(wt[h + 1], fmaxf(__uint_as_float(r[tk * HI + h + 1]), 0.f), s1);
+            }
+            const float sc = s0 + s1;
+            const bool valid = tl < nt && (full || n < nv_s[tl]);
+            if (valid) {
+              scores[((int64_t)b * g.T + t0 + tl) * score_stride + n] = sc;
+              mn[ti] = fminf(mn[ti], sc);
+              mx[ti] = fmaxf(mx[ti], sc);
             }
           }
         }
@@ -299,6 +316,17 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
         if (++acc == 2) acc = 0, acc_phase ^= 1;
+      }
+      // this warp's share of each token's range, then the CTA's into the range words
+#pragma unroll
+      for (int i = 0; i < kTh; ++i) {
+        const bool any = mx[i] >= mn[i];
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, any ? f2key(mx[i]) : 0u);
+        const uint32_t kinv = __reduce_max_sync(0xffffffffu, any ? ~f2key(mn[i]) : 0u);
+        if (lane == 0 && kmax != 0u) {
+          atomicMax(&rng_s[2 * (tl0 + i)], kinv);
+          atomicMax(&rng_s[2 * (tl0 + i) + 1], kmax);
+        }
       }
       // the item's score range per token into the range words
       named_bar(1, 32 * kGEpiWarps);
