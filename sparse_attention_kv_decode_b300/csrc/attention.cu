@@ -185,14 +185,10 @@ __device__ __forceinline__ uint32_t cswz(int c, int row, int j) {
 template <bool kMax>
 __device__ __forceinline__ float red_op(float a, float b) { return kMax ? fmaxf(a, b) : a + b; }
 
-// Reduce 32 per-thread values (heads h0..h0+31) over the 128 threads of one head
-// half (4 warps, lane quarters 0..3), max or sum, into out[h0 .. h0+31] (or added
-// to it with kAcc).
-// Reduce-scatter inside each warp (31 shuffles), then across the 4 warps in
-// shared memory under named barrier `bid`.
-template <bool kMax, bool kAcc = false>
-__device__ __forceinline__ void reduce32(const float (&v)[32], Misc& ms, float* out, int h0, int lane,
-                                         int quarter, int bid) {
+// Reduce-scatter of 32 per-thread values (heads h0 .. h0+31) inside one warp, max or
+// sum: lane l returns the warp's result for head h0 + l (31 shuffles).
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce32(const float (&v)[32], int lane) {
   float a[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -223,11 +219,18 @@ __device__ __forceinline__ void reduce32(const float (&v)[32], Misc& ms, float* 
   }
   const bool hi = lane & 1;
   const float got = __shfl_xor_sync(0xffffffffu, hi ? d[0] : d[1], 1);
-  const float e = red_op<kMax>(hi ? d[1] : d[0], got);
-  // lane holds head index 16*b4 + 8*b3 + 4*b2 + 2*b1 + b0 of the 32
-  const int idx = ((lane >> 4) & 1) * 16 + ((lane >> 3) & 1) * 8 + ((lane >> 2) & 1) * 4 +
-                  ((lane >> 1) & 1) * 2 + (lane & 1);
-  ms.red[quarter][h0 + idx] = e;
+  // each step kept the half selected by one lane bit, so lane l ends with head l
+  return red_op<kMax>(hi ? d[1] : d[0], got);
+}
+
+// Reduce 32 per-thread values (heads h0..h0+31) over the 128 threads of one head
+// half (4 warps, lane quarters 0..3), max or sum, into out[h0 .. h0+31] (or added
+// to it with kAcc): reduce-scatter inside each warp, then across the 4 warps in
+// shared memory under named barrier `bid`.
+template <bool kMax, bool kAcc = false>
+__device__ __forceinline__ void reduce32(const float (&v)[32], Misc& ms, float* out, int h0, int lane,
+                                         int quarter, int bid) {
+  ms.red[quarter][h0 + lane] = warp_reduce32<kMax>(v, lane);
   named_sync(bid, 128);
   if (quarter == 0) {
     float r = ms.red[0][h0 + lane];
@@ -455,31 +458,34 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
       idx_row = fsrc.idx + (int64_t)qi * fsrc.K;
       if (nt_f > 0) fetch(read_idx(0));
-      ent16_next = read_idx(1);
     }
     wok = mbar_wait(bar(kQTma), 0);
     if (!wok) fail();
     else {
       const int h = wt >> 2;  // 64 rows x 72 pieces: 4 threads per row, 18 pieces each
-      uint32_t nonfinite = 0u;
+      uint32_t mag = 0u;      // largest bf16 magnitude (bits) of each half-word seen
 #pragma unroll 6
       for (int k = 0; k < 18; ++k) {
         const int pc = (wt & 3) * 18 + k;
         uint4* pp = reinterpret_cast<uint4*>(sQ + (pc >> 3) * kQChunk + h * 128 + (((pc & 7) ^ (h & 7)) << 4));
         uint4 v = *pp;
+        mag = __vmaxu2(mag, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                     __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
         v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
         v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
-        nonfinite |= h2_nonfinite(v.x) | h2_nonfinite(v.y) | h2_nonfinite(v.z) | h2_nonfinite(v.w);
         *pp = v;
       }
       // a query value outside the fp16 range (rows past H are not this query's)
-      if (nonfinite && h < H) atomicOr(status, CSA2_DEV_RANGE);
+      if (bf16_mag_beyond_fp16(mag) && h < H) atomicOr(status, CSA2_DEV_RANGE);
       fence_proxy_async_smem();
     }
     mbar_arrive(bar(kQReady));
+    // the index words of tile 1 (the gather of tile 0 is in flight)
+    if (kFp4) ent16_next = read_idx(1);
 
-    // running sums of p per head (ms.lsum) are accumulated tile by tile
-    if (quarter == 0) ms.lsum[32 * half + lane] = 0.f;
+    // running sum of p: this warp's share for head 32 * half + lane (its key rows), across
+    // tiles; the four warps of a head half are added once, after the last tile
+    float wsum = 0.f;
 
     for (int t = 0; t < ntiles; ++t) {
       const int sb = t & 1;
@@ -529,28 +535,23 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
         if (ok && wt == 0) waited_t = t;
         if (ok) {
           const bool row_ok = r_begin + t * kTK + e < r_end;
-          uint32_t nonfinite = 0u;
+          uint32_t mag = 0u;
           // bf16 -> fp16 in place; half 0 converts the first 36 pieces of row e, half 1 the rest
-          for (int g = 0; g < 5; ++g) {
-            const int c0 = g < 4 ? 2 * g : 8, nc = g < 4 ? 2 : 1;
-            for (int cc = 0; cc < nc; ++cc) {
-              const int c = c0 + cc;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                if ((c * 8 + j < 36) != (half == 0)) continue;
-                uint4* pp = reinterpret_cast<uint4*>(sC + cswz(c, e, j));
-                uint4 v = *pp;
-                v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
-                v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
-                nonfinite |= h2_nonfinite(v.x) | h2_nonfinite(v.y) | h2_nonfinite(v.z) | h2_nonfinite(v.w);
-                // rows past the window are zeroed: their p is 0, and 0 * NaN would not be
-                if (!row_ok) v = make_uint4(0, 0, 0, 0);
-                *pp = v;
-              }
-            }
+#pragma unroll 6
+          for (int k = 0; k < 36; ++k) {
+            const int pc = 36 * half + k;
+            uint4* pp = reinterpret_cast<uint4*>(sC + cswz(pc >> 3, e, pc & 7));
+            uint4 v = *pp;
+            mag = __vmaxu2(mag, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                         __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+            v.x = bf16x2_to_h2(v.x); v.y = bf16x2_to_h2(v.y);
+            v.z = bf16x2_to_h2(v.z); v.w = bf16x2_to_h2(v.w);
+            // rows past the window are zeroed: their p is 0, and 0 * NaN would not be
+            if (!row_ok) v = make_uint4(0, 0, 0, 0);
+            *pp = v;
           }
           // a window value outside the fp16 range
-          if (nonfinite && row_ok) atomicOr(status, CSA2_DEV_RANGE);
+          if (bf16_mag_beyond_fp16(mag) && row_ok) atomicOr(status, CSA2_DEV_RANGE);
           fence_proxy_async_smem();
           mbar_arrive(bar(kChunkFull));
           mbar_arrive(bar(kChunkFull + 1));
@@ -599,7 +600,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
             ms.alpha[h0 + lane] = mo == mn ? 1.f : exp2f(mo - mn);
           }
           named_sync(bid, 128);
-          if (quarter == 0) ms.lsum[h0 + lane] *= ms.alpha[h0 + lane];
+          wsum *= ms.alpha[h0 + lane];
           for (int i = 0; i < 8; ++i) {
             uint32_t r[16];
             const uint32_t ta = tmem + lane_off + kColO + 64 * (i >> 1) + 32 * half + 16 * (i & 1);
@@ -640,9 +641,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
           pf[h] = f2.x;
           pf[h + 1] = f2.y;
         }
-        reduce32<false, true>(pf, ms, ms.lsum, h0, lane, quarter, bid);
+        wsum += warp_reduce32<false>(pf, lane);
       }
     }
+    // the sums per head: the four warps of each head half
+    ms.red[quarter][32 * half + lane] = wsum;
+    named_sync(bid, 128);
+    if (quarter == 0)
+      ms.lsum[32 * half + lane] = (ms.red[0][32 * half + lane] + ms.red[1][32 * half + lane]) +
+                                  (ms.red[2][32 * half + lane] + ms.red[3][32 * half + lane]);
     if (kRows && wt == 0 && issued_t > waited_t) mbar_wait(bar(kTmaFull), issued_t & 1);
 
     // ---- wait for the last P.V, then the sums per head
@@ -798,9 +805,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     tc_fence_before();
     cluster_sync_all();
     tc_fence_after();
+    // split sp sends to sp+1, sp+2, .. (each owner gets one of its slices first)
     if (tid == 0)
-      for (int o = 0; o < (int)nsplit; ++o) {
-        if (o == sp) continue;
+      for (int k = 1; k < (int)nsplit; ++k) {
+        const int o = (sp + k) % (int)nsplit;
         const int k_st = (o - sp - 1 + (int)nsplit) % (int)nsplit;  // slot of this split at the owner
         asm volatile(
             "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

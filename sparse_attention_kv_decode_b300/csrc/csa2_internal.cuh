@@ -247,11 +247,11 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 __device__ __forceinline__ uint32_t bf16x2_to_h2(uint32_t v) {
   return pack_h2(bf16_lo(v), bf16_hi(v));
 }
-// Non-zero when either fp16 half of h2 is infinite or NaN (all-ones exponent): the
-// bf16 value it came from was outside the fp16 range (or not finite).
-__device__ __forceinline__ uint32_t h2_nonfinite(uint32_t h2) {
-  const uint32_t e = h2 & 0x7C007C00u;
-  return (uint32_t)((e & 0xFFFFu) == 0x7C00u) | (uint32_t)((e >> 16) == 0x7C00u);
+// mag holds, in each 16-bit half, the largest bf16 magnitude bits (value & 0x7FFF) seen:
+// true when one of them is above 65280 (0x477F, the largest bf16 value that fp16 holds),
+// i.e. an input that is outside the fp16 range or not finite (inf / NaN sort above).
+__device__ __forceinline__ bool bf16_mag_beyond_fp16(uint32_t mag) {
+  return (mag & 0xFFFFu) > 0x477Fu || (mag >> 16) > 0x477Fu;
 }
 
 // Quantise one 16-value block. Returns the 8 code bytes (as two u32) and the
