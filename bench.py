@@ -96,65 +96,93 @@ def aggregate_over_ranks(total_s: float, steps: int, world: int, device=None):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
-class OracleSample:
-    """The CPU oracle on one sequence of the workload, one layer at a time.
+# The FP4 cache exists before a decode step (written by the FULL layer's encode or the
+# appends), so encoding it is set-up: it runs in a spawn process pool, untimed. The timed
+# oracle work of a layer is the indexer and top-K (FULL, REINDEX), the dequantisation of
+# the selected entries, the sparse attention, the SWA branch and the merge, in the main
+# process (NumPy, float64; BLAS threads as configured).
+def _encode_rows_task(task):
+    """Spawn-pool task: FP4 codes / scales of rows [r0, r1) of a sequence's latent KV."""
+    name, layer, b, r0, r1 = task
+    from oracle import fp4
+    cfg = ci.CONFIGS[name]
+    X = ci.latent_rows(cfg, layer, b, np.arange(r0, r1))
+    return b, r0, fp4.encode(X)
 
-    Set-up (untimed) encodes the sequence's latent KV to FP4, as the cache exists
-    before a decode step; a timed layer runs the indexer and top-K (FULL,
-    REINDEX), dequantises the selected entries, and runs the sparse attention,
-    the SWA branch and the merge."""
 
-    def __init__(self, cfg, inp, b: int):
-        from oracle import fp4
-        self.cfg, self.inp, self.b = cfg, inp, b
-        X = ci.latent_rows(cfg, 0, b, np.arange(cfg.N))
-        self.codes, self.scales = fp4.encode(X)
-        self.prev = None
+_POOL = None
 
-    def layer_seconds(self, li: int) -> float:
-        from oracle import attention, fp4, indexer
-        cfg, b, L = self.cfg, self.b, self.inp.layers[li]
-        f64 = lambda a: ci.bf16_bits_to_f32(a).astype(np.float64)
-        t0 = time.perf_counter()
-        if L.mode != ci.REUSE:
-            I = indexer.scores(f64(L.q_idx[b]), L.w_idx[b], f64(L.z[b]))
-            idx = np.stack([indexer.topk(I[t], cfg.N, cfg.K) for t in range(cfg.T)])
-        else:
-            idx = self.prev
-        for t in range(cfg.T):
-            sel = idx[t][idx[t] >= 0]
-            rows = fp4.decode(self.codes[sel], self.scales[sel])
-            q = f64(L.q[b, t])
-            og, lg = attention.attend(q, rows, cfg.d_v, cfg.softmax_scale)
-            os_, ls = attention.swa_branch(q, f64(L.swa[b]), 0, cfg.W, cfg.d_v, cfg.softmax_scale)
-            attention.merge(og, lg, os_, ls)
-        self.prev = idx
-        return time.perf_counter() - t0
+
+def oracle_pool():
+    """Process pool (spawn: safe after CUDA was initialised) for the cache set-up."""
+    global _POOL
+    if _POOL is None:
+        import multiprocessing as mp
+        _POOL = mp.get_context("spawn").Pool(max(1, min(16, cpu_cores())))
+    return _POOL
+
+
+def oracle_caches(cfg, seqs, chunk=65536):
+    """FP4 cache (codes, scales) of the FULL layer for each sequence in seqs (set-up)."""
+    tasks = [(cfg.name, 0, b, r0, min(r0 + chunk, cfg.N)) for b in seqs for r0 in range(0, cfg.N, chunk)]
+    parts = {}
+    for b, r0, (c, sc) in oracle_pool().imap_unordered(_encode_rows_task, tasks):
+        parts.setdefault(b, []).append((r0, c, sc))
+    out = {}
+    for b, lst in parts.items():
+        lst.sort(key=lambda x: x[0])
+        out[b] = (np.concatenate([x[1] for x in lst]), np.concatenate([x[2] for x in lst]))
+    return out
+
+
+def oracle_layer_seconds(cfg, inp, li, b, cache, prev_idx=None, tokens=None):
+    """Timed oracle work of layer li for sequence b (query tokens `tokens`, default all).
+    Returns (seconds, idx [T', K]) where idx feeds a following REUSE layer."""
+    from oracle import attention, fp4, indexer
+    L = inp.layers[li]
+    codes, scales = cache
+    f64 = lambda a: ci.bf16_bits_to_f32(a).astype(np.float64)
+    ts = list(range(cfg.T)) if tokens is None else list(tokens)
+    t0 = time.perf_counter()
+    if L.mode != ci.REUSE:
+        I = indexer.scores(f64(L.q_idx[b][ts]), L.w_idx[b][ts], f64(L.z[b]))
+        idx = np.stack([indexer.topk(I[k], int(inp.n_visible[b * cfg.T + t]), cfg.K) for k, t in enumerate(ts)])
+    else:
+        idx = prev_idx
+    for k, t in enumerate(ts):
+        qi = b * cfg.T + t
+        sel = idx[k][idx[k] >= 0]
+        rows = fp4.decode(codes[sel], scales[sel])
+        q = f64(L.q[b, t])
+        og, lg = attention.attend(q, rows, cfg.d_v, cfg.softmax_scale)
+        os_, ls = attention.swa_branch(q, f64(L.swa[b]), int(inp.win_start[qi]), int(inp.win_len[qi]), cfg.d_v,
+                                       cfg.softmax_scale)
+        attention.merge(og, lg, os_, ls)
+    return time.perf_counter() - t0, idx
+
+
+def oracle_step_seconds(cfg, inp, caches, seqs=None, tokens=None):
+    """One oracle step: every layer of the group for every sequence in seqs (default all),
+    over the query tokens `tokens` (default all). Returns (seconds, per-layer seconds)."""
+    seqs = range(cfg.B) if seqs is None else seqs
+    per_layer = [0.0] * len(cfg.modes)
+    for b in seqs:
+        prev = None
+        for li in range(len(cfg.modes)):
+            dt, prev = oracle_layer_seconds(cfg, inp, li, b, caches[b], prev, tokens)
+            per_layer[li] += dt
+    return sum(per_layer), per_layer
 
 
 def cpu_cores() -> int:
     return len(os.sched_getaffinity(0))
 
 
-def oracle_step_seconds(cfg, inp, n_layer_samples: int, warmup: int = 0, seqs=(0, 1)):
-    """Mean oracle time per layer (by layer index) over rotating (sequence, layer) samples;
-    returns the extrapolated seconds of one full step (all layers, all sequences)."""
-    nl = len(cfg.modes)
-    samples = {i: [] for i in range(nl)}
-    k = 0
-    si = 0
-    while k < warmup + n_layer_samples:
-        smp = OracleSample(cfg, inp, seqs[si % len(seqs)])
-        si += 1
-        for li in range(nl):
-            t = smp.layer_seconds(li)
-            if k >= warmup:
-                samples[li].append(t)
-            k += 1
-            if k >= warmup + n_layer_samples and all(samples[j] for j in range(nl)):
-                break
-    per_layer = [statistics.mean(samples[li]) for li in range(nl)]
-    return sum(per_layer) * cfg.B, per_layer
+def blas_threads() -> str:
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return f"{k}={os.environ[k]}"
+    return "BLAS default (all cores)"
 
 
 def run_reference(args):
@@ -162,23 +190,97 @@ def run_reference(args):
     if rank != 0:
         return 0
     inp = ci.make_decode_inputs(CFG, with_x=False)
-    nl = len(CFG.modes)
-    step_s, per_layer = oracle_step_seconds(CFG, inp, max(args.steps, nl), warmup=args.warmup,
-                                            seqs=tuple(range(min(CFG.B, 4))))
+    wall0 = time.perf_counter()
+    caches = oracle_caches(CFG, range(CFG.B))
+    setup_s = time.perf_counter() - wall0
+    for _ in range(args.warmup):
+        oracle_step_seconds(CFG, inp, caches)
+    times, per_layer = [], None
+    for _ in range(args.steps):
+        dt, per_layer = oracle_step_seconds(CFG, inp, caches)
+        times.append(dt)
+    step_s = sum(times) / len(times)
     value = 1.0 / step_s
-    sample = (f"each step = one (sequence, layer) of the group, rotating over {nl} layers and 4 sequences; "
-              f"per-layer means {[round(x, 4) for x in per_layer]} s, summed and x{CFG.B} sequences")
+    sample = (f"every step is the full workload: {CFG.B} sequences x {len(CFG.modes)} layers (indexer, top-K, "
+              f"dequantisation of the selected entries, attention, SWA, merge), FP64 NumPy; last step's per-layer "
+              f"seconds {[round(x, 3) for x in per_layer]}; the FP4 caches ({CFG.B} x {CFG.N} entries) were encoded "
+              f"before timing ({setup_s:.1f} s in a {min(16, cpu_cores())}-process pool)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_block(),
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "blas": blas_threads()},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def cpu_baselines(bench_inp=None):
+    """The oracle timed on the host cores for every workload of the bench (a reported
+    baseline, not a target): the three decode workloads in full, the prefill chunk on 64
+    evenly spaced query tokens (first and last included) and the CED projection on 256
+    sampled rows x all 20 layers, both extrapolated linearly."""
+    out = {}
+    cores = cpu_cores()
+
+    def entry(value, unit, sample):
+        return {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample,
+                "blas": blas_threads()}
+
+    # 128K decode group: one full step
+    cfg = ci.DECODE_128K
+    inp = bench_inp if bench_inp is not None else ci.make_decode_inputs(cfg, with_x=False)
+    caches = oracle_caches(cfg, range(cfg.B))
+    step_s, per_layer = oracle_step_seconds(cfg, inp, caches)
+    out[cfg.name] = entry(1.0 / step_s, "steps/s",
+                          f"one full step: {cfg.B} sequences x {len(cfg.modes)} layers, per-layer seconds "
+                          f"{[round(x, 3) for x in per_layer]}; FP4 caches encoded before timing")
+    del caches
+    # tiny decode step: full, mean of 20 calls
+    cfg = ci.TINY
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    caches = oracle_caches(cfg, range(cfg.B))
+    ts = [oracle_step_seconds(cfg, inp, caches)[0] for _ in range(20)]
+    out[cfg.name] = entry(statistics.mean(ts) * 1e6, "us/call", "the full tiny step (one FULL layer), mean of 20")
+    # 1M decode: full
+    cfg = ci.DECODE_1M
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    caches = oracle_caches(cfg, range(cfg.B))
+    step_s, _ = oracle_step_seconds(cfg, inp, caches)
+    out[cfg.name] = entry(1.0 / step_s, "calls/s", f"the full call: {cfg.B} sequences x {cfg.N} entries")
+    del caches, inp
+    # prefill chunk: 64 evenly spaced tokens, extrapolated to 4096
+    cfg = ci.PREFILL_CHUNK
+    inp = ci.make_decode_inputs(cfg, with_x=False)
+    caches = oracle_caches(cfg, range(cfg.B))
+    toks = sorted(set(np.linspace(0, cfg.T - 1, 64).round().astype(int).tolist()))
+    dt, _ = oracle_step_seconds(cfg, inp, caches, tokens=toks)
+    call_s = dt / len(toks) * cfg.T
+    flop = 2.0 * cfg.T * cfg.H * (cfg.K + cfg.W) * (576 + cfg.d_v) + 2.0 * cfg.T * cfg.N * cfg.H_I * 64
+    out[cfg.name] = entry(1.0 / call_s, "calls/s",
+                          f"{len(toks)} evenly spaced query tokens of {cfg.T} ({dt:.2f} s), extrapolated x"
+                          f"{cfg.T / len(toks):.0f}; {flop / call_s / 1e12:.6f} TFLOP/s")
+    del caches, inp
+    # CED projection: 256 sampled rows x 20 layers, extrapolated to 32768 rows
+    from oracle import ced
+    cc = ci.CED_PROJ
+    cin = ci.make_ced_inputs(cc)
+    rows = np.linspace(0, cc.rows - 1, 256).round().astype(int)
+    f32 = lambda a: ci.bf16_bits_to_f32(a)
+    Hs = f32(cin.H[rows])
+    t0 = time.perf_counter()
+    for l in range(cc.n_layers):
+        ced.project_and_encode(Hs, f32(cin.W_kv[l]), f32(cin.W_z[l]))
+    dt = time.perf_counter() - t0
+    full_s = dt * cc.rows / len(rows)
+    flops = 2.0 * cc.rows * cc.d_model * cc.n_layers * (576 + 64)
+    out[cc.name] = entry(flops / full_s / 1e12, "TFLOP/s",
+                         f"256 evenly spaced rows x {cc.n_layers} layers ({dt:.2f} s: FP64 products, fp32 rounding, "
+                         f"FP4 encode of C, bf16 of Z), extrapolated x{cc.rows // 256} to {cc.rows} rows")
+    return out
 
 
 def config_block():
@@ -501,12 +603,16 @@ def run_ours(args):
     e2e = None if args.no_e2e else run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs,
                                            ws, world, dev)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        step_s, per_layer = oracle_step_seconds(cfg, inp, 2 * len(cfg.modes), seqs=(0, 1))
-        cpu = {"value": 1.0 / step_s, "unit": "steps/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"2 of {cfg.B} sequences x {len(cfg.modes)} layers (indexer, top-K, dequant of the "
-                         f"selected entries, attention, SWA, merge), extrapolated x{cfg.B}; per-layer means "
-                         f"{[round(x, 4) for x in per_layer]} s"}
+    if rank == 0 and not args.no_cpu_baseline:
+        inp.layers[0].X = None
+        baselines = cpu_baselines(inp)
+        cpu = baselines.pop(cfg.name)
+        if others is not None and "error" not in others:
+            for name, row in others.items():
+                if name in baselines:
+                    row["cpu_baseline"] = baselines[name]
+        if ced is not None and "error" not in ced:
+            ced["cpu_baseline"] = baselines.get(ci.CED_PROJ.name)
 
     n_launch = sum(launches_per_call[k] for _, k, _ in calls) * args.steps
     if rank == 0:
@@ -745,10 +851,12 @@ def run_step_variants(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, w
 
 def run_other_configs(args, torch, csa2, dev, peaks, flush):
     """The other decode workloads, one csa2_decode_layer(FULL) call each as a CUDA graph
-    (inputs resident, L2 flushed between replays): 4 sequences at 1M tokens (262,144
-    entries), reported against HBM (keys + selected entries + window), and a 4096-token
-    prefill chunk over 32,768 entries (causal), reported in TFLOP/s (attention over the
-    selected entries and the window, plus the indexer, as stated for that workload)."""
+    (inputs resident, L2 flushed between replays): the tiny step (one sequence, 1024
+    entries, 16 heads, K = 128; reported in microseconds per call), 4 sequences at 1M
+    tokens (262,144 entries), reported against HBM (keys + selected entries + window), and a
+    4096-token prefill chunk over 32,768 entries (causal), reported in TFLOP/s (attention
+    over the selected entries and the window, plus the indexer, as stated for that
+    workload)."""
     out = {}
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
@@ -756,7 +864,8 @@ def run_other_configs(args, torch, csa2, dev, peaks, flush):
     P = lambda t: t.data_ptr() if t is not None else None
     b16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
     t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-    for cfg, steps in ((ci.DECODE_1M, min(args.steps, 200)), (ci.PREFILL_CHUNK, min(args.steps, 20))):
+    for cfg, steps in ((ci.TINY, min(args.steps, 200)), (ci.DECODE_1M, min(args.steps, 200)),
+                       (ci.PREFILL_CHUNK, min(args.steps, 20))):
         inp = ci.make_decode_inputs(cfg)
         Lr = inp.layers[0]
         X = t32(Lr.X)
@@ -933,7 +1042,7 @@ def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bu
     for i in range(max(3, args.warmup // 4)):
         step(i)
     torch.cuda.synchronize(dev)
-    n = max(10, args.steps // 10)
+    n = max(200, args.steps // 10)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     # the timed region starts before the first upload and ends after the last download
@@ -972,9 +1081,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
-        return run_reference(args)
-    return run_ours(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args)
+        return run_ours(args)
+    finally:
+        if _POOL is not None:
+            _POOL.terminate()
 
 
 if __name__ == "__main__":

@@ -430,16 +430,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     uint4 cw[9];       // pieces [2g + k] (g < 4, k: row ra / rb) and [8] (group 4)
     uint32_t sw[5];    // their scale byte pairs: [g] = row ra | row rb << 16, [4] group 4
     int ent16 = -1, ent16_next = -1;  // entry of row 16w + lane (lanes < 16), this / next tile
-    auto read_idx = [&](int tf) -> int {  // tf: FP4 tile
+    // the index word of row 16w + lane of FP4 tile tf (checked when fetch uses it, so the
+    // load is not waited for here)
+    auto read_idx = [&](int tf) -> int {
       const int p = p_begin + tf * kTK + 16 * warp + lane;
-      int v = (lane < 16 && tf < nt_f && p < p_end) ? idx_row[p] : -1;
-      if (v < -1 || v >= fsrc.n_stride) {
-        atomicOr(status, CSA2_DEV_BAD_INDEX);
-        v = -1;
-      }
-      return v;
+      return (lane < 16 && tf < nt_f && p < p_end) ? idx_row[p] : -1;
     };
     auto fetch = [&](int e16) {
+      if (e16 < -1 || e16 >= fsrc.n_stride) {
+        atomicOr(status, CSA2_DEV_BAD_INDEX);
+        e16 = -1;
+      }
       ent16 = e16;
       const int ea = __shfl_sync(0xffffffffu, e16, lane >> 2);
       const int eb = __shfl_sync(0xffffffffu, e16, 8 + (lane >> 2));
