@@ -209,78 +209,18 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
 }
 
 // ---------------------------------------------------------------------------
-// Top-K selection: one cluster of C CTAs per query
+// Top-K selection: shared pieces
 // ---------------------------------------------------------------------------
-// CTA r of the cluster owns the visible entries [r*slice, (r+1)*slice) (slice a
-// multiple of 4) and lands their scores in shared memory with one bulk copy.
-// Every exchange is a push: before a cluster barrier each CTA writes its record
-// into slot r of every peer's receive buffer (distributed shared memory stores,
-// no remote loads), so after the barrier all reads are local and no CTA touches
-// a peer once it has passed the last barrier.
-//
-// Fast path (two barriers). The scoring kernel left the query's score range
-// [lo, hi] in the workspace; each CTA bins its scores into kNB monotone bins of
-// that range and pushes the 16-bit histogram. After the barrier every CTA knows
-// all histograms, hence the bin b* holding the K-th score, how many entries each
-// CTA has above it, and how many candidates (bin b*) each CTA holds. If they are
-// at most kCandCap, each CTA pushes its candidates; after the second barrier
-// every CTA ranks all candidates by (score desc, index asc), so it knows how
-// many each CTA contributes, i.e. its own output offset, with no further
-// exchange.
-// General path (range missing, or too many candidates in b*): rounds of
-//   round 0  min / max / count of the surviving candidates (+ the candidate
-//            list itself when small enough) -> every CTA knows the range
-//   round 1  histogram of the candidates over kNB monotone bins of that range
-//            -> the bin b* holding the K-th score: higher bins are selected,
-//            lower ones dropped; repeat from round 0 on the bin-b* survivors
-//   exact    when at most kCandCap candidates survive, each CTA ranks its own
-//            candidates against all of them by (score desc, index asc);
-//            when they all tie, the lowest indices win
-//   output   selected counts are pushed, each CTA writes its selected indices
-//            at its prefix offset (ascending by construction).
-// The bin map floor((s - lo) * kNB / (hi - lo)) (clamped) is monotone in s, so
-// bins never reorder scores; equal scores always share a bin.
+// Every selection kernel bins scores into monotone bins (equal scores share a bin,
+// bins never reorder scores), finds the bin b* holding the K-th score from the top,
+// takes the higher bins and refines b* until at most a rank-able handful remains;
+// the output lists the selected positions in ascending order.
 constexpr int kSelThreads = 1024;
-constexpr int kNBMax = 2048;        // histogram bins per refinement round (small clusters)
-constexpr int kNBMin = 1024;        // (clusters of more than 4 CTAs)
-constexpr int kCandCap = 512;       // candidates resolved exactly by ranking
 constexpr int kMaxLevels = 12;
 constexpr int kMaxCluster = 16;
 constexpr size_t kSelSmemMax = 200 * 1024;
 
-struct SelRec {
-  float lo, hi;
-  int cnt, pad;
-};
-
-struct SelShared {
-  SelRec rec_in[kMaxCluster];           // pushed candidate statistics
-  int sel_in[kMaxCluster];              // pushed selected counts
-  int above_r[kMaxCluster];             // entries above b* per CTA (fast path, pushed)
-  int cand_sel[kMaxCluster];            // selected candidates per CTA (fast path)
-  uint32_t hist_local[kNBMax];
-  int scan[kSelThreads / 32];
-  float red_f[2][kSelThreads / 32];
-  int red_i[kSelThreads / 32];
-  int bstar, above, cand_n, my_above;
-  uint64_t bar_load;
-  float cand_s[kCandCap];               // own candidates (compacted)
-  int cand_i[kCandCap];
-};
-// Regions after the header start at a 128-byte boundary (the histogram pushes
-// are 16-byte vector stores).
-constexpr size_t kSelHdr = (sizeof(SelShared) + 127) & ~size_t(127);
-// followed in dynamic shared memory by: uint16_t hist_in[C][NB] (pushed histograms),
-// float cand_in_s[C][kCandCap], int cand_in_i[C][kCandCap], float sc[slice_cap],
-// uint8_t state[slice_cap]
-
-__device__ __forceinline__ int bin_of(float s, float lo, float scl, int nb) {
-  float t = (s - lo) * scl;
-  int bi = (int)t;
-  return bi < 0 ? 0 : (bi > nb - 1 ? nb - 1 : bi);
-}
-
-// Block-wide exclusive scan of one int per thread; returns the prefix, writes the total.
+// Exclusive prefix sum of v over the block (1024 threads); total = the sum.
 __device__ __forceinline__ int block_excl_scan(int v, int* scan, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -392,454 +332,6 @@ __device__ __forceinline__ void st_remote_v4(void* local_addr, int rank, uint4 v
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
-}
-
-// Histogram of this CTA's surviving candidates over [lo, hi] into sh.hist_local,
-// pushed as 16-bit counts into slot r of every peer's hist_in.
-__device__ __forceinline__ void build_push_hist(SelShared& sh, uint16_t* hist_in, const float* sc,
-                                                const uint8_t* state, int my_len, float lo, float scl,
-                                                int NB, uint32_t C, uint32_t r) {
-  const int tid = threadIdx.x;
-  for (int i = tid; i < NB; i += kSelThreads) sh.hist_local[i] = 0u;
-  __syncthreads();
-  // loads first, 8 per thread in flight, then the atomics
-  for (int e0 = tid; e0 < my_len; e0 += 8 * kSelThreads) {
-    float v[8];
-    uint8_t s[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int e = e0 + k * kSelThreads;
-      v[k] = e < my_len ? sc[e] : 0.f;
-      s[k] = e < my_len ? state[e] : 1;
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (s[k] == 0) atomicAdd(&sh.hist_local[bin_of(v[k], lo, scl, NB)], 1u);
-  }
-  __syncthreads();
-  for (int j = tid; j < (int)C * (NB / 8); j += kSelThreads) {
-    const int peer = j / (NB / 8), o8 = j % (NB / 8);
-    const uint32_t* h = &sh.hist_local[8 * o8];
-    const uint4 v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                               h[6] | (h[7] << 16));
-    st_remote_v4(&hist_in[r * NB + 8 * o8], peer, v);
-  }
-}
-
-// Suffix counts of the summed histograms: the bin b* with above < remaining <=
-// above + count(b*) goes to sh.bstar / sh.above (thread t owns bins from the top).
-__device__ __forceinline__ void find_bstar(SelShared& sh, const uint16_t* hist_in, int NB, uint32_t C,
-                                           int remaining) {
-  const int tid = threadIdx.x;
-  const int per = NB / kSelThreads;
-  const int btop = NB - 1 - per * tid;
-  uint32_t hs[kNBMax / kSelThreads];
-  int mine = 0;
-#pragma unroll
-  for (int k = 0; k < kNBMax / kSelThreads; ++k) {
-    uint32_t h = 0;
-    if (k < per)
-      for (int rr = 0; rr < (int)C; ++rr) h += hist_in[rr * NB + btop - k];
-    hs[k] = h;
-    mine += (int)h;
-  }
-  int total;
-  int above = block_excl_scan(mine, sh.scan, total);
-#pragma unroll
-  for (int k = 0; k < kNBMax / kSelThreads; ++k) {
-    if (k < per) {
-      const int h = (int)hs[k];
-      if (above < remaining && remaining <= above + h) {
-        sh.bstar = btop - k;
-        sh.above = above;
-      }
-      above += h;
-    }
-  }
-  __syncthreads();
-}
-
-// One round of the general path: min / max / count of this CTA's surviving
-// candidates (and the candidates themselves when few) pushed to every peer,
-// then a cluster barrier. Returns the cluster-wide range and count, and the
-// number of survivors in lower-ranked CTAs.
-__device__ __noinline__ void stats_round(SelShared& sh, float* cand_in_s, int* cand_in_i, const float* sc,
-                                         const uint8_t* state, int my0, int my_len, uint32_t C, uint32_t r,
-                                         float& glo, float& ghi, int& gcnt, int& pre_cnt, int& mine_cnt) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float lo = INFINITY, hi = -INFINITY;
-  int cnt = 0;
-  for (int e = tid; e < my_len; e += kSelThreads)
-    if (state[e] == 0) {
-      const float v = sc[e];
-      lo = fminf(lo, v);
-      hi = fmaxf(hi, v);
-      ++cnt;
-    }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-  }
-  if (lane == 0) {
-    sh.red_f[0][warp] = lo;
-    sh.red_f[1][warp] = hi;
-    sh.red_i[warp] = cnt;
-  }
-  if (tid == 0) sh.cand_n = 0;
-  __syncthreads();
-  lo = INFINITY; hi = -INFINITY; cnt = 0;
-#pragma unroll 1
-  for (int w = 0; w < kSelThreads / 32; ++w) {
-    lo = fminf(lo, sh.red_f[0][w]);
-    hi = fmaxf(hi, sh.red_f[1][w]);
-    cnt += sh.red_i[w];
-  }
-  mine_cnt = cnt;
-  if (cnt <= kCandCap) {
-    for (int e = tid; e < my_len; e += kSelThreads)
-      if (state[e] == 0) {
-        const int p = atomicAdd(&sh.cand_n, 1);
-        sh.cand_s[p] = sc[e];
-        sh.cand_i[p] = my0 + e;
-      }
-  }
-  __syncthreads();
-  if (tid < (int)C)
-    st_remote_v4(&sh.rec_in[r], tid, make_uint4(__float_as_uint(lo), __float_as_uint(hi), (uint32_t)cnt, 0u));
-  if (cnt <= kCandCap) {
-    for (int j = tid; j < (int)C * cnt; j += kSelThreads) {
-      const int peer = j / cnt, k = j % cnt;
-      st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_s[r * kCandCap + k]), peer, __float_as_uint(sh.cand_s[k]));
-      st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_i[r * kCandCap + k]), peer, (uint32_t)sh.cand_i[k]);
-    }
-  }
-  cluster_barrier();
-  glo = INFINITY; ghi = -INFINITY; gcnt = 0; pre_cnt = 0;
-#pragma unroll 1
-  for (int rr = 0; rr < (int)C; ++rr) {
-    const SelRec v = sh.rec_in[rr];
-    if (v.cnt > 0) {
-      glo = fminf(glo, v.lo);
-      ghi = fmaxf(ghi, v.hi);
-    }
-    if (rr < (int)r) pre_cnt += v.cnt;
-    gcnt += v.cnt;
-  }
-}
-
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
-    const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ n_visible,
-    int64_t n_stride, int K, int slice_cap, uint32_t* __restrict__ range, int32_t* __restrict__ out_idx,
-    float* __restrict__ out_scores, uint32_t* __restrict__ status, const uint8_t* __restrict__ pf_codes,
-    const uint8_t* __restrict__ pf_scales, int T, int64_t kv_stride, const int32_t* __restrict__ pool,
-    int pool_stride) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
-  uint32_t C, r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  const int NB = C <= 4 ? kNBMax : kNBMin;
-  uint16_t* hist_in = reinterpret_cast<uint16_t*>(smem_raw + kSelHdr);
-  float* cand_in_s = reinterpret_cast<float*>(hist_in + C * NB);
-  int* cand_in_i = reinterpret_cast<int*>(cand_in_s + C * kCandCap);
-  float* sc = reinterpret_cast<float*>(cand_in_i + C * kCandCap);
-  uint8_t* state = reinterpret_cast<uint8_t*>(sc + slice_cap);
-
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int qi = blockIdx.y;
-  if (tid == 0) {
-    mbar_init(smem_u32(&sh.bar_load), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  int nvis = n_visible[qi];
-  nvis = nvis < 0 ? 0 : (nvis > n_stride ? (int)n_stride : nvis);
-  const int slice = (((nvis + (int)C - 1) / (int)C) + 3) & ~3;
-  const int my0 = (int)r * slice;
-  int my_len = nvis - my0;
-  my_len = my_len < 0 ? 0 : (my_len > slice ? slice : my_len);
-  const int need = nvis < K ? nvis : K;
-  int32_t* out = out_idx + (int64_t)qi * K;
-  float* outs = out_scores ? out_scores + (int64_t)qi * K : nullptr;
-
-  // this CTA's scores: one bulk copy (16-byte aligned start, length rounded up to 16 bytes)
-  bool loaded = true;
-  if (my_len > 0) {
-    const uint32_t bytes = (uint32_t)(((my_len + 3) & ~3) * 4);
-    if (tid == 0) {
-      mbar_arrive_expect_tx(smem_u32(&sh.bar_load), bytes);
-      bulk_g2s(smem_u32(sc), scores + (int64_t)qi * score_stride + my0, bytes, smem_u32(&sh.bar_load));
-    }
-    loaded = mbar_wait(smem_u32(&sh.bar_load), 0);
-  }
-  // the score range left by the scoring kernel (read by every CTA before the first barrier)
-  const uint32_t kminv = range[2 * qi], kmax = range[2 * qi + 1];
-  const float rlo = key2f(~kminv), rhi = key2f(kmax);
-  const bool have_range = kmax != 0u && rlo < rhi && isfinite(rlo) && isfinite(rhi);
-  if (!__syncthreads_and(loaded)) {
-    if (tid == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
-    my_len = 0;  // score nothing; the selection below still completes
-  }
-  const uint8_t init = nvis <= K ? 1 : 0;
-  for (int e = tid; e < my_len; e += kSelThreads) state[e] = init;
-  if (tid < kMaxCluster) {
-    sh.above_r[tid] = 0;
-    sh.cand_sel[tid] = 0;
-  }
-  if (tid == 0) sh.my_above = 0;
-  __syncthreads();
-
-  bool settled = false;     // output offsets known without the final exchange
-  int off_fast = 0, total_fast = 0;
-  if (nvis <= K) {
-    // everything visible is selected: CTA r's offset is the visible entries before its slice
-    settled = true;
-    off_fast = my0 < nvis ? my0 : nvis;
-    total_fast = nvis;
-    if (r == 0 && tid == 0) {
-      range[2 * qi] = 0u;
-      range[2 * qi + 1] = 0u;
-    }
-  } else {
-    int rem = need;
-    int level = 0;
-    bool done = false;
-    if (have_range) {
-      // ---- fast path: histogram of the known range, then the b* candidates
-      const float scl = (float)NB / (rhi - rlo);
-      build_push_hist(sh, hist_in, sc, state, my_len, rlo, scl, NB, C, r);
-      cluster_barrier();
-      if (r == 0 && tid == 0) {
-        range[2 * qi] = 0u;
-        range[2 * qi + 1] = 0u;
-      }
-      find_bstar(sh, hist_in, NB, C, rem);
-      const int bstar = sh.bstar;
-      rem -= sh.above;
-      level = 1;
-      int cand_tot = 0;
-#pragma unroll 1
-      for (int rr = 0; rr < (int)C; ++rr) cand_tot += hist_in[rr * NB + bstar];
-      if (tid == 0) sh.cand_n = 0;
-      __syncthreads();
-      // classify (all entries are candidates at this point), count the ones above b*
-      // and collect the b* ones
-      int n_above = 0;
-      for (int e0 = tid; e0 < my_len; e0 += 8 * kSelThreads) {
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int e = e0 + k * kSelThreads;
-          v[k] = e < my_len ? sc[e] : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int e = e0 + k * kSelThreads;
-          if (e < my_len) {
-            const int bi = bin_of(v[k], rlo, scl, NB);
-            state[e] = bi > bstar ? 1 : (bi < bstar ? 2 : 0);
-            n_above += bi > bstar;
-            if (bi == bstar && cand_tot <= kCandCap) {
-              const int p = atomicAdd(&sh.cand_n, 1);
-              sh.cand_s[p] = v[k];
-              sh.cand_i[p] = my0 + e;
-            }
-          }
-        }
-      }
-      n_above = __reduce_add_sync(0xffffffffu, n_above);
-      if (lane == 0 && n_above) atomicAdd(&sh.my_above, n_above);
-      __syncthreads();
-      if (cand_tot <= kCandCap) {
-        // push own candidates (their number, hist_in[r][b*], is known to every peer)
-        // and own count above b*
-        if (tid < (int)C) st_remote_u32(reinterpret_cast<uint32_t*>(&sh.above_r[r]), tid, (uint32_t)sh.my_above);
-        const int mine = sh.cand_n;
-        for (int j = tid; j < (int)C * mine; j += kSelThreads) {
-          const int peer = j / mine, k = j % mine;
-          st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_s[r * kCandCap + k]), peer,
-                        __float_as_uint(sh.cand_s[k]));
-          st_remote_u32(reinterpret_cast<uint32_t*>(&cand_in_i[r * kCandCap + k]), peer, (uint32_t)sh.cand_i[k]);
-        }
-        cluster_barrier();
-        // rank every candidate of every CTA (one warp per candidate, the lanes split
-        // the comparisons): own ones set the state, all of them the per-CTA counts
-        {
-          int cnt_r[kMaxCluster];
-          int tot = 0;
-#pragma unroll 1
-          for (int rr = 0; rr < (int)C; ++rr) {
-            cnt_r[rr] = hist_in[rr * NB + bstar];
-            tot += cnt_r[rr];
-          }
-          const int warp = tid >> 5;
-          for (int j = warp; j < tot; j += kSelThreads / 32) {
-            int rr = 0, k = j;
-            while (k >= cnt_r[rr]) { k -= cnt_r[rr]; ++rr; }
-            const float s = cand_in_s[rr * kCandCap + k];
-            const int i = cand_in_i[rr * kCandCap + k];
-            int rank = 0;
-            for (int c = lane; c < tot; c += 32) {
-              int r2 = 0, k2 = c;
-              while (k2 >= cnt_r[r2]) { k2 -= cnt_r[r2]; ++r2; }
-              const float t = cand_in_s[r2 * kCandCap + k2];
-              const int ti = cand_in_i[r2 * kCandCap + k2];
-              rank += (t > s) || (t == s && ti < i);
-            }
-            rank = __reduce_add_sync(0xffffffffu, rank);
-            if (lane == 0) {
-              const bool take = rank < rem;
-              if (take) atomicAdd(&sh.cand_sel[rr], 1);
-              if (rr == (int)r) state[i - my0] = take ? 1 : 2;
-            }
-          }
-        }
-        __syncthreads();
-#pragma unroll 1
-        for (int rr = 0; rr < (int)C; ++rr) {
-          const int v = sh.above_r[rr] + sh.cand_sel[rr];
-          if (rr < (int)r) off_fast += v;
-          total_fast += v;
-        }
-        settled = true;
-        done = true;
-      }
-    }
-    // ---- general path (no usable range, or too many candidates in b*)
-    while (!done) {
-      float glo, ghi;
-      int gcnt, pre_cnt, mine_cnt;
-      stats_round(sh, cand_in_s, cand_in_i, sc, state, my0, my_len, C, r, glo, ghi, gcnt, pre_cnt, mine_cnt);
-      if (level == 0 && r == 0 && tid == 0) {
-        range[2 * qi] = 0u;
-        range[2 * qi + 1] = 0u;
-      }
-      if (rem >= gcnt) {
-        for (int e = tid; e < my_len; e += kSelThreads)
-          if (state[e] == 0) state[e] = 1;
-        break;
-      }
-      if (gcnt <= kCandCap) {
-        for (int j = tid; j < mine_cnt; j += kSelThreads) {
-          const float s = sh.cand_s[j];
-          const int i = sh.cand_i[j];
-          int rank = 0;
-#pragma unroll 1
-          for (int rr = 0; rr < (int)C; ++rr) {
-            const int n = sh.rec_in[rr].cnt;
-            const float* cs = cand_in_s + rr * kCandCap;
-            const int* ci = cand_in_i + rr * kCandCap;
-            for (int c = 0; c < n; ++c) {
-              const float t = cs[c];
-              rank += (t > s) || (t == s && ci[c] < i);
-            }
-          }
-          state[i - my0] = rank < rem ? 1 : 2;
-        }
-        break;
-      }
-      if (glo == ghi || level == kMaxLevels - 1) {
-        // all candidates tie (or refinement did not settle): lowest indices first
-        if (glo != ghi && tid == 0) atomicOr(status, CSA2_DEV_TOPK_LEVELS);
-        const int chunk = (my_len + kSelThreads - 1) / kSelThreads;
-        const int e0 = tid * chunk, e1 = min(e0 + chunk, my_len);
-        int c = 0;
-        for (int e = e0; e < e1; ++e) c += state[e] == 0;
-        int total;
-        int ord = block_excl_scan(c, sh.scan, total) + pre_cnt;
-        for (int e = e0; e < e1; ++e)
-          if (state[e] == 0) {
-            state[e] = ord < rem ? 1 : 2;
-            ++ord;
-          }
-        break;
-      }
-      const float scl2 = (float)NB / (ghi - glo);
-      build_push_hist(sh, hist_in, sc, state, my_len, glo, scl2, NB, C, r);
-      cluster_barrier();
-      find_bstar(sh, hist_in, NB, C, rem);
-      const int bs = sh.bstar;
-      rem -= sh.above;
-      for (int e = tid; e < my_len; e += kSelThreads)
-        if (state[e] == 0) {
-          const int bi = bin_of(sc[e], glo, scl2, NB);
-          state[e] = bi > bs ? 1 : (bi < bs ? 2 : 0);
-        }
-      __syncthreads();
-      ++level;
-    }
-    __syncthreads();
-  }
-
-  // ---- ordered output: warp w owns a contiguous run of entries, compacted 32 at a time
-  // with ballots (a count pass, one scan of the 32 warp counts, a write pass)
-  const int warp = tid >> 5;
-  constexpr int kWarps = kSelThreads / 32;
-  const int per_warp = ((my_len + kWarps - 1) / kWarps + 31) & ~31;
-  const int wb = warp * per_warp, we = min(wb + per_warp, my_len);
-  int wc = 0;
-  for (int e0 = wb; e0 < we; e0 += 32) {
-    const int e = e0 + lane;
-    wc += __popc(__ballot_sync(0xffffffffu, e < we && state[e] == 1));
-  }
-  __syncthreads();   // sh.scan is free (any earlier use is complete)
-  if (lane == 0) sh.scan[warp] = wc;
-  __syncthreads();
-  const int wcnt = sh.scan[lane];
-  int incl = wcnt;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += t;
-  }
-  const int my_sel = __shfl_sync(0xffffffffu, incl, 31);
-  int pos = __shfl_sync(0xffffffffu, incl - wcnt, warp);
-  int offset = off_fast, total_sel = total_fast;
-  if (!settled) {
-    if (tid < (int)C) st_remote_u32(reinterpret_cast<uint32_t*>(&sh.sel_in[r]), tid, (uint32_t)my_sel);
-    cluster_barrier();
-    offset = 0;
-    total_sel = 0;
-#pragma unroll 1
-    for (int rr = 0; rr < (int)C; ++rr) {
-      const int v = sh.sel_in[rr];
-      if (rr < (int)r) offset += v;
-      total_sel += v;
-    }
-  }
-  pos += offset;
-  // the FP4 rows of the selected entries are requested into L2 for the attention that
-  // gathers them next
-  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * kv_stride * CSA2_CODE_BYTES : nullptr;
-  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * kv_stride * CSA2_SCALE_BYTES : nullptr;
-  // with a candidate pool the positions are the pool's: position j is entry
-  // block[j / 8] * 8 + j % 8
-  const int32_t* pblk = pool ? pool + (int64_t)qi * pool_stride : nullptr;
-  for (int e0 = wb; e0 < we; e0 += 32) {
-    const int e = e0 + lane;
-    const bool take = e < we && state[e] == 1;
-    const uint32_t bal = __ballot_sync(0xffffffffu, take);
-    const int p = pos + __popc(bal & ((1u << lane) - 1u));
-    if (take && p < K) {
-      const int ent = pblk ? pblk[(my0 + e) >> 3] * 8 + ((my0 + e) & 7) : my0 + e;
-      out[p] = ent;
-      if (outs) outs[p] = sc[e];
-      if (pfc && ent >= 0 && ent < kv_stride) {
-        prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
-        prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES);
-        prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES + CSA2_SCALE_BYTES - 1);
-      }
-    }
-    pos += __popc(bal);
-  }
-  if (r == C - 1)
-    for (int p = total_sel + tid; p < K; p += kSelThreads) {
-      out[p] = -1;
-      if (outs) outs[p] = __int_as_float(0x7fc00000);
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1157,6 +649,422 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_row_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Top-K selection, one cluster of C CTAs per query (few queries, long score rows)
+// ---------------------------------------------------------------------------
+// CTA r owns the positions [r*slice, (r+1)*slice) (slice a multiple of 32, so the CTAs'
+// bitmap words do not overlap), lands their scores in shared memory with a few bulk
+// copies, and visits local positions k * kRowThreads + t. Every exchange is a push into
+// the peers' receive buffers followed by one cluster barrier, and every decision after it
+// is taken from the same pushed data, so all CTAs follow the same path:
+//   round 0  local histogram over the range the scoring kernel left (kRowBins monotone
+//            bins, row_bin), pushed as 16-bit counts; after the barrier every CTA sums
+//            them: b* (the K-th score's bin), the scores above it and every CTA's share
+//            of them and of b* follow; local positions above b* are selected, b*'s stay
+//            in play (bitmap words built with ballots);
+//   exact    when at most kRowRankCap scores remain in play, each CTA pushes its
+//            (score, position) list; after the barrier every CTA ranks all of them by
+//            (score desc, position asc), so it knows every CTA's selected count;
+//   refine   otherwise the scores in play are binned by their integer keys over the
+//            cluster-wide key range (one barrier for the range, one for the histogram);
+//            when they all tie, the lowest positions win.
+// A CTA's output offset is the number selected in the CTAs before it.
+struct ClusterShared {
+  uint32_t hist[kRowBins];
+  uint32_t selw[kRowThreads / 2];    // selected bitmap (slices of at most 16384)
+  uint32_t candw[kRowThreads / 2];   // in-play bitmap
+  int scan[kRowThreads / 32];
+  float red[2][kRowThreads / 32];
+  uint4 rec_in[kMaxCluster];         // pushed (min, max, count) of each CTA
+  int cta_sel[kMaxCluster];          // selected positions of each CTA so far
+  int cta_play[kMaxCluster];         // positions in play of each CTA
+  int cta_taken[kMaxCluster];        // ranked and taken in the exact round
+  int bstar, above;
+  uint32_t rng[2];
+  uint64_t bar_load;
+};
+
+// Block-wide min of a and max of b (all threads get them).
+__device__ __forceinline__ void block_minmax(float& a, float& b, float (&red)[2][kRowThreads / 32]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+  __syncthreads();   // red may still be read by a previous call
+  if (lane == 0) {
+    red[0][warp] = a;
+    red[1][warp] = b;
+  }
+  __syncthreads();
+  a = red[0][lane];
+  b = red[1][lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+  }
+}
+
+// Push this CTA's histogram (sh.hist, as 16-bit counts) into slot r of every peer's hist_in.
+__device__ __forceinline__ void push_hist(ClusterShared& sh, uint16_t* hist_in, uint32_t C, uint32_t r) {
+  for (int j = threadIdx.x; j < (int)C * (kRowBins / 8); j += kRowThreads) {
+    const int peer = j / (kRowBins / 8), o8 = j % (kRowBins / 8);
+    const uint32_t* h = &sh.hist[8 * o8];
+    st_remote_v4(&hist_in[r * kRowBins + 8 * o8], peer,
+                 make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16)));
+  }
+}
+
+// From the C pushed histograms: b* and the count above it for the rem-th largest
+// (sh.bstar, sh.above), and for every CTA its count above b* (added to sh.cta_sel) and in
+// b* (sh.cta_play). Returns the total in b*.
+__device__ __forceinline__ int cluster_bstar(ClusterShared& sh, const uint16_t* hist_in, uint32_t C, int rem) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int b1 = kRowBins - 1 - 2 * tid, b0 = b1 - 1;
+  int h1 = 0, h0 = 0;
+  for (uint32_t rr = 0; rr < C; ++rr) {
+    h1 += hist_in[rr * kRowBins + b1];
+    h0 += hist_in[rr * kRowBins + b0];
+  }
+  int total;
+  const int above = block_excl_scan(h1 + h0, sh.scan, total);
+  if (above < rem && rem <= above + h1) {
+    sh.bstar = b1;
+    sh.above = above;
+  } else if (above + h1 < rem && rem <= above + h1 + h0) {
+    sh.bstar = b0;
+    sh.above = above + h1;
+  }
+  __syncthreads();
+  const int bstar = sh.bstar;
+  for (uint32_t rr = 0; rr < C; ++rr) {
+    const int a = (b1 > bstar ? (int)hist_in[rr * kRowBins + b1] : 0) +
+                  (b0 > bstar ? (int)hist_in[rr * kRowBins + b0] : 0);
+    const int s = __reduce_add_sync(0xffffffffu, a);
+    if (lane == 0 && s) atomicAdd(&sh.cta_sel[rr], s);
+  }
+  if (tid < (int)C) sh.cta_play[tid] = hist_in[tid * kRowBins + bstar];
+  __syncthreads();
+  int n = 0;
+  for (uint32_t rr = 0; rr < C; ++rr) n += sh.cta_play[rr];
+  return n;
+}
+
+__global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
+    const float* __restrict__ scores, int64_t score_stride, const int32_t* __restrict__ n_visible,
+    int64_t n_stride, int K, uint32_t* __restrict__ range, int32_t* __restrict__ out_idx,
+    float* __restrict__ out_scores, uint32_t* __restrict__ status, const uint8_t* __restrict__ pf_codes,
+    const uint8_t* __restrict__ pf_scales, int T, int64_t kv_stride, const int32_t* __restrict__ pool,
+    int pool_stride, int slice_cap) {
+  extern __shared__ __align__(128) uint8_t cl_raw[];
+  __shared__ ClusterShared sh;
+  uint32_t C, r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  float* sv = reinterpret_cast<float*>(cl_raw);                                     // [slice_cap]
+  uint16_t* hist_in = reinterpret_cast<uint16_t*>(cl_raw + (size_t)slice_cap * 4);  // [C][kRowBins]
+  float* cand_s = reinterpret_cast<float*>(hist_in + (size_t)C * kRowBins);          // [C][kRowRankCap]
+  int* cand_i = reinterpret_cast<int*>(cand_s + (size_t)C * kRowRankCap);            // [C][kRowRankCap]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int qi = blockIdx.y;
+  if (tid == 0) {
+    mbar_init(smem_u32(&sh.bar_load), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < kRowThreads / 2) {
+    sh.selw[tid] = 0u;
+    sh.candw[tid] = 0u;
+  }
+  if (tid < kMaxCluster) {
+    sh.cta_sel[tid] = 0;
+    sh.cta_taken[tid] = 0;
+  }
+  __syncthreads();
+  // no CTA writes into a peer's shared memory before every CTA of the cluster runs: the
+  // matching wait comes after the score load
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int nvis = clamp_nvis(n_visible, qi, n_stride);
+  const int slice = ((nvis + (int)C - 1) / (int)C + 31) & ~31;
+  auto len_of = [&](int rr) { return min(max(nvis - rr * slice, 0), slice); };
+  const int my0 = (int)r * slice;
+  int my_len = len_of((int)r);
+  const int n16 = (my_len + 3) >> 2;   // a score row is score_stride >= roundup4(nvis) floats
+  if (tid == 0) {
+    if (n16 > 0) mbar_arrive_expect_tx(smem_u32(&sh.bar_load), (uint32_t)n16 * 16);
+    sh.rng[0] = range[2 * qi];
+    sh.rng[1] = range[2 * qi + 1];
+  }
+  __syncthreads();   // expect_tx precedes every copy's completion
+  if (tid < kRowCopies && n16 > 0) {
+    const int per = (n16 + kRowCopies - 1) / kRowCopies;
+    const int a = tid * per, b = min(a + per, n16);
+    if (b > a)
+      bulk_g2s(smem_u32(sv + 4 * a), scores + (int64_t)qi * score_stride + my0 + 4 * a, (uint32_t)(b - a) * 16,
+               smem_u32(&sh.bar_load));
+  }
+  // one warp waits for the copies, the others at the barrier
+  bool loaded = n16 == 0 || tid >= 32 || mbar_wait(smem_u32(&sh.bar_load), 0);
+  loaded = __syncthreads_and(loaded);
+  if (!loaded && tid == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+  // (a copy that did not land leaves stale scores: the selection still completes, flagged)
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  const int nk = (my_len + kRowThreads - 1) / kRowThreads;
+  const int nwords = (my_len + 31) >> 5;
+  const uint32_t my_valid = [&] {
+    const int n = min(max(my_len - 32 * tid, 0), 32);
+    return n >= 32 ? 0xffffffffu : ((1u << n) - 1u);
+  }();
+  int off = 0, total = 0;
+  // the range words are set back to zero by CTA 0 once every CTA has read them, i.e. after
+  // the first cluster barrier (with nvis <= K no CTA uses them)
+  bool range_clear = false;
+  auto barrier = [&]() {
+    cluster_barrier();
+    if (!range_clear) {
+      if (r == 0 && tid == 0) {
+        range[2 * qi] = 0u;
+        range[2 * qi + 1] = 0u;
+      }
+      range_clear = true;
+    }
+  };
+  if (nvis <= K) {
+    // everything visible is selected: position order is the output order
+    if (tid < nwords) sh.selw[tid] = my_valid;
+    off = my0 < nvis ? my0 : nvis;
+    total = nvis;
+    if (r == 0 && tid == 0) {
+      range[2 * qi] = 0u;
+      range[2 * qi + 1] = 0u;
+    }
+    __syncthreads();
+  } else {
+    int rem = K;
+    float lo = key2f(~sh.rng[0]), hi = key2f(sh.rng[1]);
+    if (!(sh.rng[1] != 0u && lo < hi && isfinite(lo) && isfinite(hi))) {
+      // no range left by the scoring kernel: the cluster-wide min / max
+      float a = INFINITY, b = -INFINITY;
+      for (int k = 0; k < nk; ++k) {
+        const int p = k * kRowThreads + tid;
+        if (p < my_len) {
+          a = fminf(a, sv[p]);
+          b = fmaxf(b, sv[p]);
+        }
+      }
+      block_minmax(a, b, sh.red);
+      if (tid < (int)C) st_remote_v4(&sh.rec_in[r], tid, make_uint4(__float_as_uint(a), __float_as_uint(b), 0u, 0u));
+      barrier();
+      lo = INFINITY;
+      hi = -INFINITY;
+      for (uint32_t rr = 0; rr < C; ++rr) {
+        lo = fminf(lo, __uint_as_float(sh.rec_in[rr].x));
+        hi = fmaxf(hi, __uint_as_float(sh.rec_in[rr].y));
+      }
+    }
+    int nplay = nvis;
+    bool done = false;
+    const float scl0 = (float)(kRowBins - 1) / (hi - lo);
+    if (lo < hi && scl0 <= 1e30f) {
+      // ---- round 0 over every visible position
+      for (int i = tid; i < kRowBins; i += kRowThreads) sh.hist[i] = 0u;
+      __syncthreads();
+      for (int k = 0; k < nk; ++k) {
+        const int p = k * kRowThreads + tid;
+        if (p < my_len) atomicAdd(&sh.hist[row_bin(sv[p], lo, scl0)], 1u);
+      }
+      __syncthreads();
+      push_hist(sh, hist_in, C, r);
+      barrier();
+      nplay = cluster_bstar(sh, hist_in, C, rem);
+      const uint32_t bstar = (uint32_t)sh.bstar;
+      rem -= sh.above;
+      // lane k of each warp collects bitmap word k * 32 + warp (local positions k * 1024 + 32 warp ..)
+      uint32_t my_sel = 0u, my_cand = 0u;
+      for (int k = 0; k < nk; ++k) {
+        const int p = k * kRowThreads + tid;
+        const bool ok = p < my_len;
+        const uint32_t bi = ok ? row_bin(sv[p], lo, scl0) : 0u;
+        const uint32_t bs = __ballot_sync(0xffffffffu, ok && bi > bstar);
+        const uint32_t bc = __ballot_sync(0xffffffffu, ok && bi == bstar);
+        if (lane == k) {
+          my_sel = bs;
+          my_cand = bc;
+        }
+      }
+      if (lane < nk) {
+        sh.selw[lane * 32 + warp] = my_sel;
+        sh.candw[lane * 32 + warp] = my_cand;
+      }
+      __syncthreads();
+      if (nplay == rem) {   // every score of b* is taken
+        if (tid < nwords) sh.selw[tid] |= sh.candw[tid];
+        if (tid < (int)C) sh.cta_sel[tid] += sh.cta_play[tid];
+        done = true;
+      }
+    } else {
+      // all visible scores tie (or their range is degenerate): all in play
+      if (tid < nwords) sh.candw[tid] = my_valid;
+      if (tid < (int)C) sh.cta_play[tid] = len_of(tid);
+    }
+    __syncthreads();
+    // ---- later rounds over the positions in play (thread t: bitmap word t)
+#pragma unroll 1
+    for (int level = 1; !done; ++level) {
+      const uint32_t cw = tid < nwords ? sh.candw[tid] : 0u;
+      if (nplay <= kRowRankCap) {
+        // exact: push this CTA's (score, position) list to every peer
+        int tot;
+        int pre = block_excl_scan(__popc(cw), sh.scan, tot);
+        for (uint32_t m = cw; m; m &= m - 1u, ++pre) {
+          const int lp = 32 * tid + __ffs(m) - 1;
+          for (uint32_t pr = 0; pr < C; ++pr) {
+            st_remote_u32(reinterpret_cast<uint32_t*>(&cand_s[r * kRowRankCap + pre]), pr, __float_as_uint(sv[lp]));
+            st_remote_u32(reinterpret_cast<uint32_t*>(&cand_i[r * kRowRankCap + pre]), pr, (uint32_t)(my0 + lp));
+          }
+        }
+        barrier();
+        // rank every candidate of every CTA; the counts per CTA are sh.cta_play
+        if (tid < nplay) {
+          int rr = 0, k = tid;
+          while (k >= sh.cta_play[rr]) k -= sh.cta_play[rr++];
+          const float sc = cand_s[rr * kRowRankCap + k];
+          const int i = cand_i[rr * kRowRankCap + k];
+          int rank = 0;
+          for (uint32_t r2 = 0; r2 < C; ++r2) {
+            const int n2 = sh.cta_play[r2];
+            for (int k2 = 0; k2 < n2; ++k2) {
+              const float t2 = cand_s[r2 * kRowRankCap + k2];
+              rank += (t2 > sc) || (t2 == sc && cand_i[r2 * kRowRankCap + k2] < i);
+            }
+          }
+          if (rank < rem) {
+            atomicAdd(&sh.cta_taken[rr], 1);
+            if (rr == (int)r) atomicOr(&sh.selw[(i - my0) >> 5], 1u << ((i - my0) & 31));
+          }
+        }
+        __syncthreads();
+        if (tid < (int)C) sh.cta_sel[tid] += sh.cta_taken[tid];
+        break;
+      }
+      // the cluster-wide key range of the scores in play
+      uint32_t ka = 0xffffffffu, kb = 0u;
+      for (uint32_t m = cw; m; m &= m - 1u) {
+        const uint32_t x = f2key(sv[32 * tid + __ffs(m) - 1]);
+        ka = min(ka, x);
+        kb = max(kb, x);
+      }
+      {
+        ka = __reduce_min_sync(0xffffffffu, ka);
+        kb = __reduce_max_sync(0xffffffffu, kb);
+        __syncthreads();
+        if (lane == 0) {
+          sh.red[0][warp] = __uint_as_float(ka);
+          sh.red[1][warp] = __uint_as_float(kb);
+        }
+        __syncthreads();
+        ka = __reduce_min_sync(0xffffffffu, __float_as_uint(sh.red[0][lane]));
+        kb = __reduce_max_sync(0xffffffffu, __float_as_uint(sh.red[1][lane]));
+      }
+      if (tid < (int)C) st_remote_v4(&sh.rec_in[r], tid, make_uint4(ka, kb, 0u, 0u));
+      barrier();
+      ka = 0xffffffffu;
+      kb = 0u;
+      for (uint32_t rr = 0; rr < C; ++rr)
+        if (sh.cta_play[rr] > 0) {
+          ka = min(ka, sh.rec_in[rr].x);
+          kb = max(kb, sh.rec_in[rr].y);
+        }
+      const uint32_t span = kb - ka;
+      if (span == 0u || level >= kMaxLevels) {
+        // all tie (or the search did not settle): lowest positions first
+        if (span != 0u && r == 0 && tid == 0) atomicOr(status, CSA2_DEV_TOPK_LEVELS);
+        int pre_cta = 0;
+        for (uint32_t rr = 0; rr < r; ++rr) pre_cta += sh.cta_play[rr];
+        int tot;
+        const int pre = block_excl_scan(__popc(cw), sh.scan, tot);
+        int take = min(max(rem - pre_cta - pre, 0), __popc(cw));
+        uint32_t tk = 0u;
+        for (uint32_t m = cw; take > 0; --take) {
+          tk |= m & (~m + 1u);
+          m &= m - 1u;
+        }
+        if (tid < nwords) sh.selw[tid] |= tk;
+        __syncthreads();
+        if (tid == 0) {
+          int acc = 0;
+          for (uint32_t rr = 0; rr < C; ++rr) {
+            sh.cta_sel[rr] += min(max(rem - acc, 0), sh.cta_play[rr]);
+            acc += sh.cta_play[rr];
+          }
+        }
+        break;
+      }
+      const int shift = span < (uint32_t)kRowBins ? 0 : 32 - __clz((int)span) - 11;
+      for (int i = tid; i < kRowBins; i += kRowThreads) sh.hist[i] = 0u;
+      __syncthreads();
+      for (uint32_t m = cw; m; m &= m - 1u)
+        atomicAdd(&sh.hist[(f2key(sv[32 * tid + __ffs(m) - 1]) - ka) >> shift], 1u);
+      __syncthreads();
+      push_hist(sh, hist_in, C, r);
+      barrier();
+      nplay = cluster_bstar(sh, hist_in, C, rem);
+      const uint32_t bstar = (uint32_t)sh.bstar;
+      rem -= sh.above;
+      uint32_t ns = 0u, nc = 0u;
+      for (uint32_t m = cw; m; m &= m - 1u) {
+        const int j = __ffs(m) - 1;
+        const uint32_t bi = (f2key(sv[32 * tid + j]) - ka) >> shift;
+        ns |= (uint32_t)(bi > bstar) << j;
+        nc |= (uint32_t)(bi == bstar) << j;
+      }
+      if (tid < nwords) {
+        sh.selw[tid] |= ns | (nplay == rem ? nc : 0u);
+        sh.candw[tid] = nc;
+      }
+      __syncthreads();
+      if (nplay == rem) {
+        if (tid < (int)C) sh.cta_sel[tid] += sh.cta_play[tid];
+        break;
+      }
+    }
+    __syncthreads();
+    for (uint32_t rr = 0; rr < C; ++rr) {
+      if (rr < r) off += sh.cta_sel[rr];
+      total += sh.cta_sel[rr];
+    }
+  }
+
+  // ---- ordered output: thread t writes the selected positions of bitmap word t
+  const uint32_t sel = tid < nwords ? sh.selw[tid] : 0u;
+  int cnt;
+  int p = off + block_excl_scan(__popc(sel), sh.scan, cnt);
+  int32_t* out = out_idx + (int64_t)qi * K;
+  float* outs = out_scores ? out_scores + (int64_t)qi * K : nullptr;
+  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * kv_stride * CSA2_CODE_BYTES : nullptr;
+  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * kv_stride * CSA2_SCALE_BYTES : nullptr;
+  const int32_t* pblk = pool ? pool + (int64_t)qi * pool_stride : nullptr;
+  for (uint32_t m = sel; m && p < K; m &= m - 1u, ++p) {
+    const int lp = 32 * tid + __ffs(m) - 1;
+    const int pos = my0 + lp;
+    const int ent = pblk ? pblk[pos >> 3] * 8 + (pos & 7) : pos;
+    out[p] = ent;
+    if (outs) outs[p] = sv[lp];
+    if (pfc && ent >= 0 && ent < kv_stride) {
+      prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
+      prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES);
+      prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES + CSA2_SCALE_BYTES - 1);
+    }
+  }
+  if (r == C - 1)
+    for (int q = total + tid; q < K; q += kRowThreads) {
+      out[q] = -1;
+      if (outs) outs[q] = __int_as_float(0x7fc00000);
+    }
+}
+
 // CTAs per query: enough for at most 8192 scores each; while the grid stays within one
 // CTA per SM, more (slices of at least 2048), since the selection's phases scale with
 // the slice, not with the cluster.
@@ -1173,7 +1081,6 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
                                float* out_scores, uint32_t* status, cudaStream_t st,
                                const uint8_t* pf_codes, const uint8_t* pf_scales, int T,
                                int64_t kv_stride, const int32_t* pool, int pool_stride) {
-  static_assert(kNBMax % kSelThreads == 0 && kNBMin % kSelThreads == 0, "bins per thread");
   static_assert(kRowBins == 2 * kRowThreads, "two bins per thread in the row kernel's scan");
   if (Q == 0) return cudaSuccess;
   if (n_stride <= kRowMaxN && (int64_t)Q * select_cluster_size(n_stride, Q) > device_sm_count()) {
@@ -1199,21 +1106,19 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
                               out_scores, status, pf_codes, pf_scales, tt, kvs, pool, pool_stride);
   }
   const int C = select_cluster_size(n_stride, Q);
-  const int NB = C <= 4 ? kNBMax : kNBMin;
-  int slice_cap = (int)((n_stride + C - 1) / C);
-  slice_cap = (slice_cap + 15) & ~15;
-  const size_t smem = kSelHdr + (size_t)C * NB * 2 + (size_t)C * kCandCap * 8 +
-                      (size_t)slice_cap * 5;
+  const int slice_cap = (int)(((n_stride + C - 1) / C + 31) & ~31);
+  if (slice_cap > kRowThreads * 16 || C > kMaxCluster) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)slice_cap * 4 + (size_t)C * kRowBins * 2 + (size_t)C * kRowRankCap * 8;
   if (smem > kSelSmemMax) return cudaErrorInvalidValue;
-  cudaError_t e = set_attr_once(0, (const void*)topk_select_kernel,
+  cudaError_t e = set_attr_once(0, (const void*)topk_cluster_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemMax);
   if (e != cudaSuccess) return e;
-  e = set_attr_once(1, (const void*)topk_select_kernel,
+  e = set_attr_once(1, (const void*)topk_cluster_kernel,
                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)C, (unsigned)Q);
-  cfg.blockDim = dim3(kSelThreads);
+  cfg.blockDim = dim3(kRowThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -1225,9 +1130,9 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, topk_select_kernel, scores, score_stride, n_visible, n_stride, K,
-                            slice_cap, range, out_idx, out_scores, status, pf_codes, pf_scales,
-                            T < 1 ? 1 : T, kv_stride < 0 ? n_stride : kv_stride, pool, pool_stride);
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel, scores, score_stride, n_visible, n_stride, K, range,
+                            out_idx, out_scores, status, pf_codes, pf_scales, T < 1 ? 1 : T,
+                            kv_stride < 0 ? n_stride : kv_stride, pool, pool_stride, slice_cap);
 }
 
 __global__ void copy_idx_kernel(const int32_t* __restrict__ src, int32_t* __restrict__ dst,
