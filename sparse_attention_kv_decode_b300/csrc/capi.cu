@@ -26,11 +26,11 @@ int device_sm_count() {
 
 cudaError_t set_attr_once(int slot, const void* fn, cudaFuncAttribute attr, int value) {
   static std::mutex mu;
-  static bool done[64][16] = {};
+  static bool done[64][32] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || slot < 0 || slot >= 16) return cudaErrorInvalidValue;
+  if (dev < 0 || dev >= 64 || slot < 0 || slot >= 32) return cudaErrorInvalidValue;
   std::lock_guard<std::mutex> lk(mu);
   if (done[dev][slot]) return cudaSuccess;
   e = cudaFuncSetAttribute(fn, attr, value);
@@ -342,12 +342,15 @@ static int index_topk_impl(int mode, int B, int T, int H_I, const void* q_idx, c
                                           blocks, K));
   }
   const int64_t stride = score_pad(n_stride);
-  // many query tokens per sequence: the keys x (token, head) GEMM on the tensor cores
-  cudaError_t e = index_gemm_applies(T, H_I)
-                      ? launch_index_gemm(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores, stride, range,
-                                          status, st)
-                      : launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores, stride, range,
-                                           status, st);
+  // keys x (token, head) products on the tensor cores: N = 256 columns with many query
+  // tokens per sequence (prefill), N = 16 with few (decode)
+  cudaError_t e;
+  if (index_gemm_applies(T, H_I))
+    e = launch_index_gemm(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores, stride, range, status, st);
+  else if (index_stream_applies(B, T, H_I))
+    e = launch_index_stream(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores, stride, range, status, st);
+  else
+    e = launch_index_score(q_idx, w_idx, z, n_stride, n_visible, B, T, H_I, scores, stride, range, status, st);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_topk_select(scores, stride, n_visible, (int)Q, n_stride, K, range,
                                         out_idx, out_scores, status, st, pf_codes, pf_scales, T));

@@ -75,6 +75,10 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
 // Indexer scoring of T >= 256 / H_I query tokens per sequence as a tcgen05 GEMM (keys x
 // (token, head) tiles); same scores and range words as launch_index_score without a pool.
 bool index_gemm_applies(int T, int H_I);
+bool index_stream_applies(int B, int T, int H_I);
+cudaError_t launch_index_stream(const void* q_idx, const float* w_idx, const void* z, int64_t n_stride,
+                                const int32_t* n_visible, int B, int T, int H_I, float* scores,
+                                int64_t score_stride, uint32_t* range, uint32_t* status, cudaStream_t st);
 cudaError_t launch_index_gemm(const void* q_idx, const float* w_idx, const void* z, int64_t n_stride,
                               const int32_t* n_visible, int B, int T, int H_I, float* scores,
                               int64_t score_stride, uint32_t* range, uint32_t* status, cudaStream_t st);

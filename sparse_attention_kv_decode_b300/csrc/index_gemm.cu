@@ -346,6 +346,310 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// Few query tokens per sequence (decode): the same contraction with N = 16, i.e. the
+// indexer heads of 16 / H_I tokens, so that every key is read once per 16 / H_I tokens
+// and the tensor cores do the dot products while the key stream runs at HBM speed.
+//   warp 0      TMA producer: one 128-key z box (16 KB) per stage into a ring of
+//               kSStages stages, and the q rows (2 KB) of each (sequence, token tile)
+//               into one of two q buffers
+//   warp 1      TMEM allocation and the MMA issuer: M = 128, N = 16, K = 16 x 4,
+//               accumulators in kSAcc TMEM buffers of 16 columns
+//   warps 2..9  epilogue, two warpgroups taking alternate key tiles: thread = key row,
+//               one 16-column TMEM load, max(0, .) and the head weights per token, one
+//               fp32 score per (token, key) below the token's visible count, and the
+//               token's running min / max score (the range words)
+// The key tiles each (sequence, token tile) needs (its largest visible count, in
+// 128-key tiles) are counted on the device and the whole list is split evenly over
+// the CTAs, so ragged batches keep every SM equally busy.
+constexpr int kSN = 16;
+constexpr int kSStages = 8;
+constexpr int kSAcc = 4;
+constexpr int kSQBytes = kSN * CSA2_D_IDX * 2;   // 2 KB
+constexpr int kSThreads = 64 + 32 * kGEpiWarps;
+constexpr int kSTmemCols = 64;
+constexpr int kSMaxBj = 2048;                   // (sequence, token tile) pairs
+constexpr size_t kSSmem = 1024 + kSStages * kGZBytes + 2 * kSQBytes + 1024 + 4 * (kSMaxBj + 1);
+
+struct StreamShape {
+  int B, T, ntt, nbj;
+  int64_t n_stride;
+};
+
+// The first (sequence, token tile) whose tiles reach past tile t: pre[bj + 1] > t.
+__device__ __forceinline__ int first_bj(const int* pre, int nbj, int t) {
+  int lo = 0, hi = nbj - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid + 1] > t) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
+
+template <int HI>
+__global__ void __launch_bounds__(kSThreads, 1) index_stream_kernel(
+    const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_q,
+    const float* __restrict__ w_idx, const int32_t* __restrict__ n_visible, StreamShape g,
+    float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ range,
+    uint32_t* __restrict__ status) {
+  constexpr int TT = kSN / HI;
+  static_assert(kSN % HI == 0, "token tile");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sz = smem_u32(smem);
+  const uint32_t sq = sz + kSStages * kGZBytes;
+  uint8_t* misc = smem + kSStages * kGZBytes + 2 * kSQBytes;
+  const uint32_t bar_full = smem_u32(misc);
+  const uint32_t bar_empty = bar_full + 8 * kSStages;
+  const uint32_t bar_tfull = bar_empty + 8 * kSStages;
+  const uint32_t bar_tempty = bar_tfull + 8 * kSAcc;
+  const uint32_t bar_qfull = bar_tempty + 8 * kSAcc;
+  const uint32_t bar_qempty = bar_qfull + 16;
+  const uint32_t bar_drain = bar_qempty + 16;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(misc + 512);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 516);
+  int* pre = reinterpret_cast<int*>(misc + 1024);   // [nbj + 1] key tiles before each pair
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < kSAcc; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, 4);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_qfull + 8 * a, 1);
+      mbar_init(bar_qempty + 8 * a, 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(kSTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // inputs (and the visible counts) may be written by the preceding kernel in the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // key tiles per (sequence, token tile), then their running sum
+  for (int bj = threadIdx.x; bj < g.nbj; bj += kSThreads) {
+    const int b = bj / g.ntt, t0 = (bj % g.ntt) * TT, nt = min(TT, g.T - t0);
+    int mx = 0;
+    for (int t = 0; t < nt; ++t) {
+      int v = n_visible[(int64_t)b * g.T + t0 + t];
+      v = v < 0 ? 0 : (v > g.n_stride ? (int)g.n_stride : v);
+      mx = max(mx, v);
+    }
+    pre[bj + 1] = (mx + kGM - 1) / kGM;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < g.nbj; base += 32) {
+      const int j = base + lane;
+      int v = j < g.nbj ? pre[j + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (j < g.nbj) pre[j + 1] = v + carry;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) pre[0] = 0;
+  }
+  __syncthreads();
+  const uint32_t tmem = *tmem_holder;
+  const int total = g.nbj > 0 ? pre[g.nbj] : 0;
+  const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+
+  if (warp == 0) {
+    // ---------------- TMA producer
+    if (lane == 0 && t_begin < t_end) {
+      // bit s: stage s (q buffer s) holds a copy; its phase bit: the parity of that copy
+      uint32_t armed = 0u, armed_phase = 0u, q_armed = 0u, q_armed_phase = 0u;
+      int bj = first_bj(pre, g.nbj, t_begin), prev_bj = -1, qn = -1;
+      for (int t = t_begin, i = 0; t < t_end && !*abort_flag; ++t, ++i) {
+        while (t >= pre[bj + 1]) ++bj;
+        const int b = bj / g.ntt, t0 = (bj % g.ntt) * TT;
+        if (bj != prev_bj) {
+          ++qn;
+          const int qb = qn & 1;
+          const uint32_t qph = (uint32_t)(qn >> 1) & 1u;
+          if (!mbar_wait(bar_qempty + 8 * qb, qph ^ 1u)) {
+            atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_qfull + 8 * qb, kSQBytes);
+          q_armed |= 1u << qb;
+          q_armed_phase = (q_armed_phase & ~(1u << qb)) | (qph << qb);
+          // rows past the last token of the tile (another sequence's, or zeros past the
+          // end) only feed columns whose scores are never stored
+          tma_load_2d(sq + qb * kSQBytes, &tm_q, 0, (b * g.T + t0) * HI, bar_qfull + 8 * qb);
+          prev_bj = bj;
+        }
+        const int stage = i % kSStages;
+        const uint32_t ph = (uint32_t)(i / kSStages) & 1u;
+        if (!mbar_wait(bar_empty + 8 * stage, ph ^ 1u)) {
+          atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_full + 8 * stage, kGZBytes);
+        armed |= 1u << stage;
+        armed_phase = (armed_phase & ~(1u << stage)) | (ph << stage);
+        const int kt = t - pre[bj];
+        tma_load_2d(sz + stage * kGZBytes, &tm_z, 0, (int)((int64_t)b * g.n_stride + (int64_t)kt * kGM),
+                    bar_full + 8 * stage);
+      }
+      // drain: every armed copy has landed before the CTA may exit
+      for (int s = 0; s < kSStages; ++s)
+        if ((armed >> s) & 1u) mbar_wait(bar_full + 8 * s, (armed_phase >> s) & 1u);
+      for (int a = 0; a < 2; ++a)
+        if ((q_armed >> a) & 1u) mbar_wait(bar_qfull + 8 * a, (q_armed_phase >> a) & 1u);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0 && t_begin < t_end) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kGM, kSN);
+      bool issued = false;
+      int bj = first_bj(pre, g.nbj, t_begin), prev_bj = -1, qn = -1;
+      for (int t = t_begin, i = 0; t < t_end && !*abort_flag; ++t, ++i) {
+        while (t >= pre[bj + 1]) ++bj;
+        if (bj != prev_bj) {
+          // the previous q buffer is free once the MMAs issued so far are done
+          if (qn >= 0) umma_commit(bar_qempty + 8 * (qn & 1));
+          ++qn;
+          if (!mbar_wait(bar_qfull + 8 * (qn & 1), (uint32_t)(qn >> 1) & 1u)) {
+            atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          prev_bj = bj;
+        }
+        const int stage = i % kSStages, acc = i % kSAcc;
+        const uint32_t ph = (uint32_t)(i / kSStages) & 1u, aph = (uint32_t)(i / kSAcc) & 1u;
+        if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1u) || !mbar_wait(bar_full + 8 * stage, ph)) {
+          atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t ad = umma_desc_sw128(sz + stage * kGZBytes);
+        const uint64_t bd = umma_desc_sw128(sq + (qn & 1) * kSQBytes);
+#pragma unroll
+        for (int k = 0; k < CSA2_D_IDX / 16; ++k)
+          umma_bf16(tmem + acc * kSN, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), idesc, k != 0);
+        umma_commit(bar_empty + 8 * stage);
+        umma_commit(bar_tfull + 8 * acc);
+        issued = true;
+      }
+      if (issued) {
+        umma_commit(bar_drain);
+        mbar_wait(bar_drain, 0);
+      }
+    }
+  } else {
+    // ---------------- epilogue: warpgroup wg takes the CTA's key tiles i with i % 2 == wg
+    const int wg = (warp - 2) >> 2;
+    const int quarter = warp & 3;   // TMEM lanes 32 * quarter ..
+    const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
+    float wv[TT][HI];
+    int nv[TT];
+    float mn[TT], mx[TT];
+    int q0 = 0, nt = 0, cur_bj = -1;
+    auto flush = [&]() {
+#pragma unroll
+      for (int tl = 0; tl < TT; ++tl) {
+        const bool any = tl < nt && mx[tl] >= mn[tl];
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, any ? f2key(mx[tl]) : 0u);
+        const uint32_t kinv = __reduce_max_sync(0xffffffffu, any ? ~f2key(mn[tl]) : 0u);
+        if (lane == 0 && kmax != 0u) {
+          atomicMax(range + 2 * (int64_t)(q0 + tl), kinv);
+          atomicMax(range + 2 * (int64_t)(q0 + tl) + 1, kmax);
+        }
+      }
+    };
+    if (t_begin < t_end) {
+      int bj = first_bj(pre, g.nbj, t_begin);
+      for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+        while (t >= pre[bj + 1]) ++bj;
+        if ((i & 1) != wg) continue;
+        if (bj != cur_bj) {
+          if (cur_bj >= 0) flush();
+          const int b = bj / g.ntt, t0 = (bj % g.ntt) * TT;
+          q0 = b * g.T + t0;
+          nt = min(TT, g.T - t0);
+#pragma unroll
+          for (int tl = 0; tl < TT; ++tl) {
+            int v = tl < nt ? n_visible[q0 + tl] : 0;
+            nv[tl] = v < 0 ? 0 : (v > g.n_stride ? (int)g.n_stride : v);
+            mn[tl] = INFINITY;
+            mx[tl] = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < HI; ++h) wv[tl][h] = tl < nt ? w_idx[(int64_t)(q0 + tl) * HI + h] : 0.f;
+          }
+          cur_bj = bj;
+        }
+        const int acc = i % kSAcc;
+        const bool got = __all_sync(0xffffffffu, mbar_wait(bar_tfull + 8 * acc, (uint32_t)(i / kSAcc) & 1u));
+        if (!got) {
+          if (lane == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r[kSN];
+        tmem_ld16(tmem + acc * kSN + tlane, r);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+        const int n = (t - pre[bj]) * kGM + quarter * 32 + lane;
+#pragma unroll
+        for (int tl = 0; tl < TT; ++tl) {
+          // two independent partial sums (even / odd heads)
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int h = 0; h < HI; h += 2) {
+            s0 = fmaf(wv[tl][h], fmaxf(__uint_as_float(r[tl * HI + h]), 0.f), s0);
+            s1 = fmaf(wv[tl][h + 1], fmaxf(__uint_as_float(r[tl * HI + h + 1]), 0.f), s1);
+          }
+          const float sc = s0 + s1;
+          if (tl < nt && n < nv[tl]) {
+            scores[(int64_t)(q0 + tl) * score_stride + n] = sc;
+            mn[tl] = fminf(mn[tl], sc);
+            mx[tl] = fmaxf(mx[tl], sc);
+          }
+        }
+      }
+      if (cur_bj >= 0) flush();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kSTmemCols)
+                 : "memory");
+  }
+}
+
 }  // namespace
 
 bool index_gemm_applies(int T, int H_I) {
@@ -403,6 +707,59 @@ cudaError_t launch_index_gemm(const void* q_idx, const float* w_idx, const void*
                               status);
   return cudaLaunchKernelEx(&cfg, index_gemm_kernel<16>, tz, tq, w_idx, n_visible, g, scores, score_stride, range,
                             status);
+}
+
+
+// Worth it when a key tile serves more than one token (T >= 2 with H_I = 4 or 8): the
+// tile's TMA copies stream at a little under the HBM rate on this part, so with one token
+// per tile the direct-load scoring kernel (which keeps more bytes in flight) is faster.
+bool index_stream_applies(int B, int T, int H_I) {
+  if (!(H_I == 4 || H_I == 8) || B <= 0 || T < 2) return false;
+  const int tt = kSN / H_I;
+  return (int64_t)B * ((T + tt - 1) / tt) <= kSMaxBj;
+}
+
+cudaError_t launch_index_stream(const void* q_idx, const float* w_idx, const void* z, int64_t n_stride,
+                                const int32_t* n_visible, int B, int T, int H_I, float* scores,
+                                int64_t score_stride, uint32_t* range, uint32_t* status, cudaStream_t st) {
+  if (B == 0 || T == 0 || n_stride == 0) return cudaSuccess;
+  if (!index_stream_applies(B, T, H_I)) return cudaErrorInvalidValue;
+  if ((int64_t)B * n_stride > ((int64_t)1 << 31) - kGM || (int64_t)B * T * H_I > ((int64_t)1 << 31) - kSN)
+    return cudaErrorInvalidValue;
+  CUtensorMap tz, tq;
+  if (!encode_tensor_map_2d_bf16(&tz, z, CSA2_D_IDX, (uint64_t)B * n_stride, CSA2_D_IDX, kGM) ||
+      !encode_tensor_map_2d_bf16(&tq, q_idx, CSA2_D_IDX, (uint64_t)B * T * H_I, CSA2_D_IDX, kSN))
+    return cudaErrorInvalidValue;
+  StreamShape g;
+  g.B = B;
+  g.T = T;
+  g.n_stride = n_stride;
+  const int tt = kSN / H_I;
+  g.ntt = (T + tt - 1) / tt;
+  g.nbj = B * g.ntt;
+  const int64_t nkt = (n_stride + kGM - 1) / kGM;
+  const int n_sm = device_sm_count();
+  const int64_t most = (int64_t)g.nbj * nkt;   // key tiles with every position visible
+  const int grid = (int)(most < n_sm ? most : n_sm);
+  const void* fn = H_I == 4 ? (const void*)index_stream_kernel<4> : (const void*)index_stream_kernel<8>;
+  const int slot = H_I == 4 ? 14 : 15;
+  cudaError_t e = set_attr_once(slot, fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kSThreads);
+  cfg.dynamicSmemBytes = kSSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (H_I == 4)
+    return cudaLaunchKernelEx(&cfg, index_stream_kernel<4>, tz, tq, w_idx, n_visible, g, scores, score_stride,
+                              range, status);
+  return cudaLaunchKernelEx(&cfg, index_stream_kernel<8>, tz, tq, w_idx, n_visible, g, scores, score_stride,
+                            range, status);
 }
 
 }  // namespace csa2

@@ -36,6 +36,16 @@ constexpr int kScoreCtasPerSm = 2;
 constexpr int kScoreUnroll = 2;
 constexpr int kGroupKeys = 16;
 
+// Read-only 16-byte load that asks L2 for the whole 256-byte block (the keys are a
+// contiguous stream, so the neighbouring lines are the next requests).
+__device__ __forceinline__ uint4 ldg_key(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
 template <int NT>
 __device__ __forceinline__ void load_q_frag(const uint16_t* q_idx, const float* w_idx, int qi,
                                             int H_I, int g, int tig, uint32_t (&qa)[NT][8],
@@ -86,62 +96,68 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
   const int64_t nwarps = (int64_t)gridDim.x * (kScoreThreads / 32);
   const int64_t wid = (int64_t)blockIdx.x * (kScoreThreads / 32) + (threadIdx.x >> 5);
   const int64_t w_begin = total * wid / nwarps, w_end = total * (wid + 1) / nwarps;
+  if (w_begin >= w_end) return;
 
+  // the warp's position: query qi, its group grp; advanced incrementally
+  int qi = (int)(w_begin / gpq);
+  int grp = (int)(w_begin - (int64_t)qi * gpq);
+  int64_t left = w_end - w_begin;
   uint32_t qa[NT][8];
   float wv[NT][2];
-  int cur_q = -1, nv = 0;
-  uint32_t rmax = 0u, rmin_inv = 0u;  // score range of the current query seen by this warp
-  for (int64_t g0 = w_begin; g0 < w_end;) {
-    // fragments of up to kScoreUnroll groups (all loads issued before any use); a batch
-    // ends at a query boundary, since the indexer rows in registers are one query's
-    const int64_t q_end = (g0 / gpq + 1) * gpq;
-    const int nb = (int)min((int64_t)kScoreUnroll, min(w_end, q_end) - g0);
+  int nv = 0;
+  const uint16_t* zb = nullptr;
+  const int32_t* blk_row = nullptr;
+  // running range of the scores this thread stored for query qi
+  float smax = -INFINITY, smin = INFINITY;
+  auto start_query = [&]() {
+    load_q_frag<NT>(q_idx, w_idx, qi, H_I, g, tig, qa, wv);
+    nv = pooled ? min(max(pool_nv[qi], 0), 8 * pool_stride) : clamp_nvis(n_visible, qi, n_stride);
+    zb = z + (int64_t)(qi / T) * n_stride * CSA2_D_IDX;
+    if (pooled) blk_row = pool + (int64_t)qi * pool_stride;
+  };
+  auto flush_range = [&]() {
+    const bool any = smax >= smin;
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, any ? f2key(smax) : 0u);
+    const uint32_t kinv = __reduce_max_sync(0xffffffffu, any ? ~f2key(smin) : 0u);
+    if (lane == 0 && kmax != 0u) {
+      atomicMax(range + 2 * qi, kinv);
+      atomicMax(range + 2 * qi + 1, kmax);
+    }
+    smax = -INFINITY;
+    smin = INFINITY;
+  };
+  start_query();
+  while (left > 0) {
+    // fragments of up to kScoreUnroll groups of the current query, all loads issued
+    // before any use
+    const int nb = (int)min((int64_t)min(kScoreUnroll, gpq - grp), left);
     uint4 v[kScoreUnroll][4];
-    int qg[kScoreUnroll], key0g[kScoreUnroll], okg[kScoreUnroll];
+    int okm[kScoreUnroll];
 #pragma unroll
     for (int u = 0; u < kScoreUnroll; ++u) {
-      const int64_t gi = g0 + u;
-      const int qi = (int)(gi / gpq);
-      const int key0 = (int)(gi - (int64_t)qi * gpq) * kGroupKeys;
-      qg[u] = u < nb ? qi : -1;
-      key0g[u] = key0;
-      if (u == 0 && qi != cur_q) {
-        // a new query: flush the range of the previous one, load its indexer rows
-        if (cur_q >= 0 && lane == 0 && rmax != 0u) {
-          atomicMax(range + 2 * cur_q, rmin_inv);
-          atomicMax(range + 2 * cur_q + 1, rmax);
-        }
-        rmax = 0u;
-        rmin_inv = 0u;
-        load_q_frag<NT>(q_idx, w_idx, qi, H_I, g, tig, qa, wv);
-        nv = pooled ? min(max(pool_nv[qi], 0), 8 * pool_stride) : clamp_nvis(n_visible, qi, n_stride);
-        cur_q = qi;
-      }
-      const int b = qi / T;
+      const int key0 = (grp + u) * kGroupKeys;
       // positions key0 + g and key0 + 8 + g; their key rows (pool: the blocks' entries)
       bool oka = u < nb && key0 + g < nv, okb = u < nb && key0 + 8 + g < nv;
       int64_t ra = key0 + g, rb = ra + 8;
       if (pooled) {
-        const int32_t* blk = pool + (int64_t)qi * pool_stride + (key0 >> 3);
+        const int32_t* blk = blk_row + (key0 >> 3);
         ra = oka ? (int64_t)blk[0] * 8 + g : 0;
         rb = okb ? (int64_t)blk[1] * 8 + g : 0;
         oka = oka && ra >= 0 && ra < n_stride;
         okb = okb && rb >= 0 && rb < n_stride;
       }
-      okg[u] = (oka ? 1 : 0) | (okb ? 2 : 0);
-      const uint16_t* zb = z + (int64_t)b * n_stride * CSA2_D_IDX;
-      const uint4* pa = reinterpret_cast<const uint4*>(zb + (int64_t)ra * CSA2_D_IDX);
-      const uint4* pb = reinterpret_cast<const uint4*>(zb + (int64_t)rb * CSA2_D_IDX);
-      v[u][0] = oka ? pa[tig] : make_uint4(0, 0, 0, 0);
-      v[u][1] = oka ? pa[4 + tig] : make_uint4(0, 0, 0, 0);
-      v[u][2] = okb ? pb[tig] : make_uint4(0, 0, 0, 0);
-      v[u][3] = okb ? pb[4 + tig] : make_uint4(0, 0, 0, 0);
+      okm[u] = (oka ? 1 : 0) | (okb ? 2 : 0);
+      const uint4* pa = reinterpret_cast<const uint4*>(zb + ra * CSA2_D_IDX);
+      const uint4* pb = reinterpret_cast<const uint4*>(zb + rb * CSA2_D_IDX);
+      v[u][0] = oka ? ldg_key(pa + tig) : make_uint4(0, 0, 0, 0);
+      v[u][1] = oka ? ldg_key(pa + 4 + tig) : make_uint4(0, 0, 0, 0);
+      v[u][2] = okb ? ldg_key(pb + tig) : make_uint4(0, 0, 0, 0);
+      v[u][3] = okb ? ldg_key(pb + 4 + tig) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < kScoreUnroll; ++u) {
-      if (qg[u] < 0) continue;
-      const int qi = qg[u], key0 = key0g[u];
-      if (key0 >= nv) continue;   // past the visible keys (qi is the current query)
+      const int key0 = (grp + u) * kGroupKeys;
+      if (u >= nb || key0 >= nv) continue;   // (uniform over the warp)
       const uint32_t ra_[16] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y,
                                 v[u][1].z, v[u][1].w, v[u][2].x, v[u][2].y, v[u][2].z, v[u][2].w,
                                 v[u][3].x, v[u][3].y, v[u][3].z, v[u][3].w};
@@ -160,20 +176,27 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
       pg += __shfl_xor_sync(0xffffffffu, pg, 2);
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 1);
       pg8 += __shfl_xor_sync(0xffffffffu, pg8, 2);
-      float* srow = scores + (int64_t)qi * score_stride + key0;
-      const bool ok0 = tig == 0 && (okg[u] & 1), ok1 = tig == 1 && (okg[u] & 2);
-      if (ok0) srow[g] = pg;
-      if (ok1) srow[g + 8] = pg8;
-      const uint32_t kk = ok0 ? f2key(pg) : (ok1 ? f2key(pg8) : 0u);
-      rmax = max(rmax, __reduce_max_sync(0xffffffffu, kk));
-      rmin_inv = max(rmin_inv, __reduce_max_sync(0xffffffffu, (ok0 || ok1) ? ~kk : 0u));
+      // thread tig 0 stores row g, tig 1 row g + 8
+      const float sc = tig == 0 ? pg : pg8;
+      const bool ok = (tig == 0 && (okm[u] & 1)) || (tig == 1 && (okm[u] & 2));
+      if (ok) {
+        scores[(int64_t)qi * score_stride + key0 + g + 8 * tig] = sc;
+        smax = fmaxf(smax, sc);
+        smin = fminf(smin, sc);
+      }
     }
-    g0 += nb;
+    grp += nb;
+    left -= nb;
+    if (grp == gpq) {
+      flush_range();
+      if (left > 0) {
+        ++qi;
+        grp = 0;
+        start_query();
+      }
+    }
   }
-  if (cur_q >= 0 && lane == 0 && rmax != 0u) {
-    atomicMax(range + 2 * cur_q, rmin_inv);
-    atomicMax(range + 2 * cur_q + 1, rmax);
-  }
+  if (grp != gpq) flush_range();
 }
 
 cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void* z,
@@ -681,7 +704,7 @@ struct ClusterShared {
   int cta_taken[kMaxCluster];        // ranked and taken in the exact round
   int bstar, above;
   uint32_t rng[2];
-  uint64_t bar_load;
+  uint64_t bar_chunk[kRowThreads / 64];   // one per 1024-score chunk of the slice (<= 16384)
 };
 
 // Block-wide min of a and max of b (all threads get them).
@@ -769,8 +792,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
   int* cand_i = reinterpret_cast<int*>(cand_s + (size_t)C * kRowRankCap);            // [C][kRowRankCap]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int qi = blockIdx.y;
-  if (tid == 0) {
-    mbar_init(smem_u32(&sh.bar_load), 1);
+  if (tid < kRowThreads / 64) {
+    // the thread that initialises chunk tid's barrier also arms it and issues its copy
+    mbar_init(smem_u32(&sh.bar_chunk[tid]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < kRowThreads / 2) {
@@ -791,27 +815,27 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
   auto len_of = [&](int rr) { return min(max(nvis - rr * slice, 0), slice); };
   const int my0 = (int)r * slice;
   int my_len = len_of((int)r);
-  const int n16 = (my_len + 3) >> 2;   // a score row is score_stride >= roundup4(nvis) floats
+  const int nk = (my_len + kRowThreads - 1) / kRowThreads;
+  // chunk k (scores k * 1024 ..) lands with its own bulk copy and mbarrier, so that the
+  // first pass over it starts as soon as it is there (a score row is score_stride >=
+  // roundup4(nvis) floats)
+  if (tid < nk) {
+    const uint32_t bytes = (uint32_t)((min(my_len - tid * kRowThreads, kRowThreads) + 3) >> 2) * 16;
+    mbar_arrive_expect_tx(smem_u32(&sh.bar_chunk[tid]), bytes);
+    bulk_g2s(smem_u32(sv + tid * kRowThreads), scores + (int64_t)qi * score_stride + my0 + tid * kRowThreads, bytes,
+             smem_u32(&sh.bar_chunk[tid]));
+  }
   if (tid == 0) {
-    if (n16 > 0) mbar_arrive_expect_tx(smem_u32(&sh.bar_load), (uint32_t)n16 * 16);
     sh.rng[0] = range[2 * qi];
     sh.rng[1] = range[2 * qi + 1];
   }
-  __syncthreads();   // expect_tx precedes every copy's completion
-  if (tid < kRowCopies && n16 > 0) {
-    const int per = (n16 + kRowCopies - 1) / kRowCopies;
-    const int a = tid * per, b = min(a + per, n16);
-    if (b > a)
-      bulk_g2s(smem_u32(sv + 4 * a), scores + (int64_t)qi * score_stride + my0 + 4 * a, (uint32_t)(b - a) * 16,
-               smem_u32(&sh.bar_load));
-  }
-  // one warp waits for the copies, the others at the barrier
-  bool loaded = n16 == 0 || tid >= 32 || mbar_wait(smem_u32(&sh.bar_load), 0);
-  loaded = __syncthreads_and(loaded);
-  if (!loaded && tid == 0) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
   // (a copy that did not land leaves stale scores: the selection still completes, flagged)
+  bool load_ok = true;
+  auto wait_chunk = [&](int k) {
+    if (!mbar_wait(smem_u32(&sh.bar_chunk[k]), 0)) load_ok = false;
+  };
+  __syncthreads();
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  const int nk = (my_len + kRowThreads - 1) / kRowThreads;
   const int nwords = (my_len + 31) >> 5;
   const uint32_t my_valid = [&] {
     const int n = min(max(my_len - 32 * tid, 0), 32);
@@ -833,6 +857,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
   };
   if (nvis <= K) {
     // everything visible is selected: position order is the output order
+    for (int k = 0; k < nk; ++k) wait_chunk(k);
     if (tid < nwords) sh.selw[tid] = my_valid;
     off = my0 < nvis ? my0 : nvis;
     total = nvis;
@@ -848,6 +873,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
       // no range left by the scoring kernel: the cluster-wide min / max
       float a = INFINITY, b = -INFINITY;
       for (int k = 0; k < nk; ++k) {
+        wait_chunk(k);
         const int p = k * kRowThreads + tid;
         if (p < my_len) {
           a = fminf(a, sv[p]);
@@ -872,6 +898,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
       for (int i = tid; i < kRowBins; i += kRowThreads) sh.hist[i] = 0u;
       __syncthreads();
       for (int k = 0; k < nk; ++k) {
+        wait_chunk(k);
         const int p = k * kRowThreads + tid;
         if (p < my_len) atomicAdd(&sh.hist[row_bin(sv[p], lo, scl0)], 1u);
       }
@@ -906,6 +933,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
       }
     } else {
       // all visible scores tie (or their range is degenerate): all in play
+      for (int k = 0; k < nk; ++k) wait_chunk(k);
       if (tid < nwords) sh.candw[tid] = my_valid;
       if (tid < (int)C) sh.cta_play[tid] = len_of(tid);
     }
@@ -926,24 +954,30 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
           }
         }
         barrier();
-        // rank every candidate of every CTA; the counts per CTA are sh.cta_play
-        if (tid < nplay) {
-          int rr = 0, k = tid;
+        // rank every candidate of every CTA (the counts per CTA are sh.cta_play): eight
+        // threads per candidate, each comparing it with every eighth of the others
+        static_assert(kRowRankCap * 8 <= kRowThreads, "eight rankers per candidate");
+        const int c = tid >> 3, sub = tid & 7;
+        int rr = 0, rank = 0, i = 0;
+        if (c < nplay) {
+          int k = c;
           while (k >= sh.cta_play[rr]) k -= sh.cta_play[rr++];
           const float sc = cand_s[rr * kRowRankCap + k];
-          const int i = cand_i[rr * kRowRankCap + k];
-          int rank = 0;
+          i = cand_i[rr * kRowRankCap + k];
           for (uint32_t r2 = 0; r2 < C; ++r2) {
             const int n2 = sh.cta_play[r2];
-            for (int k2 = 0; k2 < n2; ++k2) {
+            for (int k2 = sub; k2 < n2; k2 += 8) {
               const float t2 = cand_s[r2 * kRowRankCap + k2];
               rank += (t2 > sc) || (t2 == sc && cand_i[r2 * kRowRankCap + k2] < i);
             }
           }
-          if (rank < rem) {
-            atomicAdd(&sh.cta_taken[rr], 1);
-            if (rr == (int)r) atomicOr(&sh.selw[(i - my0) >> 5], 1u << ((i - my0) & 31));
-          }
+        }
+        rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+        rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+        rank += __shfl_xor_sync(0xffffffffu, rank, 4);
+        if (c < nplay && sub == 0 && rank < rem) {
+          atomicAdd(&sh.cta_taken[rr], 1);
+          if (rr == (int)r) atomicOr(&sh.selw[(i - my0) >> 5], 1u << ((i - my0) & 31));
         }
         __syncthreads();
         if (tid < (int)C) sh.cta_sel[tid] += sh.cta_taken[tid];
@@ -1037,6 +1071,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
     }
   }
 
+  if (!load_ok) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
   // ---- ordered output: thread t writes the selected positions of bitmap word t
   const uint32_t sel = tid < nwords ? sh.selw[tid] : 0u;
   int cnt;

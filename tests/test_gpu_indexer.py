@@ -178,6 +178,24 @@ def test_warp_runs_across_query_boundaries(B, N):
     _check_all(L.q_idx, L.w_idx, L.z, np.full(B, N, np.int32), cfg.K)
 
 
+@pytest.mark.parametrize("B,T,H_I", [(40, 2, 8), (37, 3, 4), (9, 5, 8), (21, 3, 8), (12, 2, 16)])
+def test_decode_key_tiles_split_over_ctas_ragged(B, T, H_I):
+    """A few query tokens per sequence (the N = 16 tensor-core scoring for H_I = 4, 8),
+    ragged visible counts (0, 1, tile edges, full):
+    the key tiles each (sequence, token tile) needs are counted on the device and split
+    evenly over the CTAs, so a CTA's run starts and ends inside sequences and token
+    tiles; every query must get its own keys, indexer rows and weights."""
+    rng = np.random.default_rng(1000 + B * T * H_I)
+    N, K = 3000, 200
+    q = ci.bf16_bits(rng.standard_normal((B, T, H_I, 64), dtype=np.float32))
+    w = np.abs(rng.standard_normal((B, T, H_I), dtype=np.float32))
+    z = ci.bf16_bits(rng.standard_normal((B, N, 64), dtype=np.float32))
+    edges = np.array([0, 1, 127, 128, 129, 200, 201, 2999, 3000, 1500], dtype=np.int32)
+    nvis = np.where(rng.random(B * T) < 0.5, edges[rng.integers(0, edges.size, B * T)],
+                    rng.integers(0, N + 1, B * T)).astype(np.int32)
+    _check_all(q, w, z, nvis, K)
+
+
 def test_deterministic_repeat():
     cfg = ci.scaled(ci.DECODE_128K, B=4, N=8192, K=1024, modes=(ci.FULL,))
     inp = ci.make_decode_inputs(cfg, with_x=False)
