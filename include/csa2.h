@@ -249,7 +249,8 @@ CSA2_API int csa2_swa_merge(int B, int T, int H, const void* q,
  * Arguments as in those two calls; o: fp32 [B][T][H][d_v], lse: fp32 [B][T][H]
  * (nullable). Limits: H % 16 == 0, H <= 64, d_v == 512, K <= 4096, n_win <= 256.
  * An empty selection and an empty window give O = 0 and LSE = -inf. ws: the
- * 256-byte status header is enough. q and the window rows: finite, |x| <= 65504
+ * 256-byte status header is enough; csa2_workspace_bytes(B, T, H, 0, K) bytes also
+ * hold the split exchange (faster with few queries). q and the window rows: finite, |x| <= 65504
  * (CSA2_DEV_RANGE otherwise, as in csa2_sparse_decode).
  */
 CSA2_API int csa2_decode_attention(int B, int T, int H, const void* q,
@@ -334,9 +335,15 @@ CSA2_API int csa2_check_bounded_wait(int64_t limit_ns, void* ws, size_t ws_bytes
 
 /* Workspace bytes that cover every call above with these or smaller sizes: a
  * 256-byte header (the device status word), then for csa2_index_topk two uint32
- * score-range words per query (B*T*8 bytes rounded up to 256) and the fp32
- * indexer scores ([B*T][n_max rounded up to 1024]). The attention calls need
- * only the header. One workspace serves one stream at a time. */
+ * score-range words per query (B*T*8 bytes rounded up to 256), the fp32 indexer
+ * scores ([B*T][n_max rounded up to 1024]) and the REINDEX_POOL block lists, and
+ * last, when B*T <= 128, the attention calls' split exchange (512 KiB per query:
+ * with few queries each query's keys are split over a cluster of 2 or 4 CTAs, whose
+ * partial outputs meet in the last nsplit x 128 KiB per query of the workspace).
+ * The attention calls need only the header: with less room than the exchange
+ * (past the header and the range words) the splits merge through distributed
+ * shared memory instead, which is slower. One workspace serves one stream at a
+ * time. */
 CSA2_API size_t csa2_workspace_bytes(int B, int T, int H, int64_t n_max, int K);
 
 /* Zero the whole workspace (status word and score-range words) once after

@@ -109,6 +109,7 @@ struct OutArgs {
   float* lse;             // [Q][H] (nullable)
   const float* o_ext;     // external normalised branch (SWA merge), nullable
   const float* lse_ext;
+  float* xchg;            // split exchange through L2: [Q][owner][source][64][512 / nsplit], nullable
 };
 
 // AND of a predicate over the `n` threads of named barrier `id` (all get the result).
@@ -750,7 +751,121 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
   allow_dependents();
   __syncthreads();
   const bool has = ntiles > 0 && !*abort_flag;
-  if (nsplit <= 4) {
+  if (nsplit > 1 && nsplit <= 4 && out.xchg != nullptr) {
+    // CTA o owns value dims [o*Dn, (o+1)*Dn). Each split writes its unnormalised O^T
+    // rows of the peers' dims to the exchange buffer in global memory (L2) as soon as
+    // its last P.V is done, pushes its (max, sum) per head to every peer, and meets the
+    // cluster once; each owner then weights every split's rows by exp2(m_s - M) / L,
+    // adds them to its own rows (TMEM) and drops the exchange lines from L2 unwritten.
+    constexpr float kLn2 = 0.69314718055994530942f, kLog2e = 1.4426950408889634074f;
+    const int Dn = kDV / (int)nsplit, tiles_own = Dn / 128;
+    const int tid = threadIdx.x;
+    const int quarter = warp & 3, half = warp >> 2;
+    const int e = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // [owner o][source s][head][Dn dims] of this query
+    float* xq = out.xchg + (size_t)qi * nsplit * kDV * 64;
+    auto part = [&](int o, int s) { return xq + ((size_t)o * nsplit + s) * Dn * 64; };
+    if (tid < 64) {
+      const float m = has ? ms.mrun[tid] : -INFINITY;
+      const float sm = has ? ms.lsum[tid] : 0.f;
+      for (uint32_t p = 0; p < nsplit; ++p) {
+        st_cluster_f32(map_rank(smem_u32(&ms.ml_in[sp][0][tid]), p), m);
+        st_cluster_f32(map_rank(smem_u32(&ms.ml_in[sp][1][tid]), p), sm);
+      }
+    }
+    if (warp < 8) {
+      // consecutive lanes hold consecutive dims: every store of a warp is one 128-byte line
+      for (int i = 0; i < 4; ++i) {
+        const int o = i / tiles_own;
+        if (o == sp) continue;
+        uint32_t r[32];
+        if (has) {
+          tmem_ld32(tmem + lane_off + kColO + 64 * i + 32 * half, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = 0u;
+        }
+        float* dst = part(o, sp) + (128 * i + e - o * Dn);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) __stcg(dst + (size_t)(32 * half + k) * Dn, __uint_as_float(r[k]));
+      }
+    }
+    // release / acquire at cluster scope: every split's rows and (max, sum) are visible
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    // weights per (split, head) overwrite the pushed maxima
+    if (tid >= 32 && tid < 96) {
+      const int h = tid - 32;
+      float M = -INFINITY;
+      for (uint32_t s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, ms.ml_in[s2][0][h]);
+      const float Mu = M == -INFINITY ? 0.f : M;
+      float L = 0.f;
+      for (uint32_t s2 = 0; s2 < nsplit; ++s2) {
+        const float ls = ms.ml_in[s2][1][h];
+        L += ls > 0.f ? ls * exp2f(ms.ml_in[s2][0][h] - Mu) : 0.f;
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      for (uint32_t s2 = 0; s2 < nsplit; ++s2) {
+        const float ls = ms.ml_in[s2][1][h];
+        ms.ml_in[s2][0][h] = ls > 0.f ? exp2f(ms.ml_in[s2][0][h] - Mu) * inv : 0.f;
+      }
+      if (sp == 0 && out.lse && h < H)
+        out.lse[(int64_t)qi * H + h] = L > 0.f ? (Mu + log2f(L)) * kLn2 : -INFINITY;
+      (void)kLog2e;
+    }
+    __syncthreads();
+    if (warp < 8) {
+      float* o = out.o + (int64_t)qi * H * kDV;
+      for (int j = 0; j < tiles_own; ++j) {
+        const int i = sp * tiles_own + j;
+        const int dl = 128 * j + e, d = 128 * i + e;
+        uint32_t r[32];
+        if (has) {
+          tmem_ld32(tmem + lane_off + kColO + 64 * i + 32 * half, r);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = 0u;
+        }
+        float acc[32];
+#pragma unroll
+        for (int k = 0; k < 32; k += 4) {
+          const float4 w = *reinterpret_cast<const float4*>(&ms.ml_in[sp][0][32 * half + k]);
+          acc[k] = __uint_as_float(r[k]) * w.x;
+          acc[k + 1] = __uint_as_float(r[k + 1]) * w.y;
+          acc[k + 2] = __uint_as_float(r[k + 2]) * w.z;
+          acc[k + 3] = __uint_as_float(r[k + 3]) * w.w;
+        }
+        for (int s2 = 0; s2 < (int)nsplit; ++s2) {
+          if (s2 == sp) continue;
+          const float* src = part(sp, s2) + dl;
+          float v[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = __ldcg(src + (size_t)(32 * half + k) * Dn);
+#pragma unroll
+          for (int k = 0; k < 32; k += 4) {
+            const float4 w = *reinterpret_cast<const float4*>(&ms.ml_in[s2][0][32 * half + k]);
+            acc[k] += w.x * v[k]; acc[k + 1] += w.y * v[k + 1];
+            acc[k + 2] += w.z * v[k + 2]; acc[k + 3] += w.w * v[k + 3];
+          }
+          // every lane has its values: lane l drops the line of head 32 half + l that this
+          // warp read (the next call writes it again before reading it)
+          __syncwarp();
+          const float* line = part(sp, s2) + (size_t)(32 * half + lane) * Dn + 128 * j + 32 * quarter;
+          asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int h = 32 * half + k;
+          if (h < H) o[(int64_t)h * kDV + d] = acc[k];
+        }
+      }
+    }
+    // (nothing of this CTA's shared memory is read or written by a peer after the barrier)
+  } else if (nsplit <= 4) {
     // CTA o owns value dims [o*Dn, (o+1)*Dn) (whole 128-dim M-tiles). Each split
     // stages its raw O^T rows of the peers' M-tiles (rows of 64 heads, 16-byte pieces
     // swizzled by row) while the slower splits finish, and ships each peer's slice
@@ -1078,7 +1193,7 @@ static cudaError_t launch_tc(const CUtensorMap& tq, const Fp4Src& f, const RowSr
 cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t* codes,
                                const uint8_t* scales, int64_t n_stride, const int32_t* idx, int K,
                                float scale_log2, float* o_g, float* lse_g, int nsplit,
-                               uint32_t* status, cudaStream_t st) {
+                               float* xchg, uint32_t* status, cudaStream_t st) {
   const int Q = B * T;
   if (Q == 0) return cudaSuccess;
   if (nsplit < 1 || nsplit > kMaxSplitsTC || (nsplit & (nsplit - 1))) return cudaErrorInvalidValue;
@@ -1089,7 +1204,7 @@ cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t
   CUtensorMap tq, dummy;
   memset(&dummy, 0, sizeof(dummy));
   if (!encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64)) return cudaErrorInvalidValue;
-  OutArgs out{o_g, lse_g, nullptr, nullptr};
+  OutArgs out{o_g, lse_g, nullptr, nullptr, xchg};
   return launch_tc<kSparse>(tq, f, r, dummy, Q, T, H, scale_log2, nsplit, split_len, out, status, st);
 }
 
@@ -1109,7 +1224,7 @@ cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa
     return cudaErrorInvalidValue;
   Fp4Src f{nullptr, nullptr, 0, nullptr, 0};
   RowSrc r{s_stride, win_start, win_len, n_win};
-  OutArgs out{o_out, lse_out, o_g, lse_g};
+  OutArgs out{o_out, lse_out, o_g, lse_g, nullptr};
   return launch_tc<kWindow>(tq, f, r, tm, Q, T, H, scale_log2, nsplit, kTK, out, status, st);
 }
 
@@ -1117,7 +1232,7 @@ cudaError_t launch_decode_attn(int B, int T, int H, const void* q, const uint8_t
                                const uint8_t* scales, int64_t n_stride, const int32_t* idx, int K,
                                const void* swa, int64_t s_stride, const int32_t* win_start,
                                const int32_t* win_len, int n_win, float scale_log2, float* o,
-                               float* lse, int nsplit, uint32_t* status, cudaStream_t st) {
+                               float* lse, int nsplit, float* xchg, uint32_t* status, cudaStream_t st) {
   const int Q = B * T;
   if (Q == 0) return cudaSuccess;
   if (nsplit < 1 || nsplit > kMaxSplitsTC || (nsplit & (nsplit - 1))) return cudaErrorInvalidValue;
@@ -1130,7 +1245,7 @@ cudaError_t launch_decode_attn(int B, int T, int H, const void* q, const uint8_t
   if (!encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64)) return cudaErrorInvalidValue;
   if (s_stride > 0 && !encode_tensor_map_2d_bf16(&tm, swa, CSA2_D_KV, (uint64_t)B * s_stride, 64, kTK))
     return cudaErrorInvalidValue;
-  OutArgs out{o, lse, nullptr, nullptr};
+  OutArgs out{o, lse, nullptr, nullptr, xchg};
   return launch_tc<kFused>(tq, f, r, tm, Q, T, H, scale_log2, nsplit, split_len, out, status, st);
 }
 

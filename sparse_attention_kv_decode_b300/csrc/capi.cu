@@ -154,11 +154,30 @@ const char* csa2_status_string(int s) {
   }
 }
 
+// The attention's split exchange (few queries, clusters of 2 or 4 CTAs): per query
+// nsplit x 512 dims x 64 heads fp32 partial outputs, at the end of the workspace.
+constexpr size_t kXchgPerSplit = (size_t)512 * 64 * 4;
+constexpr int64_t kXchgMaxQ = 128;   // clusters of more than one CTA need Q <= SMs / 2
+static size_t xchg_bytes(int64_t Q) { return Q <= kXchgMaxQ ? (size_t)Q * 4 * kXchgPerSplit : 0; }
+static size_t index_ws_bytes(int64_t Q, int64_t n_max, int K) {
+  return kWsHeader + range_bytes(Q) + scores_bytes(Q, n_max) + pool_bytes(Q, K);
+}
+// The exchange buffer of an attention call with nsplit CTAs per query, placed at the end
+// of the workspace past its first `front` bytes; nullptr when the call needs none or the
+// workspace is too small for it (the splits then merge through distributed shared memory).
+static float* attn_xchg(void* ws, size_t ws_bytes, size_t front, int64_t Q, int nsplit) {
+  if (nsplit < 2 || nsplit > 4 || ws == nullptr) return nullptr;
+  const size_t need = (size_t)Q * nsplit * kXchgPerSplit;
+  if (ws_bytes < front + need) return nullptr;
+  const size_t at = (ws_bytes - need) & ~(size_t)255;
+  return at >= front ? reinterpret_cast<float*>(static_cast<char*>(ws) + at) : nullptr;
+}
+
 size_t csa2_workspace_bytes(int B, int T, int H, int64_t n_max, int K) {
   if (B < 0 || T < 0 || H < 0 || n_max < 0 || K < 0) return 0;
-  (void)H; (void)K;
+  (void)H;
   const int64_t Q = (int64_t)B * T;
-  return kWsHeader + range_bytes(Q) + scores_bytes(Q, n_max) + pool_bytes(Q, K);
+  return index_ws_bytes(Q, n_max, K) + xchg_bytes(Q);
 }
 
 int csa2_workspace_init(void* ws, size_t ws_bytes, void* stream) {
@@ -272,18 +291,22 @@ static int check_decode_attention(int B, int T, int H, const void* q, const uint
   return CSA2_OK;
 }
 
+// front: the workspace bytes in use by the call's other parts (the split exchange goes
+// past them)
 static int decode_attention_launch(int B, int T, int H, const void* q, const uint8_t* kv_codes,
                                    const uint8_t* kv_scales, int64_t n_stride, const int32_t* idx,
                                    int K, const void* swa_kv, int64_t s_stride,
                                    const int32_t* win_start, const int32_t* win_len, int n_win,
                                    float softmax_scale, float* o, float* lse, void* ws,
-                                   void* stream) {
-  const int nsplit = attn_splits((int64_t)B * T, K, device_sm_count());
+                                   size_t ws_bytes, size_t front, void* stream) {
+  const int64_t Q = (int64_t)B * T;
+  const int nsplit = attn_splits(Q, K, device_sm_count());
   uint32_t* status = static_cast<uint32_t*>(ws);
   const float scale_log2 = softmax_scale * 1.4426950408889634074f;
   return cuda_status(launch_decode_attn(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K, swa_kv,
                                         s_stride, win_start, win_len, n_win, scale_log2, o, lse,
-                                        nsplit, status, (cudaStream_t)stream));
+                                        nsplit, attn_xchg(ws, ws_bytes, front, Q, nsplit), status,
+                                        (cudaStream_t)stream));
 }
 
 // csa2_index_topk; pf_codes / pf_scales (nullable) name the FP4 cache whose rows of the
@@ -413,7 +436,8 @@ int csa2_sparse_decode(int B, int T, int H, const void* q, const uint8_t* kv_cod
   uint32_t* status = static_cast<uint32_t*>(ws);
   const float scale_log2 = softmax_scale * 1.4426950408889634074f;
   return cuda_status(launch_sparse_attn(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K,
-                                        scale_log2, o_g, lse_g, nsplit, status,
+                                        scale_log2, o_g, lse_g, nsplit,
+                                        attn_xchg(ws, ws_bytes, kWsHeader + range_bytes(Q), Q, nsplit), status,
                                         (cudaStream_t)stream));
 }
 
@@ -451,7 +475,8 @@ int csa2_decode_attention(int B, int T, int H, const void* q, const uint8_t* kv_
                                        lse, ws, ws_bytes);
   if (s != CSA2_OK || (int64_t)B * T == 0) return s;
   return decode_attention_launch(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K, swa_kv, s_stride,
-                                 win_start, win_len, n_win, softmax_scale, o, lse, ws, stream);
+                                 win_start, win_len, n_win, softmax_scale, o, lse, ws, ws_bytes,
+                                 kWsHeader + range_bytes((int64_t)B * T), stream);
 }
 
 int csa2_decode_layer(int mode, int B, int T, int H, int H_I, const void* q, const void* q_idx,
@@ -471,7 +496,7 @@ int csa2_decode_layer(int mode, int B, int T, int H, int H_I, const void* q, con
   if (s != CSA2_OK || (int64_t)B * T == 0) return s;
   return decode_attention_launch(B, T, H, q, kv_codes, kv_scales, n_stride, out_idx, K, swa_kv,
                                  s_stride, win_start, win_len, n_win, softmax_scale, o, lse, ws,
-                                 stream);
+                                 ws_bytes, kWsHeader + range_bytes((int64_t)B * T), stream);
 }
 
 }  // extern "C"

@@ -98,7 +98,7 @@ cudaError_t launch_copy_idx(const int32_t* src, int32_t* dst, int64_t n, cudaStr
 cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t* codes,
                                const uint8_t* scales, int64_t n_stride, const int32_t* idx,
                                int K, float scale_log2, float* o_g, float* lse_g, int nsplit,
-                               uint32_t* status, cudaStream_t st);
+                               float* xchg, uint32_t* status, cudaStream_t st);
 cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa,
                              int64_t s_stride, const int32_t* win_start, const int32_t* win_len,
                              int n_win, float scale_log2, const float* o_g, const float* lse_g,
@@ -107,7 +107,7 @@ cudaError_t launch_decode_attn(int B, int T, int H, const void* q, const uint8_t
                                const uint8_t* scales, int64_t n_stride, const int32_t* idx, int K,
                                const void* swa, int64_t s_stride, const int32_t* win_start,
                                const int32_t* win_len, int n_win, float scale_log2, float* o,
-                               float* lse, int nsplit, uint32_t* status, cudaStream_t st);
+                               float* lse, int nsplit, float* xchg, uint32_t* status, cudaStream_t st);
 cudaError_t launch_ced_project(const void* h, int64_t rows, int d_model, const void* w_kv,
                                const void* w_z, int n_layers, uint8_t* codes, uint8_t* scales,
                                void* z_out, uint32_t* status, cudaStream_t st);
