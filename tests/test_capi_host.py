@@ -108,9 +108,12 @@ def test_workspace_size_monotone(L):
     c = L.csa2_workspace_bytes(64, 1, 64, 65536, 2048)
     assert 256 < a <= b <= c
     # header + range words + fp32 scores + the candidate pool of a REINDEX call (block ids
-    # [Q][K] and one visible count per query)
-    assert a == 256 + 256 + 32 * 32768 * 4 + 32 * 2048 * 4 + 256
-    assert L.csa2_workspace_bytes(1, 1, 64, 0, 2048) == 512 + 2048 * 4 + 256
+    # [Q][K] and one visible count per query) + the attention's split exchange (up to 4
+    # splits x 512 dims x 64 heads fp32 per query, for at most 128 queries)
+    xchg = 4 * 512 * 64 * 4
+    assert a == 256 + 256 + 32 * 32768 * 4 + 32 * 2048 * 4 + 256 + 32 * xchg
+    assert L.csa2_workspace_bytes(1, 1, 64, 0, 2048) == 512 + 2048 * 4 + 256 + xchg
+    assert L.csa2_workspace_bytes(129, 1, 64, 0, 1) == 256 + 1280 + 768 + 768   # no exchange past 128
     assert L.csa2_workspace_bytes(-1, 1, 64, 10, 10) == 0
 
 
