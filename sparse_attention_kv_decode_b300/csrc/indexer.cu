@@ -686,7 +686,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_row_kernel(
 //            of them and of b* follow; local positions above b* are selected, b*'s stay
 //            in play (bitmap words built with ballots);
 //   exact    when at most kRowRankCap scores remain in play, each CTA pushes its
-//            (score, position) list; after the barrier every CTA ranks all of them by
+//            (score, position) pairs into one list of all of them (CTA r's after those
+//            of the CTAs before it); after the barrier every CTA ranks the whole list by
 //            (score desc, position asc), so it knows every CTA's selected count;
 //   refine   otherwise the scores in play are binned by their integer keys over the
 //            cluster-wide key range (one barrier for the range, one for the histogram);
@@ -702,6 +703,7 @@ struct ClusterShared {
   int cta_sel[kMaxCluster];          // selected positions of each CTA so far
   int cta_play[kMaxCluster];         // positions in play of each CTA
   int cta_taken[kMaxCluster];        // ranked and taken in the exact round
+  int cta_warp[kMaxCluster][kRowThreads / 32];   // per-warp counts above b*, per CTA
   int bstar, above;
   uint32_t rng[2];
   uint64_t bar_chunk[kRowThreads / 64];   // one per 1024-score chunk of the slice (<= 16384)
@@ -761,15 +763,20 @@ __device__ __forceinline__ int cluster_bstar(ClusterShared& sh, const uint16_t* 
     sh.above = above + h1;
   }
   __syncthreads();
-  const int bstar = sh.bstar;
+  const int bstar = sh.bstar, warp = tid >> 5;
+  // every CTA's count above b*: per-warp sums, then one warp per CTA adds its 32 of them
   for (uint32_t rr = 0; rr < C; ++rr) {
     const int a = (b1 > bstar ? (int)hist_in[rr * kRowBins + b1] : 0) +
                   (b0 > bstar ? (int)hist_in[rr * kRowBins + b0] : 0);
     const int s = __reduce_add_sync(0xffffffffu, a);
-    if (lane == 0 && s) atomicAdd(&sh.cta_sel[rr], s);
+    if (lane == 0) sh.cta_warp[rr][warp] = s;
   }
   if (tid < (int)C) sh.cta_play[tid] = hist_in[tid * kRowBins + bstar];
   __syncthreads();
+  if (warp < (int)C) {
+    const int s = __reduce_add_sync(0xffffffffu, sh.cta_warp[warp][lane]);
+    if (lane == 0) sh.cta_sel[warp] += s;
+  }
   int n = 0;
   for (uint32_t rr = 0; rr < C; ++rr) n += sh.cta_play[rr];
   return n;
@@ -788,8 +795,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   float* sv = reinterpret_cast<float*>(cl_raw);                                     // [slice_cap]
   uint16_t* hist_in = reinterpret_cast<uint16_t*>(cl_raw + (size_t)slice_cap * 4);  // [C][kRowBins]
-  float* cand_s = reinterpret_cast<float*>(hist_in + (size_t)C * kRowBins);          // [C][kRowRankCap]
-  int* cand_i = reinterpret_cast<int*>(cand_s + (size_t)C * kRowRankCap);            // [C][kRowRankCap]
+  float* cand_s = reinterpret_cast<float*>(hist_in + (size_t)C * kRowBins);          // [kRowRankCap]
+  int* cand_i = reinterpret_cast<int*>(cand_s + kRowRankCap);                        // [kRowRankCap]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int qi = blockIdx.y;
   if (tid < kRowThreads / 64) {
@@ -944,38 +951,37 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
       const uint32_t cw = tid < nwords ? sh.candw[tid] : 0u;
       if (nplay <= kRowRankCap) {
         // exact: push this CTA's (score, position) list to every peer
+        // one list of all nplay candidates, CTA r's at offset sum(cta_play[< r])
         int tot;
         int pre = block_excl_scan(__popc(cw), sh.scan, tot);
+        for (uint32_t rr = 0; rr < r; ++rr) pre += sh.cta_play[rr];
         for (uint32_t m = cw; m; m &= m - 1u, ++pre) {
           const int lp = 32 * tid + __ffs(m) - 1;
           for (uint32_t pr = 0; pr < C; ++pr) {
-            st_remote_u32(reinterpret_cast<uint32_t*>(&cand_s[r * kRowRankCap + pre]), pr, __float_as_uint(sv[lp]));
-            st_remote_u32(reinterpret_cast<uint32_t*>(&cand_i[r * kRowRankCap + pre]), pr, (uint32_t)(my0 + lp));
+            st_remote_u32(reinterpret_cast<uint32_t*>(&cand_s[pre]), pr, __float_as_uint(sv[lp]));
+            st_remote_u32(reinterpret_cast<uint32_t*>(&cand_i[pre]), pr, (uint32_t)(my0 + lp));
           }
         }
         barrier();
-        // rank every candidate of every CTA (the counts per CTA are sh.cta_play): eight
-        // threads per candidate, each comparing it with every eighth of the others
+        // rank every candidate: eight threads per candidate, each comparing it with every
+        // eighth of the others
         static_assert(kRowRankCap * 8 <= kRowThreads, "eight rankers per candidate");
         const int c = tid >> 3, sub = tid & 7;
-        int rr = 0, rank = 0, i = 0;
+        int rank = 0, i = 0;
         if (c < nplay) {
-          int k = c;
-          while (k >= sh.cta_play[rr]) k -= sh.cta_play[rr++];
-          const float sc = cand_s[rr * kRowRankCap + k];
-          i = cand_i[rr * kRowRankCap + k];
-          for (uint32_t r2 = 0; r2 < C; ++r2) {
-            const int n2 = sh.cta_play[r2];
-            for (int k2 = sub; k2 < n2; k2 += 8) {
-              const float t2 = cand_s[r2 * kRowRankCap + k2];
-              rank += (t2 > sc) || (t2 == sc && cand_i[r2 * kRowRankCap + k2] < i);
-            }
+          const float sc = cand_s[c];
+          i = cand_i[c];
+#pragma unroll 4
+          for (int k2 = sub; k2 < nplay; k2 += 8) {
+            const float t2 = cand_s[k2];
+            rank += (t2 > sc) || (t2 == sc && cand_i[k2] < i);
           }
         }
         rank += __shfl_xor_sync(0xffffffffu, rank, 1);
         rank += __shfl_xor_sync(0xffffffffu, rank, 2);
         rank += __shfl_xor_sync(0xffffffffu, rank, 4);
         if (c < nplay && sub == 0 && rank < rem) {
+          const int rr = i / slice;   // the CTA that holds candidate c
           atomicAdd(&sh.cta_taken[rr], 1);
           if (rr == (int)r) atomicOr(&sh.selw[(i - my0) >> 5], 1u << ((i - my0) & 31));
         }
@@ -1143,7 +1149,7 @@ cudaError_t launch_topk_select(const float* scores, int64_t score_stride, const 
   const int C = select_cluster_size(n_stride, Q);
   const int slice_cap = (int)(((n_stride + C - 1) / C + 31) & ~31);
   if (slice_cap > kRowThreads * 16 || C > kMaxCluster) return cudaErrorInvalidValue;
-  const size_t smem = (size_t)slice_cap * 4 + (size_t)C * kRowBins * 2 + (size_t)C * kRowRankCap * 8;
+  const size_t smem = (size_t)slice_cap * 4 + (size_t)C * kRowBins * 2 + (size_t)kRowRankCap * 8;
   if (smem > kSelSmemMax) return cudaErrorInvalidValue;
   cudaError_t e = set_attr_once(0, (const void*)topk_cluster_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemMax);
