@@ -37,7 +37,7 @@ import csa2_inputs as ci  # noqa: E402
 
 METRIC = "CSA2 FP4 decode steps/s + HBM GB/s vs 8 TB/s; CED KV-proj TFLOP/s"
 CFG = ci.DECODE_128K
-ENTRY_BYTES = 288 + 36
+ENTRY_BYTES = 288 + 36   # per entry as the method stores it (the 60 bytes padding each 384-byte row not counted)
 KEY_BYTES = 64 * 2
 SWA_ROW_BYTES = 576 * 2
 TARGET_HBM_GBS = 8000.0
@@ -724,8 +724,7 @@ def run_cache_append(args, torch, csa2, cfg, dev, stream, flush):
     B, N, W = cfg.B, cfg.N, cfg.W
     g = torch.Generator(device=dev).manual_seed(7)
     swa = torch.zeros((B, 2 * W, 576), dtype=torch.bfloat16, device=dev)
-    codes = torch.zeros((B, N, 288), dtype=torch.uint8, device=dev)
-    scales = torch.zeros((B, N, 36), dtype=torch.uint8, device=dev)
+    codes, scales = csa2.csa2_kv_cache((B, N), device=dev)
     z = torch.zeros((B, N, 64), dtype=torch.bfloat16, device=dev)
     row = torch.randn((B, 576), generator=g, device=dev).to(torch.bfloat16)
     ent = torch.randn((B, 576), generator=g, device=dev)
@@ -933,8 +932,7 @@ def run_ced(args, torch, csa2, dev, peaks):
     b16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
     h, wkv, wz = b16(inp.H), b16(inp.W_kv), b16(inp.W_z)
     del inp
-    codes = torch.empty((cfg.n_layers, cfg.rows, 288), dtype=torch.uint8, device=dev)
-    scales = torch.empty((cfg.n_layers, cfg.rows, 36), dtype=torch.uint8, device=dev)
+    codes, scales = csa2.csa2_kv_cache((cfg.n_layers, cfg.rows), device=dev)
     z = torch.empty((cfg.n_layers, cfg.rows, 64), dtype=torch.bfloat16, device=dev)
     ws = csa2.csa2_workspace(0, 0, 0, 0, 0, device=dev)
     stream = torch.cuda.Stream(device=dev)

@@ -28,6 +28,15 @@
  *    288 bytes of E2M1 codes (channel 2i in the low nibble of byte i, 2i+1 in
  *    the high nibble; sign in bit 3 of the nibble) and 36 bytes of E4M3 scales
  *    (scale j covers channels 16j..16j+15). dequant = e2m1(code) * e4m3(scale).
+ *    Entries are rows of CSA2_ENTRY_BYTES (384) bytes: every kv_codes /
+ *    kv_scales argument below is a pointer to the 288 code bytes / the 36 scale
+ *    bytes of the first entry, and entry n of either is CSA2_ENTRY_BYTES * n
+ *    bytes further on. The library's own layout (the one that saves DRAM
+ *    traffic) is one record per entry: kv_scales = kv_codes + 288, then 60
+ *    bytes of padding the library never reads or writes; with 128-byte aligned
+ *    records a gathered entry is exactly three 128-byte L2 lines (324 bytes
+ *    used of 384). Separate code and scale arrays with the same 384-byte row
+ *    stride work too (and cost more DRAM traffic).
  */
 #ifndef CSA2_H_
 #define CSA2_H_
@@ -65,6 +74,7 @@ typedef enum { CSA2_F32 = 0, CSA2_BF16 = 1 } csa2_dtype;
 #define CSA2_D_IDX 64        /* indexer key / query width                    */
 #define CSA2_CODE_BYTES 288  /* E2M1 bytes per entry                         */
 #define CSA2_SCALE_BYTES 36  /* E4M3 scale bytes per entry                   */
+#define CSA2_ENTRY_BYTES 384 /* row stride of kv_codes and kv_scales (bytes)  */
 
 /* Device status bits (csa2_read_device_status). */
 #define CSA2_DEV_BAD_INDEX 0x1u   /* sparse_decode saw idx >= n_stride or < -1 */
@@ -78,15 +88,15 @@ typedef enum { CSA2_F32 = 0, CSA2_BF16 = 1 } csa2_dtype;
  *
  * (a) Quantise-only (w_kv == NULL and w_z == NULL): h is [rows][576] in
  *     h_dtype (fp32 or bf16), d_model must be 576, n_layers must be 1 and
- *     z_out must be NULL. Writes kv_codes [rows][288] and kv_scales [rows][36].
+ *     z_out must be NULL. Writes kv_codes and kv_scales rows 0..rows-1.
  *     Per 16-channel block: s = E4M3_RNE_satfinite(fl32(amax / 6)); each code
  *     = E2M1_RNE_satfinite(fl32(x / s)); a zero scale stores zero codes and a
  *     value rounding to zero stores +0. (FP4 Main KV Cache, picx.dev summary.)
  * (b) CED projection, Eq. (1): C_l = H W_l^KV and Z_l = H W_l^Z for
  *     l = 0..n_layers-1. h is bf16 [rows][d_model]; w_kv is bf16
  *     [n_layers][576][d_model] and w_z bf16 [n_layers][64][d_model] (row c
- *     holds the weights of output channel c, i.e. W^T). Writes kv_codes
- *     [n_layers][rows][288] and kv_scales [n_layers][rows][36] (C_l quantised
+ *     holds the weights of output channel c, i.e. W^T). Writes kv_codes /
+ *     kv_scales rows l*rows .. l*rows+rows-1 for layer l (C_l quantised
  *     as in (a) from its fp32 value) and z_out bf16 [n_layers][rows][64]
  *     (round to nearest even). Requires h_dtype == CSA2_BF16,
  *     d_model % 64 == 0, rows <= 2^30, 16-byte aligned h/w_kv/w_z/kv_codes/
@@ -140,7 +150,7 @@ CSA2_API int csa2_index_topk(int mode, int B, int T, int H_I,
 
 /*
  * csa2_index_topk_prefetch - csa2_index_topk whose selection also requests the FP4
- * rows (kv_codes [B][n_stride][288], kv_scales [B][n_stride][36], the cache the
+ * rows (kv_codes / kv_scales rows [B][n_stride], the cache the
  * attention that follows gathers from) of the entries it selects into L2.
  *
  * Not in the pages: a scheduling aid with the same results as csa2_index_topk;
@@ -202,7 +212,7 @@ CSA2_API int csa2_index_topk_noalloc(int mode, int B, int T, int H_I,
  *   O_g[b,t,h,:] = sum_j softmax(s)_j * C[b, idx_j, 0:d_v],
  *   LSE_g[b,t,h] = log sum_j exp(s_j)  (natural log),
  * over the j with idx >= 0; C is dequantised in registers from kv_codes
- * [B][n_stride][288] / kv_scales [B][n_stride][36]. One KV entry is shared by
+ * / kv_scales rows [B][n_stride]. One KV entry is shared by
  * all heads (MQA). An empty selection gives O_g = 0 and LSE_g = -inf.
  * q: bf16 [B][T][H][576]; idx: int32 [B][T][K]; o_g: fp32 [B][T][H][d_v];
  * lse_g: fp32 [B][T][H]. Limits: H % 16 == 0, H <= 64, d_v == 512, K <= 4096.
@@ -299,7 +309,7 @@ CSA2_API int csa2_decode_layer(int mode, int B, int T, int H, int H_I, const voi
  *  - entry: when (p + 1) % ratio == 0 the token completes entry
  *    e = (p + 1) / ratio - 1: entry_kv [B][576] (entry_dtype fp32 or bf16; how
  *    tokens become an entry is the caller's) is quantised as csa2_encode_kv (a)
- *    into kv_codes [B][n_stride][288] / kv_scales [B][n_stride][36] row e, and
+ *    into kv_codes / kv_scales row [b][e] of [B][n_stride], and
  *    entry_z [B][64] bf16 is copied to z [B][n_stride][64] row e; an entry past
  *    the cache (e >= n_stride) is skipped and sets CSA2_DEV_BAD_INDEX;
  *  - n_visible[b] = (p + 1) / ratio (the entries visible to this token);

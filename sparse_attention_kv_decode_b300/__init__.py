@@ -30,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libcsa2.so")
 FULL, REINDEX, REUSE, REINDEX_POOL = 0, 1, 2, 3
 F32, BF16 = 0, 1
 D_KV, D_LATENT, D_IDX = 576, 512, 64
-CODE_BYTES, SCALE_BYTES = 288, 36
+CODE_BYTES, SCALE_BYTES, ENTRY_BYTES = 288, 36, 384
 
 STATUS = {0: "CSA2_OK", 1: "CSA2_ERR_INVALID_ARG", 2: "CSA2_ERR_UNSUPPORTED", 3: "CSA2_ERR_WORKSPACE",
           4: "CSA2_ERR_CUDA", 5: "CSA2_ERR_TIMEOUT", 6: "CSA2_ERR_DEVICE_CHECK"}
@@ -121,6 +121,32 @@ def _dev(t: torch.Tensor, name: str, dtypes, shape=None):
     return t
 
 
+def _dev_kv(t: torch.Tensor, name: str, lead, width: int):
+    """kv_codes / kv_scales: uint8 [*lead, width] whose rows are ENTRY_BYTES apart."""
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.uint8:
+        raise ValueError(f"{name}: dtype {t.dtype} is not uint8")
+    if lead is not None and tuple(t.shape) != tuple(lead) + (width,):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(lead) + (width,)}")
+    expect = ENTRY_BYTES
+    ok = t.stride(-1) == 1
+    for d in range(t.dim() - 2, -1, -1):
+        ok = ok and (t.shape[d] == 1 or t.stride(d) == expect)
+        expect *= t.shape[d]
+    if not ok:
+        raise ValueError(f"{name}: rows must be {ENTRY_BYTES} bytes apart (use csa2_kv_cache)")
+    return t
+
+
+def csa2_kv_cache(lead, device=None):
+    """A zeroed FP4 cache of entries [*lead]: one ENTRY_BYTES record per entry holding
+    the 288 code bytes, the 36 scale bytes and 60 bytes of padding. Returns the
+    (codes [*lead, 288], scales [*lead, 36]) views the calls take."""
+    kv = torch.zeros(tuple(lead) + (ENTRY_BYTES,), dtype=torch.uint8, device=device)
+    return kv[..., :CODE_BYTES], kv[..., CODE_BYTES:CODE_BYTES + SCALE_BYTES]
+
+
 _B16 = (torch.bfloat16, torch.int16, torch.uint16)
 
 
@@ -154,9 +180,10 @@ def csa2_encode_kv(h: torch.Tensor, w_kv: Optional[torch.Tensor] = None, w_z: Op
                    z_out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None):
     """Quantise rows h [..., 576] (fp32/bf16) to FP4, or run the CED projection.
 
-    Quantise-only returns (codes [..., 288] u8, scales [..., 36] u8).
-    With w_kv [L, 576, d] and w_z [L, 64, d] (bf16), h is bf16 [rows, d] and the
-    result is (codes [L, rows, 288], scales [L, rows, 36], z [L, rows, 64] bf16).
+    Quantise-only returns (codes [..., 288] u8, scales [..., 36] u8), views of one
+    record per entry (csa2_kv_cache). With w_kv [L, 576, d] and w_z [L, 64, d] (bf16),
+    h is bf16 [rows, d] and the result is (codes [L, rows, 288], scales [L, rows, 36],
+    z [L, rows, 64] bf16).
     """
     L = _lib()
     if w_kv is None and w_z is None:
@@ -165,12 +192,10 @@ def csa2_encode_kv(h: torch.Tensor, w_kv: Optional[torch.Tensor] = None, w_z: Op
             raise ValueError("h must have 576 channels")
         lead = tuple(h.shape[:-1])
         rows = h.numel() // D_KV
-        if kv_codes is None:
-            kv_codes = torch.empty(lead + (CODE_BYTES,), dtype=torch.uint8, device=h.device)
-        if kv_scales is None:
-            kv_scales = torch.empty(lead + (SCALE_BYTES,), dtype=torch.uint8, device=h.device)
-        _dev(kv_codes, "kv_codes", (torch.uint8,), lead + (CODE_BYTES,))
-        _dev(kv_scales, "kv_scales", (torch.uint8,), lead + (SCALE_BYTES,))
+        if kv_codes is None and kv_scales is None:
+            kv_codes, kv_scales = csa2_kv_cache(lead, device=h.device)
+        _dev_kv(kv_codes, "kv_codes", lead, CODE_BYTES)
+        _dev_kv(kv_scales, "kv_scales", lead, SCALE_BYTES)
         dt = F32 if h.dtype == torch.float32 else BF16
         _check(L.csa2_encode_kv(_ptr(h), dt, rows, D_KV, None, None, 1, _ptr(kv_codes), _ptr(kv_scales),
                                 None, None, 0, _stream(stream)), "csa2_encode_kv")
@@ -180,14 +205,12 @@ def csa2_encode_kv(h: torch.Tensor, w_kv: Optional[torch.Tensor] = None, w_z: Op
     n_layers = w_kv.shape[0]
     _dev(w_kv, "w_kv", _B16, (n_layers, D_KV, d_model))
     _dev(w_z, "w_z", _B16, (n_layers, D_IDX, d_model))
-    if kv_codes is None:
-        kv_codes = torch.empty((n_layers, rows, CODE_BYTES), dtype=torch.uint8, device=h.device)
-    if kv_scales is None:
-        kv_scales = torch.empty((n_layers, rows, SCALE_BYTES), dtype=torch.uint8, device=h.device)
+    if kv_codes is None and kv_scales is None:
+        kv_codes, kv_scales = csa2_kv_cache((n_layers, rows), device=h.device)
     if z_out is None:
         z_out = torch.empty((n_layers, rows, D_IDX), dtype=torch.bfloat16, device=h.device)
-    _dev(kv_codes, "kv_codes", (torch.uint8,), (n_layers, rows, CODE_BYTES))
-    _dev(kv_scales, "kv_scales", (torch.uint8,), (n_layers, rows, SCALE_BYTES))
+    _dev_kv(kv_codes, "kv_codes", (n_layers, rows), CODE_BYTES)
+    _dev_kv(kv_scales, "kv_scales", (n_layers, rows), SCALE_BYTES)
     _dev(z_out, "z_out", _B16, (n_layers, rows, D_IDX))
     if ws is None:
         ws = csa2_workspace(0, 0, 0, 0, 0, device=h.device, stream=stream)
@@ -295,10 +318,10 @@ def csa2_sparse_decode(q: torch.Tensor, kv_codes: torch.Tensor, kv_scales: torch
     L = _lib()
     _dev(q, "q", _B16)
     B, T, H, _ = q.shape
-    _dev(kv_codes, "kv_codes", (torch.uint8,))
+    _dev_kv(kv_codes, "kv_codes", None, CODE_BYTES)
     N = kv_codes.shape[1]
-    _dev(kv_codes, "kv_codes", (torch.uint8,), (B, N, CODE_BYTES))
-    _dev(kv_scales, "kv_scales", (torch.uint8,), (B, N, SCALE_BYTES))
+    _dev_kv(kv_codes, "kv_codes", (B, N), CODE_BYTES)
+    _dev_kv(kv_scales, "kv_scales", (B, N), SCALE_BYTES)
     _dev(idx, "idx", (torch.int32,))
     K = idx.shape[2]
     _dev(idx, "idx", (torch.int32,), (B, T, K))
@@ -355,10 +378,10 @@ def csa2_decode_attention(q: torch.Tensor, kv_codes: torch.Tensor, kv_scales: to
     L = _lib()
     _dev(q, "q", _B16)
     B, T, H, _ = q.shape
-    _dev(kv_codes, "kv_codes", (torch.uint8,))
+    _dev_kv(kv_codes, "kv_codes", None, CODE_BYTES)
     N = kv_codes.shape[1]
-    _dev(kv_codes, "kv_codes", (torch.uint8,), (B, N, CODE_BYTES))
-    _dev(kv_scales, "kv_scales", (torch.uint8,), (B, N, SCALE_BYTES))
+    _dev_kv(kv_codes, "kv_codes", (B, N), CODE_BYTES)
+    _dev_kv(kv_scales, "kv_scales", (B, N), SCALE_BYTES)
     _dev(idx, "idx", (torch.int32,))
     K = idx.shape[2]
     _dev(idx, "idx", (torch.int32,), (B, T, K))
@@ -394,10 +417,10 @@ def csa2_decode_layer(mode: int, q: torch.Tensor, kv_codes: torch.Tensor, kv_sca
     L = _lib()
     _dev(q, "q", _B16)
     B, T, H, _ = q.shape
-    _dev(kv_codes, "kv_codes", (torch.uint8,))
+    _dev_kv(kv_codes, "kv_codes", None, CODE_BYTES)
     N = kv_codes.shape[1]
-    _dev(kv_codes, "kv_codes", (torch.uint8,), (B, N, CODE_BYTES))
-    _dev(kv_scales, "kv_scales", (torch.uint8,), (B, N, SCALE_BYTES))
+    _dev_kv(kv_codes, "kv_codes", (B, N), CODE_BYTES)
+    _dev_kv(kv_scales, "kv_scales", (B, N), SCALE_BYTES)
     _dev(swa_kv, "swa_kv", _B16)
     S = swa_kv.shape[1]
     _dev(swa_kv, "swa_kv", _B16, (B, S, D_KV))
@@ -444,7 +467,8 @@ def csa2_cache_append(n_tokens: torch.Tensor, swa_row: Optional[torch.Tensor] = 
     position; < 0 = idle), swa_row [B, 576] bf16 into the mirrored window ring swa_kv
     [B, S >= 2 n_win, 576] (n_win defaults to S // 2), and every ratio-th token the
     compressed entry entry_kv [B, 576] (fp32/bf16, FP4-encoded into kv_codes [B, N, 288]
-    / kv_scales [B, N, 36]) and its key entry_z [B, 64] (into z [B, N, 64]); writes
+    / kv_scales [B, N, 36], rows ENTRY_BYTES apart as csa2_kv_cache makes them) and its
+    key entry_z [B, 64] (into z [B, N, 64]); writes
     n_visible, win_start, win_len [B] int32 when given; advance increments n_tokens."""
     L = _lib()
     _dev(n_tokens, "n_tokens", (torch.int32,))
@@ -461,11 +485,11 @@ def csa2_cache_append(n_tokens: torch.Tensor, swa_row: Optional[torch.Tensor] = 
         _dev(swa_row, "swa_row", _B16, (B, D_KV))
     N = 0
     if kv_codes is not None:
-        _dev(kv_codes, "kv_codes", (torch.uint8,))
+        _dev_kv(kv_codes, "kv_codes", None, CODE_BYTES)
         N = kv_codes.shape[1]
-        _dev(kv_codes, "kv_codes", (torch.uint8,), (B, N, CODE_BYTES))
+        _dev_kv(kv_codes, "kv_codes", (B, N), CODE_BYTES)
     if kv_scales is not None:
-        _dev(kv_scales, "kv_scales", (torch.uint8,), (B, N, SCALE_BYTES))
+        _dev_kv(kv_scales, "kv_scales", (B, N), SCALE_BYTES)
     if z is not None:
         _dev(z, "z", _B16)
         if kv_codes is None:

@@ -80,8 +80,8 @@ __global__ void __launch_bounds__(kAppendThreads) cache_append_kernel(
       if (entry_kv != nullptr && t < CSA2_D_KV / 16) {
         uint32_t lo, hi, sc;
         quant_block16(v, lo, hi, sc);
-        *reinterpret_cast<uint2*>(codes + row * CSA2_CODE_BYTES + 8 * t) = make_uint2(lo, hi);
-        scales[row * CSA2_SCALE_BYTES + t] = (uint8_t)sc;
+        *reinterpret_cast<uint2*>(codes + row * CSA2_ENTRY_BYTES + 8 * t) = make_uint2(lo, hi);
+        scales[row * CSA2_ENTRY_BYTES + t] = (uint8_t)sc;
       }
       if (entry_z != nullptr && t < CSA2_D_IDX / 8) reinterpret_cast<uint4*>(z + row * CSA2_D_IDX)[t] = zrow;
     }

@@ -92,8 +92,9 @@ static_assert(offsetof(Misc, mrun) % 16 == 0 && offsetof(Misc, ml_in) % 16 == 0 
 static_assert((kQBytes + kCBytes) % 16 == 0, "Misc placement");
 
 struct Fp4Src {
-  const uint8_t* codes;   // [B][n_stride][288]
-  const uint8_t* scales;  // [B][n_stride][36]
+  const uint8_t* codes;   // entry rows [B][n_stride], CSA2_ENTRY_BYTES apart
+  const uint8_t* scales;  // (same row stride)
+  bool record;            // scales == codes + 288: one row holds both
   int64_t n_stride;
   const int32_t* idx;     // [Q][K]
   int K;
@@ -283,8 +284,8 @@ __device__ __forceinline__ void dequant_piece(uint8_t* sC, int row, int pc, cons
 __device__ __forceinline__ void load_piece(const uint8_t* cbase, const uint8_t* sbase, int ent, int pc,
                                            uint4& w, uint32_t& s2) {
   if (ent >= 0) {
-    w = __ldg(reinterpret_cast<const uint4*>(cbase + (int64_t)ent * CSA2_CODE_BYTES) + pc);
-    s2 = __ldg(reinterpret_cast<const unsigned short*>(sbase + (int64_t)ent * CSA2_SCALE_BYTES) + pc);
+    w = __ldg(reinterpret_cast<const uint4*>(cbase + (int64_t)ent * CSA2_ENTRY_BYTES) + pc);
+    s2 = __ldg(reinterpret_cast<const unsigned short*>(sbase + (int64_t)ent * CSA2_ENTRY_BYTES) + pc);
   } else {
     w = make_uint4(0, 0, 0, 0);
     s2 = 0u;
@@ -456,8 +457,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
       load_piece(cbase, sbase, ec, 16 + (lane & 1), cw[8], sw[4]);
     };
     if (kFp4) {
-      cbase = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
-      sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
+      cbase = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_ENTRY_BYTES;
+      sbase = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_ENTRY_BYTES;
       idx_row = fsrc.idx + (int64_t)qi * fsrc.K;
       if (nt_f > 0) fetch(read_idx(0));
     }
@@ -723,8 +724,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
     // Each tile's FP4 gather is issued one tile ahead into registers; from a cold L2 its
     // latency is longer than the tile's S^T product, so every entry this split gathers
     // after its first tile is requested into L2 once, up front.
-    const uint8_t* cb = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_CODE_BYTES;
-    const uint8_t* sb = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_SCALE_BYTES;
+    const uint8_t* cb = fsrc.codes + (int64_t)b * fsrc.n_stride * CSA2_ENTRY_BYTES;
+    const uint8_t* sb = fsrc.scales + (int64_t)b * fsrc.n_stride * CSA2_ENTRY_BYTES;
     const int32_t* ir = fsrc.idx + (int64_t)qi * fsrc.K;
     // eight index loads in flight per lane before their requests go out
     constexpr int kBatch = 8;
@@ -738,10 +739,15 @@ __global__ void __launch_bounds__(kThreadsTC, 1) attn_tc_kernel(
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         if (ent[k] >= 0 && ent[k] < fsrc.n_stride) {
-          prefetch_l2_bulk(cb + (int64_t)ent[k] * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
-          const uint8_t* s0 = sb + (int64_t)ent[k] * CSA2_SCALE_BYTES;
-          prefetch_l2(s0);
-          prefetch_l2(s0 + CSA2_SCALE_BYTES - 1);
+          if (fsrc.record) {
+            // codes and scales in one row: one request for the whole row
+            prefetch_l2_bulk(cb + (int64_t)ent[k] * CSA2_ENTRY_BYTES, CSA2_ENTRY_BYTES);
+          } else {
+            prefetch_l2_bulk(cb + (int64_t)ent[k] * CSA2_ENTRY_BYTES, CSA2_CODE_BYTES);
+            const uint8_t* s0 = sb + (int64_t)ent[k] * CSA2_ENTRY_BYTES;
+            prefetch_l2(s0);
+            prefetch_l2(s0 + CSA2_SCALE_BYTES - 1);
+          }
         }
       }
     }
@@ -1199,7 +1205,7 @@ cudaError_t launch_sparse_attn(int B, int T, int H, const void* q, const uint8_t
   if (nsplit < 1 || nsplit > kMaxSplitsTC || (nsplit & (nsplit - 1))) return cudaErrorInvalidValue;
   int split_len = (K + nsplit - 1) / nsplit;
   split_len = (split_len + kTK - 1) / kTK * kTK;
-  Fp4Src f{codes, scales, n_stride, idx, K};
+  Fp4Src f{codes, scales, codes != nullptr && scales == codes + CSA2_CODE_BYTES, n_stride, idx, K};
   RowSrc r{0, nullptr, nullptr, 0};
   CUtensorMap tq, dummy;
   memset(&dummy, 0, sizeof(dummy));
@@ -1222,7 +1228,7 @@ cudaError_t launch_swa_merge(int B, int T, int H, const void* q, const void* swa
   if (!encode_tensor_map_2d_bf16(&tq, q, CSA2_D_KV, (uint64_t)Q * H, 64, 64)) return cudaErrorInvalidValue;
   if (s_stride > 0 && !encode_tensor_map_2d_bf16(&tm, swa, CSA2_D_KV, (uint64_t)B * s_stride, 64, kTK))
     return cudaErrorInvalidValue;
-  Fp4Src f{nullptr, nullptr, 0, nullptr, 0};
+  Fp4Src f{nullptr, nullptr, false, 0, nullptr, 0};
   RowSrc r{s_stride, win_start, win_len, n_win};
   OutArgs out{o_out, lse_out, o_g, lse_g, nullptr};
   return launch_tc<kWindow>(tq, f, r, tm, Q, T, H, scale_log2, nsplit, kTK, out, status, st);
@@ -1238,7 +1244,7 @@ cudaError_t launch_decode_attn(int B, int T, int H, const void* q, const uint8_t
   if (nsplit < 1 || nsplit > kMaxSplitsTC || (nsplit & (nsplit - 1))) return cudaErrorInvalidValue;
   int split_len = (K + nsplit - 1) / nsplit;
   split_len = (split_len + kTK - 1) / kTK * kTK;
-  Fp4Src f{codes, scales, n_stride, idx, K};
+  Fp4Src f{codes, scales, codes != nullptr && scales == codes + CSA2_CODE_BYTES, n_stride, idx, K};
   RowSrc r{s_stride, win_start, win_len, n_win};
   CUtensorMap tq, tm;
   memset(&tm, 0, sizeof(tm));

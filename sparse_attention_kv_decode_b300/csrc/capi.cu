@@ -137,7 +137,7 @@ static int static_scratch(cudaStream_t st, void** out) {
 
 extern "C" {
 
-int csa2_version(void) { return 100; }
+int csa2_version(void) { return 200; }
 
 const char* csa2_last_cuda_error(void) { return g_last_cuda_error; }
 

@@ -262,10 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1) ced_proj_kernel(
             cw[2 * bk + 1] = hi;
             sc4 |= sc << (8 * bk);
           }
-          uint8_t* cdst = codes + orow * CSA2_CODE_BYTES + sl * 32;
+          uint8_t* cdst = codes + orow * CSA2_ENTRY_BYTES + sl * 32;
           *reinterpret_cast<uint4*>(cdst) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
           *reinterpret_cast<uint4*>(cdst + 16) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-          *reinterpret_cast<uint32_t*>(scales + orow * CSA2_SCALE_BYTES + sl * 4) = sc4;
+          *reinterpret_cast<uint32_t*>(scales + orow * CSA2_ENTRY_BYTES + sl * 4) = sc4;
         } else {
           uint32_t pk[32];
 #pragma unroll

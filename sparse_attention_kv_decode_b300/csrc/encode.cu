@@ -5,7 +5,8 @@
 // E4M3 scale per 16 channels. Per block: s = E4M3(fl32(amax/6)), code_i =
 // E2M1(fl32(x_i/s)), both round-to-nearest-even with saturation; a zero scale
 // gives zero codes. The kernel is HBM-bound: one thread per 16-channel block,
-// 64-byte (fp32) or 32-byte (bf16) coalesced reads, 8-byte code stores.
+// 64-byte (fp32) or 32-byte (bf16) coalesced reads, 8-byte code stores into the
+// entry's CSA2_ENTRY_BYTES row.
 #include "csa2_internal.cuh"
 
 namespace csa2 {
@@ -37,8 +38,10 @@ __global__ void __launch_bounds__(256) encode_quant_kernel(const void* __restric
     }
     uint32_t lo, hi, sc;
     quant_block16(v, lo, hi, sc);
-    *reinterpret_cast<uint2*>(codes + i * 8) = make_uint2(lo, hi);
-    scales[i] = (uint8_t)sc;
+    // block j = i % 36 of entry row i / 36 (rows of CSA2_ENTRY_BYTES)
+    const int64_t row = i / (CSA2_D_KV / 16), j = i - row * (CSA2_D_KV / 16);
+    *reinterpret_cast<uint2*>(codes + row * CSA2_ENTRY_BYTES + j * 8) = make_uint2(lo, hi);
+    scales[row * CSA2_ENTRY_BYTES + j] = (uint8_t)sc;
   }
 }
 

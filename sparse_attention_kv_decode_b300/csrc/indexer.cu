@@ -652,8 +652,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_row_kernel(
   int r = block_excl_scan(__popc(sel), sh.scan, total);
   int32_t* out = out_idx + (int64_t)qi * K;
   float* outs = out_scores ? out_scores + (int64_t)qi * K : nullptr;
-  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * kv_stride * CSA2_CODE_BYTES : nullptr;
-  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * kv_stride * CSA2_SCALE_BYTES : nullptr;
+  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * kv_stride * CSA2_ENTRY_BYTES : nullptr;
+  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * kv_stride * CSA2_ENTRY_BYTES : nullptr;
+  const bool pf_record = pf_codes != nullptr && pf_scales == pf_codes + CSA2_CODE_BYTES;
   const int32_t* pblk = pool ? pool + (int64_t)qi * pool_stride : nullptr;
   for (uint32_t m = sel; m && r < K; m &= m - 1u, ++r) {
     const int pos = 32 * tid + __ffs(m) - 1;
@@ -661,9 +662,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_row_kernel(
     out[r] = ent;
     if (outs) outs[r] = sv[pos];
     if (pfc && ent >= 0 && ent < kv_stride) {
-      prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
-      prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES);
-      prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES + CSA2_SCALE_BYTES - 1);
+      if (pf_record) {
+        prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_ENTRY_BYTES, CSA2_ENTRY_BYTES);
+      } else {
+        prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_ENTRY_BYTES, CSA2_CODE_BYTES);
+        prefetch_l2(pfs + (int64_t)ent * CSA2_ENTRY_BYTES);
+        prefetch_l2(pfs + (int64_t)ent * CSA2_ENTRY_BYTES + CSA2_SCALE_BYTES - 1);
+      }
     }
   }
   for (int q = total + tid; q < K; q += kRowThreads) {
@@ -1084,8 +1089,9 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
   int p = off + block_excl_scan(__popc(sel), sh.scan, cnt);
   int32_t* out = out_idx + (int64_t)qi * K;
   float* outs = out_scores ? out_scores + (int64_t)qi * K : nullptr;
-  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * kv_stride * CSA2_CODE_BYTES : nullptr;
-  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * kv_stride * CSA2_SCALE_BYTES : nullptr;
+  const uint8_t* pfc = pf_codes ? pf_codes + (int64_t)(qi / T) * kv_stride * CSA2_ENTRY_BYTES : nullptr;
+  const uint8_t* pfs = pf_codes ? pf_scales + (int64_t)(qi / T) * kv_stride * CSA2_ENTRY_BYTES : nullptr;
+  const bool pf_record = pf_codes != nullptr && pf_scales == pf_codes + CSA2_CODE_BYTES;
   const int32_t* pblk = pool ? pool + (int64_t)qi * pool_stride : nullptr;
   for (uint32_t m = sel; m && p < K; m &= m - 1u, ++p) {
     const int lp = 32 * tid + __ffs(m) - 1;
@@ -1094,9 +1100,13 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
     out[p] = ent;
     if (outs) outs[p] = sv[lp];
     if (pfc && ent >= 0 && ent < kv_stride) {
-      prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_CODE_BYTES, CSA2_CODE_BYTES);
-      prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES);
-      prefetch_l2(pfs + (int64_t)ent * CSA2_SCALE_BYTES + CSA2_SCALE_BYTES - 1);
+      if (pf_record) {
+        prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_ENTRY_BYTES, CSA2_ENTRY_BYTES);
+      } else {
+        prefetch_l2_bulk(pfc + (int64_t)ent * CSA2_ENTRY_BYTES, CSA2_CODE_BYTES);
+        prefetch_l2(pfs + (int64_t)ent * CSA2_ENTRY_BYTES);
+        prefetch_l2(pfs + (int64_t)ent * CSA2_ENTRY_BYTES + CSA2_SCALE_BYTES - 1);
+      }
     }
   }
   if (r == C - 1)

@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.csa2_version() == 100
+    assert L.csa2_version() == 200
     for s in range(7):
         assert L.csa2_status_string(s)
     assert L.csa2_status_string(99) == b"unknown status"

@@ -38,8 +38,12 @@ def _dev_state(st):
     for k, v in st.items():
         if v.dtype == np.uint16:
             d[k] = to_dev_bf16(v, DEV)
-        else:
+        elif k not in ("kv_codes", "kv_scales"):
             d[k] = to_dev(v, DEV)
+    # the FP4 cache: one 384-byte record per entry
+    d["kv_codes"], d["kv_scales"] = csa2.csa2_kv_cache(st["kv_codes"].shape[:2], device=DEV)
+    d["kv_codes"].copy_(torch.from_numpy(st["kv_codes"]))
+    d["kv_scales"].copy_(torch.from_numpy(st["kv_scales"]))
     return d
 
 
@@ -111,8 +115,7 @@ def test_decode_after_appends_attends_over_the_token_history():
     P = [5, 77, 200]                    # tokens per sequence (the window wraps for the last two)
     S = 2 * n_win
     swa = torch.zeros((B, S, 576), dtype=torch.bfloat16, device=DEV)
-    codes = torch.zeros((B, N, 288), dtype=torch.uint8, device=DEV)
-    scales = torch.zeros((B, N, 36), dtype=torch.uint8, device=DEV)
+    codes, scales = csa2.csa2_kv_cache((B, N), device=DEV)
     nvis = torch.zeros(B, dtype=torch.int32, device=DEV)
     wst = torch.zeros(B, dtype=torch.int32, device=DEV)
     wln = torch.zeros(B, dtype=torch.int32, device=DEV)
@@ -166,8 +169,7 @@ def test_serving_loop_in_a_cuda_graph():
     tau = 1.0 / math.sqrt(576)
     dev = DEV
     swa = torch.zeros((B, 2 * n_win, 576), dtype=torch.bfloat16, device=dev)
-    codes = torch.zeros((B, N, 288), dtype=torch.uint8, device=dev)
-    scales = torch.zeros((B, N, 36), dtype=torch.uint8, device=dev)
+    codes, scales = csa2.csa2_kv_cache((B, N), device=dev)
     z = torch.zeros((B, N, 64), dtype=torch.bfloat16, device=dev)
     nvis, wst, wln = (torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(3))
     n_tok = torch.tensor([0, 9], dtype=torch.int32, device=dev)     # sequence 1 starts 9 tokens in

@@ -384,3 +384,34 @@ def test_split_merge_through_l2_and_dsmem_agree(B):
             O, LSE = attention.merge(O, LSE, Os, Ls)
         check_attention(o1[b, 0], O, f"b={b}")
         check_lse(l1[b, 0], LSE, f"b={b}")
+
+
+def test_separate_code_and_scale_rows_equal_the_record_layout():
+    """The library's cache keeps an entry's codes and scales in one 384-byte record
+    (csa2_kv_cache); code and scale arrays of their own with the same row stride must
+    give the same selection prefetch and attention results, bit for bit."""
+    cfg = ci.scaled(ci.DECODE_128K, B=4, N=2000, H=64, K=512, W=64, modes=(ci.FULL,))
+    inp = ci.make_decode_inputs(cfg)
+    L = inp.layers[0]
+    codes, scales = _cache(L.X)
+    assert scales.data_ptr() == codes.data_ptr() + 288 and codes.stride(-2) == 384
+    B, N = codes.shape[:2]
+    # separate arrays, same 384-byte row stride, the scales first in their rows
+    c2, _ = csa2.csa2_kv_cache((B, N), device=DEV)
+    s_buf = torch.full((B, N, 384), 0xEE, dtype=torch.uint8, device=DEV)
+    s2 = s_buf[..., :36]
+    c2.copy_(codes)
+    s2.copy_(scales)
+    q = to_dev_bf16(L.q, DEV)
+    swa = to_dev_bf16(L.swa, DEV)
+    args = dict(q_idx=to_dev_bf16(L.q_idx, DEV), w_idx=to_dev(L.w_idx, DEV), z=to_dev_bf16(L.z, DEV),
+                n_visible=to_dev(inp.n_visible, DEV))
+    wst, wln = to_dev(inp.win_start, DEV), to_dev(inp.win_len, DEV)
+    o1, l1, i1 = csa2.decode_layer(csa2.FULL, q, codes, scales, swa, wst, wln, cfg.W, cfg.K, fused=True, **args)
+    o2, l2, i2 = csa2.decode_layer(csa2.FULL, q, c2, s2, swa, wst, wln, cfg.W, cfg.K, fused=True, **args)
+    torch.cuda.synchronize()
+    assert torch.equal(i1, i2)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # a contiguous [B, N, 288] array is not a cache of 384-byte rows
+    with pytest.raises(ValueError):
+        csa2.csa2_decode_attention(q, codes.contiguous(), scales, i1, swa, wst, wln, cfg.W, cfg.softmax_scale)
