@@ -863,8 +863,11 @@ def run_other_configs(args, torch, csa2, dev, peaks, flush):
     P = lambda t: t.data_ptr() if t is not None else None
     b16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
     t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    chosen = [c for c in (args.configs or "").split(",") if c]
     for cfg, steps in ((ci.TINY, min(args.steps, 200)), (ci.DECODE_1M, min(args.steps, 200)),
                        (ci.PREFILL_CHUNK, min(args.steps, 20))):
+        if chosen and cfg.name not in chosen:
+            continue
         inp = ci.make_decode_inputs(cfg)
         Lr = inp.layers[0]
         X = t32(Lr.X)
@@ -1070,6 +1073,9 @@ def main():
     ap.add_argument("--no-ced", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the 1M-context decode and the prefill-chunk measurements")
+    ap.add_argument("--configs", default="",
+                    help="comma-separated subset of the other workloads to run (names as in other_configs; "
+                         "default: all)")
     ap.add_argument("--no-pool", action="store_true",
                     help="skip the side measurements (REINDEX vs REINDEX_POOL, csa2_cache_append)")
     ap.add_argument("--attn", choices=["layer", "fused", "two-call"], default="layer",
