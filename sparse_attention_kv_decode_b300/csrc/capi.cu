@@ -69,10 +69,11 @@ bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inne
   return r == CUDA_SUCCESS;
 }
 
-int attn_splits(int64_t Q, int K, int n_sm) {
+int attn_splits(int64_t Q, int K, int W, int n_sm) {
   if (Q <= 0) return 1;
   int64_t s = n_sm / Q;                  // at most one wave of one-CTA-per-SM blocks
-  int64_t max_by_k = (K + 127) / 128;    // at least one 128-key tile per split
+  // at least one 128-key tile per split; the window's tiles go to the last split
+  int64_t max_by_k = (K + 127) / 128 + (W > 0 ? (W + 127) / 128 : 0);
   if (s > max_by_k) s = max_by_k;
   if (s > kMaxSplits) s = kMaxSplits;
   int p = 1;                             // splits form one cluster: a power of two
@@ -300,7 +301,7 @@ static int decode_attention_launch(int B, int T, int H, const void* q, const uin
                                    float softmax_scale, float* o, float* lse, void* ws,
                                    size_t ws_bytes, size_t front, void* stream) {
   const int64_t Q = (int64_t)B * T;
-  const int nsplit = attn_splits(Q, K, device_sm_count());
+  const int nsplit = attn_splits(Q, K, n_win, device_sm_count());
   uint32_t* status = static_cast<uint32_t*>(ws);
   const float scale_log2 = softmax_scale * 1.4426950408889634074f;
   return cuda_status(launch_decode_attn(B, T, H, q, kv_codes, kv_scales, n_stride, idx, K, swa_kv,
@@ -431,7 +432,7 @@ int csa2_sparse_decode(int B, int T, int H, const void* q, const uint8_t* kv_cod
             aligned(o_g, 16) && aligned(lse_g, 4) && aligned(idx, 4));
   if (ws == nullptr) return CSA2_ERR_WORKSPACE;
   CHECK_ARG(aligned(ws, 256));
-  const int nsplit = attn_splits(Q, K, device_sm_count());
+  const int nsplit = attn_splits(Q, K, 0, device_sm_count());
   if (ws_bytes < kWsHeader) return CSA2_ERR_WORKSPACE;
   uint32_t* status = static_cast<uint32_t*>(ws);
   const float scale_log2 = softmax_scale * 1.4426950408889634074f;

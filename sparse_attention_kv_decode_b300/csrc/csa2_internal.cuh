@@ -29,7 +29,7 @@ inline int64_t score_pad(int64_t n) { return (n + kScoreTile - 1) / kScoreTile *
 
 // Number of key splits per query for the sparse attention (about one wave of
 // CTAs when the batch is small; one split per query when there are many).
-int attn_splits(int64_t Q, int K, int n_sm);
+int attn_splits(int64_t Q, int K, int W, int n_sm);
 
 
 // Per-query score range words (two uint32 per query) that the scoring kernel
