@@ -395,7 +395,7 @@ def run_ours(args):
 
     # the step as a list of (name, kind, thunk) C-ABI calls on `stream`: `calls` for the
     # per-call breakdown, `step_calls` for the timed step (with --attn layer one
-    # csa2_decode_layer per layer, which is csa2_index_topk_prefetch + csa2_decode_attention)
+    # csa2_decode_layer per layer, which is csa2_index_topk + csa2_decode_attention)
     calls, step_calls = [], []
     cur = None
     layer = args.attn == "layer"
@@ -403,16 +403,10 @@ def run_ours(args):
         mode = d["mode"]
         if mode != ci.REUSE:
             cur = idx_bufs[li % 2]
-            if layer:
-                calls.append((f"index_topk_prefetch[{ci.MODE_NAMES[mode]}]", "index",
-                              (lambda d=d, cur=cur, mode=mode: L.csa2_index_topk_prefetch(
-                                  mode, cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N, P(nvis),
-                                  cfg.K, None, P(cur), None, P(codes), P(scales), wsp, wsn, sp))))
-            else:
-                calls.append((f"index_topk[{ci.MODE_NAMES[mode]}]", "index",
-                              (lambda d=d, cur=cur, mode=mode: L.csa2_index_topk(
-                                  mode, cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N, P(nvis),
-                                  cfg.K, None, P(cur), None, wsp, wsn, sp))))
+            calls.append((f"index_topk[{ci.MODE_NAMES[mode]}]", "index",
+                          (lambda d=d, cur=cur, mode=mode: L.csa2_index_topk(
+                              mode, cfg.B, cfg.T, cfg.H_I, P(d["q_idx"]), P(d["w"]), P(d["z"]), cfg.N, P(nvis),
+                              cfg.K, None, P(cur), None, wsp, wsn, sp))))
         else:
             calls.append(("index_topk[REUSE]", "reuse",
                           (lambda cur=cur: L.csa2_index_topk(2, cfg.B, cfg.T, 0, None, None, None, 0, None,
@@ -654,7 +648,7 @@ def run_pool_indexer(args, torch, L, cfg, dl, codes, scales, nvis, idx_bufs, ws,
     outs = [torch.empty_like(full_sel) for _ in range(2)]
     sp = stream.cuda_stream
     P = lambda t: t.data_ptr()
-    pf = args.attn == "layer"
+    pf = False   # as in csa2_decode_layer
 
     def call(mode, prev, out):
         if pf:
@@ -1079,8 +1073,8 @@ def main():
     ap.add_argument("--no-pool", action="store_true",
                     help="skip the side measurements (REINDEX vs REINDEX_POOL, csa2_cache_append)")
     ap.add_argument("--attn", choices=["layer", "fused", "two-call"], default="layer",
-                    help="per layer: one csa2_decode_layer call (selection that prefetches the selected rows "
-                         "into L2, then the attention); csa2_index_topk + csa2_decode_attention; or "
+                    help="per layer: one csa2_decode_layer call (the selection, then the attention); "
+                         "csa2_index_topk + csa2_decode_attention; or "
                          "csa2_index_topk + csa2_sparse_decode + csa2_swa_merge")
     args = ap.parse_args()
     if args.warmup < 3:

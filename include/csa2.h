@@ -275,7 +275,7 @@ CSA2_API int csa2_decode_attention(int B, int T, int H, const void* q,
  * csa2_decode_attention over the selection it writes (CSA2 global attention with
  * its indexer and top-K, picx.dev summary; the sliding-window branch, blog repost).
  *
- * Equals csa2_index_topk_prefetch followed by csa2_decode_attention with the same
+ * Equals csa2_index_topk followed by csa2_decode_attention with the same
  * arguments (out_scores not written): out_idx [B][T][K] receives the selection
  * (REUSE: a copy of prev_idx), then o and lse the attention over it. kv_codes /
  * kv_scales and z share n_stride (one entry per compressed position).
