@@ -347,27 +347,27 @@ def test_range_flag_for_values_outside_fp16():
     assert csa2.csa2_read_device_status(ws) == (0, 0)
 
 
-@pytest.mark.parametrize("B", [32, 64])
-def test_split_merge_through_l2_and_dsmem_agree(B):
-    """With few queries each query's keys are split over a cluster of 4 (B=32) or 2
-    (B=64) CTAs. With a full workspace the splits' partial outputs meet in the exchange at
-    its end (L2); with only the status header they meet in distributed shared memory.
-    Both must give the oracle's result, and the same result up to summation order."""
+@pytest.mark.parametrize("B,T", [(32, 1), (64, 1), (16, 2)])
+def test_split_merge_through_l2_and_dsmem_agree(B, T):
+    """With few queries each query's keys are split over a cluster of 4 (32 queries) or 2
+    (64 queries) CTAs. With a full workspace the splits' partial outputs meet in the
+    exchange at its end (L2); with only the status header they meet in distributed shared
+    memory. Both must give the oracle's result, and the same result up to summation order."""
     cfg = ci.scaled(ci.DECODE_128K, B=B, N=3000, H=64, K=1024, W=128, modes=(ci.FULL,))
-    rng = np.random.default_rng(77 + B)
+    rng = np.random.default_rng(77 + B + T)
     X = rng.standard_normal((B, cfg.N, 576), dtype=np.float32)
     codes, scales = _cache(X)
-    q_bits = ci.bf16_bits(rng.standard_normal((B, 1, 64, 576), dtype=np.float32) * 0.3)
+    q_bits = ci.bf16_bits(rng.standard_normal((B, T, 64, 576), dtype=np.float32) * 0.3)
     swa_bits = ci.bf16_bits(rng.standard_normal((B, 256, 576), dtype=np.float32))
-    idx = np.stack([rng.permutation(cfg.N)[:cfg.K] for _ in range(B)]).astype(np.int32).reshape(B, 1, cfg.K)
+    idx = np.stack([rng.permutation(cfg.N)[:cfg.K] for _ in range(B * T)]).astype(np.int32).reshape(B, T, cfg.K)
     idx[B // 2, 0, 700:] = -1                      # a shorter selection
-    wst = np.full(B, 100, np.int32)
-    wln = np.full(B, 128, np.int32)
+    wst = np.full(B * T, 100, np.int32)
+    wln = np.full(B * T, 128, np.int32)
     wln[1] = 0                                     # an empty window
     q, swa = to_dev_bf16(q_bits, DEV), to_dev_bf16(swa_bits, DEV)
     args = (q, codes, scales, to_dev(idx, DEV), swa, to_dev(wst, DEV), to_dev(wln, DEV), 128, cfg.softmax_scale)
-    full_ws = csa2.csa2_workspace(B, 1, 64, 0, cfg.K, device=DEV)
-    assert full_ws.numel() >= 256 + B * 512 * 1024
+    full_ws = csa2.csa2_workspace(B, T, 64, 0, cfg.K, device=DEV)
+    assert full_ws.numel() >= 256 + B * T * 512 * 1024
     o1, l1 = csa2.csa2_decode_attention(*args, ws=full_ws)
     o2, l2 = csa2.csa2_decode_attention(*args, ws=csa2.csa2_workspace(0, 0, 0, 0, 0, device=DEV))
     torch.cuda.synchronize()
@@ -376,14 +376,16 @@ def test_split_merge_through_l2_and_dsmem_agree(B):
     o1, l1 = o1.cpu().numpy(), l1.cpu().numpy()
     for b in (0, 1, B // 2, B - 1):
         rows = fp4.decode(*fp4.encode(X[b]))
-        sel = idx[b, 0][idx[b, 0] >= 0]
-        O, LSE = attention.attend(f64(q_bits[b, 0]), rows[sel], 512, cfg.softmax_scale)
-        if wln[b] > 0:
-            Os, Ls = attention.swa_branch(f64(q_bits[b, 0]), f64(swa_bits[b]), int(wst[b]), int(wln[b]), 512,
-                                          cfg.softmax_scale)
-            O, LSE = attention.merge(O, LSE, Os, Ls)
-        check_attention(o1[b, 0], O, f"b={b}")
-        check_lse(l1[b, 0], LSE, f"b={b}")
+        for t in range(T):
+            qi = b * T + t
+            sel = idx[b, t][idx[b, t] >= 0]
+            O, LSE = attention.attend(f64(q_bits[b, t]), rows[sel], 512, cfg.softmax_scale)
+            if wln[qi] > 0:
+                Os, Ls = attention.swa_branch(f64(q_bits[b, t]), f64(swa_bits[b]), int(wst[qi]), int(wln[qi]), 512,
+                                              cfg.softmax_scale)
+                O, LSE = attention.merge(O, LSE, Os, Ls)
+            check_attention(o1[b, t], O, f"b={b} t={t}")
+            check_lse(l1[b, t], LSE, f"b={b} t={t}")
 
 
 def test_separate_code_and_scale_rows_equal_the_record_layout():
