@@ -4,9 +4,9 @@
 Workload (one "step"): a decode step of a three-layer CSA2 group FULL -> REINDEX ->
 REUSE for 32 sequences at 128K context (32768 compressed entries each), 64 query
 heads, latent 512 + rope 64 in FP4 (E2M1 + E4M3 per 16), indexer 8 x 64 in bf16,
-top-K 2048, sliding window 128. Per layer one csa2_decode_layer call: the top-K
-selection (which also requests the selected FP4 rows into L2), then the attention over
-the selected entries and the window (csa2_decode_attention); REUSE skips the indexer.
+top-K 2048, sliding window 128. Per layer one csa2_decode_layer call: the indexer and
+top-K selection, then the attention over the selected entries and the window
+(csa2_decode_attention); REUSE skips the indexer.
 --attn fused times csa2_index_topk + csa2_decode_attention instead, --attn two-call
 csa2_index_topk + csa2_sparse_decode + csa2_swa_merge. The KV caches and keys are resident in HBM (written before timing); each
 timed step re-reads them, and L2 is flushed between steps.
