@@ -270,6 +270,33 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scan, int& total) {
   return pre;
 }
 
+// The same over 64-bit words (fields that never carry into each other: several
+// independent sums in one scan).
+__device__ __forceinline__ uint64_t block_excl_scan64(uint64_t v, unsigned long long* scan) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scan[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long s = lane < kSelThreads / 32 ? scan[lane] : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < kSelThreads / 32) scan[lane] = s;
+  }
+  __syncthreads();
+  const uint64_t pre = (warp > 0 ? scan[warp - 1] : 0ull) + x - v;
+  __syncthreads();
+  return pre;
+}
+
 // ---------------------------------------------------------------------------
 // Candidate pool of the Hierarchical Sparse Indexer ("DeepSeek-V4.1-Flash", picx.dev
 // summary, Methodology / 3): the aligned 8-position blocks that hold an entry of the
@@ -680,7 +707,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_row_kernel(
 // ---------------------------------------------------------------------------
 // Top-K selection, one cluster of C CTAs per query (few queries, long score rows)
 // ---------------------------------------------------------------------------
-// CTA r owns the positions [r*slice, (r+1)*slice) (slice a multiple of 32, so the CTAs'
+// CTA r owns the positions [r*slice, (r+1)*slice) of the scored row, the visible ones
+// among them in play (slice = ceil(row / C) rounded up to a multiple of 32, so the CTAs'
 // bitmap words do not overlap), lands their scores in shared memory with a few bulk
 // copies, and visits local positions k * kRowThreads + t. Every exchange is a push into
 // the peers' receive buffers followed by one cluster barrier, and every decision after it
@@ -703,6 +731,7 @@ struct ClusterShared {
   uint32_t selw[kRowThreads / 2];    // selected bitmap (slices of at most 16384)
   uint32_t candw[kRowThreads / 2];   // in-play bitmap
   int scan[kRowThreads / 32];
+  unsigned long long scan64[kRowThreads / 32];
   float red[2][kRowThreads / 32];
   uint4 rec_in[kMaxCluster];         // pushed (min, max, count) of each CTA
   int cta_sel[kMaxCluster];          // selected positions of each CTA so far
@@ -710,7 +739,6 @@ struct ClusterShared {
   int cta_taken[kMaxCluster];        // ranked and taken in the exact round
   int cta_warp[kMaxCluster][kRowThreads / 32];   // per-warp counts above b*, per CTA
   int bstar, above;
-  uint32_t rng[2];
   uint64_t bar_chunk[kRowThreads / 64];   // one per 1024-score chunk of the slice (<= 16384)
 };
 
@@ -753,6 +781,44 @@ __device__ __forceinline__ void push_hist(ClusterShared& sh, uint16_t* hist_in, 
 __device__ __forceinline__ int cluster_bstar(ClusterShared& sh, const uint16_t* hist_in, uint32_t C, int rem) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int b1 = kRowBins - 1 - 2 * tid, b0 = b1 - 1;
+  if (C <= 4) {
+    // every CTA's counts in one scan: CTA rr's in bits [16 rr, 16 rr + 16) (a slice holds
+    // at most 16384 positions, so no field carries)
+    uint64_t v1 = 0u, v0 = 0u;
+    for (uint32_t rr = 0; rr < C; ++rr) {
+      v1 |= (uint64_t)hist_in[rr * kRowBins + b1] << (16 * rr);
+      v0 |= (uint64_t)hist_in[rr * kRowBins + b0] << (16 * rr);
+    }
+    const uint64_t pre = block_excl_scan64(v1 + v0, sh.scan64);
+    auto fsum = [](uint64_t x) {
+      return (int)((x & 0xFFFFu) + ((x >> 16) & 0xFFFFu) + ((x >> 32) & 0xFFFFu) + (x >> 48));
+    };
+    const int above = fsum(pre), h1 = fsum(v1), h0 = fsum(v0);
+    uint64_t at = 0u, in = 0u;
+    bool mine = false;
+    if (above < rem && rem <= above + h1) {
+      sh.bstar = b1;
+      sh.above = above;
+      at = pre;
+      in = v1;
+      mine = true;
+    } else if (above + h1 < rem && rem <= above + h1 + h0) {
+      sh.bstar = b0;
+      sh.above = above + h1;
+      at = pre + v1;
+      in = v0;
+      mine = true;
+    }
+    if (mine)
+      for (uint32_t rr = 0; rr < C; ++rr) {
+        sh.cta_sel[rr] += (int)((at >> (16 * rr)) & 0xFFFFu);
+        sh.cta_play[rr] = (int)((in >> (16 * rr)) & 0xFFFFu);
+      }
+    __syncthreads();
+    int n = 0;
+    for (uint32_t rr = 0; rr < C; ++rr) n += sh.cta_play[rr];
+    return n;
+  }
   int h1 = 0, h0 = 0;
   for (uint32_t rr = 0; rr < C; ++rr) {
     h1 += hist_in[rr * kRowBins + b1];
@@ -822,31 +888,32 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
   // matching wait comes after the score load
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int nvis = clamp_nvis(n_visible, qi, n_stride);
-  const int slice = ((nvis + (int)C - 1) / (int)C + 31) & ~31;
-  auto len_of = [&](int rr) { return min(max(nvis - rr * slice, 0), slice); };
+  // CTA r's slice is positions [r * slice_cap, ..) of the scored row (n_stride long), so
+  // its copies go out before the visible count is known. Chunk k (scores k * 1024 ..)
+  // lands with its own bulk copy and mbarrier, so that the first pass over it starts as
+  // soon as it is there (a score row is score_stride >= roundup4(n_stride) floats).
+  const int slice = slice_cap;
   const int my0 = (int)r * slice;
-  int my_len = len_of((int)r);
-  const int nk = (my_len + kRowThreads - 1) / kRowThreads;
-  // chunk k (scores k * 1024 ..) lands with its own bulk copy and mbarrier, so that the
-  // first pass over it starts as soon as it is there (a score row is score_stride >=
-  // roundup4(nvis) floats)
-  if (tid < nk) {
-    const uint32_t bytes = (uint32_t)((min(my_len - tid * kRowThreads, kRowThreads) + 3) >> 2) * 16;
+  const int my_cap = min(max((int)n_stride - my0, 0), slice);
+  const int nk_all = (my_cap + kRowThreads - 1) / kRowThreads;
+  if (tid < nk_all) {
+    const uint32_t bytes = (uint32_t)((min(my_cap - tid * kRowThreads, kRowThreads) + 3) >> 2) * 16;
     mbar_arrive_expect_tx(smem_u32(&sh.bar_chunk[tid]), bytes);
     bulk_g2s(smem_u32(sv + tid * kRowThreads), scores + (int64_t)qi * score_stride + my0 + tid * kRowThreads, bytes,
              smem_u32(&sh.bar_chunk[tid]));
   }
-  if (tid == 0) {
-    sh.rng[0] = range[2 * qi];
-    sh.rng[1] = range[2 * qi + 1];
-  }
+  // every thread reads the range words and the visible count itself (one request per
+  // warp), so that nothing waits for them before the first score chunk is needed
+  const uint32_t rng0 = range[2 * qi], rng1 = range[2 * qi + 1];
+  const int nvis = clamp_nvis(n_visible, qi, n_stride);
+  auto len_of = [&](int rr) { return min(max(nvis - rr * slice, 0), slice); };
+  int my_len = len_of((int)r);
+  const int nk = (my_len + kRowThreads - 1) / kRowThreads;   // chunks holding visible scores
   // (a copy that did not land leaves stale scores: the selection still completes, flagged)
   bool load_ok = true;
   auto wait_chunk = [&](int k) {
     if (!mbar_wait(smem_u32(&sh.bar_chunk[k]), 0)) load_ok = false;
   };
-  __syncthreads();
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   const int nwords = (my_len + 31) >> 5;
   const uint32_t my_valid = [&] {
@@ -880,8 +947,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
     __syncthreads();
   } else {
     int rem = K;
-    float lo = key2f(~sh.rng[0]), hi = key2f(sh.rng[1]);
-    if (!(sh.rng[1] != 0u && lo < hi && isfinite(lo) && isfinite(hi))) {
+    float lo = key2f(~rng0), hi = key2f(rng1);
+    if (!(rng1 != 0u && lo < hi && isfinite(lo) && isfinite(hi))) {
       // no range left by the scoring kernel: the cluster-wide min / max
       float a = INFINITY, b = -INFINITY;
       for (int k = 0; k < nk; ++k) {
@@ -1082,9 +1149,16 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
     }
   }
 
+  // copies of chunks past the visible scores land before the CTA exits
+  for (int k = nk; k < nk_all; ++k) wait_chunk(k);
   if (!load_ok) atomicOr(status, CSA2_DEV_PIPELINE_TIMEOUT);
-  // ---- ordered output: thread t writes the selected positions of bitmap word t
-  const uint32_t sel = tid < nwords ? sh.selw[tid] : 0u;
+  // ---- ordered output: thread t writes the selected positions of bits [t b, t b + b)
+  // of the bitmap, b = 8 (slices of at most 8192) or 16, so that every warp has a share
+  const int obits = nwords <= kRowThreads / 4 ? 8 : 16;
+  const int obit0 = tid * obits;
+  const uint32_t sel = (obit0 >> 5) < nwords
+                           ? (sh.selw[obit0 >> 5] >> (obit0 & 31)) & ((1u << obits) - 1u)
+                           : 0u;
   int cnt;
   int p = off + block_excl_scan(__popc(sel), sh.scan, cnt);
   int32_t* out = out_idx + (int64_t)qi * K;
@@ -1094,7 +1168,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) topk_cluster_kernel(
   const bool pf_record = pf_codes != nullptr && pf_scales == pf_codes + CSA2_CODE_BYTES;
   const int32_t* pblk = pool ? pool + (int64_t)qi * pool_stride : nullptr;
   for (uint32_t m = sel; m && p < K; m &= m - 1u, ++p) {
-    const int lp = 32 * tid + __ffs(m) - 1;
+    const int lp = obit0 + __ffs(m) - 1;
     const int pos = my0 + lp;
     const int ent = pblk ? pblk[pos >> 3] * 8 + (pos & 7) : pos;
     out[p] = ent;
