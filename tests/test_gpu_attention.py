@@ -347,13 +347,16 @@ def test_range_flag_for_values_outside_fp16():
     assert csa2.csa2_read_device_status(ws) == (0, 0)
 
 
-@pytest.mark.parametrize("B,T", [(32, 1), (64, 1), (16, 2)])
-def test_split_merge_through_l2_and_dsmem_agree(B, T):
-    """With few queries each query's keys are split over a cluster of 4 (32 queries) or 2
-    (64 queries) CTAs. With a full workspace the splits' partial outputs meet in the
-    exchange at its end (L2); with only the status header they meet in distributed shared
+@pytest.mark.parametrize("B,T,K", [(32, 1, 1024), (64, 1, 1024), (16, 2, 1024), (12, 1, 1024), (4, 1, 2048),
+                                   (3, 1, 1900)])
+def test_split_merge_through_l2_and_dsmem_agree(B, T, K):
+    """With few queries each query's keys are split over a cluster of CTAs: 4 (32 queries),
+    2 (64), 8 (12 queries, 9 key tiles) or 16 (4 or 3 queries, 17 or 16 key tiles; the
+    last with a ragged split and a window-only split). With a full workspace the partial
+    outputs of 2 or 4 splits meet in the exchange at its end (L2), those of 8 or 16 in
+    distributed shared memory; with only the status header all meet in distributed shared
     memory. Both must give the oracle's result, and the same result up to summation order."""
-    cfg = ci.scaled(ci.DECODE_128K, B=B, N=3000, H=64, K=1024, W=128, modes=(ci.FULL,))
+    cfg = ci.scaled(ci.DECODE_128K, B=B, N=3000, H=64, K=K, W=128, modes=(ci.FULL,))
     rng = np.random.default_rng(77 + B + T)
     X = rng.standard_normal((B, cfg.N, 576), dtype=np.float32)
     codes, scales = _cache(X)
@@ -367,7 +370,11 @@ def test_split_merge_through_l2_and_dsmem_agree(B, T):
     q, swa = to_dev_bf16(q_bits, DEV), to_dev_bf16(swa_bits, DEV)
     args = (q, codes, scales, to_dev(idx, DEV), swa, to_dev(wst, DEV), to_dev(wln, DEV), 128, cfg.softmax_scale)
     full_ws = csa2.csa2_workspace(B, T, 64, 0, cfg.K, device=DEV)
-    assert full_ws.numel() >= 256 + B * T * 512 * 1024
+    n_sm = torch.cuda.get_device_properties(DEV).multi_processor_count
+    nsplit = 1 << int(np.log2(min(16, n_sm // (B * T), (cfg.K + 127) // 128 + 1)))
+    assert nsplit == {(32, 1): 4, (64, 1): 2, (16, 2): 4, (12, 1): 8, (4, 1): 16, (3, 1): 16}[B, T]
+    if nsplit <= 4:
+        assert full_ws.numel() >= 256 + B * T * nsplit * 512 * 64 * 4
     o1, l1 = csa2.csa2_decode_attention(*args, ws=full_ws)
     o2, l2 = csa2.csa2_decode_attention(*args, ws=csa2.csa2_workspace(0, 0, 0, 0, 0, device=DEV))
     torch.cuda.synchronize()
