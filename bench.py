@@ -964,39 +964,52 @@ def run_ced(args, torch, csa2, dev, peaks):
 
 def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bufs, ws, world, dev):
     """Same step through the C ABI with host buffers, as a serving loop runs it: per step,
-    H2D of the step's queries from pinned memory and D2H of every layer's output, no graph,
-    one ctypes call per layer. The copies run on their own streams with two sets of device
-    I/O buffers, so step i+1's upload and step i-1's download overlap step i's kernels."""
+    one H2D copy of the step's queries (every layer's q, q_idx, w packed in one pinned
+    buffer) and one D2H copy of every layer's output (O and LSE packed likewise), no graph,
+    one ctypes call per layer with its arguments prepared once. The copies run on their own
+    streams with two sets of device I/O buffers, so step i+1's upload and step i-1's
+    download overlap step i's kernels."""
     comp = torch.cuda.Stream(device=dev)
     up = torch.cuda.Stream(device=dev)
     down = torch.cuda.Stream(device=dev)
     sp = comp.cuda_stream
     scale = ctypes.c_float(cfg.softmax_scale)
     P = lambda t: t.data_ptr()
-    h2d = d2h = 0
-    sets = []   # per buffer set: [(host, device) inputs], [(host, device) outputs], per-layer dicts
+
+    def packed(likes):
+        """One pinned host buffer and one device buffer holding tensors shaped like `likes`
+        (each at a 256-byte offset); returns both buffers and the per-tensor views."""
+        offs, total = [], 0
+        for t in likes:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        hb = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+        db = torch.empty(total, dtype=torch.uint8, device=dev)
+        view = lambda buf, o, t: buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        return hb, db, [view(hb, o, t) for o, t in zip(offs, likes)], [view(db, o, t) for o, t in zip(offs, likes)]
+
+    in_keys = [(li, k) for li, d in enumerate(dl) for k in ("q", "q_idx", "w") if k in d]
+    out_keys = [(li, k) for li, d in enumerate(dl) for k in ("o", "lse")]
+    sets = []   # per buffer set: (host in, device in, host out, device out, per-layer ctypes args)
     for sidx in range(2):
-        ins, outs, layers = [], [], []
-        for d in dl:
-            dd = dict(d)
-            for k in ("q", "q_idx", "w", "o", "lse"):
-                if k in d:
-                    dd[k] = d[k] if sidx == 0 else torch.empty_like(d[k])
-            for k in ("q", "q_idx", "w"):
-                if k in dd:
-                    h = torch.empty(dd[k].shape, dtype=dd[k].dtype, pin_memory=True)
-                    h.copy_(d[k].cpu())
-                    ins.append((h, dd[k]))
-                    if sidx == 0:
-                        h2d += h.numel() * h.element_size()
-            for k in ("o", "lse"):
-                h = torch.empty(dd[k].shape, dtype=dd[k].dtype, pin_memory=True)
-                outs.append((h, dd[k]))
-                if sidx == 0:
-                    d2h += h.numel() * h.element_size()
-            layers.append(dd)
-        sets.append((ins, outs, layers))
-    wsp, wsn = P(ws), ws.numel()
+        hi, di, hviews, dviews = packed([dl[li][k] for li, k in in_keys])
+        for (li, k), h in zip(in_keys, hviews):
+            h.copy_(dl[li][k].cpu())
+        ho, do, _, oviews = packed([dl[li][k] for li, k in out_keys])
+        dev_of = {key: v for key, v in zip(in_keys + out_keys, dviews + oviews)}
+        calls, cur = [], None
+        for li, d in enumerate(dl):
+            reuse = d["mode"] == ci.REUSE
+            if not reuse:
+                cur = idx_bufs[li % 2]
+            calls.append((d["mode"], cfg.B, cfg.T, cfg.H, cfg.H_I, P(dev_of[li, "q"]),
+                          None if reuse else P(dev_of[li, "q_idx"]), None if reuse else P(dev_of[li, "w"]),
+                          None if reuse else P(d["z"]), P(codes), P(scales), cfg.N,
+                          None if reuse else P(nvis), cfg.K, P(cur) if reuse else None, P(cur),
+                          P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v, scale, P(dev_of[li, "o"]),
+                          P(dev_of[li, "lse"]), P(ws), ws.numel(), sp))
+        sets.append((hi, di, ho, do, calls))
+    h2d, d2h = sets[0][0].numel(), sets[0][2].numel()
     ev = lambda: torch.cuda.Event()
     # per set: inputs landed / kernels done / outputs copied out
     up_done, comp_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
@@ -1004,40 +1017,29 @@ def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bu
 
     def step(i):
         s = i & 1
-        ins, outs, layers = sets[s]
+        hi, di, ho, do, calls = sets[s]
         with torch.cuda.stream(up):
             if started[s]:
                 up.wait_event(comp_done[s])      # the kernels of step i-2 have read this set's inputs
-            for h, dd in ins:
-                dd.copy_(h, non_blocking=True)
+            di.copy_(hi, non_blocking=True)
             up_done[s].record(up)
         comp.wait_event(up_done[s])
         if started[s]:
             comp.wait_event(down_done[s])        # step i-2's outputs have left this set
-        cur = None
-        for li, d in enumerate(layers):
-            reuse = d["mode"] == ci.REUSE
-            if not reuse:
-                cur = idx_bufs[li % 2]
-            r = L.csa2_decode_layer(d["mode"], cfg.B, cfg.T, cfg.H, cfg.H_I, P(d["q"]),
-                                    None if reuse else P(d["q_idx"]), None if reuse else P(d["w"]),
-                                    None if reuse else P(d["z"]), P(codes), P(scales), cfg.N,
-                                    None if reuse else P(nvis), cfg.K, P(cur) if reuse else None, P(cur),
-                                    P(d["swa"]), cfg.S, P(wst), P(wln), cfg.W, cfg.d_v, scale, P(d["o"]),
-                                    P(d["lse"]), wsp, wsn, sp)
+        for a in calls:
+            r = L.csa2_decode_layer(*a)
             assert r == 0
         comp_done[s].record(comp)
         with torch.cuda.stream(down):
             down.wait_event(comp_done[s])
-            for h, dd in outs:
-                h.copy_(dd, non_blocking=True)
+            ho.copy_(do, non_blocking=True)
             down_done[s].record(down)
         started[s] = True
 
     for i in range(max(3, args.warmup // 4)):
         step(i)
     torch.cuda.synchronize(dev)
-    n = max(200, args.steps // 10)
+    n = max(500, args.steps // 4)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     # the timed region starts before the first upload and ends after the last download
@@ -1051,8 +1053,9 @@ def run_e2e(args, torch, csa2, L, cfg, dl, codes, scales, nvis, wst, wln, idx_bu
     torch.cuda.synchronize(dev)
     total, value = aggregate_over_ranks(e0.elapsed_time(e1) / 1e3, n, world, dev)
     return {"value": value, "unit": "steps/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n, "note": "csa2_decode_layer calls without a graph; pinned host inputs and outputs copied "
-                                "every step on copy streams, two device I/O buffer sets (upload of step i+1 and "
+            "steps": n, "note": "csa2_decode_layer calls without a graph; every step one copy of the packed pinned "
+                                "host inputs (q, q_idx, w of every layer) and one copy of the packed outputs (O, LSE "
+                                "of every layer) on copy streams, two device I/O buffer sets (upload of step i+1 and "
                                 "download of step i-1 overlap step i)"}
 
 
