@@ -15,9 +15,9 @@
 //   warp 1      TMEM allocation and the MMA issuer: tcgen05.mma kind::f16, M=128,
 //               N=256, K=16, fp32 accumulators in TMEM, double-buffered (2 x 256
 //               columns) so the epilogue of one key tile overlaps the MMAs of the next
-//   warps 2..9  epilogue: thread = key row (TMEM lane); each warpgroup takes half of
-//               the columns, applies max(0, .), weights the heads by w[t, h] (fp32),
-//               sums them, and stores one fp32 score per (token, key) below the
+//   warps 2..17 epilogue: thread = key row (TMEM lane); each of the four warpgroups
+//               takes a quarter of the columns, applies max(0, .), weights the heads
+//               by w[t, h] (fp32), sums them, and stores one fp32 score per (token, key) below the
 //               token's causal limit, plus the token's running min / max score (the
 //               range words the selection starts from).
 // A work item is (sequence, token tile, chunk of key tiles); the key tiles past the
@@ -35,7 +35,7 @@ constexpr int kGN = 256;                         // (token, head) columns per ti
 constexpr int kGStages = 6;
 constexpr int kGZBytes = kGM * CSA2_D_IDX * 2;   // 16 KB
 constexpr int kGQBytes = kGN * CSA2_D_IDX * 2;   // 32 KB
-constexpr int kGEpiWarps = 8;
+constexpr int kGEpiWarps = 16;                   // four warpgroups, a quarter of the columns each
 constexpr int kGThreads = 64 + 32 * kGEpiWarps;
 constexpr int kGTmemCols = 512;
 constexpr int kGMaxTT = 64;                      // tokens per tile for H_I = 4
@@ -235,11 +235,12 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
       }
     }
   } else {
-    // ---------------- epilogue: thread = key row, warpgroup = half of the columns
-    const int ew = warp - 2;                 // 0..7
+    // ---------------- epilogue: thread = key row, warpgroup = a quarter of the columns
+    constexpr int kCols = kGN / (kGEpiWarps / 4);   // 64 columns per warpgroup
+    const int ew = warp - 2;                 // 0..15
     const int quarter = warp & 3;            // TMEM lanes 32 * quarter ..
-    const int half = ew >> 2;                // columns [128 half, 128 half + 128)
-    const int et = threadIdx.x - 64;         // 0..255
+    const int grp = ew >> 2;                 // columns [kCols grp, kCols grp + kCols)
+    const int et = threadIdx.x - 64;         // 0..511
     const int key = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
       if (kt0 >= kt1) continue;
       // also: the previous item's readers of w_s / nv_s / rng_s are done
       if (named_or(1, 32 * kGEpiWarps, *abort_flag != 0)) break;
-      {
+      if (et < kGN) {
         const int tl = et / HI;
         w_s[et] = tl < nt ? w_idx[((int64_t)b * g.T + t0) * HI + et] : 0.f;
         if (et < TT) {
@@ -263,10 +264,10 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
         }
       }
       named_bar(1, 32 * kGEpiWarps);
-      // this thread's tokens are tl0 .. tl0 + kTh - 1 (one half of the tile's columns);
-      // running min / max of their visible scores over the item's key tiles
-      constexpr int kTh = 128 / HI;
-      const int tl0 = 128 * half / HI;
+      // this thread's tokens are tl0 .. tl0 + kTh - 1 (its warpgroup's columns); running
+      // min / max of their visible scores over the item's key tiles
+      constexpr int kTh = kCols / HI;
+      const int tl0 = kCols * grp / HI;
       float mn[kTh], mx[kTh];
 #pragma unroll
       for (int i = 0; i < kTh; ++i) mn[i] = INFINITY, mx[i] = -INFINITY;
@@ -283,17 +284,17 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
         }
         tc_fence_after();
         const int n = kt * kGM + key;
-        // every token of this half sees every key of the tile (the common case)
+        // every token of these columns sees every key of the tile (the common case)
         const bool full = (kt + 1) * kGM <= min_nv;
-        const uint32_t tbase = tmem + acc * kGN + ((uint32_t)(quarter * 32) << 16) + 128 * half;
+        const uint32_t tbase = tmem + acc * kGN + ((uint32_t)(quarter * 32) << 16) + kCols * grp;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
+        for (int c4 = 0; c4 < kCols / 32; ++c4) {
           uint32_t r[32];
           tmem_ld32(tbase + 32 * c4, r);
           tmem_wait_ld();
 #pragma unroll
           for (int tk = 0; tk < 32 / HI; ++tk) {
-            const int ti = c4 * (32 / HI) + tk;   // token of this half
+            const int ti = c4 * (32 / HI) + tk;   // token of these columns
             const int tl = tl0 + ti;
             const float* wt = w_s + tl * HI;
             // two independent partial sums (even / odd heads)
@@ -367,7 +368,8 @@ constexpr int kSN = 16;
 constexpr int kSStages = 8;
 constexpr int kSAcc = 4;
 constexpr int kSQBytes = kSN * CSA2_D_IDX * 2;   // 2 KB
-constexpr int kSThreads = 64 + 32 * kGEpiWarps;
+constexpr int kSEpiWarps = 8;
+constexpr int kSThreads = 64 + 32 * kSEpiWarps;
 constexpr int kSTmemCols = 64;
 constexpr int kSMaxBj = 2048;                   // (sequence, token tile) pairs
 constexpr size_t kSSmem = 1024 + kSStages * kGZBytes + 2 * kSQBytes + 1024 + 4 * (kSMaxBj + 1);
