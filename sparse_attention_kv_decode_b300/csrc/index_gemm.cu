@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
     float* __restrict__ scores, int64_t score_stride, uint32_t* __restrict__ range,
     uint32_t* __restrict__ status) {
   constexpr int TT = kGN / HI;
-  static_assert(TT <= kGMaxTT && kGN % HI == 0 && 32 % HI == 0, "token tile");
+  static_assert(TT <= kGMaxTT && kGN % HI == 0 && 32 % HI == 0 && HI % 4 == 0, "token tile");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -296,7 +296,13 @@ __global__ void __launch_bounds__(kGThreads, 1) index_gemm_kernel(
           for (int tk = 0; tk < 32 / HI; ++tk) {
             const int ti = c4 * (32 / HI) + tk;   // token of these columns
             const int tl = tl0 + ti;
-            const float* wt = w_s + tl * HI;
+            // the token's head weights as 16-byte shared-memory loads
+            float wt[HI];
+#pragma unroll
+            for (int h = 0; h < HI; h += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(w_s + tl * HI + h);
+              wt[h] = w4.x; wt[h + 1] = w4.y; wt[h + 2] = w4.z; wt[h + 3] = w4.w;
+            }
             // two independent partial sums (even / odd heads)
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
