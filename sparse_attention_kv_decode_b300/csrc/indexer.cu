@@ -92,16 +92,23 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
   const bool pooled = pool != nullptr;
   const int64_t npos = pooled ? 8 * (int64_t)pool_stride : n_stride;   // positions per query
   const int gpq = (int)((npos + kGroupKeys - 1) / kGroupKeys);           // groups per query
-  const int64_t total = (int64_t)Q * gpq;
-  const int64_t nwarps = (int64_t)gridDim.x * (kScoreThreads / 32);
-  const int64_t wid = (int64_t)blockIdx.x * (kScoreThreads / 32) + (threadIdx.x >> 5);
-  const int64_t w_begin = total * wid / nwarps, w_end = total * (wid + 1) / nwarps;
-  if (w_begin >= w_end) return;
+  // Work comes in chunks of up to kScoreUnroll groups of one query (cpq per query). The
+  // CTAs split the chunks evenly; inside a CTA the warps take them one at a time from a
+  // shared counter, so that warps whose loads return sooner take more of them.
+  const int cpq = (gpq + kScoreUnroll - 1) / kScoreUnroll;
+  const int64_t total = (int64_t)Q * cpq;
+  const int k0 = (int)(total * blockIdx.x / gridDim.x), k1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  __shared__ int s_next;
+  if (threadIdx.x == 0) s_next = 0;
+  __syncthreads();
+  auto grab = [&]() {
+    int v = 0;
+    if (lane == 0) v = atomicAdd(&s_next, 1);
+    return v;
+  };
+  int k = k0 + __shfl_sync(0xffffffffu, grab(), 0);
 
-  // the warp's position: query qi, its group grp; advanced incrementally
-  int qi = (int)(w_begin / gpq);
-  int grp = (int)(w_begin - (int64_t)qi * gpq);
-  int64_t left = w_end - w_begin;
+  int qi = -1;
   uint32_t qa[NT][8];
   float wv[NT][2];
   int nv = 0;
@@ -126,11 +133,20 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
     smax = -INFINITY;
     smin = INFINITY;
   };
-  start_query();
-  while (left > 0) {
+  while (k < k1) {
+    // the next chunk is taken now; its index is needed only after this chunk
+    const int nx = grab();
+    // a warp's chunks increase, so its queries do too
+    const int cq = k / cpq;
+    if (cq != qi) {
+      if (qi >= 0) flush_range();
+      qi = cq;
+      start_query();
+    }
+    const int grp = (k - cq * cpq) * kScoreUnroll;
+    const int nb = min(kScoreUnroll, gpq - grp);
     // fragments of up to kScoreUnroll groups of the current query, all loads issued
     // before any use
-    const int nb = (int)min((int64_t)min(kScoreUnroll, gpq - grp), left);
     uint4 v[kScoreUnroll][4];
     int okm[kScoreUnroll];
 #pragma unroll
@@ -185,18 +201,9 @@ __global__ void __launch_bounds__(kScoreThreads, kScoreCtasPerSm) index_score_ke
         smin = fminf(smin, sc);
       }
     }
-    grp += nb;
-    left -= nb;
-    if (grp == gpq) {
-      flush_range();
-      if (left > 0) {
-        ++qi;
-        grp = 0;
-        start_query();
-      }
-    }
+    k = k0 + __shfl_sync(0xffffffffu, nx, 0);
   }
-  if (grp != gpq) flush_range();
+  if (qi >= 0) flush_range();
 }
 
 cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void* z,
@@ -208,7 +215,9 @@ cudaError_t launch_index_score(const void* q_idx, const float* w_idx, const void
   const int Q = B * T;
   if (n_stride == 0 || Q == 0) return cudaSuccess;
   const int64_t npos = pool ? 8 * (int64_t)pool_stride : n_stride;
-  const int64_t total = (int64_t)Q * ((npos + kGroupKeys - 1) / kGroupKeys);
+  const int64_t gpq = (npos + kGroupKeys - 1) / kGroupKeys;
+  const int64_t total = (int64_t)Q * ((gpq + kScoreUnroll - 1) / kScoreUnroll);   // chunks
+  if (total >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;
   const int64_t warps = (int64_t)device_sm_count() * kScoreCtasPerSm * (kScoreThreads / 32);
   int64_t grid = (int64_t)device_sm_count() * kScoreCtasPerSm;
   if (total < warps) grid = (total + kScoreThreads / 32 - 1) / (kScoreThreads / 32);
