@@ -20,10 +20,12 @@ namespace csa2 {
 // Scoring
 // ---------------------------------------------------------------------------
 // The scoring is a pure stream over the keys (4 MiB per query at 128K context),
-// so it is written for memory-level parallelism with nothing to synchronise:
-// every warp owns a contiguous, balanced run of 16-key groups (a query at a
-// time) and loads each group's MMA fragments straight from global memory into
-// registers, kScoreUnroll groups (8 x 16-byte loads per thread) in flight. A
+// so it is written for memory-level parallelism with almost nothing to
+// synchronise: every CTA owns a contiguous, balanced run of chunks of
+// kScoreUnroll 16-key groups of one query, its warps take the chunks one at a
+// time from a shared counter, and a warp loads each group's MMA fragments
+// straight from global memory into registers (8 x 16-byte loads per thread in
+// flight). A
 // group is scored with four m16n8k16 bf16 MMAs per 8 indexer heads: thread
 // (g = lane/4, tig = lane%4) holds, for key rows g and g+8, the 16-byte pieces
 // at byte offsets 16*tig and 64+16*tig; the MMA's k-slots are assigned to
