@@ -168,14 +168,31 @@ def test_reuse_copies_and_aliases():
 
 @pytest.mark.parametrize("B,N", [(6, 20000), (3, 40000), (33, 4099)])
 def test_warp_runs_across_query_boundaries(B, N):
-    """All entries visible, at sizes where a scoring warp's run of key groups ends inside
-    one query and continues in the next (the groups are split evenly over 148 x 32 warps,
-    not per query): every query's last groups must be scored with that query's indexer
-    rows."""
+    """All entries visible, at sizes where a scoring CTA's run of key-group chunks ends
+    inside one query and continues in the next (the chunks are split evenly over 296 CTAs,
+    not per query, and a CTA's warps take them in turn): every query's last groups must be
+    scored with that query's indexer rows."""
     cfg = ci.scaled(ci.DECODE_128K, B=B, N=N, H=16, K=256, W=8, modes=(ci.FULL,))
     inp = ci.make_decode_inputs(cfg, with_x=False)
     L = inp.layers[0]
     _check_all(L.q_idx, L.w_idx, L.z, np.full(B, N, np.int32), cfg.K)
+
+
+@pytest.mark.parametrize("B,N,H_I", [(45, 4111, 8), (70, 1000, 8), (19, 4111, 16)])
+def test_scoring_chunks_with_ragged_single_tokens(B, N, H_I):
+    """One token per sequence with ragged visible counts (0, 1, group and chunk edges,
+    full) and an odd number of 16-key groups per query, so that each query's last chunk
+    holds one group and chunk runs end inside queries: every query must be scored over
+    exactly its visible entries with its own indexer rows and weights."""
+    rng = np.random.default_rng(2000 + B + N + H_I)
+    K = 200
+    q = ci.bf16_bits(rng.standard_normal((B, 1, H_I, 64), dtype=np.float32))
+    w = np.abs(rng.standard_normal((B, 1, H_I), dtype=np.float32))
+    z = ci.bf16_bits(rng.standard_normal((B, N, 64), dtype=np.float32))
+    edges = np.array([0, 1, 15, 16, 17, 31, 32, 33, 200, 201, N - 1, N], dtype=np.int32)
+    nvis = np.where(rng.random(B) < 0.5, edges[rng.integers(0, edges.size, B)],
+                    rng.integers(0, N + 1, B)).astype(np.int32)
+    _check_all(q, w, z, nvis, K)
 
 
 @pytest.mark.parametrize("B,T,H_I", [(40, 2, 8), (37, 3, 4), (9, 5, 8), (21, 3, 8), (12, 2, 16)])
