@@ -9,7 +9,6 @@ import os
 from fractions import Fraction
 
 import numpy as np
-import pytest
 
 from oracle import fp4
 

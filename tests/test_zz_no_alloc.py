@@ -10,7 +10,6 @@ it). The file is collected last, and it also passes when run alone in a fresh pr
 Ref: "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression", picx.dev summary,
 Methodology / 2. CSA2 (the indexer's top-K of FULL / REINDEX, and REUSE).
 """
-import ctypes
 
 import numpy as np
 import pytest
