@@ -115,9 +115,13 @@ def test_scaled_group_full_reindex_reuse(fused):
 
 
 @pytest.mark.parametrize("fused", [True, False])
-@pytest.mark.parametrize("H,K,W", [(16, 200, 100), (32, 1000, 1), (48, 64, 256), (64, 130, 0), (64, 2048, 200)])
+@pytest.mark.parametrize("H,K,W", [(16, 200, 100), (32, 1000, 1), (48, 64, 256), (64, 130, 0), (64, 2048, 200),
+                                   (64, 4096, 256)])
 def test_ragged_shapes(H, K, W, fused):
-    cfg = ci.scaled(ci.DECODE_128K, B=2, N=2500, H=H, K=K, W=max(W, 1), modes=(ci.FULL, ci.REUSE))
+    """Head counts 16-64, K from 64 to the largest supported (4096), windows from none to
+    the largest (256 rows)."""
+    N = 5000 if K > 2048 else 2500
+    cfg = ci.scaled(ci.DECODE_128K, B=2, N=N, H=H, K=K, W=max(W, 1), modes=(ci.FULL, ci.REUSE))
     inp = ci.make_decode_inputs(cfg)
     if W == 0:
         inp.win_len[:] = 0

@@ -50,7 +50,8 @@ def test_tiny_config():
     _check_all(L.q_idx, L.w_idx, L.z, inp.n_visible, cfg.K)
 
 
-@pytest.mark.parametrize("N,K,H_I", [(4096, 512, 8), (3000, 256, 4), (5000, 2048, 16), (1, 4, 3), (700, 700, 8)])
+@pytest.mark.parametrize("N,K,H_I", [(4096, 512, 8), (3000, 256, 4), (5000, 2048, 16), (1, 4, 3), (700, 700, 8),
+                                     (9000, 4096, 8)])
 def test_scaled_decode_shapes(N, K, H_I):
     cfg = ci.scaled(ci.DECODE_128K, B=3, N=N, H=16, H_I=H_I, K=K, W=8, modes=(ci.FULL,))
     inp = ci.make_decode_inputs(cfg, with_x=False)
